@@ -1,0 +1,304 @@
+"""Deterministic, batch-invariant BF16 contractions for GB300 (sm_103a).
+
+A thin ctypes binding over the C ABI in ``include/rlk.h`` (librlk.so, built
+in-tree by ``build.py``).  This module only marshals arguments: PyTorch is used
+for device memory and streams; every step of every operator runs in the
+library's CUDA kernels.  There is no CPU or PyTorch fallback — if the library
+is missing, or the device is not sm_103, calls raise.
+
+Operators (web pages of the RL-Kernel project):
+  * ``linear_logp`` — "feat(linear-logp): add batch-invariant fused SM90
+    operator": log_softmax(hidden . W^T + bias)[target] and the log-sum-exp,
+    with a vocabulary split that depends on V only.  Forward only: inputs that
+    require grad are rejected (the page's author notes: backward is outside
+    the contract and fails closed).
+  * ``det_gemm_fwd / det_gemm_da / det_gemm_db`` — "feat(musa): add native
+    deterministic gemm kernel": C = A B, dA = dC B^T, dB = A^T dC with FP32
+    accumulation in a fixed ascending K order, BF16 or FP32 output; an FP32 dC
+    is rounded to BF16 first (that page's review comment).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG_DIR, "librlk.so")
+
+RLK_OK = 0
+RLK_BF16, RLK_FP32 = 0, 1
+RLK_GEMM_FWD, RLK_GEMM_DA, RLK_GEMM_DB = 0, 1, 2
+STATUS_NAMES = {0: "RLK_OK", 1: "RLK_ERR_NULL", 2: "RLK_ERR_SHAPE", 3: "RLK_ERR_DTYPE",
+                4: "RLK_ERR_ALIGN", 5: "RLK_ERR_WORKSPACE", 6: "RLK_ERR_UNSUPPORTED_DEVICE",
+                7: "RLK_ERR_CUDA", 8: "RLK_ERR_TIMEOUT"}
+
+
+class RlkError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+_P, _I64, _SZ, _I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int
+
+# name -> (restype, argtypes); mirrors include/rlk.h
+SIGNATURES = {
+    "rlk_status_string": (ctypes.c_char_p, [_I]),
+    "rlk_numerics_version": (_I, []),
+    "rlk_device_check": (_I, []),
+    "rlk_get_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
+    "rlk_vocab_split_policy": (_I, [_I64, ctypes.POINTER(_I64), ctypes.POINTER(_I64),
+                                    ctypes.POINTER(_I64)]),
+    "rlk_linear_logp_workspace_size": (_SZ, [_P, _I64, _I64, _I64, _P, _I64, _I64]),
+    "rlk_linear_logp": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _P, _I64,
+                             _P, _P, _P, _P, _SZ, _P]),
+    "rlk_linear_logp_partials": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _P, _I64,
+                                      _P, _SZ, _P]),
+    "rlk_linear_logp_combine": (_I, [_I64, _I64, _P, _I64, _P, _P, _P, _P, _SZ, _P]),
+    "rlk_det_gemm_workspace_size": (_SZ, [_I, _P, _I, _I64, _I64, _I64, _P, _I, _I64, _I64, _I64]),
+    "rlk_det_gemm_fwd": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _I, _I64, _P, _SZ, _P]),
+    "rlk_det_gemm_da": (_I, [_P, _I, _I64, _I64, _I64, _P, _I64, _I64, _P, _I, _I64, _P, _SZ, _P]),
+    "rlk_det_gemm_db": (_I, [_P, _I64, _I64, _I64, _P, _I, _I64, _I64, _P, _I, _I64, _P, _SZ, _P]),
+}
+
+_LIB = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded librlk.so; raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"librlk.so is not built ({LIB_PATH}); build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        cdll = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(cdll, name)
+            f.restype = res
+            f.argtypes = args
+        _LIB = cdll
+    return _LIB
+
+
+def status_string(status: int) -> str:
+    return lib().rlk_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != RLK_OK:
+        raise RlkError(status, what)
+
+
+def numerics_version() -> int:
+    return int(lib().rlk_numerics_version())
+
+
+def vocab_split_policy(V: int):
+    """(num_splits, vtiles_per_split, num_vtiles) for a vocabulary of V ids."""
+    s, v, t = _I64(), _I64(), _I64()
+    _check(lib().rlk_vocab_split_policy(V, ctypes.byref(s), ctypes.byref(v), ctypes.byref(t)),
+           "rlk_vocab_split_policy")
+    return s.value, v.value, t.value
+
+
+def device_error(stream=None) -> int:
+    """Reads and clears the library's device error word (synchronises the stream)."""
+    flags = ctypes.c_uint32(0)
+    st = lib().rlk_get_device_error(_stream_ptr(stream), ctypes.byref(flags))
+    if st not in (RLK_OK, 8):
+        _check(st, "rlk_get_device_error")
+    return flags.value
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _matrix(t: torch.Tensor, name: str):
+    """(tensor, leading dimension) for a 2-D row-major operand (unit column stride)."""
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D, got shape {tuple(t.shape)}")
+    if t.stride(1) != 1 or (t.size(0) > 1 and t.stride(0) < t.size(1)):
+        t = t.contiguous()
+    ld = t.stride(0) if t.size(0) > 1 else max(t.size(1), t.stride(0))
+    return t, ld
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("rlk operates on CUDA tensors only (no CPU fallback)")
+
+
+_DT = {torch.bfloat16: RLK_BF16, torch.float32: RLK_FP32}
+
+
+# ------------------------------------------------------------------ linear-logp
+def linear_logp_workspace(hidden2d, weight, ldh, ldw, N, H, V) -> torch.Tensor:
+    n = lib().rlk_linear_logp_workspace_size(_ptr(hidden2d), N, H, ldh, _ptr(weight), V, ldw)
+    if n == 0 and N > 0:
+        raise RlkError(2, "rlk_linear_logp_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=hidden2d.device)
+
+
+def linear_logp(hidden: torch.Tensor, weight: torch.Tensor, target: torch.Tensor,
+                bias: torch.Tensor | None = None, *, return_target_logit: bool = False,
+                stream=None):
+    """logp, lse (FP32, shaped like hidden's leading dims) [, target logit].
+
+    hidden [..., H] bf16, weight [V, H] bf16, target [...] int64 (any strides,
+    including an expanded zero-stride target), bias [V] fp32 or None.
+    """
+    if hidden.requires_grad or weight.requires_grad or (bias is not None and bias.requires_grad):
+        raise RuntimeError("linear_logp is forward-only: inputs that require grad are rejected")
+    _require_cuda(hidden, weight, target, bias)
+    if hidden.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:
+        raise TypeError("hidden and weight must be bfloat16")
+    if target.dtype != torch.int64:
+        raise TypeError("target must be int64")
+    if bias is not None and (bias.dtype != torch.float32 or bias.dim() != 1):
+        raise TypeError("bias must be a 1-D float32 tensor")
+    lead = hidden.shape[:-1]
+    H = hidden.size(-1)
+    h2, ldh = _matrix(hidden.reshape(-1, H), "hidden")
+    w2, ldw = _matrix(weight, "weight")
+    N, V = h2.size(0), w2.size(0)
+    if w2.size(1) != H:
+        raise ValueError("weight must be [V, H] with the hidden size H")
+    t1 = target.reshape(-1)
+    if t1.numel() != N:
+        raise ValueError("target must have one id per hidden row")
+    tstride = t1.stride(0) if N > 1 else 1
+    if bias is not None:
+        bias = bias.contiguous()
+        if bias.numel() != V:
+            raise ValueError("bias must have V entries")
+    dev = hidden.device
+    logp = torch.empty(N, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    zt = torch.empty(N, dtype=torch.float32, device=dev) if return_target_logit else None
+    with torch.cuda.device(dev):
+        ws = linear_logp_workspace(h2, w2, ldh, ldw, N, H, V)
+        st = lib().rlk_linear_logp(_ptr(h2), N, H, ldh, _ptr(w2), V, ldw, _ptr(bias), _ptr(t1),
+                                   tstride, _ptr(logp), _ptr(lse), _ptr(zt), _ptr(ws), ws.numel(),
+                                   _stream_ptr(stream))
+    _check(st, "rlk_linear_logp")
+    out = (logp.reshape(lead), lse.reshape(lead))
+    if return_target_logit:
+        out = out + (zt.reshape(lead),)
+    return out
+
+
+class LinearLogpCall:
+    """A prepared linear-logp call on fixed tensors (outputs and workspace
+    allocated once), runnable as the whole operator or as its two stages."""
+
+    def __init__(self, hidden, weight, target, bias=None, *, target_logit: bool = False):
+        _require_cuda(hidden, weight, target, bias)
+        self.h, self.ldh = _matrix(hidden, "hidden")
+        self.w, self.ldw = _matrix(weight, "weight")
+        self.t = target.reshape(-1)
+        self.bias = None if bias is None else bias.contiguous()
+        self.N, self.H = self.h.shape
+        self.V = self.w.size(0)
+        self.tstride = self.t.stride(0) if self.N > 1 else 1
+        dev = hidden.device
+        self.logp = torch.empty(self.N, dtype=torch.float32, device=dev)
+        self.lse = torch.empty(self.N, dtype=torch.float32, device=dev)
+        self.zt = torch.empty(self.N, dtype=torch.float32, device=dev) if target_logit else None
+        with torch.cuda.device(dev):
+            self.ws = linear_logp_workspace(self.h, self.w, self.ldh, self.ldw, self.N, self.H, self.V)
+
+    def partials(self, stream=None):
+        _check(lib().rlk_linear_logp_partials(
+            _ptr(self.h), self.N, self.H, self.ldh, _ptr(self.w), self.V, self.ldw, _ptr(self.bias),
+            _ptr(self.t), self.tstride, _ptr(self.ws), self.ws.numel(), _stream_ptr(stream)),
+            "rlk_linear_logp_partials")
+
+    def combine(self, stream=None):
+        _check(lib().rlk_linear_logp_combine(
+            self.N, self.V, _ptr(self.t), self.tstride, _ptr(self.logp), _ptr(self.lse),
+            _ptr(self.zt), _ptr(self.ws), self.ws.numel(), _stream_ptr(stream)),
+            "rlk_linear_logp_combine")
+
+    def __call__(self, stream=None):
+        _check(lib().rlk_linear_logp(
+            _ptr(self.h), self.N, self.H, self.ldh, _ptr(self.w), self.V, self.ldw, _ptr(self.bias),
+            _ptr(self.t), self.tstride, _ptr(self.logp), _ptr(self.lse), _ptr(self.zt),
+            _ptr(self.ws), self.ws.numel(), _stream_ptr(stream)), "rlk_linear_logp")
+        return self.logp, self.lse
+
+
+# ------------------------------------------------------------------ det_gemm
+def _gemm_ws(op, x, xdt, xld, y, ydt, yld, device):
+    n = lib().rlk_det_gemm_workspace_size(op, _ptr(x), xdt, x.size(0), x.size(1), xld,
+                                          _ptr(y), ydt, y.size(0), y.size(1), yld)
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=device), n
+
+
+def _flatten_rows(t: torch.Tensor) -> torch.Tensor:
+    return t.reshape(-1, t.size(-1)) if t.dim() != 2 else t
+
+
+def det_gemm_fwd(A: torch.Tensor, B: torch.Tensor, out_dtype=torch.bfloat16, *, stream=None):
+    """C = A . B; A [..., M, K] bf16 (leading dims flattened into rows), B [K, N] bf16."""
+    _require_cuda(A, B)
+    lead = A.shape[:-1]
+    A2, lda = _matrix(_flatten_rows(A), "A")
+    B2, ldb = _matrix(B, "B")
+    M, K = A2.shape
+    if B2.size(0) != K:
+        raise ValueError("A and B disagree on K")
+    N = B2.size(1)
+    C = torch.empty(M, N, dtype=out_dtype, device=A.device)
+    with torch.cuda.device(A.device):
+        ws, n = _gemm_ws(RLK_GEMM_FWD, A2, RLK_BF16, lda, B2, RLK_BF16, ldb, A.device)
+        _check(lib().rlk_det_gemm_fwd(_ptr(A2), M, K, lda, _ptr(B2), N, ldb, _ptr(C), _DT[out_dtype],
+                                      N, _ptr(ws), n, _stream_ptr(stream)), "rlk_det_gemm_fwd")
+    return C.reshape(*lead, N)
+
+
+def det_gemm_da(dC: torch.Tensor, B: torch.Tensor, out_dtype=torch.bfloat16, *, stream=None):
+    """dA = dC . B^T; dC [..., M, N] bf16 or fp32 (fp32 is rounded to bf16 first), B [K, N]."""
+    _require_cuda(dC, B)
+    lead = dC.shape[:-1]
+    d2, lddc = _matrix(_flatten_rows(dC), "dC")
+    B2, ldb = _matrix(B, "B")
+    M, N = d2.shape
+    K = B2.size(0)
+    if B2.size(1) != N:
+        raise ValueError("dC and B disagree on N")
+    dA = torch.empty(M, K, dtype=out_dtype, device=dC.device)
+    with torch.cuda.device(dC.device):
+        ws, n = _gemm_ws(RLK_GEMM_DA, d2, _DT[d2.dtype], lddc, B2, RLK_BF16, ldb, dC.device)
+        _check(lib().rlk_det_gemm_da(_ptr(d2), _DT[d2.dtype], M, N, lddc, _ptr(B2), K, ldb, _ptr(dA),
+                                     _DT[out_dtype], K, _ptr(ws), n, _stream_ptr(stream)),
+               "rlk_det_gemm_da")
+    return dA.reshape(*lead, K)
+
+
+def det_gemm_db(A: torch.Tensor, dC: torch.Tensor, out_dtype=torch.bfloat16, *, stream=None):
+    """dB = A^T . dC summed over every row; A [..., M, K] bf16, dC [..., M, N] bf16 or fp32."""
+    _require_cuda(A, dC)
+    A2, lda = _matrix(_flatten_rows(A), "A")
+    d2, lddc = _matrix(_flatten_rows(dC), "dC")
+    M, K = A2.shape
+    if d2.size(0) != M:
+        raise ValueError("A and dC disagree on M")
+    N = d2.size(1)
+    dB = torch.empty(K, N, dtype=out_dtype, device=A.device)
+    with torch.cuda.device(A.device):
+        ws, n = _gemm_ws(RLK_GEMM_DB, A2, RLK_BF16, lda, d2, _DT[d2.dtype], lddc, A.device)
+        _check(lib().rlk_det_gemm_db(_ptr(A2), M, K, lda, _ptr(d2), _DT[d2.dtype], N, lddc, _ptr(dB),
+                                     _DT[out_dtype], N, _ptr(ws), n, _stream_ptr(stream)),
+               "rlk_det_gemm_db")
+    return dB

@@ -1,0 +1,185 @@
+// Shared host logic of the rlk library: status strings, the device check,
+// TMA descriptor encoding, the vocabulary split policy, operand staging
+// kernels and the device error word.
+#include <mutex>
+
+#include <cuda_bf16.h>
+
+#include "rlk.h"
+#include "rlk_internal.h"
+
+namespace rlk {
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+std::mutex g_mutex;
+EncodeTiledFn g_encode = nullptr;
+constexpr int kMaxDevices = 64;
+int g_dev_state[kMaxDevices];      // 0 unknown, 1 ready, -1 unsupported
+int g_dev_sms[kMaxDevices];
+
+EncodeTiledFn get_encode() {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  return g_encode;
+}
+
+}  // namespace
+
+rlk_status device_ready(DeviceInfo* info) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return RLK_ERR_UNSUPPORTED_DEVICE;
+  }
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_dev_state[dev] == 0) {
+      int major = 0, minor = 0, sms = 0;
+      bool ok = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) ==
+                    cudaSuccess &&
+                cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) ==
+                    cudaSuccess &&
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
+      cudaGetLastError();
+      g_dev_state[dev] = (ok && major == 10 && minor == 3 && sms > 0) ? 1 : -1;
+      g_dev_sms[dev] = sms;
+    }
+    if (g_dev_state[dev] != 1) return RLK_ERR_UNSUPPORTED_DEVICE;
+    info->device = dev;
+    info->sm_count = g_dev_sms[dev];
+  }
+  if (!get_encode()) return RLK_ERR_CUDA;
+  return RLK_OK;
+}
+
+bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                    uint64_t ld, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- staging kernels
+namespace {
+
+__global__ void stage_bf16_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t cols,
+                                  int64_t ld_src, uint16_t* __restrict__ dst, int64_t ld_dst) {
+  const int64_t total = rows * ld_dst;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / ld_dst, c = i - r * ld_dst;
+    dst[i] = c < cols ? src[r * ld_src + c] : (uint16_t)0;
+  }
+}
+
+__global__ void cast_f32_bf16_kernel(const float* __restrict__ src, int64_t rows, int64_t cols,
+                                     int64_t ld_src, uint16_t* __restrict__ dst, int64_t ld_dst) {
+  const int64_t total = rows * ld_dst;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / ld_dst, c = i - r * ld_dst;
+    uint16_t v = 0;
+    if (c < cols) {
+      __nv_bfloat16 b = __float2bfloat16_rn(src[r * ld_src + c]);
+      v = *reinterpret_cast<uint16_t*>(&b);
+    }
+    dst[i] = v;
+  }
+}
+
+int stage_grid(int64_t total) {
+  int64_t g = ceil_div(total, 256);
+  return (int)(g < 4096 ? (g > 0 ? g : 1) : 4096);
+}
+
+}  // namespace
+
+cudaError_t launch_stage_bf16(const uint16_t* src, int64_t rows, int64_t cols, int64_t ld_src,
+                              uint16_t* dst, int64_t ld_dst, cudaStream_t stream) {
+  stage_bf16_kernel<<<stage_grid(rows * ld_dst), 256, 0, stream>>>(src, rows, cols, ld_src, dst,
+                                                                   ld_dst);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cast_f32_bf16(const float* src, int64_t rows, int64_t cols, int64_t ld_src,
+                                 uint16_t* dst, int64_t ld_dst, cudaStream_t stream) {
+  cast_f32_bf16_kernel<<<stage_grid(rows * ld_dst), 256, 0, stream>>>(src, rows, cols, ld_src, dst,
+                                                                      ld_dst);
+  return cudaGetLastError();
+}
+
+}  // namespace rlk
+
+// ====================================================================== C ABI
+extern "C" {
+
+const char* rlk_status_string(int status) {
+  switch (status) {
+    case RLK_OK: return "RLK_OK";
+    case RLK_ERR_NULL: return "RLK_ERR_NULL: a required pointer is NULL";
+    case RLK_ERR_SHAPE: return "RLK_ERR_SHAPE: a size or leading dimension is out of range";
+    case RLK_ERR_DTYPE: return "RLK_ERR_DTYPE: unsupported dtype";
+    case RLK_ERR_ALIGN: return "RLK_ERR_ALIGN: pointer not aligned to its element size";
+    case RLK_ERR_WORKSPACE: return "RLK_ERR_WORKSPACE: workspace missing or too small";
+    case RLK_ERR_UNSUPPORTED_DEVICE:
+      return "RLK_ERR_UNSUPPORTED_DEVICE: no CUDA device, or the device is not sm_103";
+    case RLK_ERR_CUDA: return "RLK_ERR_CUDA: the CUDA runtime rejected a call";
+    case RLK_ERR_TIMEOUT: return "RLK_ERR_TIMEOUT: a kernel wait expired";
+    default: return "RLK_ERR_UNKNOWN";
+  }
+}
+
+int rlk_numerics_version(void) { return RLK_NUMERICS_VERSION; }
+
+rlk_status rlk_device_check(void) {
+  rlk::DeviceInfo info;
+  return rlk::device_ready(&info);
+}
+
+rlk_status rlk_get_device_error(void* stream, uint32_t* flags) {
+  if (!flags) return RLK_ERR_NULL;
+  *flags = 0;
+  rlk::DeviceInfo info;
+  rlk_status st = rlk::device_ready(&info);
+  if (st != RLK_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return RLK_ERR_CUDA;
+  }
+  *flags = rlk::take_error_linear_logp() | rlk::take_error_det_gemm();
+  return *flags ? RLK_ERR_TIMEOUT : RLK_OK;
+}
+
+rlk_status rlk_vocab_split_policy(int64_t V, int64_t* num_splits, int64_t* vtiles_per_split,
+                                  int64_t* num_vtiles) {
+  if (!num_splits || !vtiles_per_split || !num_vtiles) return RLK_ERR_NULL;
+  if (V < 1 || V >= (int64_t(1) << 31)) return RLK_ERR_SHAPE;
+  const int64_t vt = rlk::ceil_div(V, rlk::kVocabTile);
+  const int64_t vps = rlk::ceil_div(vt, rlk::kMaxVocabSplits);
+  *num_vtiles = vt;
+  *vtiles_per_split = vps;
+  *num_splits = rlk::ceil_div(vt, vps);
+  return RLK_OK;
+}
+
+}  // extern "C"

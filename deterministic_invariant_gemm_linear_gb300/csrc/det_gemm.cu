@@ -1,0 +1,354 @@
+// Deterministic BF16 GEMM family on sm_103a.
+//
+// "feat(musa): add native deterministic gemm kernel", Summary: forward
+// C = A B, dA = dC B^T and dB = A^T dC with FP32 accumulation in a fixed,
+// ascending K order; BF16 or FP32 output.  Review comment on that page: when the
+// forward produced FP32, grad_output is rounded to BF16 before dA / dB.
+// "Support musa", review comment: det_gemm never falls back to a
+// non-deterministic matmul; unsupported cases fail explicitly.
+//
+// One kernel template serves all three products through the operands'
+// majorness (which of the two extents of each operand is contiguous):
+//   forward  A [M,K] reduction-contiguous (K-major), B [K,N] N-contiguous (MN-major)
+//   dA       dC [M,N] K-major,                       B [K,N] K-major (N is reduced)
+//   dB       A [M,K] MN-major (output rows = K),      dC [M,N] MN-major (M is reduced)
+// Output tiles are 128 x 256, the reduction runs over blocks of 64 in
+// ascending order, each tile's accumulation starts from zero, and there is no
+// split of the reduction: every output bit is a function of its own row of the
+// left operand and column of the right operand only.
+#include <mutex>
+
+#include <cuda_bf16.h>
+
+#include "rlk.h"
+#include "rlk_internal.h"
+#include "rlk_pipeline.cuh"
+
+namespace rlk {
+
+__device__ unsigned int g_err_det_gemm = 0;
+
+namespace {
+
+struct GemmSched {
+  int num_mb;   // 128-row output blocks
+  int num_nb;   // 256-column output blocks
+  int nkb;      // 64-wide reduction blocks
+  __device__ __forceinline__ int num_units() const { return num_mb * num_nb; }
+  __device__ __forceinline__ int unit_tiles(int) const { return 1; }
+  __device__ __forceinline__ void tile_coords(int u, int, int& a0, int& b0) const {
+    const int nb = u / num_mb;
+    a0 = (u - nb * num_mb) * kBM;
+    b0 = nb * kBN;
+  }
+};
+
+struct GemmOut {
+  int M, N;          // output extent
+  void* C;
+  int64_t ldc;       // elements
+  int fp32;          // 1: FP32 output, 0: BF16
+  int vec_ok;        // 16-byte vector stores allowed (aligned base and pitch)
+};
+
+__device__ __forceinline__ void store_chunk(const GemmOut& o, int row, int col0,
+                                            const uint32_t (&r)[32]) {
+  const bool full = o.vec_ok && col0 + 32 <= o.N;
+  if (o.fp32) {
+    float* dst = static_cast<float*>(o.C) + (int64_t)row * o.ldc + col0;
+    if (full) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        reinterpret_cast<uint4*>(dst)[i] = make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (col0 + i < o.N) dst[i] = __uint_as_float(r[i]);
+    }
+  } else {
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(o.C) + (int64_t)row * o.ldc + col0;
+    if (full) {
+      uint32_t p[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+        p[i] = *reinterpret_cast<uint32_t*>(&b);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        reinterpret_cast<uint4*>(dst)[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (col0 + i < o.N) dst[i] = __float2bfloat16_rn(__uint_as_float(r[i]));
+    }
+  }
+}
+
+template <bool kAMN, bool kBMN>
+__global__ void __launch_bounds__(kThreads, 1)
+    det_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                    GemmSched sc, GemmOut out) {
+  extern __shared__ uint8_t smem_raw[];
+  const PipeSmem ps = pipe_smem(smem_raw);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tm_a);
+    tma_prefetch_desc(&tm_b);
+  }
+  const uint32_t tmem = pipe_setup(ps);
+  using TA = OperandTile<kAMN, kBM>;
+  using TB = OperandTile<kBMN, kBN>;
+
+  if (warp == 0) {
+    if (lane == 0) producer_role<TA, TB>(&tm_a, &tm_b, sc, ps, &g_err_det_gemm);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) mma_role<TA, TB>(sc, ps, tmem, idesc_bf16_f32(kBM, kBN, kAMN, kBMN), &g_err_det_gemm);
+    __syncwarp();
+  } else {
+    const int q = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const int units = sc.num_units();
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      if (!epilogue_acquire(ps, acc, acc_phase, &g_err_det_gemm)) break;
+      int m0, n0;
+      sc.tile_coords(u, 0, m0, n0);
+      const int row = m0 + q * 32 + lane;
+      const uint32_t taddr = tmem + acc * kAccCols + lane_off;
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        const int col0 = n0 + c * 32;
+        if (col0 >= out.N) break;               // uniform: depends on the tile only
+        uint32_t r[32];
+        tmem_ld32(taddr + c * 32, r);
+        tmem_wait_ld();
+        if (row < out.M) store_chunk(out, row, col0, r);
+      }
+      epilogue_release(ps, acc);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+  pipe_teardown(tmem);
+}
+
+std::mutex g_attr_mutex;
+bool g_attr_set[64];
+
+template <bool kAMN, bool kBMN>
+cudaError_t set_attr() {
+  return cudaFuncSetAttribute(det_gemm_kernel<kAMN, kBMN>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+}
+
+cudaError_t ensure_attrs(int dev) {
+  std::lock_guard<std::mutex> lock(g_attr_mutex);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!g_attr_set[dev]) {
+    cudaError_t e = set_attr<false, true>();
+    if (e == cudaSuccess) e = set_attr<false, false>();
+    if (e == cudaSuccess) e = set_attr<true, true>();
+    if (e != cudaSuccess) return e;
+    g_attr_set[dev] = true;
+  }
+  return cudaSuccess;
+}
+
+inline bool dtype_ok(int d) { return d == RLK_BF16 || d == RLK_FP32; }
+inline int esize(int d) { return d == RLK_FP32 ? 4 : 2; }
+inline bool ptr_aligned(const void* p, int a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+constexpr int64_t kDimLimit = int64_t(1) << 31;
+constexpr int64_t kLdLimit = int64_t(1) << 36;
+
+// One input operand of a product and how the kernel will read it.
+struct Operand {
+  const void* ptr;
+  int dtype;
+  int64_t rows, cols, ld;
+  bool staged = false;        // copied / rounded into the workspace first
+  int64_t eff_ld = 0;         // pitch the kernel reads
+  size_t ws_off = 0, ws_bytes = 0;
+};
+
+void plan_operand(Operand& o, size_t& off) {
+  o.staged = o.dtype == RLK_FP32 || !tma_ready(o.ptr, o.ld);
+  o.eff_ld = o.staged ? staged_ld(o.cols) : o.ld;
+  o.ws_off = off;
+  o.ws_bytes = o.staged ? align_up((size_t)o.rows * o.eff_ld * 2, 256) : 0;
+  off += o.ws_bytes;
+}
+
+rlk_status check_operand(const Operand& o, bool allow_fp32) {
+  if (!dtype_ok(o.dtype) || (o.dtype == RLK_FP32 && !allow_fp32)) return RLK_ERR_DTYPE;
+  if (o.rows < 0 || o.rows >= kDimLimit || o.cols < 1 || o.cols >= kDimLimit) return RLK_ERR_SHAPE;
+  if (o.ld < o.cols || o.ld >= kLdLimit) return RLK_ERR_SHAPE;
+  return RLK_OK;
+}
+
+// Stages (if planned) and returns the BF16 pointer the kernel reads.
+rlk_status materialise(Operand& o, uint8_t* ws, cudaStream_t s, const void** out) {
+  if (!o.staged) {
+    *out = o.ptr;
+    return RLK_OK;
+  }
+  uint16_t* dst = reinterpret_cast<uint16_t*>(ws + o.ws_off);
+  cudaError_t e = o.dtype == RLK_FP32
+                      ? launch_cast_f32_bf16(static_cast<const float*>(o.ptr), o.rows, o.cols, o.ld,
+                                             dst, o.eff_ld, s)
+                      : launch_stage_bf16(static_cast<const uint16_t*>(o.ptr), o.rows, o.cols, o.ld,
+                                          dst, o.eff_ld, s);
+  *out = dst;
+  return e == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
+}
+
+enum class Kind { kFwd, kDa, kDb };
+
+// Shared driver: x and y are the op's two inputs in argument order; the output
+// is out_rows x out_cols, reduced over `red`.
+rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t out_cols,
+                    int64_t red, void* C, int c_dtype, int64_t ldc, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  if (!dtype_ok(c_dtype)) return RLK_ERR_DTYPE;
+  if (ldc < out_cols || ldc >= kLdLimit) return RLK_ERR_SHAPE;
+  const int64_t num_mb = ceil_div(out_rows, kBM), num_nb = ceil_div(out_cols, kBN);
+  if (num_mb * num_nb >= kDimLimit) return RLK_ERR_SHAPE;
+  size_t off = 0;
+  plan_operand(x, off);
+  plan_operand(y, off);
+  if (out_rows == 0) return RLK_OK;
+  if (!C) return RLK_ERR_NULL;
+  if (red > 0 && (!x.ptr || !y.ptr)) return RLK_ERR_NULL;
+  if (!ptr_aligned(x.ptr, esize(x.dtype)) || !ptr_aligned(y.ptr, esize(y.dtype)) ||
+      !ptr_aligned(C, esize(c_dtype)))
+    return RLK_ERR_ALIGN;
+  if (off > 0 && (!workspace || !ptr_aligned(workspace, 16) || workspace_bytes < off))
+    return RLK_ERR_WORKSPACE;
+  DeviceInfo dev;
+  rlk_status st = device_ready(&dev);
+  if (st != RLK_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (red == 0) {   // empty reduction (dB with M == 0): the product is all zeros
+    const size_t es = esize(c_dtype);
+    if (cudaMemset2DAsync(C, ldc * es, 0, out_cols * es, out_rows, s) != cudaSuccess) {
+      cudaGetLastError();
+      return RLK_ERR_CUDA;
+    }
+    return RLK_OK;
+  }
+  if (ensure_attrs(dev.device) != cudaSuccess) return RLK_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const void *xp, *yp;
+  if ((st = materialise(x, ws, s, &xp)) != RLK_OK) return st;
+  if ((st = materialise(y, ws, s, &yp)) != RLK_OK) return st;
+
+  // Tensor maps: {contiguous extent, row count}, pitch, box.
+  CUtensorMap ta, tb;
+  bool ok = false;
+  switch (kind) {
+    case Kind::kFwd:   // A [M,K] K-major; B [K,N] MN-major
+      ok = encode_bf16_2d(&ta, xp, x.cols, x.rows, x.eff_ld, kBK, kBM) &&
+           encode_bf16_2d(&tb, yp, y.cols, y.rows, y.eff_ld, 64, kBK);
+      break;
+    case Kind::kDa:    // dC [M,N] K-major; B [K,N] K-major (N reduced)
+      ok = encode_bf16_2d(&ta, xp, x.cols, x.rows, x.eff_ld, kBK, kBM) &&
+           encode_bf16_2d(&tb, yp, y.cols, y.rows, y.eff_ld, kBK, kBN);
+      break;
+    case Kind::kDb:    // A [M,K] MN-major; dC [M,N] MN-major (M reduced)
+      ok = encode_bf16_2d(&ta, xp, x.cols, x.rows, x.eff_ld, 64, kBK) &&
+           encode_bf16_2d(&tb, yp, y.cols, y.rows, y.eff_ld, 64, kBK);
+      break;
+  }
+  if (!ok) return RLK_ERR_CUDA;
+
+  GemmSched sc;
+  sc.num_mb = (int)num_mb;
+  sc.num_nb = (int)num_nb;
+  sc.nkb = (int)ceil_div(red, kBK);
+  GemmOut o;
+  o.M = (int)out_rows;
+  o.N = (int)out_cols;
+  o.C = C;
+  o.ldc = ldc;
+  o.fp32 = c_dtype == RLK_FP32;
+  o.vec_ok = ptr_aligned(C, 16) && ((ldc * esize(c_dtype)) % 16) == 0;
+  const int64_t units = num_mb * num_nb;
+  const int grid = (int)(units < dev.sm_count ? units : dev.sm_count);
+  switch (kind) {
+    case Kind::kFwd: det_gemm_kernel<false, true><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, sc, o); break;
+    case Kind::kDa: det_gemm_kernel<false, false><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, sc, o); break;
+    case Kind::kDb: det_gemm_kernel<true, true><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, sc, o); break;
+  }
+  return cudaGetLastError() == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
+}
+
+}  // namespace
+
+uint32_t take_error_det_gemm() {
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err_det_gemm, sizeof v) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaMemcpyToSymbol(g_err_det_gemm, &zero, sizeof zero);
+  cudaGetLastError();
+  return v;
+}
+
+}  // namespace rlk
+
+using namespace rlk;
+
+extern "C" {
+
+size_t rlk_det_gemm_workspace_size(int op, const void* x, int x_dtype, int64_t x_rows,
+                                   int64_t x_cols, int64_t ldx, const void* y, int y_dtype,
+                                   int64_t y_rows, int64_t y_cols, int64_t ldy) {
+  Operand a{x, x_dtype, x_rows, x_cols, ldx};
+  Operand b{y, y_dtype, y_rows, y_cols, ldy};
+  const bool fp32_x = op == RLK_GEMM_DA, fp32_y = op == RLK_GEMM_DB;
+  if (op < RLK_GEMM_FWD || op > RLK_GEMM_DB) return 0;
+  if (check_operand(a, fp32_x) != RLK_OK || check_operand(b, fp32_y) != RLK_OK) return 0;
+  size_t off = 0;
+  plan_operand(a, off);
+  plan_operand(b, off);
+  return off;
+}
+
+rlk_status rlk_det_gemm_fwd(const void* A, int64_t M, int64_t K, int64_t lda, const void* B,
+                            int64_t N, int64_t ldb, void* C, int c_dtype, int64_t ldc,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  Operand a{A, RLK_BF16, M, K, lda};
+  Operand b{B, RLK_BF16, K, N, ldb};
+  rlk_status st;
+  if ((st = check_operand(a, false)) != RLK_OK || (st = check_operand(b, false)) != RLK_OK) return st;
+  if (K < 1) return RLK_ERR_SHAPE;
+  return run_gemm(Kind::kFwd, a, b, M, N, K, C, c_dtype, ldc, workspace, workspace_bytes, stream);
+}
+
+rlk_status rlk_det_gemm_da(const void* dC, int dc_dtype, int64_t M, int64_t N, int64_t lddc,
+                           const void* B, int64_t K, int64_t ldb, void* dA, int out_dtype,
+                           int64_t ldda, void* workspace, size_t workspace_bytes, void* stream) {
+  Operand a{dC, dc_dtype, M, N, lddc};
+  Operand b{B, RLK_BF16, K, N, ldb};
+  rlk_status st;
+  if ((st = check_operand(a, true)) != RLK_OK || (st = check_operand(b, false)) != RLK_OK) return st;
+  if (K < 1) return RLK_ERR_SHAPE;
+  return run_gemm(Kind::kDa, a, b, M, K, N, dA, out_dtype, ldda, workspace, workspace_bytes,
+                  stream);
+}
+
+rlk_status rlk_det_gemm_db(const void* A, int64_t M, int64_t K, int64_t lda, const void* dC,
+                           int dc_dtype, int64_t N, int64_t lddc, void* dB, int out_dtype,
+                           int64_t lddb, void* workspace, size_t workspace_bytes, void* stream) {
+  Operand a{A, RLK_BF16, M, K, lda};
+  Operand b{dC, dc_dtype, M, N, lddc};
+  rlk_status st;
+  if ((st = check_operand(a, false)) != RLK_OK || (st = check_operand(b, true)) != RLK_OK) return st;
+  return run_gemm(Kind::kDb, a, b, K, N, M, dB, out_dtype, lddb, workspace, workspace_bytes,
+                  stream);
+}
+
+}  // extern "C"

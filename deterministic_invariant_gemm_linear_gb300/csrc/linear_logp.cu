@@ -1,0 +1,428 @@
+// Fused linear log-probability on sm_103a.
+//
+// Operator ("feat(linear-logp): add batch-invariant fused SM90 operator",
+// Walkthrough and PR body): for each row r, z[r, v] = hidden[r] . W[v] (+ bias[v]);
+// lse[r] = log sum_v exp z[r, v]; logp[r] = z[r, target[r]] - lse[r]; the [N, V]
+// logits are never written to memory.
+//
+// Stage 1 (linear_logp_partials_kernel): the tcgen05 main loop computes 128 x 256
+// FP32 logit tiles in TMEM; the epilogue keeps, per row and per vocabulary split,
+// an online maximum m and sum of exponentials s over the split's tiles in
+// ascending vocabulary order, and captures the target logit.  Work unit =
+// (vocabulary split j, 128-row block); units are ordered split-major so that
+// the CTAs running at the same time share W tiles through L2.
+//
+// Stage 2 (linear_logp_combine_kernel): one warp per row merges the row's S
+// partials in a fixed order (lane l takes splits l, l+32, ... ascending, then a
+// fixed xor butterfly) and writes lse and logp.
+//
+// The split (S, tiles per split) comes from V alone (the page's author notes:
+// V -> split count -> contiguous ranges -> ordered merge; N, the row block and
+// the SM count never enter), so each row's arithmetic is the same whatever N,
+// its position and its neighbours are.
+#include <math.h>
+
+#include <mutex>
+
+#include "rlk.h"
+#include "rlk_internal.h"
+#include "rlk_pipeline.cuh"
+
+namespace rlk {
+
+__device__ unsigned int g_err_linear_logp = 0;
+
+namespace {
+
+struct LogpSched {
+  int num_rb;      // 128-row blocks
+  int S;           // vocabulary splits
+  int vps;         // 256-id tiles per split
+  int vtiles;      // 256-id tiles in the vocabulary
+  int nkb;         // 64-wide blocks of H
+  __device__ __forceinline__ int num_units() const { return num_rb * S; }
+  __device__ __forceinline__ int split_of(int u) const { return u / num_rb; }
+  __device__ __forceinline__ int rb_of(int u) const { return u - (u / num_rb) * num_rb; }
+  __device__ __forceinline__ int first_tile(int u) const { return split_of(u) * vps; }
+  __device__ __forceinline__ int unit_tiles(int u) const {
+    const int t0 = first_tile(u);
+    return min(vps, vtiles - t0);
+  }
+  __device__ __forceinline__ void tile_coords(int u, int i, int& a0, int& b0) const {
+    a0 = rb_of(u) * kBM;
+    b0 = (first_tile(u) + i) * kBN;
+  }
+};
+
+struct LogpArgs {
+  int N, V;
+  int64_t tstride;
+  const float* bias;          // [V] or null
+  const int64_t* target;
+  float2* ws_ms;              // [N][S]: (m, s) per row and split
+  float* ws_zt;               // [N]: target logit
+};
+
+// One 32-column chunk of a row: bias, vocabulary-tail mask, target capture and
+// the online (m, s) update.  z values are natural-unit logits; each exponential
+// is 2^((z - m) * log2(e)) with z - m formed first, so the running maximum's own
+// term is exactly 2^0 = 1: s >= 1 always, hence lse >= max logit and logp <= 0
+// hold exactly in FP32.
+__device__ __forceinline__ void logp_chunk(const uint32_t (&r)[32], int vbase, int V,
+                                           const float* bias, int64_t tgt, float& m, float& s,
+                                           bool& have_zt, float& zt) {
+  float z[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) z[i] = __uint_as_float(r[i]);
+  if (bias != nullptr) {
+    if (vbase + 32 <= V) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z[i] = __fadd_rn(z[i], __ldg(bias + vbase + i));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (vbase + i < V) z[i] = __fadd_rn(z[i], __ldg(bias + vbase + i));
+    }
+  }
+  if (vbase + 32 > V) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (vbase + i >= V) z[i] = -INFINITY;
+  }
+  const int64_t d = tgt - vbase;
+  if (d >= 0 && d < 32) {
+    // z[d] through a fixed 5-level select tree (keeps z in registers)
+    const int di = (int)d;
+    float t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) t[i] = (di & 16) ? z[i + 16] : z[i];
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+      for (int i = 0; i < w; ++i) t[i] = (di & w) ? t[i + w] : t[i];
+    zt = t[0];
+    have_zt = true;
+  }
+  // chunk maximum (fixed pairwise tree)
+  float t[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) t[i] = fmaxf(z[2 * i], z[2 * i + 1]);
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) t[i] = fmaxf(t[i], t[i + w]);
+  const float mn = fmaxf(m, t[0]);            // finite: vbase < V so z[0] is a real logit
+  const float scale = ex2_approx(__fmul_rn(__fsub_rn(m, mn), kLog2e));   // m = -inf -> 0
+  float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    a[i & 3] = __fadd_rn(a[i & 3], ex2_approx(__fmul_rn(__fsub_rn(z[i], mn), kLog2e)));
+  const float cs = __fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3]));
+  s = __fadd_rn(__fmul_rn(s, scale), cs);
+  m = mn;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    linear_logp_partials_kernel(const __grid_constant__ CUtensorMap tm_hidden,
+                                const __grid_constant__ CUtensorMap tm_weight, LogpSched sc,
+                                LogpArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  const PipeSmem ps = pipe_smem(smem_raw);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tm_hidden);
+    tma_prefetch_desc(&tm_weight);
+  }
+  const uint32_t tmem = pipe_setup(ps);
+  using TA = OperandTile<false, kBM>;
+  using TB = OperandTile<false, kBN>;
+
+  if (warp == 0) {
+    if (lane == 0) producer_role<TA, TB>(&tm_hidden, &tm_weight, sc, ps, &g_err_linear_logp);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0)
+      mma_role<TA, TB>(sc, ps, tmem, idesc_bf16_f32(kBM, kBN, false, false), &g_err_linear_logp);
+    __syncwarp();
+  } else {
+    // Epilogue: warp w reads TMEM lanes 32*(w%4) .. +31, i.e. tile rows q*32 + lane.
+    const int q = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool run = true;
+    const int units = sc.num_units();
+    for (int u = blockIdx.x; run && u < units; u += gridDim.x) {
+      const int j = sc.split_of(u);
+      const int row = sc.rb_of(u) * kBM + q * 32 + lane;
+      const bool valid = row < args.N;
+      const int64_t tgt = valid ? __ldg(args.target + (int64_t)row * args.tstride) : -1;
+      float m = -INFINITY, s = 0.f, zt = 0.f;
+      bool have_zt = false;
+      const int t0 = sc.first_tile(u), nt = sc.unit_tiles(u);
+      for (int i = 0; i < nt; ++i) {
+        if (!epilogue_acquire(ps, acc, acc_phase, &g_err_linear_logp)) {
+          run = false;
+          break;
+        }
+        const int v0 = (t0 + i) * kBN;
+        const uint32_t taddr = tmem + acc * kAccCols + lane_off;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          const int vbase = v0 + c * 32;
+          if (vbase >= args.V) break;          // uniform: depends on the tile only
+          uint32_t r[32];
+          tmem_ld32(taddr + c * 32, r);
+          tmem_wait_ld();
+          logp_chunk(r, vbase, args.V, args.bias, tgt, m, s, have_zt, zt);
+        }
+        epilogue_release(ps, acc);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (!run) break;
+      if (valid) {
+        args.ws_ms[(int64_t)row * sc.S + j] = make_float2(m, s);
+        if (have_zt) args.ws_zt[row] = zt;
+      }
+    }
+  }
+  pipe_teardown(tmem);
+}
+
+// (m, s) pair merge with explicit roundings, so merge(a, b) == merge(b, a) bitwise.
+__device__ __forceinline__ void merge_ms(float& M, float& s, float m2, float s2) {
+  if (m2 == -INFINITY) return;
+  if (M == -INFINITY) {
+    M = m2;
+    s = s2;
+    return;
+  }
+  const float Mn = fmaxf(M, m2);
+  const float e1 = ex2_approx(__fmul_rn(__fsub_rn(M, Mn), kLog2e));
+  const float e2 = ex2_approx(__fmul_rn(__fsub_rn(m2, Mn), kLog2e));
+  s = __fadd_rn(__fmul_rn(s, e1), __fmul_rn(s2, e2));
+  M = Mn;
+}
+
+__global__ void __launch_bounds__(256)
+    linear_logp_combine_kernel(const float2* __restrict__ ws_ms, const float* __restrict__ ws_zt,
+                               const int64_t* __restrict__ target, int64_t tstride, int N, int S,
+                               int V, float* __restrict__ logp, float* __restrict__ lse,
+                               float* __restrict__ zt_out) {
+  const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  if (row >= N) return;
+  const float2* p = ws_ms + (int64_t)row * S;
+  float M = -INFINITY, s = 0.f;
+  for (int j = lane; j < S; j += 32) {
+    const float2 v = p[j];
+    merge_ms(M, s, v.x, v.y);
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, M, off);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+    merge_ms(M, s, m2, s2);
+  }
+  if (lane == 0) {
+    const float L = __fadd_rn(M, logf(s));
+    const int64_t t = __ldg(target + (int64_t)row * tstride);
+    const float z = (t >= 0 && t < V) ? ws_zt[row] : __int_as_float(0x7fc00000);
+    lse[row] = L;
+    logp[row] = __fsub_rn(z, L);
+    if (zt_out) zt_out[row] = z;
+  }
+}
+
+std::mutex g_attr_mutex;
+bool g_attr_set[64];
+
+cudaError_t ensure_attrs(int dev) {
+  std::lock_guard<std::mutex> lock(g_attr_mutex);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!g_attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(linear_logp_partials_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    g_attr_set[dev] = true;
+  }
+  return cudaSuccess;
+}
+
+// Workspace plan: [partials N*S float2][target logits N float][staged hidden][staged W].
+struct LogpPlan {
+  int64_t S = 0, vps = 0, vtiles = 0;
+  bool stage_h = false, stage_w = false;
+  int64_t ldh = 0, ldw = 0;        // pitches the kernel reads
+  size_t off_zt = 0, off_h = 0, off_w = 0, total = 0;
+};
+
+rlk_status check_shapes(int64_t N, int64_t H, int64_t ldh, int64_t V, int64_t ldw) {
+  if (N < 0 || N >= (int64_t(1) << 31)) return RLK_ERR_SHAPE;
+  if (H < 1 || H >= (int64_t(1) << 20)) return RLK_ERR_SHAPE;
+  if (V < 1 || V >= (int64_t(1) << 31)) return RLK_ERR_SHAPE;
+  if (ldh < H || ldw < H) return RLK_ERR_SHAPE;
+  if (ldh >= (int64_t(1) << 36) || ldw >= (int64_t(1) << 36)) return RLK_ERR_SHAPE;
+  return RLK_OK;
+}
+
+rlk_status plan(const void* hidden, int64_t N, int64_t H, int64_t ldh, const void* weight,
+                int64_t V, int64_t ldw, LogpPlan* p) {
+  rlk_status st = check_shapes(N, H, ldh, V, ldw);
+  if (st != RLK_OK) return st;
+  st = rlk_vocab_split_policy(V, &p->S, &p->vps, &p->vtiles);
+  if (st != RLK_OK) return st;
+  p->stage_h = !tma_ready(hidden, ldh);
+  p->stage_w = !tma_ready(weight, ldw);
+  p->ldh = p->stage_h ? staged_ld(H) : ldh;
+  p->ldw = p->stage_w ? staged_ld(H) : ldw;
+  size_t off = align_up((size_t)N * p->S * sizeof(float2), 256);
+  p->off_zt = off;
+  off = align_up(off + (size_t)N * sizeof(float), 256);
+  p->off_h = off;
+  if (p->stage_h) off = align_up(off + (size_t)N * p->ldh * 2, 256);
+  p->off_w = off;
+  if (p->stage_w) off = align_up(off + (size_t)V * p->ldw * 2, 256);
+  p->total = off;
+  return RLK_OK;
+}
+
+}  // namespace
+
+uint32_t take_error_linear_logp() {
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err_linear_logp, sizeof v) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaMemcpyToSymbol(g_err_linear_logp, &zero, sizeof zero);
+  cudaGetLastError();
+  return v;
+}
+
+}  // namespace rlk
+
+using namespace rlk;
+
+extern "C" {
+
+size_t rlk_linear_logp_workspace_size(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
+                                      const void* weight, int64_t V, int64_t ld_weight) {
+  LogpPlan p;
+  if (plan(hidden, N, H, ld_hidden, weight, V, ld_weight, &p) != RLK_OK) return 0;
+  return p.total;
+}
+
+rlk_status rlk_linear_logp_partials(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
+                                    const void* weight, int64_t V, int64_t ld_weight,
+                                    const float* bias, const int64_t* target,
+                                    int64_t target_stride, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  LogpPlan p;
+  rlk_status st = plan(hidden, N, H, ld_hidden, weight, V, ld_weight, &p);
+  if (st != RLK_OK) return st;
+  if (target_stride < 0) return RLK_ERR_SHAPE;
+  if (N == 0) return RLK_OK;
+  if (!hidden || !weight || !target) return RLK_ERR_NULL;
+  if (!workspace) return RLK_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(hidden) & 1u) || (reinterpret_cast<uintptr_t>(weight) & 1u) ||
+      (reinterpret_cast<uintptr_t>(target) & 7u) || (reinterpret_cast<uintptr_t>(bias) & 3u))
+    return RLK_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 15u) || workspace_bytes < p.total)
+    return RLK_ERR_WORKSPACE;
+  DeviceInfo dev;
+  st = device_ready(&dev);
+  if (st != RLK_OK) return st;
+  if (ensure_attrs(dev.device) != cudaSuccess) return RLK_ERR_CUDA;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const void* h_src = hidden;
+  const void* w_src = weight;
+  if (p.stage_h) {
+    if (launch_stage_bf16(static_cast<const uint16_t*>(hidden), N, H, ld_hidden,
+                          reinterpret_cast<uint16_t*>(ws + p.off_h), p.ldh, s) != cudaSuccess)
+      return RLK_ERR_CUDA;
+    h_src = ws + p.off_h;
+  }
+  if (p.stage_w) {
+    if (launch_stage_bf16(static_cast<const uint16_t*>(weight), V, H, ld_weight,
+                          reinterpret_cast<uint16_t*>(ws + p.off_w), p.ldw, s) != cudaSuccess)
+      return RLK_ERR_CUDA;
+    w_src = ws + p.off_w;
+  }
+  CUtensorMap tm_h, tm_w;
+  if (!encode_bf16_2d(&tm_h, h_src, H, N, p.ldh, kBK, kBM) ||
+      !encode_bf16_2d(&tm_w, w_src, H, V, p.ldw, kBK, kBN))
+    return RLK_ERR_CUDA;
+
+  LogpSched sc;
+  sc.num_rb = (int)ceil_div(N, kBM);
+  sc.S = (int)p.S;
+  sc.vps = (int)p.vps;
+  sc.vtiles = (int)p.vtiles;
+  sc.nkb = (int)ceil_div(H, kBK);
+  LogpArgs a;
+  a.N = (int)N;
+  a.V = (int)V;
+  a.tstride = target_stride;
+  a.bias = bias;
+  a.target = target;
+  a.ws_ms = reinterpret_cast<float2*>(ws);
+  a.ws_zt = reinterpret_cast<float*>(ws + p.off_zt);
+  const int64_t units = (int64_t)sc.num_rb * sc.S;
+  const int grid = (int)(units < dev.sm_count ? units : dev.sm_count);
+  linear_logp_partials_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_h, tm_w, sc, a);
+  return cudaGetLastError() == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
+}
+
+rlk_status rlk_linear_logp_combine(int64_t N, int64_t V, const int64_t* target,
+                                   int64_t target_stride, float* logp, float* lse,
+                                   float* target_logit, const void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  if (N < 0 || N >= (int64_t(1) << 31) || V < 1 || V >= (int64_t(1) << 31) || target_stride < 0)
+    return RLK_ERR_SHAPE;
+  if (N == 0) return RLK_OK;
+  if (!target || !logp || !lse) return RLK_ERR_NULL;
+  if (!workspace) return RLK_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(target) & 7u) || (reinterpret_cast<uintptr_t>(logp) & 3u) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(target_logit) & 3u))
+    return RLK_ERR_ALIGN;
+  int64_t S, vps, vt;
+  rlk_vocab_split_policy(V, &S, &vps, &vt);
+  const size_t off_zt = align_up((size_t)N * S * sizeof(float2), 256);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 15u) ||
+      workspace_bytes < off_zt + (size_t)N * sizeof(float))
+    return RLK_ERR_WORKSPACE;
+  DeviceInfo dev;
+  rlk_status st = device_ready(&dev);
+  if (st != RLK_OK) return st;
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  const int rows_per_block = 256 / 32;
+  const int grid = (int)ceil_div(N, rows_per_block);
+  linear_logp_combine_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const float2*>(ws), reinterpret_cast<const float*>(ws + off_zt), target,
+      target_stride, (int)N, (int)S, (int)V, logp, lse, target_logit);
+  return cudaGetLastError() == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
+}
+
+rlk_status rlk_linear_logp(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
+                           const void* weight, int64_t V, int64_t ld_weight, const float* bias,
+                           const int64_t* target, int64_t target_stride, float* logp, float* lse,
+                           float* target_logit, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  // Validate everything the second stage needs before the first one launches.
+  if (N > 0 && (!logp || !lse)) return RLK_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(logp) & 3u) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(target_logit) & 3u))
+    return RLK_ERR_ALIGN;
+  rlk_status st = rlk_linear_logp_partials(hidden, N, H, ld_hidden, weight, V, ld_weight, bias,
+                                           target, target_stride, workspace, workspace_bytes,
+                                           stream);
+  if (st != RLK_OK) return st;
+  return rlk_linear_logp_combine(N, V, target, target_stride, logp, lse, target_logit, workspace,
+                                 workspace_bytes, stream);
+}
+
+}  // extern "C"

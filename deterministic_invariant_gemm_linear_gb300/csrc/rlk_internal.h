@@ -1,0 +1,56 @@
+// Host-side helpers shared by the rlk translation units (not part of the ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "rlk.h"
+
+namespace rlk {
+
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+};
+
+// Checks that a CUDA device is current and is sm_103 (cached per device).
+rlk_status device_ready(DeviceInfo* info);
+
+// 2-D BF16 tensor map with 128-byte swizzle; zero fill outside the tensor.
+// inner = contiguous extent (elements), outer = row count, ld = row pitch
+// (elements).  Returns false when the driver rejects the description.
+bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                    uint64_t ld, uint32_t box_inner, uint32_t box_outer);
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// A BF16 operand can be read by TMA in place when its base is 16-byte aligned
+// and its row pitch is a multiple of 16 bytes.
+inline bool tma_ready(const void* p, int64_t ld) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0 && (ld % 8) == 0;
+}
+// Padded pitch of a staged copy: the column count rounded up to 8 elements.
+inline int64_t staged_ld(int64_t cols) { return ceil_div(cols, 8) * 8; }
+
+// Copies rows x cols BF16 from src (pitch ld_src) to dst (pitch ld_dst),
+// writing zeros into columns [cols, ld_dst).
+cudaError_t launch_stage_bf16(const uint16_t* src, int64_t rows, int64_t cols, int64_t ld_src,
+                              uint16_t* dst, int64_t ld_dst, cudaStream_t stream);
+
+// Rounds rows x cols FP32 to BF16 (nearest even) into dst (pitch ld_dst),
+// zero-filling columns [cols, ld_dst).
+cudaError_t launch_cast_f32_bf16(const float* src, int64_t rows, int64_t cols, int64_t ld_src,
+                                 uint16_t* dst, int64_t ld_dst, cudaStream_t stream);
+
+// Vocabulary split policy (function of V only).
+constexpr int64_t kVocabTile = 256;
+constexpr int64_t kMaxVocabSplits = 1024;
+
+// Per-translation-unit device error words: read-and-clear after a stream sync.
+uint32_t take_error_linear_logp();
+uint32_t take_error_det_gemm();
+
+}  // namespace rlk

@@ -1,0 +1,261 @@
+/*
+ * rlk — deterministic, batch-invariant BF16 contractions on GB300 (sm_103a).
+ *
+ * A C ABI over hand-written tcgen05 / TMEM / TMA kernels.  Every entry point
+ * takes plain pointers, sizes and leading dimensions; no framework types cross
+ * this boundary.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Memory.  Every operand, output and workspace pointer is DEVICE memory on
+ *    the current CUDA device, owned by the caller.  The library allocates no
+ *    device memory and keeps no per-call state; its only device-resident state
+ *    is a small error word (see rlk_get_device_error).
+ *  - Layout.  Matrices are row-major with an explicit leading dimension ld (in
+ *    elements, ld >= number of columns).  BF16 is passed as its 16-bit pattern.
+ *  - Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *    default stream).  Work is enqueued asynchronously; outputs are valid once
+ *    the stream reaches that point.
+ *  - Errors.  Arguments are validated on the host before anything is launched;
+ *    on any error nothing is launched and no output is touched.  A launch that
+ *    the CUDA runtime rejects returns RLK_ERR_CUDA.  A zero-row call (N == 0 in
+ *    rlk_linear_logp, M == 0 in rlk_det_gemm_fwd / _da) is a no-op that
+ *    returns RLK_OK.
+ *  - Determinism.  For fixed inputs every output bit is identical run to run,
+ *    across streams, across leading dimensions and pointer alignment, and across
+ *    the number of rows in the call (row chunking).  Tile shapes, the K
+ *    reduction order and the vocabulary split depend only on the reduction and
+ *    vocabulary extents, never on the row count, the GPU's SM count or the
+ *    operands' alignment.  rlk_numerics_version() changes whenever any of
+ *    those choices change output bits.
+ *  - Alignment.  An operand whose base address is not 16-byte aligned, or
+ *    whose leading dimension is not a multiple of 8 elements, is first copied
+ *    into the workspace with a padded leading dimension (bit-identical result;
+ *    the padding is zeros, which add exactly nothing).  The *_workspace_size
+ *    functions account for that copy.
+ *
+ * Sources (web pages of the RL-Kernel project):
+ *  [P3] "feat(linear-logp): add batch-invariant fused SM90 operator":
+ *       Walkthrough (operator: hidden, lm-head weight, target ids, optional
+ *       bias -> log-probability and log-sum-exp, never materialising the
+ *       [N, V] logits), author notes (the vocabulary split is chosen from V
+ *       only: V -> split count -> contiguous ranges -> ordered merge; backward
+ *       is outside the contract and fails closed), PR body (online-softmax
+ *       partials per split and an ordered combine).
+ *  [P1] "feat(musa): add native deterministic gemm kernel": Summary (fixed
+ *       ascending K-order reduction with FP32 accumulation; forward,
+ *       dA = dC B^T, dB = A^T dC; FP32-output forward variant), review comment
+ *       (an FP32-output forward's grad_output is cast to BF16 before dA / dB).
+ *  [P2] "Support musa": review comment (det_gemm must never fall back to a
+ *       non-deterministic matmul; it fails explicitly instead).
+ */
+#ifndef RLK_H
+#define RLK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define RLK_API __attribute__((visibility("default")))
+#else
+#define RLK_API
+#endif
+
+#define RLK_NUMERICS_VERSION 1
+
+typedef enum rlk_status {
+    RLK_OK = 0,
+    RLK_ERR_NULL = 1,               /* a required pointer is NULL                       */
+    RLK_ERR_SHAPE = 2,              /* a size or leading dimension is out of range      */
+    RLK_ERR_DTYPE = 3,              /* an rlk_dtype argument is not a supported value   */
+    RLK_ERR_ALIGN = 4,              /* a pointer is not aligned to its element size     */
+    RLK_ERR_WORKSPACE = 5,          /* workspace NULL or smaller than required          */
+    RLK_ERR_UNSUPPORTED_DEVICE = 6, /* no CUDA device, or the device is not sm_103      */
+    RLK_ERR_CUDA = 7,               /* the CUDA runtime rejected a launch or query      */
+    RLK_ERR_TIMEOUT = 8             /* a kernel's bounded wait expired (device error)   */
+} rlk_status;
+
+typedef enum rlk_dtype {
+    RLK_BF16 = 0,                   /* bfloat16, 2 bytes                                */
+    RLK_FP32 = 1                    /* IEEE binary32, 4 bytes                           */
+} rlk_dtype;
+
+/* Device error-word bits reported by rlk_get_device_error. */
+#define RLK_DEVERR_TIMEOUT 0x1u     /* an mbarrier wait gave up after its time limit   */
+
+/* Human-readable name of a status code (static storage, never NULL). */
+RLK_API const char* rlk_status_string(int status);
+
+/* Bumped whenever a tile shape, reduction order or split policy change would
+ * change output bits.  Equal versions => bit-identical outputs. */
+RLK_API int rlk_numerics_version(void);
+
+/* RLK_OK when the current CUDA device is sm_103 and usable, else the reason. */
+RLK_API rlk_status rlk_device_check(void);
+
+/*
+ * Reads and clears the device error word after synchronising `stream`.
+ * *flags receives the OR of RLK_DEVERR_* bits raised by kernels since the last
+ * call (0 when nothing went wrong).  Returns RLK_ERR_TIMEOUT when a bit was set.
+ */
+RLK_API rlk_status rlk_get_device_error(void* stream, uint32_t* flags);
+
+/* ===================================================================== *
+ *  Fused linear log-probability                                  [P3]  *
+ * ===================================================================== */
+
+/*
+ * The vocabulary split used by rlk_linear_logp, a function of V alone [P3
+ * author notes].  The vocabulary is cut into vtiles = ceil(V / 256) tiles of
+ * 256 ids; tiles are grouped into S contiguous, non-empty splits of
+ * vtiles_per_split tiles (the last split may be shorter), with S no larger
+ * than 1024:
+ *     vtiles_per_split = ceil(vtiles / 1024),  S = ceil(vtiles / vtiles_per_split).
+ * Split j covers vocabulary ids [j * vps * 256, min((j + 1) * vps * 256, V)).
+ * Host-only; needs no device.  Returns RLK_ERR_SHAPE for V < 1 or V >= 2^31.
+ */
+RLK_API rlk_status rlk_vocab_split_policy(int64_t V, int64_t* num_splits, int64_t* vtiles_per_split,
+                                  int64_t* num_vtiles);
+
+/*
+ * Workspace bytes that rlk_linear_logp needs for exactly these operands:
+ * N * S * 8 bytes of per-(row, split) online-softmax partials, N * 4 bytes for
+ * the gathered target logits, plus a padded copy of hidden and/or weight when
+ * that operand is misaligned (see "Alignment").  Each region starts on a
+ * 256-byte boundary.  Returns 0 for invalid arguments.
+ */
+RLK_API size_t rlk_linear_logp_workspace_size(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
+                                      const void* weight, int64_t V, int64_t ld_weight);
+
+/*
+ * logp[r] = z[r, target[r]] - lse[r],   lse[r] = log sum_v exp(z[r, v]),
+ * z[r, v] = sum_h hidden[r, h] * weight[v, h] (+ bias[v])          [P3 Walkthrough]
+ *
+ *  hidden        BF16 [N, H], leading dimension ld_hidden (>= H)
+ *  weight        BF16 [V, H] (the lm-head weight), leading dimension ld_weight (>= H)
+ *  bias          FP32 [V] or NULL; added in FP32 after the full H reduction
+ *  target        int64, row r reads target[r * target_stride]; stride 0 means one
+ *                id shared by every row (an expanded target)
+ *  logp, lse     FP32 [N] outputs
+ *  target_logit  FP32 [N] output or NULL: the logit z[r, target[r]] exactly as it
+ *                entered the log-sum-exp
+ *  workspace     >= rlk_linear_logp_workspace_size(...) bytes, 16-byte aligned
+ *
+ * Shapes: 0 <= N < 2^31, 1 <= H < 2^20, 1 <= V < 2^31.  A target outside
+ * [0, V) yields logp = NaN (and target_logit = NaN) for that row; lse is
+ * still valid; nothing is read out of bounds.
+ *
+ * Arithmetic (fixed; depends on V and H only): FP32 accumulation over H in
+ * ascending blocks of 64 (tensor cores, 16 per instruction); per 256-id tile
+ * and per row an online max / sum-of-exponentials in ascending vocabulary
+ * order; S = rlk_vocab_split_policy(V) partials per row merged in a fixed
+ * order (lane j%32 ascending, then a fixed xor-butterfly).  Each row's bits
+ * are therefore independent of N, of the row's position and of its
+ * neighbours.  Equivalent to rlk_linear_logp_partials followed by
+ * rlk_linear_logp_combine on the same stream.
+ */
+RLK_API rlk_status rlk_linear_logp(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
+                           const void* weight, int64_t V, int64_t ld_weight,
+                           const float* bias, const int64_t* target, int64_t target_stride,
+                           float* logp, float* lse, float* target_logit,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * First stage of rlk_linear_logp: one fused tensor-core kernel (projection
+ * tiles + online-softmax epilogue) that writes the per-(row, split) partials
+ * and the target logits into `workspace`.  Arguments as for rlk_linear_logp.
+ */
+RLK_API rlk_status rlk_linear_logp_partials(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
+                                    const void* weight, int64_t V, int64_t ld_weight,
+                                    const float* bias, const int64_t* target,
+                                    int64_t target_stride, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
+/*
+ * Second stage: merges the S partials of each row in the fixed order and
+ * writes logp, lse and (optionally) target_logit.  `workspace` must hold the
+ * partials written by rlk_linear_logp_partials with the same N, H, V, operand
+ * pointers and leading dimensions (those fix where the partials sit).
+ */
+RLK_API rlk_status rlk_linear_logp_combine(int64_t N, int64_t V, const int64_t* target,
+                                   int64_t target_stride, float* logp, float* lse,
+                                   float* target_logit, const void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
+/* ===================================================================== *
+ *  Deterministic GEMM family                                      [P1]  *
+ * ===================================================================== */
+/*
+ * All three products accumulate in FP32 over the reduction index in ascending
+ * blocks of 64 (16 per tensor-core instruction) with no split of the
+ * reduction, no atomics and no data-dependent order, so every output is
+ * bitwise reproducible.  Output tiles are 128 x 256 whatever the problem size.
+ * Outputs are BF16 (round to nearest even from the FP32 accumulator) or FP32.
+ * A batched operand [b, M, K] is passed flattened as [b * M, K] (a leading
+ * shape is a row count), so fwd and dA are bitwise equal per row whatever the
+ * batching, and dB sums over all b * M rows in ascending order.
+ * Shapes: 0 <= M < 2^31 and 1 <= K, N < 2^31 (M is the row count of A / dC,
+ * K the column count of A and row count of B, N the column count of B / dC).
+ * Leading dimensions >= the column count of their matrix.
+ */
+
+#define RLK_GEMM_FWD 0
+#define RLK_GEMM_DA 1
+#define RLK_GEMM_DB 2
+
+/*
+ * Workspace bytes the given op needs for exactly these inputs: padded copies
+ * of misaligned BF16 operands and, for an FP32 dC, its BF16 rounding.
+ * (x, y) are the op's two inputs in argument order:
+ *   RLK_GEMM_FWD: x = A [M, K] (BF16),       y = B [K, N] (BF16)
+ *   RLK_GEMM_DA:  x = dC [M, N] (x_dtype),   y = B [K, N] (BF16)
+ *   RLK_GEMM_DB:  x = A [M, K] (BF16),       y = dC [M, N] (y_dtype)
+ * Returns 0 when nothing needs staging or the arguments are invalid.
+ */
+RLK_API size_t rlk_det_gemm_workspace_size(int op,
+                                   const void* x, int x_dtype, int64_t x_rows, int64_t x_cols,
+                                   int64_t ldx,
+                                   const void* y, int y_dtype, int64_t y_rows, int64_t y_cols,
+                                   int64_t ldy);
+
+/*
+ * C[M, N] = A[M, K] . B[K, N]                               [P1 Summary: forward]
+ *  A  BF16 [M, K] (ld lda);  B  BF16 [K, N] (ld ldb);  C  c_dtype [M, N] (ld ldc).
+ */
+RLK_API rlk_status rlk_det_gemm_fwd(const void* A, int64_t M, int64_t K, int64_t lda,
+                            const void* B, int64_t N, int64_t ldb,
+                            void* C, int c_dtype, int64_t ldc,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * dA[M, K] = dC[M, N] . B[K, N]^T                                  [P1 Summary: dA]
+ *  dC dc_dtype [M, N] (ld lddc): an FP32 dC (the gradient of an FP32-output
+ *     forward) is rounded to BF16 (nearest even) before the product, as the
+ *     FP32-output backward requires [P1 review comment].
+ *  B  BF16 [K, N] (ld ldb);  dA out_dtype [M, K] (ld ldda).
+ */
+RLK_API rlk_status rlk_det_gemm_da(const void* dC, int dc_dtype, int64_t M, int64_t N, int64_t lddc,
+                           const void* B, int64_t K, int64_t ldb,
+                           void* dA, int out_dtype, int64_t ldda,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * dB[K, N] = A[M, K]^T . dC[M, N]                                  [P1 Summary: dB]
+ *  Reduction over all M rows in ascending order.  dC as for rlk_det_gemm_da.
+ *  A  BF16 [M, K] (ld lda);  dB out_dtype [K, N] (ld lddb).
+ *  M == 0 is a valid empty reduction: dB is written with zeros.
+ */
+RLK_API rlk_status rlk_det_gemm_db(const void* A, int64_t M, int64_t K, int64_t lda,
+                           const void* dC, int dc_dtype, int64_t N, int64_t lddc,
+                           void* dB, int out_dtype, int64_t lddb,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RLK_H */

@@ -1,0 +1,90 @@
+"""Shared helpers for the GPU parity tests: device guard, tolerance checks."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+# Tolerances (stated once, used everywhere):
+LOGP_ATOL = 1e-3          # |delta logp|, |delta lse| against the FP64 oracle
+GEMM_FP32_REL_FRO = 1e-5  # relative Frobenius error of an FP32-output GEMM
+# BF16-output GEMM: within one BF16 ulp of the oracle's exact result rounded to
+# BF16, except where cancellation makes the exact result small against the FP32
+# accumulation error bound (see bf16_within_one_ulp).
+
+
+def cuda_or_skip():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    return torch.device("cuda:0")
+
+
+def dec_bf16(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    """Spacing of BF16 values at |x| (8 significant bits; subnormal spacing 2^-133)."""
+    ax = np.abs(x)
+    e = np.floor(np.log2(np.where(ax > 0, ax, 1.0)))
+    e = np.maximum(e, -126)
+    return np.ldexp(1.0, (e - 7).astype(np.int64))
+
+
+def bf16_within_one_ulp(gpu_bf16: np.ndarray, ref: np.ndarray, ref_rne_bits: np.ndarray,
+                        abs_terms: np.ndarray, K: int):
+    """Elementwise BF16 check.
+
+    gpu_bf16      decoded GPU BF16 outputs
+    ref           exact (FP64) results
+    ref_rne_bits  the oracle's single rounding of ref to BF16
+    abs_terms     sum_k |a_ik b_kj| per element
+    Every element must be within 1 BF16 ulp of RNE(ref).  The FP32 accumulator
+    itself can be off by up to about K * 2^-24 * abs_terms; where that bound
+    exceeds half a BF16 ulp of ref (heavy cancellation) the element is instead
+    checked against |gpu - ref| <= 1 ulp + K * 2^-23 * abs_terms.
+    Returns (n_checked_strict, n_cancelled, worst_ratio); raises on failure.
+    """
+    rne = dec_bf16(ref_rne_bits)
+    acc_bound = K * 2.0 ** -24 * abs_terms
+    ulp = np.maximum(bf16_ulp(rne), bf16_ulp(ref))
+    strict = acc_bound <= 0.5 * bf16_ulp(ref)
+    d_strict = np.abs(gpu_bf16 - rne)
+    ok_strict = d_strict <= ulp
+    loose_tol = ulp + 2 * acc_bound
+    ok_loose = np.abs(gpu_bf16 - ref) <= loose_tol
+    bad = np.where(strict, ~ok_strict, ~ok_loose)
+    if bad.any():
+        i = np.flatnonzero(bad)[:5]
+        raise AssertionError(f"{bad.sum()} BF16 outputs off: gpu={gpu_bf16.flat[i]} ref={ref.flat[i]} "
+                             f"rne={rne.flat[i]} ulp={ulp.flat[i]}")
+    ratio = float(np.max(np.where(strict, d_strict / ulp, np.abs(gpu_bf16 - ref) / loose_tol)))
+    return int(strict.sum()), int((~strict).sum()), ratio
+
+
+def rel_fro(gpu: np.ndarray, ref: np.ndarray) -> float:
+    den = np.linalg.norm(ref)
+    return float(np.linalg.norm(gpu - ref) / (den if den > 0 else 1.0))
+
+
+def sample_rows(N: int, k: int, seed: int = 0, must=()) -> np.ndarray:
+    """Sorted unique rows: the edge rows, the given ones, and k seeded random rows."""
+    rng = np.random.default_rng(seed)
+    base = {0, N - 1, min(127, N - 1), min(128, N - 1), *[m for m in must if 0 <= m < N]}
+    extra = rng.choice(N, size=min(k, N), replace=False) if N > 0 else []
+    return np.array(sorted(base.union(int(x) for x in extra)), dtype=np.int64)
+
+
+def assert_logp_close(logp, lse, ref_logp, ref_lse, what=""):
+    lp = np.asarray(logp, np.float64)
+    ls = np.asarray(lse, np.float64)
+    dl = np.abs(lp - ref_logp)
+    ds = np.abs(ls - ref_lse)
+    assert np.all(np.isfinite(lp)) and np.all(np.isfinite(ls)), what
+    assert dl.max() <= LOGP_ATOL, f"{what}: max |dlogp| = {dl.max()}"
+    assert ds.max() <= LOGP_ATOL, f"{what}: max |dlse| = {ds.max()}"
+    return float(dl.max()), float(ds.max())
+
+
+def ln(x):
+    return math.log(x)

@@ -1,0 +1,186 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports every
+symbol include/rlk.h declares, validates arguments before touching a device,
+and its integer vocabulary-split policy depends on V only."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import deterministic_invariant_gemm_linear_gb300 as rlk
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rlk.h")
+
+# Fake, never-dereferenced addresses: every call below fails validation first.
+P16 = ctypes.c_void_p(0x10000)
+NULL = None
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from deterministic_invariant_gemm_linear_gb300 import build as b
+    b.build()
+    return rlk.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"RLK_API\s+[^;(]*?\b(rlk_\w+)\s*\(", text)))
+
+
+def test_header_symbols_exported(lib):
+    names = declared_symbols()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(rlk.SIGNATURES), "binding signatures must mirror the header"
+
+
+def test_status_strings_and_version(lib):
+    for code, name in rlk.STATUS_NAMES.items():
+        assert rlk.status_string(code).startswith(name)
+    assert rlk.status_string(99) == "RLK_ERR_UNKNOWN"
+    m = re.search(r"#define RLK_NUMERICS_VERSION (\d+)", open(HEADER).read())
+    assert rlk.numerics_version() == int(m.group(1))
+
+
+@pytest.mark.parametrize("V", [1, 2, 255, 256, 257, 1024, 32003, 151936, 152064, 262144, 262145,
+                               1 << 20, (1 << 31) - 1])
+def test_vocab_split_policy(lib, V):
+    S, vps, vt = rlk.vocab_split_policy(V)
+    assert vt == -(-V // 256)
+    assert 1 <= S <= 1024
+    assert vps == -(-vt // 1024)
+    # S contiguous, non-empty ranges covering every tile exactly once
+    covered = 0
+    for j in range(S):
+        t0, t1 = j * vps, min((j + 1) * vps, vt)
+        assert t1 > t0
+        covered += t1 - t0
+        assert j * vps * 256 < V                # each split holds at least one real id
+    assert covered == vt
+
+
+def test_vocab_split_policy_known_values(lib):
+    # the configurations' vocabularies: one 256-id tile per split up to 1024 tiles
+    assert rlk.vocab_split_policy(151936) == (594, 1, 594)
+    assert rlk.vocab_split_policy(152064) == (594, 1, 594)
+    assert rlk.vocab_split_policy(32003) == (126, 1, 126)
+    assert rlk.vocab_split_policy(1024) == (4, 1, 4)
+    assert rlk.vocab_split_policy(262145) == (513, 2, 1025)
+
+
+def test_vocab_split_policy_rejects(lib):
+    s = ctypes.c_int64()
+    for V in (0, -5, 1 << 31):
+        assert lib.rlk_vocab_split_policy(V, ctypes.byref(s), ctypes.byref(s), ctypes.byref(s)) == 2
+    assert lib.rlk_vocab_split_policy(10, None, ctypes.byref(s), ctypes.byref(s)) == 1
+
+
+def test_linear_logp_workspace_size(lib):
+    f = lib.rlk_linear_logp_workspace_size
+    # aligned operands: partials N*S*8 (256-aligned) + target logits N*4 (256-aligned)
+    N, H, V = 4096, 4096, 151936
+    S = 594
+    want = -(-N * S * 8 // 256) * 256 + -(-N * 4 // 256) * 256
+    assert f(P16, N, H, H, P16, V, H) == want
+    # odd pitch of hidden: a padded copy N x 8*ceil(H/8) bf16 is added
+    base = f(P16, 10, 100, 104, P16, 300, 104)
+    staged = f(P16, 10, 100, 101, P16, 300, 104)
+    assert staged - base == -(-(10 * 104 * 2) // 256) * 256
+    # misaligned base of weight: a padded copy of W
+    mis = f(ctypes.c_void_p(0x10002), 10, 100, 104, P16, 300, 104)
+    assert mis - base == -(-(10 * 104 * 2) // 256) * 256
+    # invalid shapes -> 0
+    assert f(P16, 10, 0, 1, P16, 10, 1) == 0
+    assert f(P16, 10, 8, 4, P16, 10, 8) == 0
+    assert f(P16, 10, 8, 8, P16, 0, 8) == 0
+    # N = 0 is valid and needs no partials
+    assert f(P16, 0, 8, 8, P16, 10, 8) == 0
+
+
+def test_linear_logp_validation(lib):
+    f = lib.rlk_linear_logp
+    ws = ctypes.c_void_p(0x20000)
+    # shape errors come first
+    assert f(P16, 4, 0, 8, P16, 10, 8, NULL, P16, 1, P16, P16, NULL, ws, 1 << 20, NULL) == 2
+    assert f(P16, 4, 8, 8, P16, 0, 8, NULL, P16, 1, P16, P16, NULL, ws, 1 << 20, NULL) == 2
+    assert f(P16, 4, 8, 8, P16, 10, 8, NULL, P16, -1, P16, P16, NULL, ws, 1 << 20, NULL) == 2
+    # missing pointers
+    assert f(NULL, 4, 8, 8, P16, 10, 8, NULL, P16, 1, P16, P16, NULL, ws, 1 << 20, NULL) == 1
+    assert f(P16, 4, 8, 8, P16, 10, 8, NULL, NULL, 1, P16, P16, NULL, ws, 1 << 20, NULL) == 1
+    assert f(P16, 4, 8, 8, P16, 10, 8, NULL, P16, 1, NULL, P16, NULL, ws, 1 << 20, NULL) == 1
+    # misaligned target / bias
+    assert f(P16, 4, 8, 8, P16, 10, 8, NULL, ctypes.c_void_p(0x10004), 1, P16, P16, NULL, ws,
+             1 << 20, NULL) == 4
+    assert f(P16, 4, 8, 8, P16, 10, 8, ctypes.c_void_p(0x10002), P16, 1, P16, P16, NULL, ws,
+             1 << 20, NULL) == 4
+    # workspace missing or too small
+    assert f(P16, 4, 8, 8, P16, 10, 8, NULL, P16, 1, P16, P16, NULL, NULL, 1 << 20, NULL) == 5
+    assert f(P16, 4, 8, 8, P16, 10, 8, NULL, P16, 1, P16, P16, NULL, ws, 16, NULL) == 5
+    # N == 0 is a no-op
+    assert f(NULL, 0, 8, 8, NULL, 10, 8, NULL, NULL, 1, NULL, NULL, NULL, NULL, 0, NULL) == 0
+
+
+def test_det_gemm_validation(lib):
+    fwd, da, db = lib.rlk_det_gemm_fwd, lib.rlk_det_gemm_da, lib.rlk_det_gemm_db
+    ws = ctypes.c_void_p(0x20000)
+    # bad dtype / shapes / leading dims
+    assert fwd(P16, 4, 8, 8, P16, 8, 8, P16, 7, 8, ws, 0, NULL) == 3
+    assert fwd(P16, 4, 0, 8, P16, 8, 8, P16, 0, 8, ws, 0, NULL) == 2
+    assert fwd(P16, 4, 8, 7, P16, 8, 8, P16, 0, 8, ws, 0, NULL) == 2
+    assert fwd(P16, 4, 8, 8, P16, 8, 8, P16, 0, 7, ws, 0, NULL) == 2
+    assert da(P16, 5, 4, 8, 8, P16, 8, 8, P16, 0, 8, ws, 0, NULL) == 3
+    assert db(P16, 4, 8, 8, P16, 0, 0, 8, P16, 0, 8, ws, 0, NULL) == 2
+    # null output / inputs
+    assert fwd(P16, 4, 8, 8, P16, 8, 8, NULL, 0, 8, ws, 0, NULL) == 1
+    assert fwd(NULL, 4, 8, 8, P16, 8, 8, P16, 0, 8, ws, 0, NULL) == 1
+    # misaligned FP32 output, misaligned FP32 dC
+    assert fwd(P16, 4, 8, 8, P16, 8, 8, ctypes.c_void_p(0x10002), 1, 8, ws, 0, NULL) == 4
+    assert da(ctypes.c_void_p(0x10002), 1, 4, 8, 8, P16, 8, 8, P16, 0, 8, ws, 1 << 20, NULL) == 4
+    # staging needed (odd pitch / FP32 dC) but no workspace
+    assert fwd(P16, 4, 9, 9, P16, 8, 8, P16, 0, 8, NULL, 0, NULL) == 5
+    assert da(P16, 1, 4, 8, 8, P16, 8, 8, P16, 0, 8, NULL, 0, NULL) == 5
+    # M == 0 forward / dA: no-op
+    assert fwd(NULL, 0, 8, 8, NULL, 8, 8, NULL, 0, 8, NULL, 0, NULL) == 0
+    assert da(NULL, 0, 0, 8, 8, NULL, 8, 8, NULL, 0, 8, NULL, 0, NULL) == 0
+
+
+def test_det_gemm_workspace_size(lib):
+    f = lib.rlk_det_gemm_workspace_size
+    # aligned BF16 operands need nothing
+    assert f(0, P16, 0, 64, 64, 64, P16, 0, 64, 64, 64) == 0
+    # an FP32 dC is always rounded into the workspace: M x 8*ceil(N/8) bf16
+    assert f(1, P16, 1, 33, 33, 33, P16, 0, 33, 33, 40) == -(-(33 * 40 * 2) // 256) * 256
+    assert f(2, P16, 0, 10, 16, 16, P16, 1, 10, 20, 20) == -(-(10 * 24 * 2) // 256) * 256
+    # odd pitches stage both operands
+    assert f(0, P16, 0, 3, 5, 5, P16, 0, 5, 7, 7) == 2 * 256
+    # FP32 where BF16 is required, bad op -> 0
+    assert f(0, P16, 1, 4, 8, 8, P16, 0, 8, 8, 8) == 0
+    assert f(3, P16, 0, 4, 8, 8, P16, 0, 8, 8, 8) == 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_no_device_is_reported(lib):
+    assert lib.rlk_device_check() == 6
+    ws = ctypes.c_void_p(0x20000)
+    # valid arguments: the device check is what fails, before anything launches
+    assert lib.rlk_linear_logp(P16, 4, 8, 8, P16, 10, 8, NULL, P16, 1, P16, P16, NULL, ws,
+                               1 << 20, NULL) == 6
+    assert lib.rlk_det_gemm_fwd(P16, 4, 8, 8, P16, 8, 8, P16, 0, 8, ws, 0, NULL) == 6
+    flags = ctypes.c_uint32(7)
+    assert lib.rlk_get_device_error(NULL, ctypes.byref(flags)) == 6 and flags.value == 0
+
+
+def test_binding_rejects_cpu_and_grad(lib):
+    h = torch.zeros(4, 8, dtype=torch.bfloat16)
+    w = torch.zeros(10, 8, dtype=torch.bfloat16)
+    t = torch.zeros(4, dtype=torch.int64)
+    with pytest.raises(ValueError, match="CUDA"):
+        rlk.linear_logp(h, w, t)
+    with pytest.raises(RuntimeError, match="require grad"):
+        rlk.linear_logp(h.float().requires_grad_(), w, t)
+    with pytest.raises(ValueError, match="CUDA"):
+        rlk.det_gemm_fwd(h, w.T)

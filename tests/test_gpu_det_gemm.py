@@ -1,0 +1,208 @@
+"""GPU parity of the deterministic GEMM family against the FP64 oracle.
+
+"feat(musa): add native deterministic gemm kernel", Summary: C = A B,
+dA = dC B^T, dB = A^T dC, FP32 accumulation in ascending K order, BF16 or FP32
+output; review comment: an FP32 dC (gradient of an FP32-output forward) is
+rounded to BF16 before dA / dB.  Tolerances: FP32 output within relative
+Frobenius error 1e-5; BF16 output within one BF16 ulp of the exact result's
+rounding (see helpers.bf16_within_one_ulp); integer-valued inputs bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import deterministic_invariant_gemm_linear_gb300 as rlk
+import seeded_inputs as si
+from helpers import (GEMM_FP32_REL_FRO, bf16_within_one_ulp, cuda_or_skip, dec_bf16, rel_fro,
+                     sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return cuda_or_skip()
+
+
+def np64(t):
+    return t.detach().cpu().double().numpy()
+
+
+def call(op, x, y, out_dtype):
+    f = {"fwd": rlk.det_gemm_fwd, "da": rlk.det_gemm_da, "db": rlk.det_gemm_db}[op]
+    out = f(x, y, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    return out
+
+
+def oracle(orc, op, x, y, rows=None):
+    xb = si.bf16_bits(x) if x.dtype == torch.bfloat16 else orc.f32_to_bf16_rne(x.cpu().numpy())
+    yb = si.bf16_bits(y) if y.dtype == torch.bfloat16 else orc.f32_to_bf16_rne(y.cpu().numpy())
+    return {"fwd": orc.gemm_fwd, "da": orc.gemm_da, "db": orc.gemm_db}[op](xb, yb, rows=rows)
+
+
+def abs_terms(op, x, y, rows):
+    """sum_k |a_ik b_kj| for the sampled output rows (numpy float64)."""
+    X = np.abs(np64(x.float().to(torch.bfloat16)))
+    Y = np.abs(np64(y.float().to(torch.bfloat16)))
+    if op == "fwd":
+        return X[rows] @ Y
+    if op == "da":
+        return X[rows] @ Y.T
+    return X.T[rows] @ Y
+
+
+OPS = ["fwd", "da", "db"]
+
+
+def operands(op, A, B, dC):
+    return {"fwd": (A, B), "da": (dC, B), "db": (A, dC)}[op]
+
+
+@pytest.mark.parametrize("op", OPS)
+@pytest.mark.parametrize("shape", [(1, 1, 1), (33, 33, 33), (128, 64, 256), (300, 200, 520),
+                                   (257, 1000, 129)])
+def test_integer_inputs_bit_exact(dev, op, shape):
+    """|a|, |b| <= 16 with K <= 4096: every partial sum is an integer below 2^24,
+    so the FP32 result is exact in any order and must equal int64 matmul."""
+    M, K, N = shape
+    A = si.integer_bf16((M, K), -16, 16, seed=1)
+    B = si.integer_bf16((K, N), -16, 16, seed=2)
+    dC = si.integer_bf16((M, N), -16, 16, seed=3)
+    x, y = operands(op, A, B, dC)
+    out = call(op, x.to(dev), y.to(dev), torch.float32)
+    a, b, d = (t.float().numpy().astype(np.int64) for t in (A, B, dC))
+    want = {"fwd": a @ b, "da": d @ b.T, "db": a.T @ d}[op]
+    assert np.array_equal(out.cpu().numpy().astype(np.int64), want)
+    assert np.array_equal(out.cpu().numpy(), want.astype(np.float32))
+
+
+@pytest.mark.parametrize("op", OPS)
+def test_4096_parity_sampled(dev, orc, op):
+    A, B, dC = si.det_gemm_inputs(4096, 4096, 4096, seed=0, device=dev)
+    x, y = operands(op, A, B, dC)
+    c32 = call(op, x, y, torch.float32)
+    c16 = call(op, x, y, torch.bfloat16)
+    rows = sample_rows(4096, 40, seed=3, must=(255, 256, 4000))
+    ref = oracle(orc, op, x, y, rows)
+    assert rel_fro(c32.cpu().numpy()[rows].astype(np.float64), ref) <= GEMM_FP32_REL_FRO
+    # BF16 output: the epilogue's rounding of the very same accumulator ...
+    assert torch.equal(c16, c32.to(torch.bfloat16))
+    # ... and within one BF16 ulp of the exact result's rounding
+    g = dec_bf16(si.bf16_bits(c16)[rows])
+    bf16_within_one_ulp(g, ref, orc.f64_to_bf16_rne(ref), abs_terms(op, x, y, rows), 4096)
+    assert rlk.device_error() == 0
+
+
+@pytest.mark.parametrize("n", si.DET_GEMM_RAGGED)
+def test_ragged_fp32_output_backward(dev, orc, n):
+    """FP32-output forward, then dA / dB from an FP32 grad rounded to BF16."""
+    A, B, _ = si.det_gemm_inputs(n, n, n, seed=n, device="cpu")
+    dC32 = torch.randn(n, n, generator=torch.Generator().manual_seed(n + 1))
+    C = call("fwd", A.to(dev), B.to(dev), torch.float32)
+    assert C.dtype == torch.float32
+    ref = oracle(orc, "fwd", A, B)
+    assert rel_fro(np64(C), ref) <= GEMM_FP32_REL_FRO
+    for op, (x, y) in (("da", (dC32, B)), ("db", (A, dC32))):
+        for out_dtype in (torch.float32, torch.bfloat16):
+            out = call(op, x.to(dev), y.to(dev), out_dtype)
+            ref = oracle(orc, op, x, y)                  # oracle rounds dC with its own RNE
+            if out_dtype == torch.float32:
+                assert rel_fro(np64(out), ref) <= GEMM_FP32_REL_FRO, (op, n)
+            else:
+                rows = np.arange(ref.shape[0])
+                bf16_within_one_ulp(dec_bf16(si.bf16_bits(out)), ref, orc.f64_to_bf16_rne(ref),
+                                    abs_terms(op, x, y, rows), n)
+            # the FP32 grad path equals feeding the BF16-rounded grad directly
+            xb = x.to(torch.bfloat16) if x.dtype == torch.float32 else x
+            yb = y.to(torch.bfloat16) if y.dtype == torch.float32 else y
+            assert torch.equal(out, call(op, xb.to(dev), yb.to(dev), out_dtype))
+
+
+def test_batched_3d_is_flattened(dev):
+    """A[8, 512, 4096]: forward and dA equal the flattened 2-D call and each
+    batch slice on its own (row invariance); dB sums over all 4096 rows."""
+    A, B, dC = si.det_gemm_inputs(4096, 4096, 4096, seed=5, device=dev)
+    A3, dC3 = A.view(8, 512, 4096), dC.view(8, 512, 4096)
+    C3 = rlk.det_gemm_fwd(A3, B)
+    assert C3.shape == (8, 512, 4096)
+    assert torch.equal(C3.reshape(4096, 4096), rlk.det_gemm_fwd(A, B))
+    for b in (0, 3, 7):
+        assert torch.equal(C3[b], rlk.det_gemm_fwd(A3[b], B))
+    dA3 = rlk.det_gemm_da(dC3, B)
+    assert torch.equal(dA3.reshape(4096, 4096), rlk.det_gemm_da(dC, B))
+    assert torch.equal(dA3[5], rlk.det_gemm_da(dC3[5], B))
+    assert torch.equal(rlk.det_gemm_db(A3, dC3), rlk.det_gemm_db(A, dC))
+
+
+def test_run_to_run_bitwise(dev):
+    A, B, dC = si.det_gemm_inputs(4096, 4096, 4096, seed=6, device=dev)
+    for op in OPS:
+        x, y = operands(op, A, B, dC)
+        first = call(op, x, y, torch.bfloat16)
+        first32 = call(op, x, y, torch.float32)
+        for _ in range(4):
+            assert torch.equal(call(op, x, y, torch.bfloat16), first)
+            assert torch.equal(call(op, x, y, torch.float32), first32)
+
+
+def test_row_chunking_bitwise(dev):
+    """fwd / dA rows do not depend on which other rows are in the call."""
+    A, B, dC = si.det_gemm_inputs(1000, 768, 640, seed=7, device=dev)
+    full = rlk.det_gemm_fwd(A, B, out_dtype=torch.float32)
+    for chunk in (1, 7, 129):
+        parts = [rlk.det_gemm_fwd(A[s:s + chunk], B, out_dtype=torch.float32)
+                 for s in range(0, 1000, chunk)]
+        assert torch.equal(torch.cat(parts), full)
+    full_da = rlk.det_gemm_da(dC, B)
+    parts = [rlk.det_gemm_da(dC[s:s + 77], B) for s in range(0, 1000, 77)]
+    assert torch.equal(torch.cat(parts), full_da)
+
+
+def test_strided_and_misaligned_operands_bitwise(dev):
+    """A leading dimension wider than the row, an odd pitch (staged through the
+    workspace) and a contiguous copy all give the same bits."""
+    A, B, dC = si.det_gemm_inputs(300, 200, 264, seed=8, device=dev)
+    ref = rlk.det_gemm_fwd(A, B)
+    wide = torch.zeros(300, 264, dtype=torch.bfloat16, device=dev)
+    wide[:, :200] = A
+    assert torch.equal(rlk.det_gemm_fwd(wide[:, :200], B), ref)
+    odd = torch.zeros(300, 201, dtype=torch.bfloat16, device=dev)
+    odd[:, :200] = A
+    assert torch.equal(rlk.det_gemm_fwd(odd[:, :200], B), ref)
+    oddB = torch.zeros(200, 265, dtype=torch.bfloat16, device=dev)
+    oddB[:, :264] = B
+    assert torch.equal(rlk.det_gemm_fwd(A, oddB[:, :264]), ref)
+    ref_db = rlk.det_gemm_db(A, dC)
+    oddd = torch.zeros(300, 265, dtype=torch.bfloat16, device=dev)
+    oddd[:, :264] = dC
+    assert torch.equal(rlk.det_gemm_db(odd[:, :200], oddd[:, :264]), ref_db)
+
+
+def test_output_guard_bands(dev):
+    """Writes stay inside the output: canaries around a strided output survive."""
+    A, B, _ = si.det_gemm_inputs(33, 40, 33, seed=9, device=dev)
+    canary = torch.full((35, 48), -7.0, dtype=torch.float32, device=dev)
+    out = canary[1:34, 2:35]
+    st = rlk.lib().rlk_det_gemm_fwd(
+        rlk._ptr(A), 33, 40, 40, rlk._ptr(B), 33, 33, rlk._ptr(out), rlk.RLK_FP32, 48,
+        None, 0, rlk._stream_ptr(None))
+    # B's pitch (33) needs staging: without a workspace the call must refuse
+    assert st == 5
+    ws = torch.empty(1 << 16, dtype=torch.uint8, device=dev)
+    st = rlk.lib().rlk_det_gemm_fwd(
+        rlk._ptr(A), 33, 40, 40, rlk._ptr(B), 33, 33, rlk._ptr(out), rlk.RLK_FP32, 48,
+        rlk._ptr(ws), ws.numel(), rlk._stream_ptr(None))
+    assert st == 0
+    torch.cuda.synchronize()
+    assert torch.equal(out, rlk.det_gemm_fwd(A, B, out_dtype=torch.float32))
+    mask = torch.ones_like(canary, dtype=torch.bool)
+    mask[1:34, 2:35] = False
+    assert bool((canary[mask] == -7.0).all())
+
+
+def test_db_empty_reduction_is_zero(dev):
+    A = torch.empty(0, 24, dtype=torch.bfloat16, device=dev)
+    dC = torch.empty(0, 40, dtype=torch.bfloat16, device=dev)
+    out = rlk.det_gemm_db(A, dC, out_dtype=torch.float32)
+    assert out.shape == (24, 40) and bool((out == 0).all())

@@ -1,0 +1,122 @@
+"""Bitwise determinism and batch invariance of the fused linear-logp.
+
+The page "feat(linear-logp): add batch-invariant fused SM90 operator" fixes the
+contract: the same row with the same V gives the same bits whatever the batch
+(author notes: full-batch bits == concatenation of the chunks' bits, checked
+with exact equality, never allclose; PR body: batch size, row position,
+neighbouring rows, chunking, layouts, vocabulary boundaries and CUDA streams).
+Every check here is torch.equal.
+"""
+import pytest
+import torch
+
+import deterministic_invariant_gemm_linear_gb300 as rlk
+import seeded_inputs as si
+from helpers import cuda_or_skip
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return cuda_or_skip()
+
+
+@pytest.fixture(scope="module")
+def mid(dev):
+    return si.workload_inputs(si.MID, seed=11, device=dev)
+
+
+def lp(hidden, weight, target, bias=None, stream=None):
+    return rlk.linear_logp(hidden, weight, target, bias, return_target_logit=True, stream=stream)
+
+
+def chunked(hidden, weight, target, bias, chunk):
+    outs = [lp(hidden[s:s + chunk], weight, target[s:s + chunk], bias)
+            for s in range(0, hidden.size(0), chunk)]
+    return tuple(torch.cat([o[i] for o in outs]) for i in range(3))
+
+
+def assert_same(a, b, what):
+    for x, y, name in zip(a, b, ("logp", "lse", "target_logit")):
+        assert torch.equal(x, y), f"{what}: {name} bits differ"
+
+
+def test_run_to_run_mid(mid):
+    hidden, weight, bias, target = mid
+    first = lp(hidden, weight, target, bias)
+    for _ in range(9):
+        assert_same(lp(hidden, weight, target, bias), first, "run-to-run")
+    assert rlk.device_error() == 0
+
+
+@pytest.mark.parametrize("chunk", [1, 7, 512])
+def test_chunking_mid(mid, chunk):
+    hidden, weight, bias, target = mid
+    full = lp(hidden, weight, target, bias)
+    assert_same(chunked(hidden, weight, target, bias, chunk), full, f"chunk {chunk}")
+
+
+def test_chunking_large(dev):
+    hidden, weight, bias, target = si.workload_inputs(si.LARGE, seed=12, device=dev)
+    full = lp(hidden, weight, target, bias)
+    for chunk in (7, 2048):
+        assert_same(chunked(hidden, weight, target, bias, chunk), full, f"large chunk {chunk}")
+
+
+def test_row_position_and_neighbours(dev):
+    H, V, N = 1024, 40000, 300
+    hidden, weight, bias, target = si.linear_logp_inputs(N, H, V, bias=True, seed=13, device=dev)
+    row, t = hidden[5].clone(), target[5].clone()
+    ref = lp(row[None], weight, t[None], bias)
+    g = torch.Generator(device=dev).manual_seed(99)
+    for pos in (0, 127, 128, N - 1):
+        h = torch.randn(N, H, generator=g, device=dev).to(torch.bfloat16)   # fresh neighbours
+        tt = torch.randint(0, V, (N,), generator=g, device=dev)
+        h[pos], tt[pos] = row, t
+        out = lp(h, weight, tt, bias)
+        assert_same(tuple(o[pos:pos + 1] for o in out), ref, f"position {pos}")
+
+
+def test_vocab_boundary_targets(dev):
+    """Targets on tile / split edges and the last id of a ragged vocabulary."""
+    H, V = 512, 32003
+    hidden, weight, bias, _ = si.linear_logp_inputs(16, H, V, bias=True, seed=14, device=dev)
+    edges = torch.tensor([0, 255, 256, 511, 512, 31999, 32000, 32002, 1, 254, 257, 1023, 1024,
+                          16383, 16384, 32001], device=dev)
+    full = lp(hidden, weight, edges, bias)
+    for i in range(16):
+        one = lp(hidden[i:i + 1], weight, edges[i:i + 1], bias)
+        assert_same(tuple(o[i:i + 1] for o in full), one, f"edge target {int(edges[i])}")
+
+
+def test_streams(mid):
+    hidden, weight, bias, target = mid
+    ref = lp(hidden[:1000], weight, target[:1000], bias)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s1):
+        a = lp(hidden[:1000], weight, target[:1000], bias, stream=s1)
+    with torch.cuda.stream(s2):
+        b = lp(hidden[:1000], weight, target[:1000], bias, stream=s2)
+    torch.cuda.synchronize()
+    assert_same(a, ref, "stream 1")
+    assert_same(b, ref, "stream 2")
+
+
+def test_layouts(dev):
+    """Contiguous, wider-pitch view and odd-pitch (staged) hidden give the same bits."""
+    N, H, V = 257, 2048, 32003
+    hidden, weight, bias, target = si.linear_logp_inputs(N, H, V, seed=15, device=dev)
+    ref = lp(hidden, weight, target, bias)
+    wide = torch.zeros(N, H + 64, dtype=torch.bfloat16, device=dev)
+    wide[:, :H] = hidden
+    assert_same(lp(wide[:, :H], weight, target, bias), ref, "wide pitch")
+    odd = torch.zeros(N, H + 1, dtype=torch.bfloat16, device=dev)
+    odd[:, :H] = hidden
+    assert_same(lp(odd[:, :H], weight, target, bias), ref, "odd pitch (staged)")
+    wodd = torch.zeros(V, H + 3, dtype=torch.bfloat16, device=dev)
+    wodd[:, :H] = weight
+    assert_same(lp(hidden, wodd[:, :H], target, bias), ref, "odd weight pitch (staged)")
+    t_strided = torch.stack([target, target], dim=1)[:, 0]           # stride 2
+    assert_same(lp(hidden, weight, t_strided, bias), ref, "strided target")

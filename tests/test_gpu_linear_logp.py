@@ -1,0 +1,179 @@
+"""GPU parity of the fused linear-logp against the FP64 oracle.
+
+Every configuration of the operator ("feat(linear-logp): add batch-invariant
+fused SM90 operator": log_softmax(hidden . W^T + bias)[target] and the
+log-sum-exp) is compared element by element with the oracle on the same
+seeded inputs: in full where the oracle finishes in seconds, on sampled rows
+(always including the tile-edge rows) at the full sizes.  Tolerance:
+|delta logp|, |delta lse| <= 1e-3 absolute.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import deterministic_invariant_gemm_linear_gb300 as rlk
+import seeded_inputs as si
+from helpers import LOGP_ATOL, assert_logp_close, cuda_or_skip, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return cuda_or_skip()
+
+
+def run(dev, hidden, weight, target, bias=None):
+    logp, lse, zt = rlk.linear_logp(hidden.to(dev), weight.to(dev), target.to(dev),
+                                    None if bias is None else bias.to(dev), return_target_logit=True)
+    torch.cuda.synchronize()
+    return logp.cpu().numpy(), lse.cpu().numpy(), zt.cpu().numpy()
+
+
+def oracle_rows(orc, hidden, weight, target, bias, rows=None):
+    return orc.linear_logp(si.bf16_bits(hidden), si.bf16_bits(weight), target.cpu().numpy(),
+                           None if bias is None else bias.cpu().numpy(), rows=rows)
+
+
+def test_tiny_full_parity(dev, orc):
+    hidden, weight, bias, target = si.workload_inputs(si.TINY, seed=0)
+    lp, ls, zt = run(dev, hidden, weight, target, bias)
+    rlp, rls, rzt = oracle_rows(orc, hidden, weight, target, bias)
+    assert_logp_close(lp, ls, rlp, rls, "tiny")
+    assert np.abs(zt - rzt).max() <= 1e-4
+    assert np.all(lp <= 0.0)
+    assert rlk.device_error() == 0
+
+
+@pytest.mark.parametrize("N", si.RAGGED_N)
+def test_ragged_parity(dev, orc, N):
+    w = si.ragged(N)
+    hidden, weight, bias, target = si.workload_inputs(w, seed=N)
+    # targets at the vocabulary's edges and at tile / split boundaries
+    edges = [0, w.V - 1, 255, 256, 32000, 32002]
+    for i, e in enumerate(edges[:N]):
+        target[(i * 7919) % N] = e
+    lp, ls, zt = run(dev, hidden, weight, target, bias)
+    rows = np.arange(N) if N <= 255 else sample_rows(N, 48, seed=N)
+    rlp, rls, rzt = oracle_rows(orc, hidden, weight, target, bias, rows)
+    assert_logp_close(lp[rows], ls[rows], rlp, rls, f"ragged N={N}")
+    assert np.abs(zt[rows] - rzt).max() <= 1e-4
+    assert np.all(lp <= 0.0)
+
+
+def test_mid_parity_sampled(dev, orc):
+    w = si.MID
+    hidden, weight, bias, target = si.workload_inputs(w, seed=0, device=dev)
+    logp, lse, zt = rlk.linear_logp(hidden, weight, target, bias, return_target_logit=True)
+    torch.cuda.synchronize()
+    rows = sample_rows(w.N, 40, seed=1, must=(511, 512, 2047, 2048, 4095))
+    rlp, rls, rzt = oracle_rows(orc, hidden[rows], weight, target[rows], bias)
+    assert_logp_close(logp.cpu().numpy()[rows], lse.cpu().numpy()[rows], rlp, rls, "mid")
+    assert np.abs(zt.cpu().numpy()[rows] - rzt).max() <= 1e-4
+    assert bool((logp <= 0).all())
+    assert rlk.device_error() == 0
+
+
+def test_large_parity_sampled(dev, orc):
+    w = si.LARGE
+    hidden, weight, bias, target = si.workload_inputs(w, seed=0, device=dev)
+    assert int((target == 0).sum()) >= (w.N * 10) // 100
+    h3 = hidden.view(*w.lead_shape, w.H)
+    logp, lse, zt = rlk.linear_logp(h3, weight, target.view(*w.lead_shape), bias,
+                                    return_target_logit=True)
+    torch.cuda.synchronize()
+    assert logp.shape == w.lead_shape
+    logp, lse, zt = logp.reshape(-1), lse.reshape(-1), zt.reshape(-1)
+    id0 = torch.nonzero(target == 0).flatten().cpu().numpy()[:6]
+    rows = sample_rows(w.N, 24, seed=2, must=tuple(int(i) for i in id0) + (2047, 2048, 16383))
+    rlp, rls, rzt = oracle_rows(orc, hidden[rows], weight, target[rows], bias)
+    assert_logp_close(logp.cpu().numpy()[rows], lse.cpu().numpy()[rows], rlp, rls, "large")
+    assert np.abs(zt.cpu().numpy()[rows] - rzt).max() <= 1e-4
+    assert rlk.device_error() == 0
+
+
+def test_integer_logits_bit_exact(dev, orc):
+    """Integer-valued hidden and W: every logit is an exact integer in FP32, so
+    the gathered target logit must equal the oracle's bit for bit (pins the
+    gather and index path); lse/logp stay within tolerance."""
+    N, H, V = 200, 320, 2000
+    hidden = si.integer_bf16((N, H), -4, 4, seed=1)
+    weight = si.integer_bf16((V, H), -4, 4, seed=2)
+    target = torch.randint(0, V, (N,), generator=torch.Generator().manual_seed(3))
+    lp, ls, zt = run(dev, hidden, weight, target)
+    rlp, rls, rzt = oracle_rows(orc, hidden, weight, target, None)
+    assert np.array_equal(zt.astype(np.float64), rzt)
+    # lse is large here (logits up to a few hundred); compare in relative terms too
+    assert np.abs(ls - rls).max() <= LOGP_ATOL * max(1.0, np.abs(rls).max() / 100)
+    assert np.abs(lp - rlp).max() <= LOGP_ATOL * max(1.0, np.abs(rls).max() / 100)
+
+
+def test_invariants_on_gpu(dev):
+    """Properties the definition fixes, checked on the GPU's own outputs."""
+    H, V = 512, 3000
+    hidden, weight, bias, target = si.linear_logp_inputs(6, H, V, bias=True, seed=4)
+    # logp summed over every target of a row is 1; lse identical across the copies
+    for r in range(2):
+        hr = hidden[r:r + 1].expand(V, H).contiguous()
+        lp, ls, _ = run(dev, hr, weight, torch.arange(V), bias)
+        assert abs(math.fsum(np.exp(lp.astype(np.float64))) - 1.0) <= 1e-4
+        assert np.all(ls == ls[0])
+        assert np.all(lp <= 0.0)
+    # all W rows equal and no bias: logp = -log V
+    weq = weight[:1].expand(V, H).contiguous()
+    lp, _, _ = run(dev, hidden, weq, target)
+    assert np.abs(lp + math.log(V)).max() <= 1e-5
+    # V = 1: logp = 0 exactly, lse = the single logit
+    lp, ls, zt = run(dev, hidden, weight[:1], torch.zeros(6, dtype=torch.int64), bias[:1])
+    assert np.all(lp == 0.0) and np.array_equal(ls, zt)
+    # a bias shift c moves lse by c and leaves logp unchanged (to rounding)
+    lp0, ls0, _ = run(dev, hidden, weight, target, bias)
+    lp1, ls1, _ = run(dev, hidden, weight, target, bias + 2.0)
+    assert np.abs(ls1 - ls0 - 2.0).max() <= 1e-4 and np.abs(lp1 - lp0).max() <= 1e-4
+    # out-of-range targets: NaN logp, lse unchanged bit for bit
+    tb = target.clone()
+    tb[0], tb[1] = -1, V
+    lp2, ls2, zt2 = run(dev, hidden, weight, tb, bias)
+    assert math.isnan(lp2[0]) and math.isnan(lp2[1]) and math.isnan(zt2[0])
+    assert np.array_equal(ls2, ls0) and np.array_equal(lp2[2:], lp0[2:])
+
+
+def test_expanded_target_and_lead_shape(dev):
+    hidden, weight, bias, _ = si.linear_logp_inputs(24, 256, 700, bias=True, seed=5)
+    t_exp = torch.tensor([17]).expand(24)           # zero-stride target
+    assert t_exp.stride(0) == 0
+    lp_a, ls_a, _ = run(dev, hidden, weight, t_exp, bias)
+    lp_b, ls_b, _ = run(dev, hidden, weight, torch.full((24,), 17), bias)
+    assert np.array_equal(lp_a, lp_b) and np.array_equal(ls_a, ls_b)
+    h3 = hidden.view(4, 6, 256).to(dev)
+    t2 = torch.full((4, 6), 17).to(dev)
+    lp3, ls3 = rlk.linear_logp(h3, weight.to(dev), t2, bias.to(dev))
+    assert lp3.shape == (4, 6)
+    assert np.array_equal(lp3.reshape(-1).cpu().numpy(), lp_b)
+
+
+def test_bias_none_vs_zero_bias(dev):
+    hidden, weight, _, target = si.linear_logp_inputs(40, 256, 999, seed=6)
+    lp_a, ls_a, _ = run(dev, hidden, weight, target, None)
+    lp_b, ls_b, _ = run(dev, hidden, weight, target, torch.zeros(999))
+    assert np.array_equal(lp_a, lp_b) and np.array_equal(ls_a, ls_b)
+
+
+def test_small_and_odd_hidden_sizes(dev, orc):
+    """H below one reduction block, H not a multiple of 8 (staged through the
+    workspace), V below one tile."""
+    for (N, H, V) in [(5, 8, 3), (130, 33, 257), (3, 1, 1), (129, 100, 513)]:
+        hidden, weight, bias, target = si.linear_logp_inputs(N, H, V, bias=True, seed=H)
+        lp, ls, zt = run(dev, hidden, weight, target, bias)
+        rlp, rls, rzt = oracle_rows(orc, hidden, weight, target, bias)
+        assert_logp_close(lp, ls, rlp, rls, f"N={N} H={H} V={V}")
+        assert np.abs(zt - rzt).max() <= 1e-4
+
+
+def test_zero_rows(dev):
+    hidden = torch.empty(0, 256, dtype=torch.bfloat16, device=dev)
+    weight = torch.zeros(10, 256, dtype=torch.bfloat16, device=dev)
+    lp, ls = rlk.linear_logp(hidden, weight, torch.empty(0, dtype=torch.int64, device=dev))
+    assert lp.numel() == 0 and ls.numel() == 0
