@@ -1,0 +1,410 @@
+"""Benchmark of the deterministic, batch-invariant linear-logp (and det_gemm) on GB300.
+
+Default line: fused linear-logp on N=4096 rows, H=4096, V=151936 (BF16 operands,
+FP32 accumulation, no bias, uniform int64 targets, seeded synthetic data).  One
+step = the whole operator: the fused projection + online-softmax kernel and the
+split-merge kernel, on inputs resident in HBM.  The weight (1.245 GB) is larger
+than the 129 MB L2, so every step streams it from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mid|large|det_gemm]
+  python bench.py --impl reference ...     # the FP64 CPU oracle on the host cores
+
+Printed: one JSON line (rank 0).  Under torchrun (N > 1) every rank runs an
+independent replica of the workload on its own GPU (the operator needs no
+exchange between GPUs); the timed region is bracketed by a barrier and the
+slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import seeded_inputs as si  # noqa: E402
+
+METRIC = "linear-logp tokens/s & TFLOP/s (N=4096,H=4096,V=151936); % BF16 dense peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- distributed
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        rank = dist.get_rank()
+        local = int(os.environ.get("LOCAL_RANK", rank))
+        return rank, world, local
+    return 0, 1, 0
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+def oracle_tokens_per_s(hidden, weight, target, bias, rows: int):
+    """Time the FP64 oracle on `rows` rows of the workload (host cores)."""
+    import oracle
+    orc = oracle.load()
+    cores = min(orc.max_threads(), rows)
+    hb, wb = si.bf16_bits(hidden[:rows]), si.bf16_bits(weight)
+    tb = target[:rows].cpu().numpy()
+    bb = None if bias is None else bias.cpu().numpy()
+    t0 = time.perf_counter()
+    orc.linear_logp(hb, wb, tb, bb, threads=cores)
+    dt = time.perf_counter() - t0
+    return rows / dt, dt, cores
+
+
+# ---------------------------------------------------------------- workloads
+def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
+    import deterministic_invariant_gemm_linear_gb300 as rlk
+    w = {"mid": si.MID, "large": si.LARGE}[args.workload]
+    if args.rows:
+        w = si.LinearLogpWorkload(f"{w.name} (rows={args.rows})", N=args.rows, H=w.H, V=w.V,
+                                  bias=w.bias, target_mode=w.target_mode)
+    hidden, weight, bias, target = si.workload_inputs(w, seed=rank, device=dev)
+    call = rlk.LinearLogpCall(hidden, weight, target, bias)
+    stream = torch.cuda.current_stream()
+    flops = 2.0 * w.N * w.H * w.V
+    # warm-up (untimed)
+    for _ in range(args.warmup):
+        call.partials()
+        call.combine()
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        start.record(stream)
+        for k in range(K):
+            ev[k][0].record(stream)
+            call.partials()
+            ev[k][1].record(stream)
+            call.combine()
+            ev[k][2].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    t_local = start.elapsed_time(end) / 1e3
+    t = max_over_ranks(t_local, world, dev)
+    assert rlk.device_error() == 0, "device error word set during the bench"
+    part_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
+    comb_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    ms_step = t / K * 1e3
+    tokens = w.N * world * K
+    value = tokens / t
+    achieved = flops / (part_ms / 1e3) / 1e12
+    peak = peaks["bf16_tflops"]
+    line = {
+        "metric": METRIC if (args.workload == "mid" and not args.rows) else
+        f"linear-logp tokens/s & TFLOP/s (N={w.N},H={w.H},V={w.V}); % BF16 dense peak",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name}: N={w.N} H={w.H} V={w.V}" + (" +bias" if w.bias else "")
+                   + ", hidden~N(0,1), W~N(0,1/sqrt(H)), uniform int64 targets, seed=rank",
+                   "global_batch": w.N * world, "seq_len": None, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: W {weight.numel() * 2 / 1e9:.3f} GB streamed per step"},
+        "tflops": flops * world * K / t / 1e12,
+        "frac_bf16_peak": flops * K / t_local / 1e12 / peak,
+        "kernels_ms": {"linear_logp_partials": part_ms, "linear_logp_combine": comb_ms},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_kind": f"{peak_src} burst bf16 (sustained {peaks['bf16_tflops_sustained']})",
+                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                     "kernel": "linear_logp_partials_kernel",
+                     "algorithmic": f"2*N*H*V = {flops:.4g} FLOP per launch"},
+        "clocks": clocks.summary(),
+        "gpu_launches": 2 * K,
+    }
+    # ---- e2e through the public API with host buffers (pinned), copies timed
+    if not args.no_e2e:
+        hh = hidden.cpu().pin_memory()
+        wh = weight.cpu().pin_memory()
+        th = target.cpu().pin_memory()
+        bh = None if bias is None else bias.cpu().pin_memory()
+        out_lp = torch.empty(w.N, dtype=torch.float32).pin_memory()
+        out_ls = torch.empty(w.N, dtype=torch.float32).pin_memory()
+        E = max(3, min(K, 20))
+        for i in range(E + 2):
+            if i == 2:
+                torch.cuda.synchronize()
+                barrier(world)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            hidden.copy_(hh, non_blocking=True)
+            weight.copy_(wh, non_blocking=True)
+            target.copy_(th, non_blocking=True)
+            if bias is not None:
+                bias.copy_(bh, non_blocking=True)
+            call()
+            out_lp.copy_(call.logp, non_blocking=True)
+            out_ls.copy_(call.lse, non_blocking=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        te = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
+        h2d = hh.numel() * 2 + wh.numel() * 2 + th.numel() * 8 + (0 if bh is None else bh.numel() * 4)
+        line["e2e"] = {"value": w.N * world * E / te, "unit": "tokens/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 8 * w.N,
+                       "ms_per_step": te / E * 1e3}
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+        rows = 2 * oracle.load().max_threads()
+        tps, dt, cores = oracle_tokens_per_s(hidden, weight, target, bias, rows)
+        line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": f"{rows} rows of the {w.name} workload (full V, full H), "
+                                          f"FP64, {dt:.2f} s wall"}
+    return line
+
+
+def det_gemm_bench(args, dev, rank, world, peaks, peak_src):
+    import deterministic_invariant_gemm_linear_gb300 as rlk
+    M = K_ = N = 4096
+    A, B, dC = si.det_gemm_inputs(M, K_, N, seed=rank, device=dev)
+    flop = 2.0 * M * N * K_
+    ops = [("fwd", lambda: rlk.det_gemm_fwd(A, B)), ("da", lambda: rlk.det_gemm_da(dC, B)),
+           ("db", lambda: rlk.det_gemm_db(A, dC))]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # 256 MB > L2
+    for _ in range(args.warmup):
+        for _, f in ops:
+            f()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    K = args.steps
+    per = {n: [] for n, _ in ops}
+    total = 0.0
+    barrier(world)
+    with ClockSampler(dev.index) as clocks:
+        for _ in range(K):
+            flush.zero_()
+            s = torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            prev = s
+            for n, f in ops:
+                f()
+                e = torch.cuda.Event(enable_timing=True)
+                e.record(stream)
+                per[n].append((prev, e))
+                prev = e
+            torch.cuda.synchronize()
+            total += s.elapsed_time(prev) / 1e3
+    t = max_over_ranks(total, world, dev)
+    ms = {n: float(np.mean([a.elapsed_time(b) for a, b in v])) for n, v in per.items()}
+    peak = peaks["bf16_tflops"]
+    # cuBLAS bf16 matmul on the same box, as context only
+    for _ in range(3):
+        torch.matmul(A, B)
+    torch.cuda.synchronize()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for _ in range(10):
+        torch.matmul(A, B)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    cublas = flop / (c0.elapsed_time(c1) / 10 / 1e3) / 1e12
+    best = min(ms, key=ms.get)
+    return {
+        "metric": "det_gemm fwd+da+db TFLOP/s (M=N=K=4096, BF16 in/out, FP32 accumulate)",
+        "value": 3 * flop * world * K / t / 1e12, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": t / K * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "det_gemm 4096^3 fwd+da+db, A,B~N(0,1/sqrt(K)), dC~N(0,1)",
+                   "l2": "L2 flushed (256 MB write) before every step"},
+        "kernels_ms": ms,
+        "tflops_per_op": {n: flop / (v / 1e3) / 1e12 for n, v in ms.items()},
+        "roofline": {"bound": "tensor", "achieved": flop / (ms[best] / 1e3) / 1e12, "peak": peak,
+                     "unit": "TFLOP/s", "frac": flop / (ms[best] / 1e3) / 1e12 / peak,
+                     "traffic": None, "kernel": f"det_gemm_kernel ({best})",
+                     "peak_kind": f"{peak_src} burst bf16"},
+        "cublas_bf16_tflops_context": cublas,
+        "clocks": clocks.summary(),
+        "gpu_launches": 3 * K,
+    }
+
+
+def reference_arm(args):
+    """The FP64 CPU oracle as the reference implementation, on a bounded sample.
+
+    Each step runs the oracle on `cores` rows (one per host thread) against a
+    contiguous slice of Vs vocabulary rows, Vs sized so that warm-up + steps end
+    within about 150 s; the oracle's cost is linear in V, so its throughput is
+    reported in full-vocabulary rows per second (rows * Vs / V per step).
+    """
+    import oracle
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    orc = oracle.load()
+    w = {"mid": si.MID, "large": si.LARGE}.get(args.workload, si.MID)
+    cores = orc.max_threads()
+    g = torch.Generator().manual_seed(0)
+    hidden = torch.randn(cores, w.H, generator=g).to(torch.bfloat16)
+    weight = (torch.randn(w.V, w.H, generator=g) / math.sqrt(w.H)).to(torch.bfloat16)
+    target = torch.randint(0, w.V, (cores,), generator=g)
+    bias = (torch.randn(w.V, generator=g) * 0.01) if w.bias else None
+    hb, wb, tb = si.bf16_bits(hidden), si.bf16_bits(weight), target.numpy()
+    bb = None if bias is None else bias.numpy()
+    t0 = time.perf_counter()
+    orc.linear_logp(hb[:1], wb, tb[:1], bb, threads=1)          # one full row, one thread
+    t_row = time.perf_counter() - t0
+    step_budget = 150.0 / (args.steps + args.warmup)
+    Vs = max(256, min(w.V, int(w.V * step_budget / max(t_row, 1e-9))))
+    ws, tsb = wb[:Vs], tb % Vs
+    bs = None if bb is None else bb[:Vs]
+    for _ in range(args.warmup):
+        orc.linear_logp(hb, ws, tsb, bs, threads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        orc.linear_logp(hb, ws, tsb, bs, threads=cores)
+    dt = time.perf_counter() - t0
+    value = cores * (Vs / w.V) * args.steps / dt
+    sample = (f"{cores} rows x {Vs} of {w.V} vocabulary rows per step of the {w.name} workload "
+              f"(full H); reported as full-vocabulary rows/s")
+    return {
+        "impl": "reference", "metric": METRIC if args.workload == "mid" else args.workload,
+        "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}: N={w.N} H={w.H} V={w.V}", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="mid", choices=["mid", "large", "det_gemm"])
+    ap.add_argument("--impl", default="rlk", choices=["rlk", "reference"])
+    ap.add_argument("--rows", type=int, default=0,
+                    help="override the row count N of a linear-logp workload (profiling cases)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    if args.impl == "reference":
+        line = reference_arm(args)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    rank, world, local = dist_setup(args.gpus)
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the product path has no CPU fallback)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks, src = load_peaks()
+    if args.workload == "det_gemm":
+        line = det_gemm_bench(args, dev, rank, world, peaks, src)
+    else:
+        line = linear_logp_bench(args, dev, rank, world, peaks, src)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
