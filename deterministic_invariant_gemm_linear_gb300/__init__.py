@@ -57,6 +57,8 @@ SIGNATURES = {
     "rlk_linear_logp_partials": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _P, _I64,
                                       _P, _SZ, _P]),
     "rlk_linear_logp_combine": (_I, [_I64, _I64, _P, _I64, _P, _P, _P, _P, _SZ, _P]),
+    "rlk_linear_logp_noalloc": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _P, _I64,
+                                     _P, _P, _P, _P]),
     "rlk_det_gemm_workspace_size": (_SZ, [_I, _P, _I, _I64, _I64, _I64, _P, _I, _I64, _I64, _I64]),
     "rlk_det_gemm_fwd": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _I, _I64, _P, _SZ, _P]),
     "rlk_det_gemm_da": (_I, [_P, _I, _I64, _I64, _I64, _P, _I64, _I64, _P, _I, _I64, _P, _SZ, _P]),

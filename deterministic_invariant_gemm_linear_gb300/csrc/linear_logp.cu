@@ -426,3 +426,71 @@ rlk_status rlk_linear_logp(const void* hidden, int64_t N, int64_t H, int64_t ld_
 }
 
 }  // extern "C"
+
+// ======================================================================
+// Linear-logp without any caller-provided or library-allocated workspace.
+//
+// Some callers cannot allocate device memory at the point where they need this
+// operator: a plugin running inside a host framework that owns the device
+// allocator and offers no way to request scratch buffers, code under a device
+// memory budget fixed in advance, or a latency-critical loop that must not call
+// cudaMalloc / cudaFree because those calls can synchronise the device.  For
+// them the partials live in one fixed, file-scope device array that is part of
+// the library image: every GPU that loads this library holds these 32 MiB
+// until the process exits.
+//
+// The array is shared by every call on a device and keeps whatever the last
+// call left in it.  Nothing in it has to start at zero: each call overwrites
+// every partial it later reads, and a target logit is read only for rows whose
+// target was written in the same call.  Calls whose GPU work overlaps (for
+// example on two streams without ordering between them) use the same array and
+// race; order them on one stream or with events.
+namespace rlk {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;   // 32 MiB per device
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[64];     // device address of g_noalloc_scratch, per device
+
+// Host code cannot use g_noalloc_scratch's name as an address (on the host it
+// names a stand-in object); the device address is looked up once per device,
+// with that device current, and cached.
+rlk_status noalloc_scratch(int dev, void** out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return RLK_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return RLK_OK;
+}
+
+}  // namespace
+}  // namespace rlk
+
+extern "C" rlk_status rlk_linear_logp_noalloc(const void* hidden, int64_t N, int64_t H,
+                                              int64_t ld_hidden, const void* weight, int64_t V,
+                                              int64_t ld_weight, const float* bias,
+                                              const int64_t* target, int64_t target_stride,
+                                              float* logp, float* lse, float* target_logit,
+                                              void* stream) {
+  const size_t need = rlk_linear_logp_workspace_size(hidden, N, H, ld_hidden, weight, V, ld_weight);
+  if (need > rlk::kNoAllocScratchBytes) return RLK_ERR_WORKSPACE;
+  if (N == 0 || need == 0)   // empty call, or arguments the regular entry point rejects
+    return rlk_linear_logp(hidden, N, H, ld_hidden, weight, V, ld_weight, bias, target,
+                           target_stride, logp, lse, target_logit, nullptr, 0, stream);
+  rlk::DeviceInfo dev;
+  rlk_status st = rlk::device_ready(&dev);
+  if (st != RLK_OK) return st;
+  void* scratch = nullptr;
+  if ((st = rlk::noalloc_scratch(dev.device, &scratch)) != RLK_OK) return st;
+  return rlk_linear_logp(hidden, N, H, ld_hidden, weight, V, ld_weight, bias, target,
+                         target_stride, logp, lse, target_logit, scratch,
+                         rlk::kNoAllocScratchBytes, stream);
+}

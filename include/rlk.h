@@ -186,6 +186,37 @@ RLK_API rlk_status rlk_linear_logp_combine(int64_t N, int64_t V, const int64_t* 
                                    float* target_logit, const void* workspace,
                                    size_t workspace_bytes, void* stream);
 
+/*
+ * rlk_linear_logp without a workspace argument, for callers that cannot
+ * allocate device memory where they call it: a plugin inside a host framework
+ * that owns the device allocator and exposes no scratch-buffer hook, code that
+ * runs under a device-memory budget fixed in advance, or a latency-critical loop
+ * that must not call cudaMalloc / cudaFree (they can synchronise the device).
+ * The pages have no counterpart to this entry point; it exists for those callers.
+ *
+ * Same arguments, arithmetic and output bits as rlk_linear_logp.  Scratch comes
+ * from one fixed 32 MiB array in the library's own device image, which every GPU
+ * that loads the library holds until the process exits.  Nothing is allocated:
+ * no cudaMalloc, no cudaFree, no allocating library routine.
+ *  - Limit: the call needs N * S * 8 + N * 4 bytes (each rounded up to 256; S from
+ *    rlk_vocab_split_policy(V)), plus a padded copy of any misaligned operand;
+ *    more than RLK_NOALLOC_SCRATCH_BYTES returns RLK_ERR_WORKSPACE and launches
+ *    nothing.  (V = 151936: up to about 7,000 rows per call.)
+ *  - The first call on each device looks up the array's device address (with that
+ *    device current) and caches it; make that first call before any stream
+ *    capture.
+ *  - Every call on a device shares the array and leaves its contents behind; no
+ *    part of it needs to start at zero.  Calls whose GPU work overlaps (two streams
+ *    without ordering between them) race on it: order them.
+ */
+#define RLK_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+RLK_API rlk_status rlk_linear_logp_noalloc(const void* hidden, int64_t N, int64_t H,
+                                           int64_t ld_hidden, const void* weight, int64_t V,
+                                           int64_t ld_weight, const float* bias,
+                                           const int64_t* target, int64_t target_stride,
+                                           float* logp, float* lse, float* target_logit,
+                                           void* stream);
+
 /* ===================================================================== *
  *  Deterministic GEMM family                                      [P1]  *
  * ===================================================================== */
