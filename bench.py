@@ -45,6 +45,32 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+# ---------------------------------------------------------------- measured traffic
+KERNEL_SOURCES = ["rlk_device.cuh", "rlk_pipeline.cuh", "linear_logp.cu", "det_gemm.cu", "common.cu"]
+
+
+def kernel_sources_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "deterministic_invariant_gemm_linear_gb300", "csrc")
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu capture, or None when there is
+    none for this kernel / workload or the kernel sources changed since."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(f"{kernel}@{workload}")
+    if not rec or rec.get("sources_sha256") != kernel_sources_sha256():
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
 # ---------------------------------------------------------------- distributed
 def dist_setup(n_gpus):
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -151,8 +177,11 @@ def oracle_tokens_per_s(hidden, weight, target, bias, rows: int):
 # ---------------------------------------------------------------- workloads
 def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
     import deterministic_invariant_gemm_linear_gb300 as rlk
-    w = {"mid": si.MID, "large": si.LARGE}[args.workload]
-    if args.rows:
+    if args.workload == "ragged":
+        w = si.ragged(args.rows or 17)
+    else:
+        w = {"mid": si.MID, "large": si.LARGE}[args.workload]
+    if args.rows and args.workload != "ragged":
         w = si.LinearLogpWorkload(f"{w.name} (rows={args.rows})", N=args.rows, H=w.H, V=w.V,
                                   bias=w.bias, target_mode=w.target_mode)
     hidden, weight, bias, target = si.workload_inputs(w, seed=rank, device=dev)
@@ -165,6 +194,10 @@ def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
         call.combine()
     torch.cuda.synchronize()
     K = args.steps
+    # W larger than L2 streams from HBM by itself; smaller weights get an L2 flush
+    # (a 256 MB write) before every step, outside the per-step kernel events.
+    w_bytes = weight.numel() * 2
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if w_bytes < (512 << 20) else None
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -173,6 +206,8 @@ def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
     with ClockSampler(dev.index) as clocks:
         start.record(stream)
         for k in range(K):
+            if flush is not None:
+                flush.zero_()
             ev[k][0].record(stream)
             call.partials()
             ev[k][1].record(stream)
@@ -181,7 +216,10 @@ def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
         end.record(stream)
         torch.cuda.synchronize()
     barrier(world)
-    t_local = start.elapsed_time(end) / 1e3
+    if flush is None:
+        t_local = start.elapsed_time(end) / 1e3
+    else:
+        t_local = sum(e[0].elapsed_time(e[2]) for e in ev) / 1e3
     t = max_over_ranks(t_local, world, dev)
     assert rlk.device_error() == 0, "device error word set during the bench"
     part_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
@@ -189,7 +227,26 @@ def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
     ms_step = t / K * 1e3
     tokens = w.N * world * K
     value = tokens / t
-    achieved = flops / (part_ms / 1e3) / 1e12
+    S = rlk.vocab_split_policy(w.V)[0]
+    alg_bytes = 2 * w.V * w.H + 2 * w.N * w.H + 8 * w.N + 8 * w.N * S + 4 * w.N + (4 * w.V if w.bias else 0)
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    hbm_bound = flops / alg_bytes < ridge
+    traffic = measured_traffic("linear_logp_partials_kernel", w.name)
+    if hbm_bound:
+        achieved = alg_bytes / (part_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                "peak_kind": f"{peak_src} HBM copy bandwidth",
+                "algorithmic": f"{alg_bytes} bytes per launch (W + hidden + targets + partials)"}
+    else:
+        achieved = flops / (part_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
+                "peak_kind": f"{peak_src} burst bf16 (sustained {peaks['bf16_tflops_sustained']})",
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                "algorithmic": f"2*N*H*V = {flops:.4g} FLOP per launch"}
+    roof["kernel"] = "linear_logp_partials_kernel"
+    roof["traffic_unit"] = "bytes per launch (ncu dram read+write)"
     peak = peaks["bf16_tflops"]
     line = {
         "metric": METRIC if (args.workload == "mid" and not args.rows) else
@@ -200,16 +257,13 @@ def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
         "config": {"workload": f"{w.name}: N={w.N} H={w.H} V={w.V}" + (" +bias" if w.bias else "")
                    + ", hidden~N(0,1), W~N(0,1/sqrt(H)), uniform int64 targets, seed=rank",
                    "global_batch": w.N * world, "seq_len": None, "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2: W {weight.numel() * 2 / 1e9:.3f} GB streamed per step"},
+                   "l2": (f"inputs larger than L2: W {w_bytes / 1e9:.3f} GB streamed per step"
+                          if flush is None else "L2 flushed (256 MB write) before every step; "
+                          "step time = sum of per-step kernel events")},
         "tflops": flops * world * K / t / 1e12,
         "frac_bf16_peak": flops * K / t_local / 1e12 / peak,
         "kernels_ms": {"linear_logp_partials": part_ms, "linear_logp_combine": comb_ms},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
-                     "peak_kind": f"{peak_src} burst bf16 (sustained {peaks['bf16_tflops_sustained']})",
-                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                     "kernel": "linear_logp_partials_kernel",
-                     "algorithmic": f"2*N*H*V = {flops:.4g} FLOP per launch"},
+        "roofline": roof,
         "clocks": clocks.summary(),
         "gpu_launches": 2 * K,
     }
@@ -247,7 +301,7 @@ def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
     if rank == 0 and world == 1 and not args.no_cpu:
         import oracle
-        rows = 2 * oracle.load().max_threads()
+        rows = min(w.N, 2 * oracle.load().max_threads())
         tps, dt, cores = oracle_tokens_per_s(hidden, weight, target, bias, rows)
         line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": f"{rows} rows of the {w.name} workload (full V, full H), "
@@ -312,7 +366,11 @@ def det_gemm_bench(args, dev, rank, world, peaks, peak_src):
         "tflops_per_op": {n: flop / (v / 1e3) / 1e12 for n, v in ms.items()},
         "roofline": {"bound": "tensor", "achieved": flop / (ms[best] / 1e3) / 1e12, "peak": peak,
                      "unit": "TFLOP/s", "frac": flop / (ms[best] / 1e3) / 1e12 / peak,
-                     "traffic": None, "kernel": f"det_gemm_kernel ({best})",
+                     "traffic": measured_traffic("det_gemm_kernel", f"det_gemm 4096^3 {best}"),
+                     "traffic_unit": "bytes per launch (ncu dram read+write)",
+                     "kernel": f"det_gemm_kernel ({best})",
+                     "algorithmic": f"2*M*N*K = {flop:.4g} FLOP per launch; "
+                                    f"{2 * (M * K_ + K_ * N) + 2 * M * N} bytes (bf16 out)",
                      "peak_kind": f"{peak_src} burst bf16"},
         "cublas_bf16_tflops_context": cublas,
         "clocks": clocks.summary(),
@@ -375,7 +433,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="mid", choices=["mid", "large", "det_gemm"])
+    ap.add_argument("--workload", default="mid", choices=["mid", "large", "ragged", "det_gemm"])
     ap.add_argument("--impl", default="rlk", choices=["rlk", "reference"])
     ap.add_argument("--rows", type=int, default=0,
                     help="override the row count N of a linear-logp workload (profiling cases)")
