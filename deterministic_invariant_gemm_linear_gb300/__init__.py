@@ -30,6 +30,7 @@ LIB_PATH = os.path.join(_PKG_DIR, "librlk.so")
 RLK_OK = 0
 RLK_BF16, RLK_FP32 = 0, 1
 RLK_GEMM_FWD, RLK_GEMM_DA, RLK_GEMM_DB = 0, 1, 2
+RLK_GEMM_LINEAR_FWD, RLK_GEMM_LINEAR_DX, RLK_GEMM_LINEAR_DW, RLK_GEMM_FWD_ACCUM = 3, 4, 5, 6
 STATUS_NAMES = {0: "RLK_OK", 1: "RLK_ERR_NULL", 2: "RLK_ERR_SHAPE", 3: "RLK_ERR_DTYPE",
                 4: "RLK_ERR_ALIGN", 5: "RLK_ERR_WORKSPACE", 6: "RLK_ERR_UNSUPPORTED_DEVICE",
                 7: "RLK_ERR_CUDA", 8: "RLK_ERR_TIMEOUT"}
@@ -49,6 +50,7 @@ SIGNATURES = {
     "rlk_numerics_version": (_I, []),
     "rlk_device_check": (_I, []),
     "rlk_get_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
+    "rlk_selftest_bounded_wait": (_I, [ctypes.c_uint32, _P]),
     "rlk_vocab_split_policy": (_I, [_I64, ctypes.POINTER(_I64), ctypes.POINTER(_I64),
                                     ctypes.POINTER(_I64)]),
     "rlk_linear_logp_workspace_size": (_SZ, [_P, _I64, _I64, _I64, _P, _I64, _I64]),
@@ -63,6 +65,11 @@ SIGNATURES = {
     "rlk_det_gemm_fwd": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _I, _I64, _P, _SZ, _P]),
     "rlk_det_gemm_da": (_I, [_P, _I, _I64, _I64, _I64, _P, _I64, _I64, _P, _I, _I64, _P, _SZ, _P]),
     "rlk_det_gemm_db": (_I, [_P, _I64, _I64, _I64, _P, _I, _I64, _I64, _P, _I, _I64, _P, _SZ, _P]),
+    "rlk_det_gemm_fwd_accum_fp32": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _I64, _P, _SZ,
+                                         _P]),
+    "rlk_det_linear_fwd": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _I, _I64, _P, _SZ, _P]),
+    "rlk_det_linear_dx": (_I, [_P, _I, _I64, _I64, _I64, _P, _I64, _I64, _P, _I, _I64, _P, _SZ, _P]),
+    "rlk_det_linear_dw": (_I, [_P, _I, _I64, _I64, _I64, _P, _I64, _I64, _P, _I, _I64, _P, _SZ, _P]),
 }
 
 _LIB = None
@@ -304,3 +311,81 @@ def det_gemm_db(A: torch.Tensor, dC: torch.Tensor, out_dtype=torch.bfloat16, *, 
                                      _DT[out_dtype], N, _ptr(ws), n, _stream_ptr(stream)),
                "rlk_det_gemm_db")
     return dB
+
+
+def det_gemm_fwd_accum_fp32_(C: torch.Tensor, A: torch.Tensor, B: torch.Tensor, *, stream=None):
+    """In place: C (fp32 [M, N]) += A . B, the product formed as by det_gemm_fwd and
+    added to C once, after the full K reduction."""
+    _require_cuda(C, A, B)
+    if C.dtype != torch.float32:
+        raise TypeError("C must be float32")
+    A2, lda = _matrix(A, "A")
+    B2, ldb = _matrix(B, "B")
+    if C.dim() != 2 or C.stride(1) != 1:
+        raise ValueError("C must be a 2-D row-major tensor (it is updated in place)")
+    M, K = A2.shape
+    N = B2.size(1)
+    if B2.size(0) != K or tuple(C.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    ldc = C.stride(0) if M > 1 else N
+    with torch.cuda.device(A.device):
+        ws, n = _gemm_ws(RLK_GEMM_FWD_ACCUM, A2, RLK_BF16, lda, B2, RLK_BF16, ldb, A.device)
+        _check(lib().rlk_det_gemm_fwd_accum_fp32(_ptr(A2), M, K, lda, _ptr(B2), N, ldb, _ptr(C), ldc,
+                                                 _ptr(ws), n, _stream_ptr(stream)),
+               "rlk_det_gemm_fwd_accum_fp32")
+    return C
+
+
+def det_linear(X: torch.Tensor, W: torch.Tensor, out_dtype=torch.bfloat16, *, stream=None):
+    """Y = X . W^T with the weight stored [N, K]; X [..., K] bf16 (leading dims are rows)."""
+    _require_cuda(X, W)
+    lead = X.shape[:-1]
+    X2, ldx = _matrix(_flatten_rows(X), "X")
+    W2, ldw = _matrix(W, "W")
+    M, K = X2.shape
+    N = W2.size(0)
+    if W2.size(1) != K:
+        raise ValueError("W must be [N, K]")
+    Y = torch.empty(M, N, dtype=out_dtype, device=X.device)
+    with torch.cuda.device(X.device):
+        ws, n = _gemm_ws(RLK_GEMM_LINEAR_FWD, X2, RLK_BF16, ldx, W2, RLK_BF16, ldw, X.device)
+        _check(lib().rlk_det_linear_fwd(_ptr(X2), M, K, ldx, _ptr(W2), N, ldw, _ptr(Y), _DT[out_dtype],
+                                        N, _ptr(ws), n, _stream_ptr(stream)), "rlk_det_linear_fwd")
+    return Y.reshape(*lead, N)
+
+
+def det_linear_dx(dY: torch.Tensor, W: torch.Tensor, out_dtype=torch.bfloat16, *, stream=None):
+    """dX = dY . W for Y = X . W^T; dY [..., N] bf16 or fp32 (fp32 rounded to bf16 first)."""
+    _require_cuda(dY, W)
+    lead = dY.shape[:-1]
+    d2, lddy = _matrix(_flatten_rows(dY), "dY")
+    W2, ldw = _matrix(W, "W")
+    M, N = d2.shape
+    K = W2.size(1)
+    if W2.size(0) != N:
+        raise ValueError("W must be [N, K]")
+    dX = torch.empty(M, K, dtype=out_dtype, device=dY.device)
+    with torch.cuda.device(dY.device):
+        ws, n = _gemm_ws(RLK_GEMM_LINEAR_DX, d2, _DT[d2.dtype], lddy, W2, RLK_BF16, ldw, dY.device)
+        _check(lib().rlk_det_linear_dx(_ptr(d2), _DT[d2.dtype], M, N, lddy, _ptr(W2), K, ldw, _ptr(dX),
+                                       _DT[out_dtype], K, _ptr(ws), n, _stream_ptr(stream)),
+               "rlk_det_linear_dx")
+    return dX.reshape(*lead, K)
+
+
+def det_linear_dw(dY: torch.Tensor, X: torch.Tensor, out_dtype=torch.bfloat16, *, stream=None):
+    """dW [N, K] = dY^T . X summed over every row; dY [..., N] bf16 or fp32, X [..., K] bf16."""
+    _require_cuda(dY, X)
+    d2, lddy = _matrix(_flatten_rows(dY), "dY")
+    X2, ldx = _matrix(_flatten_rows(X), "X")
+    M, N = d2.shape
+    if X2.size(0) != M:
+        raise ValueError("dY and X disagree on the row count")
+    K = X2.size(1)
+    dW = torch.empty(N, K, dtype=out_dtype, device=dY.device)
+    with torch.cuda.device(dY.device):
+        ws, n = _gemm_ws(RLK_GEMM_LINEAR_DW, d2, _DT[d2.dtype], lddy, X2, RLK_BF16, ldx, dY.device)
+        _check(lib().rlk_det_linear_dw(_ptr(d2), _DT[d2.dtype], M, N, lddy, _ptr(X2), K, ldx, _ptr(dW),
+                                       _DT[out_dtype], K, _ptr(ws), n, _stream_ptr(stream)),
+               "rlk_det_linear_dw")
+    return dW

@@ -6,9 +6,12 @@
 #include <cuda_bf16.h>
 
 #include "rlk.h"
+#include "rlk_device.cuh"
 #include "rlk_internal.h"
 
 namespace rlk {
+
+__device__ unsigned int g_err_common = 0;
 
 namespace {
 
@@ -128,6 +131,31 @@ cudaError_t launch_cast_f32_bf16(const float* src, int64_t rows, int64_t cols, i
   return cudaGetLastError();
 }
 
+// One thread waits on a shared-memory mbarrier that nothing ever arrives on,
+// through the same bounded wait the tensor-core kernels use: the wait gives up
+// after timeout_ns, raises the error word and the kernel returns.
+__global__ void selftest_wait_kernel(uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    (void)mbar_wait(smem_u32(&bar), 0, &abort_flag, &g_err_common, timeout_ns);
+  }
+}
+
+uint32_t take_error_common() {
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err_common, sizeof v) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaMemcpyToSymbol(g_err_common, &zero, sizeof zero);
+  cudaGetLastError();
+  return v;
+}
+
 }  // namespace rlk
 
 // ====================================================================== C ABI
@@ -166,8 +194,18 @@ rlk_status rlk_get_device_error(void* stream, uint32_t* flags) {
     cudaGetLastError();
     return RLK_ERR_CUDA;
   }
-  *flags = rlk::take_error_linear_logp() | rlk::take_error_det_gemm();
+  *flags = rlk::take_error_linear_logp() | rlk::take_error_det_gemm() | rlk::take_error_common();
   return *flags ? RLK_ERR_TIMEOUT : RLK_OK;
+}
+
+rlk_status rlk_selftest_bounded_wait(uint32_t timeout_us, void* stream) {
+  if (timeout_us < 1 || timeout_us > 2000000u) return RLK_ERR_SHAPE;
+  rlk::DeviceInfo info;
+  rlk_status st = rlk::device_ready(&info);
+  if (st != RLK_OK) return st;
+  rlk::selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      (uint64_t)timeout_us * 1000u);
+  return cudaGetLastError() == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
 }
 
 rlk_status rlk_vocab_split_policy(int64_t V, int64_t* num_splits, int64_t* vtiles_per_split,

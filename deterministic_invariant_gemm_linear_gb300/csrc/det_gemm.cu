@@ -48,6 +48,7 @@ struct GemmOut {
   void* C;
   int64_t ldc;       // elements
   int fp32;          // 1: FP32 output, 0: BF16
+  int accum;         // 1: FP32 C += product (C read once, added after the full reduction)
   int vec_ok;        // 16-byte vector stores allowed (aligned base and pitch)
 };
 
@@ -56,7 +57,23 @@ __device__ __forceinline__ void store_chunk(const GemmOut& o, int row, int col0,
   const bool full = o.vec_ok && col0 + 32 <= o.N;
   if (o.fp32) {
     float* dst = static_cast<float*>(o.C) + (int64_t)row * o.ldc + col0;
-    if (full) {
+    if (o.accum) {
+      if (full) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float4 c = reinterpret_cast<const float4*>(dst)[i];
+          c.x = __fadd_rn(c.x, __uint_as_float(r[4 * i]));
+          c.y = __fadd_rn(c.y, __uint_as_float(r[4 * i + 1]));
+          c.z = __fadd_rn(c.z, __uint_as_float(r[4 * i + 2]));
+          c.w = __fadd_rn(c.w, __uint_as_float(r[4 * i + 3]));
+          reinterpret_cast<float4*>(dst)[i] = c;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (col0 + i < o.N) dst[i] = __fadd_rn(dst[i], __uint_as_float(r[i]));
+      }
+    } else if (full) {
 #pragma unroll
       for (int i = 0; i < 8; ++i)
         reinterpret_cast<uint4*>(dst)[i] = make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
@@ -207,11 +224,13 @@ rlk_status materialise(Operand& o, uint8_t* ws, cudaStream_t s, const void** out
 enum class Kind { kFwd, kDa, kDb };
 
 // Shared driver: x and y are the op's two inputs in argument order; the output
-// is out_rows x out_cols, reduced over `red`.
+// is out_rows x out_cols, reduced over `red`.  The kind fixes how each operand
+// is read: kFwd (x K-major, y MN-major), kDa (both K-major), kDb (both MN-major).
 rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t out_cols,
                     int64_t red, void* C, int c_dtype, int64_t ldc, void* workspace,
-                    size_t workspace_bytes, void* stream) {
+                    size_t workspace_bytes, void* stream, bool accum = false) {
   if (!dtype_ok(c_dtype)) return RLK_ERR_DTYPE;
+  if (accum && c_dtype != RLK_FP32) return RLK_ERR_DTYPE;
   if (ldc < out_cols || ldc >= kLdLimit) return RLK_ERR_SHAPE;
   const int64_t num_mb = ceil_div(out_rows, kBM), num_nb = ceil_div(out_cols, kBN);
   if (num_mb * num_nb >= kDimLimit) return RLK_ERR_SHAPE;
@@ -230,6 +249,7 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
   rlk_status st = device_ready(&dev);
   if (st != RLK_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (red == 0 && accum) return RLK_OK;   // C += 0
   if (red == 0) {   // empty reduction (dB with M == 0): the product is all zeros
     const size_t es = esize(c_dtype);
     if (cudaMemset2DAsync(C, ldc * es, 0, out_cols * es, out_rows, s) != cudaSuccess) {
@@ -273,6 +293,7 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
   o.C = C;
   o.ldc = ldc;
   o.fp32 = c_dtype == RLK_FP32;
+  o.accum = accum ? 1 : 0;
   o.vec_ok = ptr_aligned(C, 16) && ((ldc * esize(c_dtype)) % 16) == 0;
   const int64_t units = num_mb * num_nb;
   const int grid = (int)(units < dev.sm_count ? units : dev.sm_count);
@@ -308,8 +329,10 @@ size_t rlk_det_gemm_workspace_size(int op, const void* x, int x_dtype, int64_t x
                                    int64_t y_rows, int64_t y_cols, int64_t ldy) {
   Operand a{x, x_dtype, x_rows, x_cols, ldx};
   Operand b{y, y_dtype, y_rows, y_cols, ldy};
-  const bool fp32_x = op == RLK_GEMM_DA, fp32_y = op == RLK_GEMM_DB;
-  if (op < RLK_GEMM_FWD || op > RLK_GEMM_DB) return 0;
+  // which input may be an FP32 gradient (rounded to BF16 in the workspace)
+  const bool fp32_x = op == RLK_GEMM_DA || op == RLK_GEMM_LINEAR_DX || op == RLK_GEMM_LINEAR_DW;
+  const bool fp32_y = op == RLK_GEMM_DB;
+  if (op < RLK_GEMM_FWD || op > RLK_GEMM_FWD_ACCUM) return 0;
   if (check_operand(a, fp32_x) != RLK_OK || check_operand(b, fp32_y) != RLK_OK) return 0;
   size_t off = 0;
   plan_operand(a, off);
@@ -348,6 +371,53 @@ rlk_status rlk_det_gemm_db(const void* A, int64_t M, int64_t K, int64_t lda, con
   rlk_status st;
   if ((st = check_operand(a, false)) != RLK_OK || (st = check_operand(b, true)) != RLK_OK) return st;
   return run_gemm(Kind::kDb, a, b, K, N, M, dB, out_dtype, lddb, workspace, workspace_bytes,
+                  stream);
+}
+
+rlk_status rlk_det_gemm_fwd_accum_fp32(const void* A, int64_t M, int64_t K, int64_t lda,
+                                      const void* B, int64_t N, int64_t ldb, float* C,
+                                      int64_t ldc, void* workspace, size_t workspace_bytes,
+                                      void* stream) {
+  Operand a{A, RLK_BF16, M, K, lda};
+  Operand b{B, RLK_BF16, K, N, ldb};
+  rlk_status st;
+  if ((st = check_operand(a, false)) != RLK_OK || (st = check_operand(b, false)) != RLK_OK) return st;
+  return run_gemm(Kind::kFwd, a, b, M, N, K, C, RLK_FP32, ldc, workspace, workspace_bytes, stream,
+                  /*accum=*/true);
+}
+
+rlk_status rlk_det_linear_fwd(const void* X, int64_t M, int64_t K, int64_t ldx, const void* W,
+                              int64_t N, int64_t ldw, void* Y, int y_dtype, int64_t ldy,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  Operand a{X, RLK_BF16, M, K, ldx};
+  Operand b{W, RLK_BF16, N, K, ldw};
+  rlk_status st;
+  if ((st = check_operand(a, false)) != RLK_OK || (st = check_operand(b, false)) != RLK_OK) return st;
+  // X [M,K] and W [N,K] are both reduction-contiguous: the dA configuration.
+  return run_gemm(Kind::kDa, a, b, M, N, K, Y, y_dtype, ldy, workspace, workspace_bytes, stream);
+}
+
+rlk_status rlk_det_linear_dx(const void* dY, int dy_dtype, int64_t M, int64_t N, int64_t lddy,
+                             const void* W, int64_t K, int64_t ldw, void* dX, int out_dtype,
+                             int64_t lddx, void* workspace, size_t workspace_bytes, void* stream) {
+  Operand a{dY, dy_dtype, M, N, lddy};
+  Operand b{W, RLK_BF16, N, K, ldw};
+  rlk_status st;
+  if ((st = check_operand(a, true)) != RLK_OK || (st = check_operand(b, false)) != RLK_OK) return st;
+  // dX [M,K] = dY [M,N] . W [N,K]: the forward configuration with W as the right operand.
+  return run_gemm(Kind::kFwd, a, b, M, K, N, dX, out_dtype, lddx, workspace, workspace_bytes,
+                  stream);
+}
+
+rlk_status rlk_det_linear_dw(const void* dY, int dy_dtype, int64_t M, int64_t N, int64_t lddy,
+                             const void* X, int64_t K, int64_t ldx, void* dW, int out_dtype,
+                             int64_t lddw, void* workspace, size_t workspace_bytes, void* stream) {
+  Operand a{dY, dy_dtype, M, N, lddy};
+  Operand b{X, RLK_BF16, M, K, ldx};
+  rlk_status st;
+  if ((st = check_operand(a, true)) != RLK_OK || (st = check_operand(b, false)) != RLK_OK) return st;
+  // dW [N,K] = dY^T . X: the dB configuration with the gradient as the left operand.
+  return run_gemm(Kind::kDb, a, b, N, K, M, dW, out_dtype, lddw, workspace, workspace_bytes,
                   stream);
 }
 

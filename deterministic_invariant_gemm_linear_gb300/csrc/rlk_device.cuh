@@ -80,19 +80,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Waits for the phase of parity `parity` to complete.  Returns false when the
 // CTA is winding down (abort flag set by another role) or when this wait ran
-// past kWaitTimeoutNs; in the latter case it sets the abort flag and ORs
+// past timeout_ns (kWaitTimeoutNs unless given); in the latter case it sets the abort flag and ORs
 // kDevErrTimeout into *err.  Every wait ends: either the phase completes, the
 // abort flag is seen, or the time limit passes (with a hard cap on polls as a
 // second bound).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned int* err) {
+                                          unsigned int* err,
+                                          uint64_t timeout_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((n & 31u) == 0u) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs || n > (1u << 30)) {
+      if (globaltimer_ns() - t0 > timeout_ns || n > (1u << 30)) {
         *abort_flag = 1;
         atomicOr(err, kDevErrTimeout);
         return false;

@@ -52,5 +52,6 @@ constexpr int64_t kMaxVocabSplits = 1024;
 // Per-translation-unit device error words: read-and-clear after a stream sync.
 uint32_t take_error_linear_logp();
 uint32_t take_error_det_gemm();
+uint32_t take_error_common();
 
 }  // namespace rlk

@@ -104,6 +104,17 @@ RLK_API rlk_status rlk_device_check(void);
  */
 RLK_API rlk_status rlk_get_device_error(void* stream, uint32_t* flags);
 
+/*
+ * Diagnostic for the kernels' bounded waits.  Launches one CTA whose thread
+ * waits on a shared-memory mbarrier that nothing ever completes, through the
+ * same bounded-wait routine every tensor-core kernel uses, with a limit of
+ * timeout_us microseconds (1 .. 2,000,000).  The wait gives up, raises
+ * RLK_DEVERR_TIMEOUT in the device error word and the kernel returns, leaving
+ * the CUDA context usable; rlk_get_device_error then reports RLK_ERR_TIMEOUT.
+ * Returns RLK_ERR_SHAPE for a limit out of range.
+ */
+RLK_API rlk_status rlk_selftest_bounded_wait(uint32_t timeout_us, void* stream);
+
 /* ===================================================================== *
  *  Fused linear log-probability                                  [P3]  *
  * ===================================================================== */
@@ -237,6 +248,10 @@ RLK_API rlk_status rlk_linear_logp_noalloc(const void* hidden, int64_t N, int64_
 #define RLK_GEMM_FWD 0
 #define RLK_GEMM_DA 1
 #define RLK_GEMM_DB 2
+#define RLK_GEMM_LINEAR_FWD 3
+#define RLK_GEMM_LINEAR_DX 4
+#define RLK_GEMM_LINEAR_DW 5
+#define RLK_GEMM_FWD_ACCUM 6
 
 /*
  * Workspace bytes the given op needs for exactly these inputs: padded copies
@@ -245,6 +260,10 @@ RLK_API rlk_status rlk_linear_logp_noalloc(const void* hidden, int64_t N, int64_
  *   RLK_GEMM_FWD: x = A [M, K] (BF16),       y = B [K, N] (BF16)
  *   RLK_GEMM_DA:  x = dC [M, N] (x_dtype),   y = B [K, N] (BF16)
  *   RLK_GEMM_DB:  x = A [M, K] (BF16),       y = dC [M, N] (y_dtype)
+ *   RLK_GEMM_LINEAR_FWD: x = X [M, K] (BF16),  y = W [N, K] (BF16)
+ *   RLK_GEMM_LINEAR_DX:  x = dY [M, N] (x_dtype), y = W [N, K] (BF16)
+ *   RLK_GEMM_LINEAR_DW:  x = dY [M, N] (x_dtype), y = X [M, K] (BF16)
+ *   RLK_GEMM_FWD_ACCUM:  as RLK_GEMM_FWD
  * Returns 0 when nothing needs staging or the arguments are invalid.
  */
 RLK_API size_t rlk_det_gemm_workspace_size(int op,
@@ -284,6 +303,44 @@ RLK_API rlk_status rlk_det_gemm_db(const void* A, int64_t M, int64_t K, int64_t 
                            const void* dC, int dc_dtype, int64_t N, int64_t lddc,
                            void* dB, int out_dtype, int64_t lddb,
                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * C[M, N] += A[M, K] . B[K, N] with C in FP32 — the accumulate-into-FP32 forward
+ * [P1 Implementation: forward_accum_fp32].  Reading taken: the product is formed
+ * exactly as by rlk_det_gemm_fwd (same tiles, same ascending K order) and the
+ * existing C is added to it once, in FP32 round-to-nearest, after the full K sum;
+ * so the result equals C + rlk_det_gemm_fwd(..., RLK_FP32) evaluated in FP32.
+ * C must not alias A or B.  K == 0 leaves C unchanged.
+ */
+RLK_API rlk_status rlk_det_gemm_fwd_accum_fp32(const void* A, int64_t M, int64_t K, int64_t lda,
+                                              const void* B, int64_t N, int64_t ldb, float* C,
+                                              int64_t ldc, void* workspace, size_t workspace_bytes,
+                                              void* stream);
+
+/*
+ * The linear layout, weight stored [N, K] as in a linear layer
+ * [P1 Implementation: transposed-RHS forward, linear(A, weight[N, K]), canonical
+ * transposed dB for [N, K] weight gradients]:
+ *   rlk_det_linear_fwd:  Y[M, N]  = X[M, K] . W[N, K]^T     (W's transpose never formed)
+ *   rlk_det_linear_dx:   dX[M, K] = dY[M, N] . W[N, K]
+ *   rlk_det_linear_dw:   dW[N, K] = dY[M, N]^T . X[M, K]    (ascending over all M rows)
+ * dY may be BF16 or FP32; an FP32 dY (the gradient of an FP32-output forward) is
+ * rounded to BF16 first [P1 review comment].  Same tile shape, reduction order,
+ * output dtypes, staging and error rules as the three products above; rows of Y
+ * and dX are bitwise independent of the other rows in the call.
+ */
+RLK_API rlk_status rlk_det_linear_fwd(const void* X, int64_t M, int64_t K, int64_t ldx,
+                                     const void* W, int64_t N, int64_t ldw, void* Y, int y_dtype,
+                                     int64_t ldy, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+RLK_API rlk_status rlk_det_linear_dx(const void* dY, int dy_dtype, int64_t M, int64_t N,
+                                    int64_t lddy, const void* W, int64_t K, int64_t ldw, void* dX,
+                                    int out_dtype, int64_t lddx, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+RLK_API rlk_status rlk_det_linear_dw(const void* dY, int dy_dtype, int64_t M, int64_t N,
+                                    int64_t lddy, const void* X, int64_t K, int64_t ldx, void* dW,
+                                    int out_dtype, int64_t lddw, void* workspace,
+                                    size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }
