@@ -61,6 +61,9 @@ SIGNATURES = {
     "rlk_linear_logp_combine": (_I, [_I64, _I64, _P, _I64, _P, _P, _P, _P, _SZ, _P]),
     "rlk_linear_logp_noalloc": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _P, _I64,
                                      _P, _P, _P, _P]),
+    "rlk_linear_logp_backward_workspace_size": (_SZ, [_I64, _I64]),
+    "rlk_linear_logp_backward": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _P, _I64, _P, _P,
+                                      _P, _I, _I64, _P, _I, _I64, _P, _P, _SZ, _P]),
     "rlk_det_gemm_workspace_size": (_SZ, [_I, _P, _I, _I64, _I64, _I64, _P, _I, _I64, _I64, _I64]),
     "rlk_det_gemm_fwd": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _I, _I64, _P, _SZ, _P]),
     "rlk_det_gemm_da": (_I, [_P, _I, _I64, _I64, _I64, _P, _I64, _I64, _P, _I, _I64, _P, _SZ, _P]),
@@ -245,6 +248,50 @@ class LinearLogpCall:
             _ptr(self.t), self.tstride, _ptr(self.logp), _ptr(self.lse), _ptr(self.zt),
             _ptr(self.ws), self.ws.numel(), _stream_ptr(stream)), "rlk_linear_logp")
         return self.logp, self.lse
+
+
+def linear_logp_backward(hidden: torch.Tensor, weight: torch.Tensor, target: torch.Tensor,
+                         lse: torch.Tensor, grad_logp: torch.Tensor, bias: torch.Tensor | None = None,
+                         *, grad_hidden: bool = True, grad_weight: bool = True,
+                         grad_bias: bool | None = None, out_dtype=torch.bfloat16,
+                         return_grad_logits: bool = False, stream=None):
+    """(grad_hidden [..., H], grad_weight [V, H], grad_bias [V] | None) for logp = linear_logp(...).
+
+    lse is the forward's lse; grad_logp is dL/dlogp (same leading shape as hidden's rows).
+    With return_grad_logits, also returns G = dL/dz as the BF16 [N, V] view the kernels used.
+    """
+    _require_cuda(hidden, weight, target, lse, grad_logp, bias)
+    lead = hidden.shape[:-1]
+    H = hidden.size(-1)
+    h2, ldh = _matrix(hidden.reshape(-1, H), "hidden")
+    w2, ldw = _matrix(weight, "weight")
+    N, V = h2.size(0), w2.size(0)
+    t1 = target.reshape(-1)
+    tstride = t1.stride(0) if N > 1 else 1
+    l1 = lse.reshape(-1).contiguous().float()
+    g1 = grad_logp.reshape(-1).contiguous().float()
+    if bias is not None:
+        bias = bias.contiguous()
+    if grad_bias is None:
+        grad_bias = bias is not None
+    dev = hidden.device
+    gh = torch.empty(N, H, dtype=out_dtype, device=dev) if grad_hidden else None
+    gw = torch.empty(V, H, dtype=out_dtype, device=dev) if grad_weight else None
+    gb = torch.empty(V, dtype=torch.float32, device=dev) if grad_bias else None
+    with torch.cuda.device(dev):
+        n = lib().rlk_linear_logp_backward_workspace_size(N, V)
+        ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+        dt = _DT[out_dtype]
+        _check(lib().rlk_linear_logp_backward(
+            _ptr(h2), N, H, ldh, _ptr(w2), V, ldw, _ptr(bias), _ptr(t1), tstride, _ptr(l1), _ptr(g1),
+            _ptr(gh), dt, H, _ptr(gw), dt, H, _ptr(gb), _ptr(ws), n, _stream_ptr(stream)),
+            "rlk_linear_logp_backward")
+    out = (None if gh is None else gh.reshape(*lead, H), gw, gb)
+    if return_grad_logits:
+        ldG = -(-V // 8) * 8
+        G = ws[:N * ldG * 2].view(torch.bfloat16).view(N, ldG)[:, :V]
+        out = out + (G,)
+    return out
 
 
 # ------------------------------------------------------------------ det_gemm

@@ -194,7 +194,8 @@ rlk_status rlk_get_device_error(void* stream, uint32_t* flags) {
     cudaGetLastError();
     return RLK_ERR_CUDA;
   }
-  *flags = rlk::take_error_linear_logp() | rlk::take_error_det_gemm() | rlk::take_error_common();
+  *flags = rlk::take_error_linear_logp() | rlk::take_error_det_gemm() | rlk::take_error_common() |
+           rlk::take_error_linear_logp_bwd();
   return *flags ? RLK_ERR_TIMEOUT : RLK_OK;
 }
 

@@ -1,0 +1,295 @@
+// Backward of the fused linear log-probability on sm_103a.
+//
+// Forward ("feat(linear-logp): add batch-invariant fused SM90 operator",
+// Walkthrough): logp[r] = z[r, t_r] - lse[r], z = hidden . W^T (+ bias).  That
+// page fails closed on backward ("outside the first contract"); this is the
+// next step of the same path.  With an upstream gradient g[r] = dL/dlogp[r]:
+//   G[r, v]        = dL/dz[r, v] = g[r] * ([v == t_r] - exp(z[r, v] - lse[r]))
+//   grad_hidden    = G . W           (reduction over V in ascending order)
+//   grad_weight    = G^T . hidden    (reduction over the N rows in ascending order)
+//   grad_bias[v]   = sum_r G[r, v]   (ascending r)
+//
+// Stage 1 (linear_logp_grad_kernel): the same tcgen05 main loop as the forward
+// recomputes each 128 x 256 logit tile; the epilogue forms G in FP32 from the
+// forward's lse and rounds it to BF16 (nearest even) into the workspace.  Rows
+// are independent, so a row's G (hence its grad_hidden row) does not depend on
+// the other rows in the call.
+// Stage 2: grad_hidden and grad_weight are the deterministic GEMMs
+// (rlk_det_gemm_fwd and rlk_det_gemm_db) on that BF16 G; grad_bias is a
+// column sum of G in ascending row order.
+#include <math.h>
+
+#include <mutex>
+
+#include <cuda_bf16.h>
+
+#include "rlk.h"
+#include "rlk_internal.h"
+#include "rlk_pipeline.cuh"
+
+namespace rlk {
+
+__device__ unsigned int g_err_linear_logp_bwd = 0;
+
+namespace {
+
+struct GradSched {
+  int num_rb;      // 128-row blocks
+  int vtiles;      // 256-id vocabulary tiles
+  int nkb;         // 64-wide blocks of H
+  __device__ __forceinline__ int num_units() const { return num_rb * vtiles; }
+  __device__ __forceinline__ int unit_tiles(int) const { return 1; }
+  __device__ __forceinline__ void tile_coords(int u, int, int& a0, int& b0) const {
+    const int vt = u / num_rb;
+    a0 = (u - vt * num_rb) * kBM;
+    b0 = vt * kBN;
+  }
+};
+
+struct GradArgs {
+  int N, V;
+  int64_t tstride;
+  const float* bias;
+  const int64_t* target;
+  const float* lse;
+  const float* grad;
+  uint16_t* G;          // [N, ldG] BF16
+  int64_t ldG;          // multiple of 8 elements
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    linear_logp_grad_kernel(const __grid_constant__ CUtensorMap tm_hidden,
+                            const __grid_constant__ CUtensorMap tm_weight, GradSched sc,
+                            GradArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const PipeSmem ps = pipe_smem(smem_raw);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tm_hidden);
+    tma_prefetch_desc(&tm_weight);
+  }
+  const uint32_t tmem = pipe_setup(ps);
+  using TA = OperandTile<false, kBM>;
+  using TB = OperandTile<false, kBN>;
+
+  if (warp == 0) {
+    if (lane == 0) producer_role<TA, TB>(&tm_hidden, &tm_weight, sc, ps, &g_err_linear_logp_bwd);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0)
+      mma_role<TA, TB>(sc, ps, tmem, idesc_bf16_f32(kBM, kBN, false, false), &g_err_linear_logp_bwd);
+    __syncwarp();
+  } else {
+    const int q = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const int units = sc.num_units();
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      if (!epilogue_acquire(ps, acc, acc_phase, &g_err_linear_logp_bwd)) break;
+      int r0, v0;
+      sc.tile_coords(u, 0, r0, v0);
+      const int row = r0 + q * 32 + lane;
+      const bool valid = row < a.N;
+      int64_t t = -1;
+      float g = 0.f, L = 0.f;
+      if (valid) {
+        t = __ldg(a.target + (int64_t)row * a.tstride);
+        g = __ldg(a.grad + row);
+        L = __ldg(a.lse + row);
+      }
+      // A row whose target is outside [0, V) has no log-probability: zero gradient.
+      const bool live = valid && t >= 0 && t < a.V;
+      const uint32_t taddr = tmem + acc * kAccCols + lane_off;
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        const int vbase = v0 + c * 32;
+        if (vbase >= a.V) break;                 // uniform: depends on the tile only
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(taddr + c * 32, r);
+        tmem_wait_ld();
+        float G[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int v = vbase + i;
+          float z = __uint_as_float(r[i]);
+          if (a.bias != nullptr && v < a.V) z = __fadd_rn(z, __ldg(a.bias + v));
+          const float p = ex2_approx(__fmul_rn(__fsub_rn(z, L), kLog2e));
+          const float onehot = (int64_t)v == t ? 1.f : 0.f;
+          G[i] = (live && v < a.V) ? __fmul_rn(g, __fsub_rn(onehot, p)) : 0.f;
+        }
+        if (valid) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            __nv_bfloat162 b = __floats2bfloat162_rn(G[2 * i], G[2 * i + 1]);
+            pk[i] = *reinterpret_cast<uint32_t*>(&b);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(a.G + (int64_t)row * a.ldG + vbase);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)   // 8 columns per store; groups past V stay within ldG
+            if (vbase + 8 * k < a.V)
+              dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        }
+      }
+      epilogue_release(ps, acc);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+  pipe_teardown(tmem);
+}
+
+// grad_bias[v] = sum over rows r = 0..N-1 (ascending) of G[r, v], two columns per thread.
+__global__ void __launch_bounds__(256)
+    column_sum_bf16_kernel(const uint16_t* __restrict__ G, int N, int V, int64_t ldG,
+                           float* __restrict__ out) {
+  const int v = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (v >= V) return;
+  float s0 = 0.f, s1 = 0.f;
+  const uint32_t* p = reinterpret_cast<const uint32_t*>(G + v);
+  const int64_t step = ldG / 2;
+#pragma unroll 8
+  for (int r = 0; r < N; ++r) {
+    const uint32_t w = __ldg(p + (int64_t)r * step);
+    s0 = __fadd_rn(s0, __uint_as_float(w << 16));
+    s1 = __fadd_rn(s1, __uint_as_float(w & 0xffff0000u));
+  }
+  out[v] = s0;
+  if (v + 1 < V) out[v + 1] = s1;
+}
+
+std::mutex g_attr_mutex;
+bool g_attr_set[64];
+
+cudaError_t ensure_attrs(int dev) {
+  std::lock_guard<std::mutex> lock(g_attr_mutex);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!g_attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(linear_logp_grad_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    g_attr_set[dev] = true;
+  }
+  return cudaSuccess;
+}
+
+inline int64_t grad_ld(int64_t V) { return ceil_div(V, 8) * 8; }
+
+}  // namespace
+
+uint32_t take_error_linear_logp_bwd() {
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err_linear_logp_bwd, sizeof v) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaMemcpyToSymbol(g_err_linear_logp_bwd, &zero, sizeof zero);
+  cudaGetLastError();
+  return v;
+}
+
+}  // namespace rlk
+
+using namespace rlk;
+
+extern "C" {
+
+size_t rlk_linear_logp_backward_workspace_size(int64_t N, int64_t V) {
+  if (N < 0 || N >= (int64_t(1) << 31) || V < 1 || V >= (int64_t(1) << 31)) return 0;
+  return align_up((size_t)N * grad_ld(V) * 2, 256);
+}
+
+rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
+                                    const void* weight, int64_t V, int64_t ld_weight,
+                                    const float* bias, const int64_t* target,
+                                    int64_t target_stride, const float* lse, const float* grad_logp,
+                                    void* grad_hidden, int grad_hidden_dtype,
+                                    int64_t ld_grad_hidden, void* grad_weight,
+                                    int grad_weight_dtype, int64_t ld_grad_weight, float* grad_bias,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  if (N < 0 || N >= (int64_t(1) << 31) || H < 1 || H >= (int64_t(1) << 20) || V < 1 ||
+      V >= (int64_t(1) << 31) || ld_hidden < H || ld_weight < H || target_stride < 0 ||
+      ld_hidden >= (int64_t(1) << 36) || ld_weight >= (int64_t(1) << 36))
+    return RLK_ERR_SHAPE;
+  if (grad_hidden && ld_grad_hidden < H) return RLK_ERR_SHAPE;
+  if (grad_weight && ld_grad_weight < H) return RLK_ERR_SHAPE;
+  if ((grad_hidden && grad_hidden_dtype != RLK_BF16 && grad_hidden_dtype != RLK_FP32) ||
+      (grad_weight && grad_weight_dtype != RLK_BF16 && grad_weight_dtype != RLK_FP32))
+    return RLK_ERR_DTYPE;
+  const size_t need = rlk_linear_logp_backward_workspace_size(N, V);
+  if (N == 0) {
+    // No rows: grad_hidden is empty; grad_weight and grad_bias are the empty sums.
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!grad_weight && !grad_bias) return RLK_OK;
+    DeviceInfo dev;
+    rlk_status st = device_ready(&dev);
+    if (st != RLK_OK) return st;
+    if (grad_weight) {
+      const size_t es = grad_weight_dtype == RLK_FP32 ? 4 : 2;
+      if (cudaMemset2DAsync(grad_weight, ld_grad_weight * es, 0, H * es, V, s) != cudaSuccess)
+        return RLK_ERR_CUDA;
+    }
+    if (grad_bias && cudaMemsetAsync(grad_bias, 0, V * sizeof(float), s) != cudaSuccess)
+      return RLK_ERR_CUDA;
+    return RLK_OK;
+  }
+  if (!hidden || !weight || !target || !lse || !grad_logp) return RLK_ERR_NULL;
+  if (!tma_ready(hidden, ld_hidden) || !tma_ready(weight, ld_weight)) return RLK_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(target) & 7u) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(grad_logp) & 3u) || (reinterpret_cast<uintptr_t>(bias) & 3u) ||
+      (reinterpret_cast<uintptr_t>(grad_bias) & 3u))
+    return RLK_ERR_ALIGN;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return RLK_ERR_WORKSPACE;
+  DeviceInfo dev;
+  rlk_status st = device_ready(&dev);
+  if (st != RLK_OK) return st;
+  if (ensure_attrs(dev.device) != cudaSuccess) return RLK_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  CUtensorMap tm_h, tm_w;
+  if (!encode_bf16_2d(&tm_h, hidden, H, N, ld_hidden, kBK, kBM) ||
+      !encode_bf16_2d(&tm_w, weight, H, V, ld_weight, kBK, kBN))
+    return RLK_ERR_CUDA;
+  GradSched sc;
+  sc.num_rb = (int)ceil_div(N, kBM);
+  sc.vtiles = (int)ceil_div(V, kBN);
+  sc.nkb = (int)ceil_div(H, kBK);
+  if ((int64_t)sc.num_rb * sc.vtiles >= (int64_t(1) << 31)) return RLK_ERR_SHAPE;
+  GradArgs a;
+  a.N = (int)N;
+  a.V = (int)V;
+  a.tstride = target_stride;
+  a.bias = bias;
+  a.target = target;
+  a.lse = lse;
+  a.grad = grad_logp;
+  a.G = static_cast<uint16_t*>(workspace);
+  a.ldG = grad_ld(V);
+  const int64_t units = (int64_t)sc.num_rb * sc.vtiles;
+  const int grid = (int)(units < dev.sm_count ? units : dev.sm_count);
+  linear_logp_grad_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_h, tm_w, sc, a);
+  if (cudaGetLastError() != cudaSuccess) return RLK_ERR_CUDA;
+
+  if (grad_hidden) {   // [N, H] = G [N, V] . W [V, H]
+    st = rlk_det_gemm_fwd(a.G, N, V, a.ldG, weight, H, ld_weight, grad_hidden, grad_hidden_dtype,
+                          ld_grad_hidden, nullptr, 0, stream);
+    if (st != RLK_OK) return st;
+  }
+  if (grad_weight) {   // [V, H] = G^T . hidden
+    st = rlk_det_gemm_db(a.G, N, V, a.ldG, hidden, RLK_BF16, H, ld_hidden, grad_weight,
+                         grad_weight_dtype, ld_grad_weight, nullptr, 0, stream);
+    if (st != RLK_OK) return st;
+  }
+  if (grad_bias) {
+    const int threads = 256;
+    const int grid_b = (int)ceil_div(ceil_div(V, 2), threads);
+    column_sum_bf16_kernel<<<grid_b, threads, 0, s>>>(a.G, (int)N, (int)V, a.ldG, grad_bias);
+    if (cudaGetLastError() != cudaSuccess) return RLK_ERR_CUDA;
+  }
+  return RLK_OK;
+}
+
+}  // extern "C"

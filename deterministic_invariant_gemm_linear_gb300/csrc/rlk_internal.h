@@ -53,5 +53,6 @@ constexpr int64_t kMaxVocabSplits = 1024;
 uint32_t take_error_linear_logp();
 uint32_t take_error_det_gemm();
 uint32_t take_error_common();
+uint32_t take_error_linear_logp_bwd();
 
 }  // namespace rlk

@@ -228,6 +228,48 @@ RLK_API rlk_status rlk_linear_logp_noalloc(const void* hidden, int64_t N, int64_
                                            float* logp, float* lse, float* target_logit,
                                            void* stream);
 
+/*
+ * Backward of rlk_linear_logp for an upstream gradient g = dL/dlogp [N].
+ * The page fails closed on backward ("outside the first contract", [P3] author
+ * notes); this is that next step.  With z = hidden . W^T (+ bias):
+ *   G[r, v]       = g[r] * ([v == target[r]] - exp(z[r, v] - lse[r]))   (= dL/dz)
+ *   grad_hidden   = G . W             [N, H]   (ascending over V)
+ *   grad_weight   = G^T . hidden      [V, H]   (ascending over the N rows)
+ *   grad_bias[v]  = sum_r G[r, v]     [V]      (ascending over the N rows)
+ * G is formed in FP32 from the recomputed logits and the forward's lse, then
+ * rounded to BF16 (nearest even); the three reductions run on that BF16 G with
+ * FP32 accumulation (the products are rlk_det_gemm_fwd and rlk_det_gemm_db).
+ * A row whose target is outside [0, V) contributes zero gradient.
+ *
+ *  hidden, weight, bias, target, target_stride  as for rlk_linear_logp; hidden
+ *                and weight must be 16-byte aligned with a pitch that is a
+ *                multiple of 8 elements (else RLK_ERR_ALIGN)
+ *  lse           FP32 [N], the forward's lse for these inputs
+ *  grad_logp     FP32 [N]
+ *  grad_hidden   [N, H] in grad_hidden_dtype (RLK_BF16 / RLK_FP32), pitch
+ *                ld_grad_hidden; NULL to skip
+ *  grad_weight   [V, H] in grad_weight_dtype, pitch ld_grad_weight; NULL to skip
+ *  grad_bias     FP32 [V] or NULL to skip
+ *  workspace     >= rlk_linear_logp_backward_workspace_size(N, V) bytes, 256-byte
+ *                aligned.  After the call its first N * 8*ceil(V/8) * 2 bytes hold
+ *                G as BF16 [N, 8*ceil(V/8)] (row pitch 8*ceil(V/8)).
+ * Determinism: every output is bitwise reproducible; a grad_hidden row depends
+ * only on its own row's inputs (batch invariant), while grad_weight and
+ * grad_bias sum over the rows of the call.  N == 0 writes zeros to grad_weight
+ * and grad_bias.
+ */
+RLK_API size_t rlk_linear_logp_backward_workspace_size(int64_t N, int64_t V);
+RLK_API rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H,
+                                            int64_t ld_hidden, const void* weight, int64_t V,
+                                            int64_t ld_weight, const float* bias,
+                                            const int64_t* target, int64_t target_stride,
+                                            const float* lse, const float* grad_logp,
+                                            void* grad_hidden, int grad_hidden_dtype,
+                                            int64_t ld_grad_hidden, void* grad_weight,
+                                            int grad_weight_dtype, int64_t ld_grad_weight,
+                                            float* grad_bias, void* workspace,
+                                            size_t workspace_bytes, void* stream);
+
 /* ===================================================================== *
  *  Deterministic GEMM family                                      [P1]  *
  * ===================================================================== */

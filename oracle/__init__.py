@@ -65,6 +65,9 @@ def _bind(lib):
     lib.oracle_linear_logp.argtypes = [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _P, _I64,
                                        _P, _I64, _P, _P, _P, ctypes.c_int]
     lib.oracle_linear_logp.restype = ctypes.c_int
+    lib.oracle_linear_logp_grad_logits.argtypes = [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _P,
+                                                   _I64, _P, _P, ctypes.c_int]
+    lib.oracle_linear_logp_grad_logits.restype = ctypes.c_int
     lib.oracle_logits.argtypes = [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _P]
     lib.oracle_logits.restype = None
     for name in ("oracle_gemm_fwd", "oracle_gemm_da", "oracle_gemm_db"):
@@ -155,6 +158,34 @@ class Oracle:
         if rc != 0:
             raise MemoryError("oracle scratch allocation failed")
         return logp, lse, zt
+
+    # -- backward of linear log-probability --------------------------------
+    def grad_logits(self, hidden, weight, target, grad, bias=None, threads: int = 0,
+                    target_stride: int = 1) -> np.ndarray:
+        """G = dL/dz [N, V] for L = sum_r grad[r] * logp[r] (small cases)."""
+        hidden, weight = self._u16(hidden), self._u16(weight)
+        N, H = hidden.shape
+        V = weight.shape[0]
+        target = np.ascontiguousarray(target, dtype=np.int64)
+        g = np.ascontiguousarray(grad, dtype=np.float64)
+        b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+        G = np.empty((N, V), np.float64)
+        rc = self.lib.oracle_linear_logp_grad_logits(
+            self._ptr(hidden), N, H, H, self._ptr(weight), V, H, self._ptr(b), self._ptr(target),
+            target_stride, self._ptr(g), self._ptr(G), threads)
+        if rc != 0:
+            raise MemoryError("oracle scratch allocation failed")
+        return G
+
+    def linear_logp_backward(self, hidden, weight, target, grad, bias=None, threads: int = 0):
+        """(grad_hidden [N,H], grad_weight [V,H], grad_bias [V], G [N,V]) in float64.
+
+        G from grad_logits (the definition); the three reductions of G are library
+        float64 matrix products / sums (numpy) over the decoded BF16 inputs."""
+        G = self.grad_logits(hidden, weight, target, grad, bias, threads)
+        hd = self.bf16_to_f64(hidden)
+        wd = self.bf16_to_f64(weight)
+        return G @ wd, G.T @ hd, G.sum(axis=0), G
 
     # -- deterministic GEMM family ----------------------------------------
     def gemm_fwd(self, A, B, rows=None, threads: int = 0) -> np.ndarray:

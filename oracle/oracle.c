@@ -47,7 +47,8 @@
  *   3: log-sum-exp loses its max term   4: logp sign flipped
  *   5: forward reads B transposed       6: dA reads B as if it were [N, K]
  *      (square operands only)              (square operands only)
- *   7: dB drops the last row of A / dC  8: BF16 rounding sends ties away from 0 */
+ *   7: dB drops the last row of A / dC  8: BF16 rounding sends ties away from 0
+ *   9: dL/dz sign flipped              10: dL/dz loses its one-hot term          */
 #ifndef ORACLE_MUTANT
 #define ORACLE_MUTANT 0
 #endif
@@ -213,6 +214,55 @@ int oracle_linear_logp(const uint16_t* hidden, int64_t N, int64_t H, int64_t ld_
 #endif
             lse[i] = l;
             if (zt) zt[i] = zv;
+        }
+        free(z);
+    }
+    return failed ? -1 : 0;
+}
+
+/*
+ * Gradient of the loss L = sum_r g[r] * logp[r] with respect to the logits:
+ *   G[r, v] = dL/dz[r, v] = g[r] * ([v == t_r] - exp(z[r, v] - lse[r]))
+ * (the derivative of log_softmax(z)[t] is onehot(t) - softmax(z)).  A row whose
+ * target is outside [0, V) has no log-probability and gets a zero row.
+ * Writes all N x V entries of G (small cases only).  Returns 0, or -1 when
+ * scratch memory cannot be allocated.
+ */
+int oracle_linear_logp_grad_logits(const uint16_t* hidden, int64_t N, int64_t H, int64_t ld_h,
+                                   const uint16_t* weight, int64_t V, int64_t ld_w,
+                                   const float* bias, const int64_t* target,
+                                   int64_t target_stride, const double* g, double* G,
+                                   int n_threads) {
+    int failed = 0;
+    set_threads(n_threads);
+#pragma omp parallel
+    {
+        double* z = (double*)malloc((size_t)(V > 0 ? V : 1) * sizeof(double));
+        if (!z) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < N; ++r) {
+            if (!z) continue;
+            double* Gr = G + r * V;
+            int64_t t = target[r * target_stride];
+            if (t < 0 || t >= V) {
+                for (int64_t v = 0; v < V; ++v) Gr[v] = 0.0;
+                continue;
+            }
+            logits_row(hidden + r * ld_h, H, weight, ld_w, V, bias, z);
+            double l = logsumexp(z, V);
+            for (int64_t v = 0; v < V; ++v) {
+                double p = exp(z[v] - l);
+#if ORACLE_MUTANT == 9
+                Gr[v] = g[r] * (p - (v == t ? 1.0 : 0.0));
+#elif ORACLE_MUTANT == 10
+                Gr[v] = g[r] * (0.0 - p);
+#else
+                Gr[v] = g[r] * ((v == t ? 1.0 : 0.0) - p);
+#endif
+            }
         }
         free(z);
     }

@@ -1,0 +1,122 @@
+"""GPU parity, determinism and batch invariance of the linear-logp backward.
+
+G = dL/dz = g * (onehot(t) - exp(z - lse)) is formed in FP32 and rounded to
+BF16; grad_hidden = G.W, grad_weight = G^T.hidden, grad_bias = sum_r G.
+Checks:
+  * G within one BF16 ulp of the oracle's exact G (plus the FP32 error of p);
+  * each product exactly as the deterministic GEMM of the GPU's own G
+    (tolerance-free), and within 1e-5 relative Frobenius of the FP64 product of
+    that same G (pure GEMM accuracy);
+  * end to end within 1e-2 relative Frobenius of the oracle's exact gradients
+    (BF16 rounding of G dominates);
+  * grad_hidden rows bitwise independent of the other rows; everything
+    bitwise run to run.
+"""
+import numpy as np
+import pytest
+import torch
+
+import deterministic_invariant_gemm_linear_gb300 as rlk
+import seeded_inputs as si
+from helpers import bf16_ulp, cuda_or_skip, dec_bf16, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return cuda_or_skip()
+
+
+def _case(N, H, V, bias, seed, dev):
+    hidden, weight, b, target = si.linear_logp_inputs(N, H, V, bias=bias, seed=seed)
+    g = torch.randn(N, generator=torch.Generator().manual_seed(seed + 7))
+    return hidden.to(dev), weight.to(dev), None if b is None else b.to(dev), target.to(dev), g.to(dev)
+
+
+def _backward(hidden, weight, target, g, b, out_dtype=torch.float32):
+    _, lse = rlk.linear_logp(hidden, weight, target, b)
+    return rlk.linear_logp_backward(hidden, weight, target, lse, g, b, out_dtype=out_dtype,
+                                    return_grad_logits=True)
+
+
+@pytest.mark.parametrize("N,H,V,bias", [(300, 512, 5000, True), (130, 1024, 3001, False),
+                                        (5, 64, 257, True)])
+def test_backward_parity(dev, orc, N, H, V, bias):
+    hidden, weight, b, target, g = _case(N, H, V, bias, seed=N + V, dev=dev)
+    target[1] = -3                                    # out of range: zero gradient row
+    dh, dw, db, G = _backward(hidden, weight, target, g, b)
+    torch.cuda.synchronize()
+    hb, wb = si.bf16_bits(hidden), si.bf16_bits(weight)
+    ref_dh, ref_dw, ref_db, ref_G = orc.linear_logp_backward(
+        hb, wb, target.cpu().numpy(), g.cpu().double().numpy(),
+        None if b is None else b.cpu().numpy())
+    # G: one BF16 ulp of the exact value, plus the FP32 error of exp(z - lse)
+    Gg = dec_bf16(si.bf16_bits(G))
+    slack = 1e-5 * np.abs(g.cpu().double().numpy())[:, None]
+    assert np.all(np.abs(Gg - ref_G) <= bf16_ulp(ref_G) + slack)
+    assert np.all(Gg[1] == 0.0)
+    # the products are the deterministic GEMMs of the GPU's own BF16 G (bitwise) ...
+    Gc = G.contiguous()
+    assert torch.equal(dh, rlk.det_gemm_fwd(Gc, weight, out_dtype=torch.float32))
+    assert torch.equal(dw, rlk.det_gemm_db(Gc, hidden, out_dtype=torch.float32))
+    # ... accurate as GEMMs on that G ...
+    hd, wd = dec_bf16(hb), dec_bf16(wb)
+    assert rel_fro(dh.cpu().double().numpy(), Gg @ wd) <= 1e-5
+    assert rel_fro(dw.cpu().double().numpy(), Gg.T @ hd) <= 1e-5
+    if b is not None:
+        assert rel_fro(db.cpu().double().numpy(), Gg.sum(axis=0)) <= 1e-5
+    # ... and end to end close to the exact gradient (BF16 G dominates the error)
+    assert rel_fro(dh.cpu().double().numpy(), ref_dh) <= 1e-2
+    assert rel_fro(dw.cpu().double().numpy(), ref_dw) <= 1e-2
+    if b is not None:
+        assert rel_fro(db.cpu().double().numpy(), ref_db) <= 1e-2
+    assert np.all(dh.cpu().numpy()[1] == 0.0)
+    assert rlk.device_error() == 0
+
+
+def test_backward_bf16_outputs_round_fp32(dev):
+    hidden, weight, b, target, g = _case(200, 768, 4000, True, seed=3, dev=dev)
+    dh32, dw32, db32, _ = _backward(hidden, weight, target, g, b, torch.float32)
+    dh16, dw16, db16, _ = _backward(hidden, weight, target, g, b, torch.bfloat16)
+    assert torch.equal(dh16, dh32.to(torch.bfloat16))
+    assert torch.equal(dw16, dw32.to(torch.bfloat16))
+    assert torch.equal(db16, db32)                    # grad_bias is always FP32
+
+
+def test_backward_rows_invariant_and_deterministic(dev):
+    N, H, V = 700, 1024, 9000
+    hidden, weight, b, target, g = _case(N, H, V, True, seed=4, dev=dev)
+    dh, dw, db, G = _backward(hidden, weight, target, g, b)
+    for _ in range(2):
+        dh2, dw2, db2, G2 = _backward(hidden, weight, target, g, b)
+        assert torch.equal(dh, dh2) and torch.equal(dw, dw2) and torch.equal(db, db2)
+        assert torch.equal(G, G2)
+    _, lse = rlk.linear_logp(hidden, weight, target, b)
+    for chunk in (1, 129):
+        parts = [rlk.linear_logp_backward(hidden[s:s + chunk], weight, target[s:s + chunk],
+                                          lse[s:s + chunk], g[s:s + chunk], b, grad_weight=False,
+                                          grad_bias=False, out_dtype=torch.float32)[0]
+                 for s in range(0, N, chunk)]
+        assert torch.equal(torch.cat(parts), dh), f"chunk {chunk}"
+
+
+def test_backward_mid_shape_runs_deterministically(dev):
+    w = si.MID
+    hidden, weight, b, target = si.workload_inputs(w, seed=5, device=dev)
+    hidden, target = hidden[:1024], target[:1024]
+    g = torch.randn(1024, device=dev)
+    dh, dw, db, _ = _backward(hidden, weight, target, g, b, torch.bfloat16)
+    dh2, dw2, _, _ = _backward(hidden, weight, target, g, b, torch.bfloat16)
+    assert torch.equal(dh, dh2) and torch.equal(dw, dw2)
+    assert bool(torch.isfinite(dh.float()).all()) and bool(torch.isfinite(dw.float()).all())
+    assert rlk.device_error() == 0
+
+
+def test_backward_zero_rows(dev):
+    weight = torch.randn(50, 64, device=dev).to(torch.bfloat16)
+    e = torch.empty(0, 64, dtype=torch.bfloat16, device=dev)
+    dh, dw, db = rlk.linear_logp_backward(e, weight, torch.empty(0, dtype=torch.int64, device=dev),
+                                          torch.empty(0, device=dev), torch.empty(0, device=dev),
+                                          torch.zeros(50, device=dev), out_dtype=torch.float32)
+    assert dh.numel() == 0 and bool((dw == 0).all()) and bool((db == 0).all())

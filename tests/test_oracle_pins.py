@@ -289,7 +289,64 @@ def pin_bf16_rounding(orc):
     assert float(_dec(orc.f64_to_bf16_rne(np.array([x])))[0]) == 1 + 2 ** -7
 
 
-PINS = [pin_closed_forms_logp, pin_brute_force, pin_torch_log_softmax, pin_invariants,
+# ------------------------------------------------------------------ backward
+def _bwd_case(seed, N=7, H=12, V=30, bias=True):
+    hidden, weight, b, target = si.linear_logp_inputs(N, H, V, bias=bias, seed=seed)
+    g = torch.randn(N, generator=torch.Generator().manual_seed(seed + 100), dtype=torch.float64)
+    return hidden, weight, b, target, g
+
+
+def pin_backward_torch_autograd(orc):
+    """torch float64 autograd of sum_r g_r * log_softmax(h W^T + b)[r, t_r] (library code)."""
+    hidden, weight, b, target, g = _bwd_case(21)
+    target[3] = 0
+    dh, dw, db, _ = orc.linear_logp_backward(si.bf16_bits(hidden), si.bf16_bits(weight),
+                                             target.numpy(), g.numpy(), b.numpy())
+    h = hidden.double().requires_grad_()
+    w = weight.double().requires_grad_()
+    bb = b.double().requires_grad_()
+    lp = torch.log_softmax(h @ w.T + bb, dim=-1).gather(1, target[:, None])[:, 0]
+    (g * lp).sum().backward()
+    assert np.allclose(dh, h.grad.numpy(), rtol=0, atol=1e-12)
+    assert np.allclose(dw, w.grad.numpy(), rtol=0, atol=1e-12)
+    assert np.allclose(db, bb.grad.numpy(), rtol=0, atol=1e-12)
+
+
+def pin_backward_finite_difference(orc):
+    """dL/dbias_v against central differences of the (pinned) forward oracle."""
+    hidden, weight, b, target, g = _bwd_case(22, N=5, H=8, V=12)
+    hb, wb, t = si.bf16_bits(hidden), si.bf16_bits(weight), target.numpy()
+    _, _, db, _ = orc.linear_logp_backward(hb, wb, t, g.numpy(), b.numpy())
+    eps = 2.0 ** -10                       # exact in fp32 around |b| < 1
+    for v in range(12):
+        bp, bm = b.numpy().copy(), b.numpy().copy()
+        bp[v] += eps
+        bm[v] -= eps
+        lp_p, _, _ = orc.linear_logp(hb, wb, t, bp)
+        lp_m, _, _ = orc.linear_logp(hb, wb, t, bm)
+        fd = (g.numpy() @ lp_p - g.numpy() @ lp_m) / (float(bp[v]) - float(bm[v]))
+        assert abs(fd - db[v]) <= 1e-6 * max(1.0, abs(db[v])), (v, fd, db[v])
+
+
+def pin_backward_invariants(orc):
+    hidden, weight, b, target, g = _bwd_case(23)
+    target[2] = -1                          # out of range: zero gradient row
+    G = orc.grad_logits(si.bf16_bits(hidden), si.bf16_bits(weight), target.numpy(), g.numpy(),
+                        b.numpy())
+    live = np.ones(len(target), bool)
+    live[2] = False
+    assert np.all(G[2] == 0.0)
+    # sum_v (onehot - softmax) = 0 for every live row
+    assert np.allclose(G[live].sum(axis=1), 0.0, rtol=0, atol=1e-14)
+    # the target column carries g * (1 - p) with sign(g); all other entries carry -g * p
+    for r in np.flatnonzero(live):
+        others = np.delete(G[r], int(target[r]))
+        assert np.all(np.sign(others) != np.sign(g[r].item())) or g[r] == 0
+        assert np.sign(G[r, int(target[r])]) == np.sign(g[r].item())
+
+
+PINS = [pin_backward_torch_autograd, pin_backward_finite_difference, pin_backward_invariants,
+        pin_closed_forms_logp, pin_brute_force, pin_torch_log_softmax, pin_invariants,
         pin_row_subset_and_stride, pin_closed_forms_gemm, pin_integer_gemm_exact,
         pin_gemm_special_cases, pin_gemm_torch_f64, pin_gemm_cross_entry, pin_bf16_rounding]
 
@@ -299,7 +356,7 @@ def test_pin(orc, pin):
     pin(orc)
 
 
-@pytest.mark.parametrize("mutant", range(1, 9))
+@pytest.mark.parametrize("mutant", range(1, 11))
 def test_planted_mistake_is_caught(mutant):
     """Every planted oracle mistake fails at least one pin."""
     import oracle
