@@ -310,6 +310,84 @@ def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
     return line
 
 
+def backward_bench(args, dev, rank, world, peaks, peak_src):
+    """One step = the whole linear-logp backward (grad_hidden + grad_weight) on the mid shape."""
+    import deterministic_invariant_gemm_linear_gb300 as rlk
+    w = si.MID
+    N = args.rows or w.N
+    hidden, weight, bias, target = si.workload_inputs(w, seed=rank, device=dev)
+    hidden, target = hidden[:N].contiguous(), target[:N].contiguous()
+    g = torch.randn(N, generator=torch.Generator(device=dev).manual_seed(7), device=dev)
+    _, lse = rlk.linear_logp(hidden, weight, target, bias)
+    lib = rlk.lib()
+    H, V = w.H, w.V
+    ldG = -(-V // 8) * 8
+    ws = torch.empty(lib.rlk_linear_logp_backward_workspace_size(N, V), dtype=torch.uint8, device=dev)
+    dh = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
+    dw = torch.empty(V, H, dtype=torch.bfloat16, device=dev)
+    sp = rlk._stream_ptr(None)
+    P = rlk._ptr
+
+    def step():
+        rlk._check(lib.rlk_linear_logp_backward(
+            P(hidden), N, H, H, P(weight), V, H, None, P(target), 1, P(lse), P(g),
+            P(dh), rlk.RLK_BF16, H, P(dw), rlk.RLK_BF16, H, None, P(ws), ws.numel(), sp),
+            "rlk_linear_logp_backward")
+
+    def gemm_dh():
+        rlk._check(lib.rlk_det_gemm_fwd(P(ws), N, V, ldG, P(weight), H, H, P(dh), rlk.RLK_BF16, H,
+                                        None, 0, sp), "rlk_det_gemm_fwd")
+
+    def gemm_dw():
+        rlk._check(lib.rlk_det_gemm_db(P(ws), N, V, ldG, P(hidden), rlk.RLK_BF16, H, H, P(dw),
+                                       rlk.RLK_BF16, H, None, 0, sp), "rlk_det_gemm_db")
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+
+    def timed(fn):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(K):
+            fn()
+        e.record(stream)
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / 1e3
+
+    barrier(world)
+    with ClockSampler(dev.index) as clocks:
+        t_local = timed(step)
+    t = max_over_ranks(t_local, world, dev)
+    t_dh, t_dw = timed(gemm_dh), timed(gemm_dw)
+    assert rlk.device_error() == 0
+    flop_one = 2.0 * N * H * V
+    flops = 3 * flop_one
+    part = {"grad_logits_kernel (by difference)": (t_local - t_dh - t_dw) / K * 1e3,
+            "grad_hidden det_gemm_fwd": t_dh / K * 1e3, "grad_weight det_gemm_db": t_dw / K * 1e3}
+    peak = peaks["bf16_tflops"]
+    achieved = flops * K / t_local / 1e12
+    return {
+        "metric": f"linear-logp backward TFLOP/s (N={N},H={H},V={V}; grad_hidden + grad_weight)",
+        "value": flops * world * K / t / 1e12, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": t / K * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"linear-logp backward: N={N} H={H} V={V}, g~N(0,1), BF16 outputs",
+                   "l2": f"inputs larger than L2: W {V * H * 2 / 1e9:.3f} GB and G {N * ldG * 2 / 1e9:.3f} GB per step"},
+        "tokens_per_s": N * world * K / t,
+        "kernels_ms": part,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "whole backward step (3 tensor-core launches + none else)",
+                     "algorithmic": f"3 x 2*N*H*V = {flops:.4g} FLOP per step",
+                     "peak_kind": f"{peak_src} burst bf16"},
+        "clocks": clocks.summary(),
+        "gpu_launches": 3 * K,
+    }
+
+
 def det_gemm_bench(args, dev, rank, world, peaks, peak_src):
     import deterministic_invariant_gemm_linear_gb300 as rlk
     M = K_ = N = 4096
@@ -434,7 +512,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="mid", choices=["mid", "large", "ragged", "det_gemm"])
+    ap.add_argument("--workload", default="mid",
+                    choices=["mid", "large", "ragged", "det_gemm", "backward"])
     ap.add_argument("--impl", default="rlk", choices=["rlk", "reference"])
     ap.add_argument("--rows", type=int, default=0,
                     help="override the row count N of a linear-logp workload (profiling cases)")
@@ -456,6 +535,8 @@ def main():
     peaks, src = load_peaks()
     if args.workload == "det_gemm":
         line = det_gemm_bench(args, dev, rank, world, peaks, src)
+    elif args.workload == "backward":
+        line = backward_bench(args, dev, rank, world, peaks, src)
     else:
         line = linear_logp_bench(args, dev, rank, world, peaks, src)
     if rank == 0:
