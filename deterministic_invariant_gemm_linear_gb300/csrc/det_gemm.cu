@@ -31,14 +31,14 @@ __device__ unsigned int g_err_det_gemm = 0;
 namespace {
 
 struct GemmSched {
-  int num_mb;   // 128-row output blocks
-  int num_nb;   // 256-column output blocks
+  Banded order; // rows = 128-row output blocks, cols = 256-column output blocks
   int nkb;      // 64-wide reduction blocks
-  __device__ __forceinline__ int num_units() const { return num_mb * num_nb; }
+  __device__ __forceinline__ int num_units() const { return order.count(); }
   __device__ __forceinline__ int unit_tiles(int) const { return 1; }
   __device__ __forceinline__ void tile_coords(int u, int, int& a0, int& b0) const {
-    const int nb = u / num_mb;
-    a0 = (u - nb * num_mb) * kBM;
+    int mb, nb;
+    order.unit(u, mb, nb);
+    a0 = mb * kBM;
     b0 = nb * kBN;
   }
 };
@@ -284,8 +284,9 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
   if (!ok) return RLK_ERR_CUDA;
 
   GemmSched sc;
-  sc.num_mb = (int)num_mb;
-  sc.num_nb = (int)num_nb;
+  sc.order.rows = (int)num_mb;
+  sc.order.cols = (int)num_nb;
+  sc.order.band = band_rows(num_mb, red);
   sc.nkb = (int)ceil_div(red, kBK);
   GemmOut o;
   o.M = (int)out_rows;

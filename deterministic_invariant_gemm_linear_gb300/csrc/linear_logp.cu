@@ -35,14 +35,22 @@ __device__ unsigned int g_err_linear_logp = 0;
 namespace {
 
 struct LogpSched {
-  int num_rb;      // 128-row blocks
+  Banded order;    // rows = 128-row blocks, cols = vocabulary splits
   int S;           // vocabulary splits
   int vps;         // 256-id tiles per split
   int vtiles;      // 256-id tiles in the vocabulary
   int nkb;         // 64-wide blocks of H
-  __device__ __forceinline__ int num_units() const { return num_rb * S; }
-  __device__ __forceinline__ int split_of(int u) const { return u / num_rb; }
-  __device__ __forceinline__ int rb_of(int u) const { return u - (u / num_rb) * num_rb; }
+  __device__ __forceinline__ int num_units() const { return order.count(); }
+  __device__ __forceinline__ int split_of(int u) const {
+    int rb, j;
+    order.unit(u, rb, j);
+    return j;
+  }
+  __device__ __forceinline__ int rb_of(int u) const {
+    int rb, j;
+    order.unit(u, rb, j);
+    return rb;
+  }
   __device__ __forceinline__ int first_tile(int u) const { return split_of(u) * vps; }
   __device__ __forceinline__ int unit_tiles(int u) const {
     const int t0 = first_tile(u);
@@ -358,7 +366,9 @@ rlk_status rlk_linear_logp_partials(const void* hidden, int64_t N, int64_t H, in
     return RLK_ERR_CUDA;
 
   LogpSched sc;
-  sc.num_rb = (int)ceil_div(N, kBM);
+  sc.order.rows = (int)ceil_div(N, kBM);
+  sc.order.cols = (int)p.S;
+  sc.order.band = band_rows(sc.order.rows, H);
   sc.S = (int)p.S;
   sc.vps = (int)p.vps;
   sc.vtiles = (int)p.vtiles;
@@ -371,7 +381,8 @@ rlk_status rlk_linear_logp_partials(const void* hidden, int64_t N, int64_t H, in
   a.target = target;
   a.ws_ms = reinterpret_cast<float2*>(ws);
   a.ws_zt = reinterpret_cast<float*>(ws + p.off_zt);
-  const int64_t units = (int64_t)sc.num_rb * sc.S;
+  const int64_t units = (int64_t)sc.order.rows * sc.S;
+  if (units >= (int64_t(1) << 31)) return RLK_ERR_SHAPE;
   const int grid = (int)(units < dev.sm_count ? units : dev.sm_count);
   linear_logp_partials_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_h, tm_w, sc, a);
   return cudaGetLastError() == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;

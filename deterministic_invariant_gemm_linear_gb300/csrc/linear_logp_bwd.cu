@@ -34,14 +34,14 @@ __device__ unsigned int g_err_linear_logp_bwd = 0;
 namespace {
 
 struct GradSched {
-  int num_rb;      // 128-row blocks
-  int vtiles;      // 256-id vocabulary tiles
+  Banded order;    // rows = 128-row blocks, cols = 256-id vocabulary tiles
   int nkb;         // 64-wide blocks of H
-  __device__ __forceinline__ int num_units() const { return num_rb * vtiles; }
+  __device__ __forceinline__ int num_units() const { return order.count(); }
   __device__ __forceinline__ int unit_tiles(int) const { return 1; }
   __device__ __forceinline__ void tile_coords(int u, int, int& a0, int& b0) const {
-    const int vt = u / num_rb;
-    a0 = (u - vt * num_rb) * kBM;
+    int rb, vt;
+    order.unit(u, rb, vt);
+    a0 = rb * kBM;
     b0 = vt * kBN;
   }
 };
@@ -254,10 +254,11 @@ rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H, in
       !encode_bf16_2d(&tm_w, weight, H, V, ld_weight, kBK, kBN))
     return RLK_ERR_CUDA;
   GradSched sc;
-  sc.num_rb = (int)ceil_div(N, kBM);
-  sc.vtiles = (int)ceil_div(V, kBN);
+  sc.order.rows = (int)ceil_div(N, kBM);
+  sc.order.cols = (int)ceil_div(V, kBN);
+  sc.order.band = band_rows(sc.order.rows, H);
   sc.nkb = (int)ceil_div(H, kBK);
-  if ((int64_t)sc.num_rb * sc.vtiles >= (int64_t(1) << 31)) return RLK_ERR_SHAPE;
+  if ((int64_t)sc.order.rows * sc.order.cols >= (int64_t(1) << 31)) return RLK_ERR_SHAPE;
   GradArgs a;
   a.N = (int)N;
   a.V = (int)V;
@@ -268,7 +269,7 @@ rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H, in
   a.grad = grad_logp;
   a.G = static_cast<uint16_t*>(workspace);
   a.ldG = grad_ld(V);
-  const int64_t units = (int64_t)sc.num_rb * sc.vtiles;
+  const int64_t units = (int64_t)sc.order.rows * sc.order.cols;
   const int grid = (int)(units < dev.sm_count ? units : dev.sm_count);
   linear_logp_grad_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_h, tm_w, sc, a);
   if (cudaGetLastError() != cudaSuccess) return RLK_ERR_CUDA;

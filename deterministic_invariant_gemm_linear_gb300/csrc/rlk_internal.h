@@ -45,6 +45,16 @@ cudaError_t launch_stage_bf16(const uint16_t* src, int64_t rows, int64_t cols, i
 cudaError_t launch_cast_f32_bf16(const float* src, int64_t rows, int64_t cols, int64_t ld_src,
                                  uint16_t* dst, int64_t ld_dst, cudaStream_t stream);
 
+// Row blocks per band of the work order: as many 128-row blocks of a
+// K-element BF16 row operand as fit in 32 MiB of L2 (at least 1, at most rows).
+inline int band_rows(int64_t rows, int64_t K) {
+  const int64_t per = 128 * K * 2;
+  int64_t b = (int64_t(32) << 20) / (per > 0 ? per : 1);
+  if (b < 1) b = 1;
+  if (b > rows) b = rows;
+  return (int)(b > 0 ? b : 1);
+}
+
 // Vocabulary split policy (function of V only).
 constexpr int64_t kVocabTile = 256;
 constexpr int64_t kMaxVocabSplits = 1024;
