@@ -5,12 +5,13 @@
 // lse[r] = log sum_v exp z[r, v]; logp[r] = z[r, target[r]] - lse[r]; the [N, V]
 // logits are never written to memory.
 //
-// Stage 1 (linear_logp_partials_kernel): the tcgen05 main loop computes 128 x 256
-// FP32 logit tiles in TMEM; the epilogue keeps, per row and per vocabulary split,
+// Stage 1 (linear_logp_partials_kernel): the 2-SM tcgen05 main loop (a cluster
+// of two CTAs, M=256 x N=256 per MMA) computes 256 x 256 FP32 logit tiles, each
+// CTA holding its 128 rows in TMEM; the epilogue keeps, per row and per vocabulary split,
 // an online maximum m and sum of exponentials s over the split's tiles in
 // ascending vocabulary order, and captures the target logit.  Work unit =
-// (vocabulary split j, 128-row block); units are ordered split-major so that
-// the CTAs running at the same time share W tiles through L2.
+// (vocabulary split j, 256-row block), dealt in L2-sized bands of row blocks so
+// that the clusters running at the same time share hidden and W tiles in L2.
 //
 // Stage 2 (linear_logp_combine_kernel): one warp per row merges the row's S
 // partials in a fixed order (lane l takes splits l, l+32, ... ascending, then a
@@ -26,7 +27,7 @@
 
 #include "rlk.h"
 #include "rlk_internal.h"
-#include "rlk_pipeline.cuh"
+#include "rlk_pipeline2.cuh"
 
 namespace rlk {
 
@@ -56,8 +57,9 @@ struct LogpSched {
     const int t0 = first_tile(u);
     return min(vps, vtiles - t0);
   }
+  int rows_per_unit;   // 256: the rows of a CTA pair
   __device__ __forceinline__ void tile_coords(int u, int i, int& a0, int& b0) const {
-    a0 = rb_of(u) * kBM;
+    a0 = rb_of(u) * rows_per_unit;
     b0 = (first_tile(u) + i) * kBN;
   }
 };
@@ -130,46 +132,47 @@ __device__ __forceinline__ void logp_chunk(const uint32_t (&r)[32], int vbase, i
   m = mn;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// A cluster of two CTAs computes a unit = (split j, 256-row block) on the 2-SM
+// tcgen05 loop; the CTA of rank r owns rows [256 * block + 128 r, +128).  Each
+// epilogue thread owns one row: for every 256-id tile of the split, in
+// ascending order, it folds the tile's logits into (m, s) 32 columns at a time.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     linear_logp_partials_kernel(const __grid_constant__ CUtensorMap tm_hidden,
-                                const __grid_constant__ CUtensorMap tm_weight, LogpSched sc,
-                                LogpArgs args) {
+                                     const __grid_constant__ CUtensorMap tm_weight, LogpSched sc,
+                                     LogpArgs args) {
   extern __shared__ uint8_t smem_raw[];
-  const PipeSmem ps = pipe_smem(smem_raw);
+  const Pipe2Smem ps = pipe2_smem(smem_raw);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_hidden);
     tma_prefetch_desc(&tm_weight);
   }
-  const uint32_t tmem = pipe_setup(ps);
-  using TA = OperandTile<false, kBM>;
-  using TB = OperandTile<false, kBN>;
+  const uint32_t tmem = pipe2_setup(ps);
 
   if (warp == 0) {
-    if (lane == 0) producer_role<TA, TB>(&tm_hidden, &tm_weight, sc, ps, &g_err_linear_logp);
+    if (lane == 0) producer2_role(&tm_hidden, &tm_weight, sc, ps, &g_err_linear_logp);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0)
-      mma_role<TA, TB>(sc, ps, tmem, idesc_bf16_f32(kBM, kBN, false, false), &g_err_linear_logp);
+    if (lane == 0 && ps.rank == 0)
+      mma2_role(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, false, false), &g_err_linear_logp);
     __syncwarp();
   } else {
-    // Epilogue: warp w reads TMEM lanes 32*(w%4) .. +31, i.e. tile rows q*32 + lane.
     const int q = warp & 3;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool run = true;
     const int units = sc.num_units();
-    for (int u = blockIdx.x; run && u < units; u += gridDim.x) {
+    for (int u = cluster_index(); run && u < units; u += cluster_count()) {
       const int j = sc.split_of(u);
-      const int row = sc.rb_of(u) * kBM + q * 32 + lane;
+      const int row = sc.rb_of(u) * kPairRows + (int)ps.rank * kHalfRows + q * 32 + lane;
       const bool valid = row < args.N;
       const int64_t tgt = valid ? __ldg(args.target + (int64_t)row * args.tstride) : -1;
       float m = -INFINITY, s = 0.f, zt = 0.f;
       bool have_zt = false;
       const int t0 = sc.first_tile(u), nt = sc.unit_tiles(u);
       for (int i = 0; i < nt; ++i) {
-        if (!epilogue_acquire(ps, acc, acc_phase, &g_err_linear_logp)) {
+        if (!epilogue2_acquire(ps, acc, acc_phase, &g_err_linear_logp)) {
           run = false;
           break;
         }
@@ -180,11 +183,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int vbase = v0 + c * 32;
           if (vbase >= args.V) break;          // uniform: depends on the tile only
           uint32_t r[32];
+          __syncwarp();
           tmem_ld32(taddr + c * 32, r);
           tmem_wait_ld();
           logp_chunk(r, vbase, args.V, args.bias, tgt, m, s, have_zt, zt);
         }
-        epilogue_release(ps, acc);
+        epilogue2_release(ps, acc);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
@@ -195,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  pipe_teardown(tmem);
+  pipe2_teardown(tmem);
 }
 
 // (m, s) pair merge with explicit roundings, so merge(a, b) == merge(b, a) bitwise.
@@ -251,7 +255,7 @@ cudaError_t ensure_attrs(int dev) {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!g_attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(linear_logp_partials_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2Bytes);
     if (e != cudaSuccess) return e;
     g_attr_set[dev] = true;
   }
@@ -360,15 +364,17 @@ rlk_status rlk_linear_logp_partials(const void* hidden, int64_t N, int64_t H, in
       return RLK_ERR_CUDA;
     w_src = ws + p.off_w;
   }
+  constexpr int kRowsPerUnit = kPairRows, kBoxRows = kHalfRows;
   CUtensorMap tm_h, tm_w;
   if (!encode_bf16_2d(&tm_h, h_src, H, N, p.ldh, kBK, kBM) ||
-      !encode_bf16_2d(&tm_w, w_src, H, V, p.ldw, kBK, kBN))
+      !encode_bf16_2d(&tm_w, w_src, H, V, p.ldw, kBK, kBoxRows))
     return RLK_ERR_CUDA;
 
   LogpSched sc;
-  sc.order.rows = (int)ceil_div(N, kBM);
+  sc.order.rows = (int)ceil_div(N, kRowsPerUnit);
   sc.order.cols = (int)p.S;
-  sc.order.band = band_rows(sc.order.rows, H);
+  sc.order.band = band_rows(sc.order.rows, H, kRowsPerUnit);
+  sc.rows_per_unit = kRowsPerUnit;
   sc.S = (int)p.S;
   sc.vps = (int)p.vps;
   sc.vtiles = (int)p.vtiles;
@@ -383,8 +389,10 @@ rlk_status rlk_linear_logp_partials(const void* hidden, int64_t N, int64_t H, in
   a.ws_zt = reinterpret_cast<float*>(ws + p.off_zt);
   const int64_t units = (int64_t)sc.order.rows * sc.S;
   if (units >= (int64_t(1) << 31)) return RLK_ERR_SHAPE;
-  const int grid = (int)(units < dev.sm_count ? units : dev.sm_count);
-  linear_logp_partials_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_h, tm_w, sc, a);
+  // One cluster of two CTAs per pair of SMs, persistent over the units.
+  const int64_t clusters = dev.sm_count / 2;
+  const int grid = 2 * (int)(units < clusters ? units : clusters);
+  linear_logp_partials_kernel<<<grid, kThreads, kSmem2Bytes, s>>>(tm_h, tm_w, sc, a);
   return cudaGetLastError() == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
 }
 

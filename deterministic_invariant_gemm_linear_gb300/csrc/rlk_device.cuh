@@ -192,6 +192,28 @@ __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- work order
+// Grouped order of a 2-D grid of work units (rows x cols): units are dealt in
+// bands of `band` consecutive row blocks; inside a band the row block varies
+// fastest, then the column.  CTAs that run at the same time then share a band's
+// row operands and a few columns' operands in L2.  The order decides only which
+// CTA computes a unit, never how.
+struct Banded {
+  int rows;    // row blocks
+  int cols;    // column blocks (vocabulary splits / tiles, output column blocks)
+  int band;    // row blocks per band (>= 1)
+  __device__ __forceinline__ int count() const { return rows * cols; }
+  __device__ __forceinline__ void unit(int u, int& row, int& col) const {
+    const int full = band * cols;
+    const int b = u / full;
+    const int r0 = b * band;
+    const int n = min(band, rows - r0);
+    const int rem = u - b * full;
+    col = rem / n;
+    row = r0 + (rem - col * n);
+  }
+};
+
 // ---------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading and
 // stride byte offsets (all >> 4), descriptor version 1 at bit 46, and the

@@ -47,8 +47,8 @@ cudaError_t launch_cast_f32_bf16(const float* src, int64_t rows, int64_t cols, i
 
 // Row blocks per band of the work order: as many 128-row blocks of a
 // K-element BF16 row operand as fit in 32 MiB of L2 (at least 1, at most rows).
-inline int band_rows(int64_t rows, int64_t K) {
-  const int64_t per = 128 * K * 2;
+inline int band_rows(int64_t rows, int64_t K, int64_t rows_per_block = 128) {
+  const int64_t per = rows_per_block * K * 2;
   int64_t b = (int64_t(32) << 20) / (per > 0 ? per : 1);
   if (b < 1) b = 1;
   if (b > rows) b = rows;

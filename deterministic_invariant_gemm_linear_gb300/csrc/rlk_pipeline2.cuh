@@ -1,0 +1,291 @@
+// The 2-SM (cta_group::2) variant of the warp-specialised tcgen05 main loop.
+//
+// A cluster of two CTAs on two SMs computes one 256 x 256 FP32 accumulator
+// tile per MMA chain: rank r holds rows [128 r, 128 r + 128) of the left
+// operand and rows [128 r, 128 r + 128) of the right operand's 256-row tile in
+// its own shared memory, and its own 128 rows of the accumulator in its own
+// TMEM.  Rank 0 issues tcgen05.mma.cta_group::2 (M=256, N=256, K=16) for both.
+//   warp 0, lane 0  TMA producer in each CTA; both CTAs' copies complete on
+//                   rank 0's full barrier (rank 0 arms it for both halves).
+//   warp 1          allocates 512 TMEM columns collectively with the peer; in
+//                   rank 0, lane 0 issues the MMAs and commits to both CTAs'
+//                   empty / accumulator-full barriers (multicast).
+//   warps 2..5      epilogue on the CTA's own 128 accumulator rows; each warp
+//                   releases the accumulator on rank 0's barrier (8 arrivals).
+// Per SM this halves the right-operand shared-memory reads and L2 traffic of
+// the one-CTA loop at the same accumulator shape per row.
+#pragma once
+
+#include "rlk_device.cuh"
+
+namespace rlk {
+
+constexpr int kStages2 = 6;
+constexpr int kHalfRows = 128;                        // rows of each operand per CTA
+constexpr int kA2Bytes = kHalfRows * kBK * 2;         // 16 KiB
+constexpr int kB2Bytes = kHalfRows * kBK * 2;         // 16 KiB
+constexpr int kStage2Bytes = kA2Bytes + kB2Bytes;
+constexpr int kSmem2Bytes = kStages2 * kStage2Bytes + 1024 + 256;
+static_assert(kSmem2Bytes <= 232448, "exceeds the 227 KiB per-CTA shared memory limit");
+static_assert(kSmem2Bytes > 232448 / 2, "tcgen05 kernels must own their SM");
+constexpr int kPairRows = 2 * kHalfRows;              // accumulator rows per cluster
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_index() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory offset in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+// Tile load into this CTA's shared memory whose completion is counted on an
+// mbarrier of either CTA of the pair (here always rank 0's).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t mbar,
+                                                 int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void umma_pair_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once, on the barrier at this shared offset in every CTA of `mask`,
+// when all MMAs issued so far by this thread are done.
+__device__ __forceinline__ void umma_pair_commit(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar), "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+struct Pipe2Barriers {
+  uint64_t full[kStages2];    // used in rank 0 only: both CTAs' copies for a stage
+  uint64_t empty[kStages2];   // per CTA: the stage's shared memory may be refilled
+  uint64_t acc_full[2];       // per CTA: accumulator b holds a finished tile
+  uint64_t acc_empty[2];      // rank 0: both CTAs' epilogues released accumulator b
+  uint64_t drained;           // rank 0: every issued MMA has completed
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(Pipe2Barriers) <= 256, "barrier block overflows its reserved bytes");
+
+struct Pipe2Smem {
+  uint32_t stages;
+  Pipe2Barriers* bars;
+  uint32_t rank;
+  __device__ __forceinline__ uint32_t full(int s) const { return smem_u32(&bars->full[s]); }
+  __device__ __forceinline__ uint32_t empty(int s) const { return smem_u32(&bars->empty[s]); }
+  __device__ __forceinline__ uint32_t acc_full(int b) const { return smem_u32(&bars->acc_full[b]); }
+  __device__ __forceinline__ uint32_t acc_empty(int b) const {
+    return smem_u32(&bars->acc_empty[b]);
+  }
+  __device__ __forceinline__ volatile int* abort_flag() const { return &bars->abort_flag; }
+};
+
+__device__ __forceinline__ Pipe2Smem pipe2_smem(uint8_t* raw) {
+  const uint32_t base = smem_u32(raw);
+  const uint32_t pad = (1024u - (base & 1023u)) & 1023u;
+  Pipe2Smem p;
+  p.stages = base + pad;
+  p.bars = reinterpret_cast<Pipe2Barriers*>(raw + pad + kStages2 * kStage2Bytes);
+  p.rank = cluster_rank();
+  return p;
+}
+
+// Barrier initialisation, collective TMEM allocation, then a cluster barrier
+// so that no CTA touches its peer's barriers before they exist.
+__device__ __forceinline__ uint32_t pipe2_setup(const Pipe2Smem& ps) {
+  const int warp = threadIdx.x / 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages2; ++s) {
+      mbar_init(ps.full(s), 1);
+      mbar_init(ps.empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(ps.acc_full(b), 1);
+      mbar_init(ps.acc_empty(b), 2 * (kEpilogueThreads / 32));
+    }
+    mbar_init(smem_u32(&ps.bars->drained), 1);
+    ps.bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(&ps.bars->tmem_base), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  return ps.bars->tmem_base;
+}
+
+// Cluster barrier (no CTA leaves while its peer may still signal it or read
+// its shared memory), then the collective TMEM release.
+__device__ __forceinline__ void pipe2_teardown(uint32_t tmem) {
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (threadIdx.x / 32 == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kTmemCols);
+  }
+}
+
+// Schedule interface as for the one-CTA loop, with a0 = first row of the
+// cluster's 256-row block and b0 = first row of the 256-row right-operand tile.
+template <class Sched>
+__device__ __forceinline__ void producer2_role(const CUtensorMap* ta, const CUtensorMap* tb,
+                                               const Sched& sc, const Pipe2Smem& ps,
+                                               unsigned int* err) {
+  int stage = 0;
+  uint32_t phase = 0, issued = 0, last_parity = 0;
+  bool run = true;
+  const int32_t half = (int32_t)ps.rank * kHalfRows;
+  const int units = sc.num_units();
+  for (int u = cluster_index(); run && u < units; u += cluster_count()) {
+    const int nt = sc.unit_tiles(u);
+    for (int i = 0; run && i < nt; ++i) {
+      int a0, b0;
+      sc.tile_coords(u, i, a0, b0);
+      for (int kb = 0; kb < sc.nkb; ++kb) {
+        if (!mbar_wait(ps.empty(stage), phase ^ 1u, ps.abort_flag(), err)) {
+          run = false;
+          break;
+        }
+        if (ps.rank == 0) mbar_arrive_expect_tx(ps.full(stage), 2 * kStage2Bytes);
+        const uint32_t leader_full = mapa_shared(ps.full(stage), 0);
+        const uint32_t sa = ps.stages + stage * kStage2Bytes;
+        tma_load_2d_pair(sa, ta, leader_full, kb * kBK, a0 + half);
+        tma_load_2d_pair(sa + kA2Bytes, tb, leader_full, kb * kBK, b0 + half);
+        issued |= 1u << stage;
+        last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == kStages2) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  }
+  if (ps.rank == 0) {
+    // Rank 0's full barriers count both CTAs' bytes: once they complete, every
+    // copy of the pair has landed.
+    for (int s = 0; s < kStages2; ++s)
+      if ((issued >> s) & 1u) mbar_wait_drain(ps.full(s), (last_parity >> s) & 1u, err);
+  } else if (!run) {
+    // Winding down early: rank 1 cannot observe rank 0's barriers, so it gives
+    // its last copies a bounded 1 ms to land before the CTA may exit.
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 1000000ull) {
+    }
+  }
+}
+
+template <class Sched>
+__device__ __forceinline__ void mma2_role(const Sched& sc, const Pipe2Smem& ps, uint32_t tmem,
+                                          uint32_t idesc, unsigned int* err) {
+  int stage = 0, acc = 0;
+  uint32_t phase = 0, acc_phase = 0;
+  bool run = true;
+  const int units = sc.num_units();
+  for (int u = cluster_index(); run && u < units; u += cluster_count()) {
+    const int nt = sc.unit_tiles(u);
+    for (int i = 0; run && i < nt; ++i) {
+      if (!mbar_wait(ps.acc_empty(acc), acc_phase ^ 1u, ps.abort_flag(), err)) {
+        run = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d = tmem + acc * kAccCols;
+      for (int kb = 0; kb < sc.nkb; ++kb) {
+        if (!mbar_wait(ps.full(stage), phase, ps.abort_flag(), err)) {
+          run = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = ps.stages + stage * kStage2Bytes;
+        const uint32_t sb = sa + kA2Bytes;
+#pragma unroll
+        for (int k = 0; k < kBK / kUmmaK; ++k)
+          umma_pair_bf16(d, OperandTile<false, kHalfRows>::desc(sa, k),
+                         OperandTile<false, kHalfRows>::desc(sb, k), idesc,
+                         (kb | k) != 0 ? 1u : 0u);
+        umma_pair_commit(ps.empty(stage), 0x3);
+        if (++stage == kStages2) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!run) break;
+      umma_pair_commit(ps.acc_full(acc), 0x3);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+  umma_pair_commit(smem_u32(&ps.bars->drained), 0x1);
+  mbar_wait_drain(smem_u32(&ps.bars->drained), 0, err);
+}
+
+__device__ __forceinline__ bool epilogue2_acquire(const Pipe2Smem& ps, int acc, uint32_t parity,
+                                                  unsigned int* err) {
+  const bool ok = mbar_wait(ps.acc_full(acc), parity, ps.abort_flag(), err);
+  const bool all = __all_sync(0xffffffffu, ok);
+  tc_fence_after();
+  return all;
+}
+
+// Warp-level release of an accumulator on rank 0's barrier.
+__device__ __forceinline__ void epilogue2_release(const Pipe2Smem& ps, int acc) {
+  tc_fence_before();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) {
+    if (ps.rank == 0)
+      mbar_arrive(ps.acc_empty(acc));
+    else
+      mbar_arrive_cluster(mapa_shared(ps.acc_empty(acc), 0));
+  }
+}
+
+}  // namespace rlk
