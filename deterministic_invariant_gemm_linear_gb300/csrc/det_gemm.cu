@@ -12,8 +12,8 @@
 //   forward  A [M,K] reduction-contiguous (K-major), B [K,N] N-contiguous (MN-major)
 //   dA       dC [M,N] K-major,                       B [K,N] K-major (N is reduced)
 //   dB       A [M,K] MN-major (output rows = K),      dC [M,N] MN-major (M is reduced)
-// Output tiles are 128 x 256, the reduction runs over blocks of 64 in
-// ascending order, each tile's accumulation starts from zero, and there is no
+// Output tiles are 256 x 256 per CTA pair (2-SM tcgen05 loop, M=256 x N=256 x
+// K=16 per MMA), the reduction runs over blocks of 64 in ascending order, each tile's accumulation starts from zero, and there is no
 // split of the reduction: every output bit is a function of its own row of the
 // left operand and column of the right operand only.
 #include <mutex>
@@ -22,7 +22,7 @@
 
 #include "rlk.h"
 #include "rlk_internal.h"
-#include "rlk_pipeline.cuh"
+#include "rlk_pipeline2.cuh"
 
 namespace rlk {
 
@@ -31,14 +31,14 @@ __device__ unsigned int g_err_det_gemm = 0;
 namespace {
 
 struct GemmSched {
-  Banded order; // rows = 128-row output blocks, cols = 256-column output blocks
+  Banded order; // rows = 256-row output blocks (one per CTA pair), cols = 256-column blocks
   int nkb;      // 64-wide reduction blocks
   __device__ __forceinline__ int num_units() const { return order.count(); }
   __device__ __forceinline__ int unit_tiles(int) const { return 1; }
   __device__ __forceinline__ void tile_coords(int u, int, int& a0, int& b0) const {
     int mb, nb;
     order.unit(u, mb, nb);
-    a0 = mb * kBM;
+    a0 = mb * kPairRows;
     b0 = nb * kBN;
   }
 };
@@ -102,26 +102,30 @@ __device__ __forceinline__ void store_chunk(const GemmOut& o, int row, int col0,
   }
 }
 
+// One 256 x 256 output tile per CTA pair (2-SM loop): rank r stages rows
+// [a0 + 128 r, +128) of the left operand and rows / columns [b0 + 128 r, +128) of
+// the right operand, and stores its own 128 output rows.
 template <bool kAMN, bool kBMN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     det_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     GemmSched sc, GemmOut out) {
   extern __shared__ uint8_t smem_raw[];
-  const PipeSmem ps = pipe_smem(smem_raw);
+  const Pipe2Smem ps = pipe2_smem(smem_raw);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_b);
   }
-  const uint32_t tmem = pipe_setup(ps);
-  using TA = OperandTile<kAMN, kBM>;
-  using TB = OperandTile<kBMN, kBN>;
+  const uint32_t tmem = pipe2_setup(ps);
+  using TA = OperandTile<kAMN, kHalfRows>;
+  using TB = OperandTile<kBMN, kHalfRows>;
 
   if (warp == 0) {
-    if (lane == 0) producer_role<TA, TB>(&tm_a, &tm_b, sc, ps, &g_err_det_gemm);
+    if (lane == 0) producer2_role<TA, TB>(&tm_a, &tm_b, sc, ps, &g_err_det_gemm);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) mma_role<TA, TB>(sc, ps, tmem, idesc_bf16_f32(kBM, kBN, kAMN, kBMN), &g_err_det_gemm);
+    if (lane == 0 && ps.rank == 0)
+      mma2_role<TA, TB>(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, kAMN, kBMN), &g_err_det_gemm);
     __syncwarp();
   } else {
     const int q = warp & 3;
@@ -129,27 +133,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     const int units = sc.num_units();
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      if (!epilogue_acquire(ps, acc, acc_phase, &g_err_det_gemm)) break;
+    for (int u = cluster_index(); u < units; u += cluster_count()) {
+      if (!epilogue2_acquire(ps, acc, acc_phase, &g_err_det_gemm)) break;
       int m0, n0;
       sc.tile_coords(u, 0, m0, n0);
-      const int row = m0 + q * 32 + lane;
+      const int row = m0 + (int)ps.rank * kHalfRows + q * 32 + lane;
       const uint32_t taddr = tmem + acc * kAccCols + lane_off;
 #pragma unroll 1
       for (int c = 0; c < kBN / 32; ++c) {
         const int col0 = n0 + c * 32;
         if (col0 >= out.N) break;               // uniform: depends on the tile only
         uint32_t r[32];
+        __syncwarp();
         tmem_ld32(taddr + c * 32, r);
         tmem_wait_ld();
         if (row < out.M) store_chunk(out, row, col0, r);
       }
-      epilogue_release(ps, acc);
+      epilogue2_release(ps, acc);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
   }
-  pipe_teardown(tmem);
+  pipe2_teardown(tmem);
 }
 
 std::mutex g_attr_mutex;
@@ -158,7 +163,7 @@ bool g_attr_set[64];
 template <bool kAMN, bool kBMN>
 cudaError_t set_attr() {
   return cudaFuncSetAttribute(det_gemm_kernel<kAMN, kBMN>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2Bytes);
 }
 
 cudaError_t ensure_attrs(int dev) {
@@ -232,7 +237,7 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
   if (!dtype_ok(c_dtype)) return RLK_ERR_DTYPE;
   if (accum && c_dtype != RLK_FP32) return RLK_ERR_DTYPE;
   if (ldc < out_cols || ldc >= kLdLimit) return RLK_ERR_SHAPE;
-  const int64_t num_mb = ceil_div(out_rows, kBM), num_nb = ceil_div(out_cols, kBN);
+  const int64_t num_mb = ceil_div(out_rows, kPairRows), num_nb = ceil_div(out_cols, kBN);
   if (num_mb * num_nb >= kDimLimit) return RLK_ERR_SHAPE;
   size_t off = 0;
   plan_operand(x, off);
@@ -264,17 +269,17 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
   if ((st = materialise(x, ws, s, &xp)) != RLK_OK) return st;
   if ((st = materialise(y, ws, s, &yp)) != RLK_OK) return st;
 
-  // Tensor maps: {contiguous extent, row count}, pitch, box.
+  // Tensor maps: {contiguous extent, row count}, pitch, box (128-row halves per CTA).
   CUtensorMap ta, tb;
   bool ok = false;
   switch (kind) {
     case Kind::kFwd:   // A [M,K] K-major; B [K,N] MN-major
-      ok = encode_bf16_2d(&ta, xp, x.cols, x.rows, x.eff_ld, kBK, kBM) &&
+      ok = encode_bf16_2d(&ta, xp, x.cols, x.rows, x.eff_ld, kBK, kHalfRows) &&
            encode_bf16_2d(&tb, yp, y.cols, y.rows, y.eff_ld, 64, kBK);
       break;
     case Kind::kDa:    // dC [M,N] K-major; B [K,N] K-major (N reduced)
-      ok = encode_bf16_2d(&ta, xp, x.cols, x.rows, x.eff_ld, kBK, kBM) &&
-           encode_bf16_2d(&tb, yp, y.cols, y.rows, y.eff_ld, kBK, kBN);
+      ok = encode_bf16_2d(&ta, xp, x.cols, x.rows, x.eff_ld, kBK, kHalfRows) &&
+           encode_bf16_2d(&tb, yp, y.cols, y.rows, y.eff_ld, kBK, kHalfRows);
       break;
     case Kind::kDb:    // A [M,K] MN-major; dC [M,N] MN-major (M reduced)
       ok = encode_bf16_2d(&ta, xp, x.cols, x.rows, x.eff_ld, 64, kBK) &&
@@ -286,7 +291,7 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
   GemmSched sc;
   sc.order.rows = (int)num_mb;
   sc.order.cols = (int)num_nb;
-  sc.order.band = band_rows(num_mb, red);
+  sc.order.band = band_rows(num_mb, red, kPairRows);
   sc.nkb = (int)ceil_div(red, kBK);
   GemmOut o;
   o.M = (int)out_rows;
@@ -297,11 +302,12 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
   o.accum = accum ? 1 : 0;
   o.vec_ok = ptr_aligned(C, 16) && ((ldc * esize(c_dtype)) % 16) == 0;
   const int64_t units = num_mb * num_nb;
-  const int grid = (int)(units < dev.sm_count ? units : dev.sm_count);
+  const int64_t clusters = dev.sm_count / 2;
+  const int grid = 2 * (int)(units < clusters ? units : clusters);
   switch (kind) {
-    case Kind::kFwd: det_gemm_kernel<false, true><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, sc, o); break;
-    case Kind::kDa: det_gemm_kernel<false, false><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, sc, o); break;
-    case Kind::kDb: det_gemm_kernel<true, true><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, sc, o); break;
+    case Kind::kFwd: det_gemm_kernel<false, true><<<grid, kThreads, kSmem2Bytes, s>>>(ta, tb, sc, o); break;
+    case Kind::kDa: det_gemm_kernel<false, false><<<grid, kThreads, kSmem2Bytes, s>>>(ta, tb, sc, o); break;
+    case Kind::kDb: det_gemm_kernel<true, true><<<grid, kThreads, kSmem2Bytes, s>>>(ta, tb, sc, o); break;
   }
   return cudaGetLastError() == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
 }

@@ -148,13 +148,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_weight);
   }
   const uint32_t tmem = pipe2_setup(ps);
+  using THalf = OperandTile<false, kHalfRows>;
 
   if (warp == 0) {
-    if (lane == 0) producer2_role(&tm_hidden, &tm_weight, sc, ps, &g_err_linear_logp);
+    if (lane == 0) producer2_role<THalf, THalf>(&tm_hidden, &tm_weight, sc, ps, &g_err_linear_logp);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0 && ps.rank == 0)
-      mma2_role(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, false, false), &g_err_linear_logp);
+      mma2_role<THalf, THalf>(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, false, false),
+                              &g_err_linear_logp);
     __syncwarp();
   } else {
     const int q = warp & 3;

@@ -9,8 +9,8 @@
 //   grad_weight    = G^T . hidden    (reduction over the N rows in ascending order)
 //   grad_bias[v]   = sum_r G[r, v]   (ascending r)
 //
-// Stage 1 (linear_logp_grad_kernel): the same tcgen05 main loop as the forward
-// recomputes each 128 x 256 logit tile; the epilogue forms G in FP32 from the
+// Stage 1 (linear_logp_grad_kernel): the same 2-SM tcgen05 loop as the forward
+// recomputes each 256 x 256 logit tile (128 rows per CTA of the pair); the epilogue forms G in FP32 from the
 // forward's lse and rounds it to BF16 (nearest even) into the workspace.  Rows
 // are independent, so a row's G (hence its grad_hidden row) does not depend on
 // the other rows in the call.
@@ -25,7 +25,7 @@
 
 #include "rlk.h"
 #include "rlk_internal.h"
-#include "rlk_pipeline.cuh"
+#include "rlk_pipeline2.cuh"
 
 namespace rlk {
 
@@ -34,14 +34,14 @@ __device__ unsigned int g_err_linear_logp_bwd = 0;
 namespace {
 
 struct GradSched {
-  Banded order;    // rows = 128-row blocks, cols = 256-id vocabulary tiles
+  Banded order;    // rows = 256-row blocks (one per CTA pair), cols = 256-id vocabulary tiles
   int nkb;         // 64-wide blocks of H
   __device__ __forceinline__ int num_units() const { return order.count(); }
   __device__ __forceinline__ int unit_tiles(int) const { return 1; }
   __device__ __forceinline__ void tile_coords(int u, int, int& a0, int& b0) const {
     int rb, vt;
     order.unit(u, rb, vt);
-    a0 = rb * kBM;
+    a0 = rb * kPairRows;
     b0 = vt * kBN;
   }
 };
@@ -57,27 +57,27 @@ struct GradArgs {
   int64_t ldG;          // multiple of 8 elements
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     linear_logp_grad_kernel(const __grid_constant__ CUtensorMap tm_hidden,
                             const __grid_constant__ CUtensorMap tm_weight, GradSched sc,
                             GradArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  const PipeSmem ps = pipe_smem(smem_raw);
+  const Pipe2Smem ps = pipe2_smem(smem_raw);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_hidden);
     tma_prefetch_desc(&tm_weight);
   }
-  const uint32_t tmem = pipe_setup(ps);
-  using TA = OperandTile<false, kBM>;
-  using TB = OperandTile<false, kBN>;
+  const uint32_t tmem = pipe2_setup(ps);
+  using THalf = OperandTile<false, kHalfRows>;
 
   if (warp == 0) {
-    if (lane == 0) producer_role<TA, TB>(&tm_hidden, &tm_weight, sc, ps, &g_err_linear_logp_bwd);
+    if (lane == 0) producer2_role<THalf, THalf>(&tm_hidden, &tm_weight, sc, ps, &g_err_linear_logp_bwd);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0)
-      mma_role<TA, TB>(sc, ps, tmem, idesc_bf16_f32(kBM, kBN, false, false), &g_err_linear_logp_bwd);
+    if (lane == 0 && ps.rank == 0)
+      mma2_role<THalf, THalf>(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, false, false),
+                              &g_err_linear_logp_bwd);
     __syncwarp();
   } else {
     const int q = warp & 3;
@@ -85,11 +85,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     const int units = sc.num_units();
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      if (!epilogue_acquire(ps, acc, acc_phase, &g_err_linear_logp_bwd)) break;
+    for (int u = cluster_index(); u < units; u += cluster_count()) {
+      if (!epilogue2_acquire(ps, acc, acc_phase, &g_err_linear_logp_bwd)) break;
       int r0, v0;
       sc.tile_coords(u, 0, r0, v0);
-      const int row = r0 + q * 32 + lane;
+      const int row = r0 + (int)ps.rank * kHalfRows + q * 32 + lane;
       const bool valid = row < a.N;
       int64_t t = -1;
       float g = 0.f, L = 0.f;
@@ -133,12 +133,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
         }
       }
-      epilogue_release(ps, acc);
+      epilogue2_release(ps, acc);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
   }
-  pipe_teardown(tmem);
+  pipe2_teardown(tmem);
 }
 
 // grad_bias[v] = sum over rows r = 0..N-1 (ascending) of G[r, v], two columns per thread.
@@ -168,7 +168,7 @@ cudaError_t ensure_attrs(int dev) {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!g_attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(linear_logp_grad_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2Bytes);
     if (e != cudaSuccess) return e;
     g_attr_set[dev] = true;
   }
@@ -250,13 +250,13 @@ rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H, in
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   CUtensorMap tm_h, tm_w;
-  if (!encode_bf16_2d(&tm_h, hidden, H, N, ld_hidden, kBK, kBM) ||
-      !encode_bf16_2d(&tm_w, weight, H, V, ld_weight, kBK, kBN))
+  if (!encode_bf16_2d(&tm_h, hidden, H, N, ld_hidden, kBK, kHalfRows) ||
+      !encode_bf16_2d(&tm_w, weight, H, V, ld_weight, kBK, kHalfRows))
     return RLK_ERR_CUDA;
   GradSched sc;
-  sc.order.rows = (int)ceil_div(N, kBM);
+  sc.order.rows = (int)ceil_div(N, kPairRows);
   sc.order.cols = (int)ceil_div(V, kBN);
-  sc.order.band = band_rows(sc.order.rows, H);
+  sc.order.band = band_rows(sc.order.rows, H, kPairRows);
   sc.nkb = (int)ceil_div(H, kBK);
   if ((int64_t)sc.order.rows * sc.order.cols >= (int64_t(1) << 31)) return RLK_ERR_SHAPE;
   GradArgs a;
@@ -270,8 +270,9 @@ rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H, in
   a.G = static_cast<uint16_t*>(workspace);
   a.ldG = grad_ld(V);
   const int64_t units = (int64_t)sc.order.rows * sc.order.cols;
-  const int grid = (int)(units < dev.sm_count ? units : dev.sm_count);
-  linear_logp_grad_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_h, tm_w, sc, a);
+  const int64_t clusters = dev.sm_count / 2;
+  const int grid = 2 * (int)(units < clusters ? units : clusters);
+  linear_logp_grad_kernel<<<grid, kThreads, kSmem2Bytes, s>>>(tm_h, tm_w, sc, a);
   if (cudaGetLastError() != cudaSuccess) return RLK_ERR_CUDA;
 
   if (grad_hidden) {   // [N, H] = G [N, V] . W [V, H]

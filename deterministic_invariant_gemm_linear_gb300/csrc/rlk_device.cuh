@@ -248,16 +248,33 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
 //    the MN extent (LBO = 8 KiB between 64-element MN atoms); reduction rows are
 //    128 bytes apart with 8-row groups 1024 bytes apart (SBO); the 16-element
 //    reduction step advances the start address by 2 groups = 2048 bytes.
+// 2-D tiled load into this CTA's shared memory whose completion is counted on
+// an mbarrier of either CTA of a cluster pair (`cta_group::2`).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t mbar,
+                                                 int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
 template <bool kMN, int kRows>
 struct OperandTile {
   static constexpr uint32_t kBytes = kRows * kBK * 2;
+  // kPair: the copies complete on a barrier that may live in the pair's other CTA.
+  template <bool kPair = false>
   static __device__ __forceinline__ void load(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                               int32_t row0, int32_t k0) {
     if constexpr (!kMN) {
-      tma_load_2d(dst, map, bar, k0, row0);
+      if constexpr (kPair) tma_load_2d_pair(dst, map, bar, k0, row0);
+      else tma_load_2d(dst, map, bar, k0, row0);
     } else {
 #pragma unroll
-      for (int i = 0; i < kRows / 64; ++i) tma_load_2d(dst + i * 8192, map, bar, row0 + 64 * i, k0);
+      for (int i = 0; i < kRows / 64; ++i) {
+        if constexpr (kPair) tma_load_2d_pair(dst + i * 8192, map, bar, row0 + 64 * i, k0);
+        else tma_load_2d(dst + i * 8192, map, bar, row0 + 64 * i, k0);
+      }
     }
   }
   static __device__ __forceinline__ uint64_t desc(uint32_t base, int kstep) {

@@ -60,16 +60,6 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
-// Tile load into this CTA's shared memory whose completion is counted on an
-// mbarrier of either CTA of the pair (here always rank 0's).
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t mbar,
-                                                 int32_t c0, int32_t c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar), "r"(c0), "r"(c1)
-      : "memory");
-}
 __device__ __forceinline__ void umma_pair_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -175,11 +165,13 @@ __device__ __forceinline__ void pipe2_teardown(uint32_t tmem) {
 }
 
 // Schedule interface as for the one-CTA loop, with a0 = first row of the
-// cluster's 256-row block and b0 = first row of the 256-row right-operand tile.
-template <class Sched>
+// cluster's 256-row block and b0 = first row of the 256-row right-operand tile;
+// TA / TB are the 128-row operand halves (OperandTile<majorness, 128>).
+template <class TA, class TB, class Sched>
 __device__ __forceinline__ void producer2_role(const CUtensorMap* ta, const CUtensorMap* tb,
                                                const Sched& sc, const Pipe2Smem& ps,
                                                unsigned int* err) {
+  static_assert(TA::kBytes == kA2Bytes && TB::kBytes == kB2Bytes, "operand halves are 128 rows");
   int stage = 0;
   uint32_t phase = 0, issued = 0, last_parity = 0;
   bool run = true;
@@ -198,8 +190,8 @@ __device__ __forceinline__ void producer2_role(const CUtensorMap* ta, const CUte
         if (ps.rank == 0) mbar_arrive_expect_tx(ps.full(stage), 2 * kStage2Bytes);
         const uint32_t leader_full = mapa_shared(ps.full(stage), 0);
         const uint32_t sa = ps.stages + stage * kStage2Bytes;
-        tma_load_2d_pair(sa, ta, leader_full, kb * kBK, a0 + half);
-        tma_load_2d_pair(sa + kA2Bytes, tb, leader_full, kb * kBK, b0 + half);
+        TA::template load<true>(sa, ta, leader_full, a0 + half, kb * kBK);
+        TB::template load<true>(sa + kA2Bytes, tb, leader_full, b0 + half, kb * kBK);
         issued |= 1u << stage;
         last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == kStages2) {
@@ -223,7 +215,7 @@ __device__ __forceinline__ void producer2_role(const CUtensorMap* ta, const CUte
   }
 }
 
-template <class Sched>
+template <class TA, class TB, class Sched>
 __device__ __forceinline__ void mma2_role(const Sched& sc, const Pipe2Smem& ps, uint32_t tmem,
                                           uint32_t idesc, unsigned int* err) {
   int stage = 0, acc = 0;
@@ -249,9 +241,7 @@ __device__ __forceinline__ void mma2_role(const Sched& sc, const Pipe2Smem& ps, 
         const uint32_t sb = sa + kA2Bytes;
 #pragma unroll
         for (int k = 0; k < kBK / kUmmaK; ++k)
-          umma_pair_bf16(d, OperandTile<false, kHalfRows>::desc(sa, k),
-                         OperandTile<false, kHalfRows>::desc(sb, k), idesc,
-                         (kb | k) != 0 ? 1u : 0u);
+          umma_pair_bf16(d, TA::desc(sa, k), TB::desc(sb, k), idesc, (kb | k) != 0 ? 1u : 0u);
         umma_pair_commit(ps.empty(stage), 0x3);
         if (++stage == kStages2) {
           stage = 0;
