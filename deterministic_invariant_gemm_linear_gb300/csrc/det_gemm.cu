@@ -22,7 +22,7 @@
 
 #include "rlk.h"
 #include "rlk_internal.h"
-#include "rlk_pipeline2.cuh"
+#include "rlk_pipeline.cuh"
 
 namespace rlk {
 
@@ -110,22 +110,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     det_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     GemmSched sc, GemmOut out) {
   extern __shared__ uint8_t smem_raw[];
-  const Pipe2Smem ps = pipe2_smem(smem_raw);
+  const PipeSmem ps = pipe_smem(smem_raw);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_a);
     tma_prefetch_desc(&tm_b);
   }
-  const uint32_t tmem = pipe2_setup(ps);
+  const uint32_t tmem = pipe_setup(ps);
   using TA = OperandTile<kAMN, kHalfRows>;
   using TB = OperandTile<kBMN, kHalfRows>;
 
   if (warp == 0) {
-    if (lane == 0) producer2_role<TA, TB>(&tm_a, &tm_b, sc, ps, &g_err_det_gemm);
+    if (lane == 0) producer_role<TA, TB>(&tm_a, &tm_b, sc, ps, &g_err_det_gemm);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0 && ps.rank == 0)
-      mma2_role<TA, TB>(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, kAMN, kBMN), &g_err_det_gemm);
+      mma_role<TA, TB>(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, kAMN, kBMN), &g_err_det_gemm);
     __syncwarp();
   } else {
     const int q = warp & 3;
@@ -134,7 +134,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     const int units = sc.num_units();
     for (int u = cluster_index(); u < units; u += cluster_count()) {
-      if (!epilogue2_acquire(ps, acc, acc_phase, &g_err_det_gemm)) break;
+      if (!epilogue_acquire(ps, acc, acc_phase, &g_err_det_gemm)) break;
       int m0, n0;
       sc.tile_coords(u, 0, m0, n0);
       const int row = m0 + (int)ps.rank * kHalfRows + q * 32 + lane;
@@ -149,12 +149,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         if (row < out.M) store_chunk(out, row, col0, r);
       }
-      epilogue2_release(ps, acc);
+      epilogue_release(ps, acc);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
   }
-  pipe2_teardown(tmem);
+  pipe_teardown(tmem);
 }
 
 std::mutex g_attr_mutex;
@@ -163,7 +163,7 @@ bool g_attr_set[64];
 template <bool kAMN, bool kBMN>
 cudaError_t set_attr() {
   return cudaFuncSetAttribute(det_gemm_kernel<kAMN, kBMN>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2Bytes);
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
 }
 
 cudaError_t ensure_attrs(int dev) {
@@ -305,9 +305,9 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
   const int64_t clusters = dev.sm_count / 2;
   const int grid = 2 * (int)(units < clusters ? units : clusters);
   switch (kind) {
-    case Kind::kFwd: det_gemm_kernel<false, true><<<grid, kThreads, kSmem2Bytes, s>>>(ta, tb, sc, o); break;
-    case Kind::kDa: det_gemm_kernel<false, false><<<grid, kThreads, kSmem2Bytes, s>>>(ta, tb, sc, o); break;
-    case Kind::kDb: det_gemm_kernel<true, true><<<grid, kThreads, kSmem2Bytes, s>>>(ta, tb, sc, o); break;
+    case Kind::kFwd: det_gemm_kernel<false, true><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, sc, o); break;
+    case Kind::kDa: det_gemm_kernel<false, false><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, sc, o); break;
+    case Kind::kDb: det_gemm_kernel<true, true><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, sc, o); break;
   }
   return cudaGetLastError() == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
 }

@@ -27,7 +27,7 @@
 
 #include "rlk.h"
 #include "rlk_internal.h"
-#include "rlk_pipeline2.cuh"
+#include "rlk_pipeline.cuh"
 
 namespace rlk {
 
@@ -141,21 +141,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                      const __grid_constant__ CUtensorMap tm_weight, LogpSched sc,
                                      LogpArgs args) {
   extern __shared__ uint8_t smem_raw[];
-  const Pipe2Smem ps = pipe2_smem(smem_raw);
+  const PipeSmem ps = pipe_smem(smem_raw);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_hidden);
     tma_prefetch_desc(&tm_weight);
   }
-  const uint32_t tmem = pipe2_setup(ps);
+  const uint32_t tmem = pipe_setup(ps);
   using THalf = OperandTile<false, kHalfRows>;
 
   if (warp == 0) {
-    if (lane == 0) producer2_role<THalf, THalf>(&tm_hidden, &tm_weight, sc, ps, &g_err_linear_logp);
+    if (lane == 0) producer_role<THalf, THalf>(&tm_hidden, &tm_weight, sc, ps, &g_err_linear_logp);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0 && ps.rank == 0)
-      mma2_role<THalf, THalf>(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, false, false),
+      mma_role<THalf, THalf>(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, false, false),
                               &g_err_linear_logp);
     __syncwarp();
   } else {
@@ -174,7 +174,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool have_zt = false;
       const int t0 = sc.first_tile(u), nt = sc.unit_tiles(u);
       for (int i = 0; i < nt; ++i) {
-        if (!epilogue2_acquire(ps, acc, acc_phase, &g_err_linear_logp)) {
+        if (!epilogue_acquire(ps, acc, acc_phase, &g_err_linear_logp)) {
           run = false;
           break;
         }
@@ -190,7 +190,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           logp_chunk(r, vbase, args.V, args.bias, tgt, m, s, have_zt, zt);
         }
-        epilogue2_release(ps, acc);
+        epilogue_release(ps, acc);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
@@ -201,7 +201,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
   }
-  pipe2_teardown(tmem);
+  pipe_teardown(tmem);
 }
 
 // (m, s) pair merge with explicit roundings, so merge(a, b) == merge(b, a) bitwise.
@@ -257,7 +257,7 @@ cudaError_t ensure_attrs(int dev) {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!g_attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(linear_logp_partials_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2Bytes);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     g_attr_set[dev] = true;
   }
@@ -368,7 +368,7 @@ rlk_status rlk_linear_logp_partials(const void* hidden, int64_t N, int64_t H, in
   }
   constexpr int kRowsPerUnit = kPairRows, kBoxRows = kHalfRows;
   CUtensorMap tm_h, tm_w;
-  if (!encode_bf16_2d(&tm_h, h_src, H, N, p.ldh, kBK, kBM) ||
+  if (!encode_bf16_2d(&tm_h, h_src, H, N, p.ldh, kBK, kHalfRows) ||
       !encode_bf16_2d(&tm_w, w_src, H, V, p.ldw, kBK, kBoxRows))
     return RLK_ERR_CUDA;
 
@@ -394,7 +394,7 @@ rlk_status rlk_linear_logp_partials(const void* hidden, int64_t N, int64_t H, in
   // One cluster of two CTAs per pair of SMs, persistent over the units.
   const int64_t clusters = dev.sm_count / 2;
   const int grid = 2 * (int)(units < clusters ? units : clusters);
-  linear_logp_partials_kernel<<<grid, kThreads, kSmem2Bytes, s>>>(tm_h, tm_w, sc, a);
+  linear_logp_partials_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_h, tm_w, sc, a);
   return cudaGetLastError() == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
 }
 

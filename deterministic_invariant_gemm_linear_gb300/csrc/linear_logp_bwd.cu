@@ -25,7 +25,7 @@
 
 #include "rlk.h"
 #include "rlk_internal.h"
-#include "rlk_pipeline2.cuh"
+#include "rlk_pipeline.cuh"
 
 namespace rlk {
 
@@ -62,21 +62,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             const __grid_constant__ CUtensorMap tm_weight, GradSched sc,
                             GradArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  const Pipe2Smem ps = pipe2_smem(smem_raw);
+  const PipeSmem ps = pipe_smem(smem_raw);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_hidden);
     tma_prefetch_desc(&tm_weight);
   }
-  const uint32_t tmem = pipe2_setup(ps);
+  const uint32_t tmem = pipe_setup(ps);
   using THalf = OperandTile<false, kHalfRows>;
 
   if (warp == 0) {
-    if (lane == 0) producer2_role<THalf, THalf>(&tm_hidden, &tm_weight, sc, ps, &g_err_linear_logp_bwd);
+    if (lane == 0) producer_role<THalf, THalf>(&tm_hidden, &tm_weight, sc, ps, &g_err_linear_logp_bwd);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0 && ps.rank == 0)
-      mma2_role<THalf, THalf>(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, false, false),
+      mma_role<THalf, THalf>(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, false, false),
                               &g_err_linear_logp_bwd);
     __syncwarp();
   } else {
@@ -86,7 +86,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     const int units = sc.num_units();
     for (int u = cluster_index(); u < units; u += cluster_count()) {
-      if (!epilogue2_acquire(ps, acc, acc_phase, &g_err_linear_logp_bwd)) break;
+      if (!epilogue_acquire(ps, acc, acc_phase, &g_err_linear_logp_bwd)) break;
       int r0, v0;
       sc.tile_coords(u, 0, r0, v0);
       const int row = r0 + (int)ps.rank * kHalfRows + q * 32 + lane;
@@ -133,12 +133,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
         }
       }
-      epilogue2_release(ps, acc);
+      epilogue_release(ps, acc);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
   }
-  pipe2_teardown(tmem);
+  pipe_teardown(tmem);
 }
 
 // grad_bias[v] = sum over rows r = 0..N-1 (ascending) of G[r, v], two columns per thread.
@@ -168,7 +168,7 @@ cudaError_t ensure_attrs(int dev) {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!g_attr_set[dev]) {
     cudaError_t e = cudaFuncSetAttribute(linear_logp_grad_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2Bytes);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     g_attr_set[dev] = true;
   }
@@ -272,7 +272,7 @@ rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H, in
   const int64_t units = (int64_t)sc.order.rows * sc.order.cols;
   const int64_t clusters = dev.sm_count / 2;
   const int grid = 2 * (int)(units < clusters ? units : clusters);
-  linear_logp_grad_kernel<<<grid, kThreads, kSmem2Bytes, s>>>(tm_h, tm_w, sc, a);
+  linear_logp_grad_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_h, tm_w, sc, a);
   if (cudaGetLastError() != cudaSuccess) return RLK_ERR_CUDA;
 
   if (grad_hidden) {   // [N, H] = G [N, V] . W [V, H]

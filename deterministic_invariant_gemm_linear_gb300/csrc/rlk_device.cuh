@@ -13,25 +13,18 @@
 namespace rlk {
 
 // ---------------------------------------------------------------- tile shape
-// One CTA owns one 128 x 256 FP32 accumulator tile per MMA chain; the
-// reduction advances in blocks of 64 BF16 (128 bytes = one 128B-swizzle row).
-constexpr int kBM = 128;           // accumulator rows (TMEM lanes)
-constexpr int kBN = 256;           // accumulator columns (TMEM columns)
+// A pair of CTAs (a cluster of two, one per SM) owns one 256 x 256 FP32
+// accumulator tile per MMA chain, 128 rows in each CTA's TMEM; the reduction
+// advances in blocks of 64 BF16 (128 bytes = one 128B-swizzle row).
+constexpr int kHalfRows = 128;     // accumulator rows (TMEM lanes) per CTA; operand rows per CTA
+constexpr int kPairRows = 2 * kHalfRows;      // accumulator rows per CTA pair (MMA M)
+constexpr int kBN = 256;           // accumulator columns (TMEM columns, MMA N)
 constexpr int kBK = 64;            // reduction block per pipeline stage
 constexpr int kUmmaK = 16;         // reduction per tcgen05.mma (kind::f16)
-constexpr int kStages = 4;         // shared-memory pipeline depth
-constexpr int kAStageBytes = kBM * kBK * 2;   // 16 KiB
-constexpr int kBStageBytes = kBN * kBK * 2;   // 32 KiB
-constexpr int kStageBytes = kAStageBytes + kBStageBytes;
 constexpr int kAccCols = kBN;      // FP32 accumulator columns per buffer
 constexpr int kTmemCols = 2 * kAccCols;       // double-buffered accumulator: 512 columns
 constexpr int kThreads = 192;      // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kEpilogueThreads = 128;
-// Barriers and bookkeeping after the stage buffers, plus alignment slack.
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
-static_assert(kSmemBytes <= 232448, "exceeds the 227 KiB per-CTA shared memory limit");
-// One CTA per SM: a second resident CTA could not get TMEM columns.
-static_assert(kSmemBytes > 232448 / 2, "tcgen05 kernels must own their SM");
 
 // Bounded waits: a wait that has not completed after this long gives up,
 // raises the device error word and makes the CTA wind down.

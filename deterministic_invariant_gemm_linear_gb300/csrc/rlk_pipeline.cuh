@@ -1,46 +1,111 @@
-// The warp-specialised tcgen05 main loop shared by the fused linear-logp
-// kernel and the det_gemm kernel.
+// The warp-specialised, persistent 2-SM (cta_group::2) tcgen05 main loop shared
+// by every tensor-core kernel of the library.
 //
-// CTA layout (192 threads, one CTA per SM, persistent over work units):
-//   warp 0, lane 0  TMA producer: streams (A, B) reduction blocks of 64 into a
-//                   kStages-deep shared-memory ring (full / empty mbarriers).
-//   warp 1          allocates 512 TMEM columns; lane 0 issues tcgen05.mma
-//                   (M=128, N=256, K=16) into one of two FP32 accumulators and
-//                   commits to the stage's empty barrier and, at the end of a
-//                   tile, to the accumulator's full barrier.
-//   warps 2..5      epilogue: each thread owns one accumulator row (TMEM lane)
-//                   and releases the accumulator through its empty barrier.
-//
-// The reduction of every accumulator tile runs over its blocks in ascending
-// order and always starts from zero: the arithmetic of a tile depends only on
-// its two operand tiles, never on the schedule, the grid or the row count.
-//
-// Work description: a Schedule provides
-//   int  num_units() const;                       units are dealt round-robin
-//   int  unit_tiles(int u) const;                 accumulator tiles in unit u
-//   void tile_coords(int u, int i, int& a_row0, int& b_row0) const;
-//   int  nkb;                                     reduction blocks per tile
+// A cluster of two CTAs on two SMs computes one 256 x 256 FP32 accumulator
+// tile per MMA chain: rank r holds rows [128 r, 128 r + 128) of the left
+// operand and rows [128 r, 128 r + 128) of the right operand's 256-row tile in
+// its own shared memory, and its own 128 rows of the accumulator in its own
+// TMEM.  Rank 0 issues tcgen05.mma.cta_group::2 (M=256, N=256, K=16) for both.
+//   warp 0, lane 0  TMA producer in each CTA; both CTAs' copies complete on
+//                   rank 0's full barrier (rank 0 arms it for both halves).
+//   warp 1          allocates 512 TMEM columns collectively with the peer; in
+//                   rank 0, lane 0 issues the MMAs and commits to both CTAs'
+//                   empty / accumulator-full barriers (multicast).
+//   warps 2..5      epilogue on the CTA's own 128 accumulator rows; each warp
+//                   releases the accumulator on rank 0's barrier (8 arrivals).
+// Compared with one CTA owning a 128 x 256 tile, each SM reads half the
+// right-operand bytes from shared memory per MMA for the same accumulator shape.
 #pragma once
 
 #include "rlk_device.cuh"
 
 namespace rlk {
 
-// Shared-memory bookkeeping that follows the stage buffers.
+constexpr int kStages = 6;                            // shared-memory pipeline depth
+constexpr int kAStageBytes = kHalfRows * kBK * 2;     // 16 KiB: this CTA's left-operand half
+constexpr int kBStageBytes = kHalfRows * kBK * 2;     // 16 KiB: this CTA's right-operand half
+constexpr int kStageBytes = kAStageBytes + kBStageBytes;
+// Stage ring, alignment slack and the barrier block.
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
+static_assert(kSmemBytes <= 232448, "exceeds the 227 KiB per-CTA shared memory limit");
+// One CTA per SM: a second resident CTA could not get TMEM columns.
+static_assert(kSmemBytes > 232448 / 2, "tcgen05 kernels must own their SM");
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_index() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory offset in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+__device__ __forceinline__ void umma_pair_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once, on the barrier at this shared offset in every CTA of `mask`,
+// when all MMAs issued so far by this thread are done.
+__device__ __forceinline__ void umma_pair_commit(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar), "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
 struct PipeBarriers {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t acc_full[2];
-  uint64_t acc_empty[2];
-  uint64_t drained;
+  uint64_t full[kStages];    // used in rank 0 only: both CTAs' copies for a stage
+  uint64_t empty[kStages];   // per CTA: the stage's shared memory may be refilled
+  uint64_t acc_full[2];       // per CTA: accumulator b holds a finished tile
+  uint64_t acc_empty[2];      // rank 0: both CTAs' epilogues released accumulator b
+  uint64_t drained;           // rank 0: every issued MMA has completed
   uint32_t tmem_base;
   int abort_flag;
 };
 static_assert(sizeof(PipeBarriers) <= 256, "barrier block overflows its reserved bytes");
 
 struct PipeSmem {
-  uint32_t stages;       // shared address of stage 0 (1024-byte aligned)
-  PipeBarriers* bars;    // generic pointer to the barrier block
+  uint32_t stages;
+  PipeBarriers* bars;
+  uint32_t rank;
   __device__ __forceinline__ uint32_t full(int s) const { return smem_u32(&bars->full[s]); }
   __device__ __forceinline__ uint32_t empty(int s) const { return smem_u32(&bars->empty[s]); }
   __device__ __forceinline__ uint32_t acc_full(int b) const { return smem_u32(&bars->acc_full[b]); }
@@ -50,19 +115,18 @@ struct PipeSmem {
   __device__ __forceinline__ volatile int* abort_flag() const { return &bars->abort_flag; }
 };
 
-// Carves the dynamic shared memory: stage ring first (1024-byte aligned), then
-// the barrier block.
 __device__ __forceinline__ PipeSmem pipe_smem(uint8_t* raw) {
   const uint32_t base = smem_u32(raw);
   const uint32_t pad = (1024u - (base & 1023u)) & 1023u;
   PipeSmem p;
   p.stages = base + pad;
   p.bars = reinterpret_cast<PipeBarriers*>(raw + pad + kStages * kStageBytes);
+  p.rank = cluster_rank();
   return p;
 }
 
-// Barrier initialisation (one thread) and TMEM allocation (warp 1); ends with
-// a CTA barrier so every role sees both.
+// Barrier initialisation, collective TMEM allocation, then a cluster barrier
+// so that no CTA touches its peer's barriers before they exist.
 __device__ __forceinline__ uint32_t pipe_setup(const PipeSmem& ps) {
   const int warp = threadIdx.x / 32;
   if (threadIdx.x == 0) {
@@ -72,42 +136,57 @@ __device__ __forceinline__ uint32_t pipe_setup(const PipeSmem& ps) {
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(ps.acc_full(b), 1);
-      mbar_init(ps.acc_empty(b), kEpilogueThreads);
+      mbar_init(ps.acc_empty(b), 2 * (kEpilogueThreads / 32));
     }
     mbar_init(smem_u32(&ps.bars->drained), 1);
     ps.bars->abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ps.bars->tmem_base), kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(&ps.bars->tmem_base), kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();
   tc_fence_after();
   return ps.bars->tmem_base;
 }
 
-// Final CTA barrier and TMEM release (warp 1).  Every role has drained its
-// asynchronous work before reaching this point.
+// Cluster barrier (no CTA leaves while its peer may still signal it or read
+// its shared memory), then the collective TMEM release.
 __device__ __forceinline__ void pipe_teardown(uint32_t tmem) {
   tc_fence_before();
   __syncthreads();
+  cluster_sync();
   if (threadIdx.x / 32 == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc_pair(tmem, kTmemCols);
   }
 }
 
+// Work description: a Schedule provides
+//   int  num_units() const;                    units are dealt to clusters round-robin
+//   int  unit_tiles(int u) const;              accumulator tiles in unit u
+//   void tile_coords(int u, int i, int& a0, int& b0) const;
+//        a0 = first row of the pair's 256-row block of the left operand,
+//        b0 = first row of the 256-row right-operand tile
+//   int  nkb;                                  reduction blocks of 64 per tile
+// The reduction of every tile runs over its blocks in ascending order and starts
+// from zero, so a tile's arithmetic depends only on its operand tiles, never on
+// the schedule, the grid or the row count.  TA / TB are the 128-row operand
+// halves (OperandTile<majorness, 128>).
 template <class TA, class TB, class Sched>
 __device__ __forceinline__ void producer_role(const CUtensorMap* ta, const CUtensorMap* tb,
-                                              const Sched& sc, const PipeSmem& ps,
-                                              unsigned int* err) {
+                                               const Sched& sc, const PipeSmem& ps,
+                                               unsigned int* err) {
+  static_assert(TA::kBytes == kAStageBytes && TB::kBytes == kBStageBytes, "operand halves are 128 rows");
   int stage = 0;
   uint32_t phase = 0, issued = 0, last_parity = 0;
   bool run = true;
+  const int32_t half = (int32_t)ps.rank * kHalfRows;
   const int units = sc.num_units();
-  for (int u = blockIdx.x; run && u < units; u += gridDim.x) {
+  for (int u = cluster_index(); run && u < units; u += cluster_count()) {
     const int nt = sc.unit_tiles(u);
     for (int i = 0; run && i < nt; ++i) {
       int a0, b0;
@@ -117,11 +196,11 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* ta, const CUten
           run = false;
           break;
         }
-        const uint32_t full = ps.full(stage);
-        mbar_arrive_expect_tx(full, kStageBytes);
+        if (ps.rank == 0) mbar_arrive_expect_tx(ps.full(stage), 2 * kStageBytes);
+        const uint32_t leader_full = mapa_shared(ps.full(stage), 0);
         const uint32_t sa = ps.stages + stage * kStageBytes;
-        TA::load(sa, ta, full, a0, kb * kBK);
-        TB::load(sa + kAStageBytes, tb, full, b0, kb * kBK);
+        TA::template load<true>(sa, ta, leader_full, a0 + half, kb * kBK);
+        TB::template load<true>(sa + kAStageBytes, tb, leader_full, b0 + half, kb * kBK);
         issued |= 1u << stage;
         last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == kStages) {
@@ -131,19 +210,28 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* ta, const CUten
       }
     }
   }
-  // Let every issued copy land before the CTA can exit.
-  for (int s = 0; s < kStages; ++s)
-    if ((issued >> s) & 1u) mbar_wait_drain(ps.full(s), (last_parity >> s) & 1u, err);
+  if (ps.rank == 0) {
+    // Rank 0's full barriers count both CTAs' bytes: once they complete, every
+    // copy of the pair has landed.
+    for (int s = 0; s < kStages; ++s)
+      if ((issued >> s) & 1u) mbar_wait_drain(ps.full(s), (last_parity >> s) & 1u, err);
+  } else if (!run) {
+    // Winding down early: rank 1 cannot observe rank 0's barriers, so it gives
+    // its last copies a bounded 1 ms to land before the CTA may exit.
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 1000000ull) {
+    }
+  }
 }
 
 template <class TA, class TB, class Sched>
 __device__ __forceinline__ void mma_role(const Sched& sc, const PipeSmem& ps, uint32_t tmem,
-                                         uint32_t idesc, unsigned int* err) {
+                                          uint32_t idesc, unsigned int* err) {
   int stage = 0, acc = 0;
   uint32_t phase = 0, acc_phase = 0;
   bool run = true;
   const int units = sc.num_units();
-  for (int u = blockIdx.x; run && u < units; u += gridDim.x) {
+  for (int u = cluster_index(); run && u < units; u += cluster_count()) {
     const int nt = sc.unit_tiles(u);
     for (int i = 0; run && i < nt; ++i) {
       if (!mbar_wait(ps.acc_empty(acc), acc_phase ^ 1u, ps.abort_flag(), err)) {
@@ -162,37 +250,41 @@ __device__ __forceinline__ void mma_role(const Sched& sc, const PipeSmem& ps, ui
         const uint32_t sb = sa + kAStageBytes;
 #pragma unroll
         for (int k = 0; k < kBK / kUmmaK; ++k)
-          umma_bf16(d, TA::desc(sa, k), TB::desc(sb, k), idesc, (kb | k) != 0 ? 1u : 0u);
-        umma_commit(ps.empty(stage));
+          umma_pair_bf16(d, TA::desc(sa, k), TB::desc(sb, k), idesc, (kb | k) != 0 ? 1u : 0u);
+        umma_pair_commit(ps.empty(stage), 0x3);
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
       if (!run) break;
-      umma_commit(ps.acc_full(acc));
+      umma_pair_commit(ps.acc_full(acc), 0x3);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
   }
-  // Every MMA issued above completes before the CTA frees TMEM.
-  umma_commit(smem_u32(&ps.bars->drained));
+  umma_pair_commit(smem_u32(&ps.bars->drained), 0x1);
   mbar_wait_drain(smem_u32(&ps.bars->drained), 0, err);
 }
 
-// Epilogue-side wait for an accumulator: all 32 lanes poll, then agree, so the
-// warp-collective tcgen05.ld that follows is never reached by part of a warp.
 __device__ __forceinline__ bool epilogue_acquire(const PipeSmem& ps, int acc, uint32_t parity,
-                                                 unsigned int* err) {
+                                                  unsigned int* err) {
   const bool ok = mbar_wait(ps.acc_full(acc), parity, ps.abort_flag(), err);
   const bool all = __all_sync(0xffffffffu, ok);
   tc_fence_after();
   return all;
 }
 
+// Warp-level release of an accumulator on rank 0's barrier.
 __device__ __forceinline__ void epilogue_release(const PipeSmem& ps, int acc) {
   tc_fence_before();
-  mbar_arrive(ps.acc_empty(acc));
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) {
+    if (ps.rank == 0)
+      mbar_arrive(ps.acc_empty(acc));
+    else
+      mbar_arrive_cluster(mapa_shared(ps.acc_empty(acc), 0));
+  }
 }
 
 }  // namespace rlk
