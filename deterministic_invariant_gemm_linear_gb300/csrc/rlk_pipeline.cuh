@@ -21,7 +21,7 @@
 
 namespace rlk {
 
-constexpr int kStages = 6;                            // shared-memory pipeline depth
+constexpr int kStages = 7;                            // shared-memory pipeline depth
 constexpr int kAStageBytes = kHalfRows * kBK * 2;     // 16 KiB: this CTA's left-operand half
 constexpr int kBStageBytes = kHalfRows * kBK * 2;     // 16 KiB: this CTA's right-operand half
 constexpr int kStageBytes = kAStageBytes + kBStageBytes;
