@@ -32,6 +32,7 @@ namespace {
 
 struct GemmSched {
   Banded order; // rows = 256-row output blocks (one per CTA pair), cols = 256-column blocks
+  int* counter; // nullptr: cluster c takes units c, c + C, ... (a few rounds at most sizes)
   int nkb;      // 64-wide reduction blocks
   __device__ __forceinline__ int num_units() const { return order.count(); }
   __device__ __forceinline__ int unit_tiles(int) const { return 1; }
@@ -122,6 +123,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) producer_role<TA, TB>(&tm_a, &tm_b, sc, ps, &g_err_det_gemm);
+    if (lane == 1 && ps.rank == 0) scheduler_role(sc, ps, &g_err_det_gemm);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0 && ps.rank == 0)
@@ -132,8 +134,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     int acc = 0;
     uint32_t acc_phase = 0;
-    const int units = sc.num_units();
-    for (int u = cluster_index(); u < units; u += cluster_count()) {
+    for (int k = 0;; ++k) {
+      const int u = warp_unit_take(sc, ps, k, &g_err_det_gemm);
+      if (u < 0) break;
       if (!epilogue_acquire(ps, acc, acc_phase, &g_err_det_gemm)) break;
       int m0, n0;
       sc.tile_coords(u, 0, m0, n0);
@@ -292,6 +295,7 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
   sc.order.rows = (int)num_mb;
   sc.order.cols = (int)num_nb;
   sc.order.band = band_rows(num_mb, red, kPairRows);
+  sc.counter = nullptr;
   sc.nkb = (int)ceil_div(red, kBK);
   GemmOut o;
   o.M = (int)out_rows;

@@ -36,7 +36,8 @@ __device__ unsigned int g_err_linear_logp = 0;
 namespace {
 
 struct LogpSched {
-  Banded order;    // rows = 128-row blocks, cols = vocabulary splits
+  Banded order;    // rows = 256-row blocks, cols = vocabulary splits
+  int* counter;    // zeroed unit counter in the workspace (units handed out in order)
   int S;           // vocabulary splits
   int vps;         // 256-id tiles per split
   int vtiles;      // 256-id tiles in the vocabulary
@@ -152,6 +153,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) producer_role<THalf, THalf>(&tm_hidden, &tm_weight, sc, ps, &g_err_linear_logp);
+    if (lane == 1 && ps.rank == 0) scheduler_role(sc, ps, &g_err_linear_logp);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0 && ps.rank == 0)
@@ -164,8 +166,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool run = true;
-    const int units = sc.num_units();
-    for (int u = cluster_index(); run && u < units; u += cluster_count()) {
+    for (int k = 0; run; ++k) {
+      const int u = warp_unit_take(sc, ps, k, &g_err_linear_logp);
+      if (u < 0) break;
       const int j = sc.split_of(u);
       const int row = sc.rb_of(u) * kPairRows + (int)ps.rank * kHalfRows + q * 32 + lane;
       const bool valid = row < args.N;
@@ -264,12 +267,12 @@ cudaError_t ensure_attrs(int dev) {
   return cudaSuccess;
 }
 
-// Workspace plan: [partials N*S float2][target logits N float][staged hidden][staged W].
+// Workspace plan: [partials N*S float2][target logits N float][unit counter][staged hidden][staged W].
 struct LogpPlan {
   int64_t S = 0, vps = 0, vtiles = 0;
   bool stage_h = false, stage_w = false;
   int64_t ldh = 0, ldw = 0;        // pitches the kernel reads
-  size_t off_zt = 0, off_h = 0, off_w = 0, total = 0;
+  size_t off_zt = 0, off_ctr = 0, off_h = 0, off_w = 0, total = 0;
 };
 
 rlk_status check_shapes(int64_t N, int64_t H, int64_t ldh, int64_t V, int64_t ldw) {
@@ -294,6 +297,8 @@ rlk_status plan(const void* hidden, int64_t N, int64_t H, int64_t ldh, const voi
   size_t off = align_up((size_t)N * p->S * sizeof(float2), 256);
   p->off_zt = off;
   off = align_up(off + (size_t)N * sizeof(float), 256);
+  p->off_ctr = off;
+  off += 256;
   p->off_h = off;
   if (p->stage_h) off = align_up(off + (size_t)N * p->ldh * 2, 256);
   p->off_w = off;
@@ -377,6 +382,11 @@ rlk_status rlk_linear_logp_partials(const void* hidden, int64_t N, int64_t H, in
   sc.order.cols = (int)p.S;
   sc.order.band = band_rows(sc.order.rows, H, kRowsPerUnit);
   sc.rows_per_unit = kRowsPerUnit;
+  sc.counter = reinterpret_cast<int*>(ws + p.off_ctr);
+  if (cudaMemsetAsync(sc.counter, 0, sizeof(int), s) != cudaSuccess) {
+    cudaGetLastError();
+    return RLK_ERR_CUDA;
+  }
   sc.S = (int)p.S;
   sc.vps = (int)p.vps;
   sc.vtiles = (int)p.vtiles;

@@ -35,6 +35,7 @@ namespace {
 
 struct GradSched {
   Banded order;    // rows = 256-row blocks (one per CTA pair), cols = 256-id vocabulary tiles
+  int* counter;    // zeroed unit counter in the workspace (units handed out in order)
   int nkb;         // 64-wide blocks of H
   __device__ __forceinline__ int num_units() const { return order.count(); }
   __device__ __forceinline__ int unit_tiles(int) const { return 1; }
@@ -73,6 +74,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) producer_role<THalf, THalf>(&tm_hidden, &tm_weight, sc, ps, &g_err_linear_logp_bwd);
+    if (lane == 1 && ps.rank == 0) scheduler_role(sc, ps, &g_err_linear_logp_bwd);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0 && ps.rank == 0)
@@ -84,8 +86,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     int acc = 0;
     uint32_t acc_phase = 0;
-    const int units = sc.num_units();
-    for (int u = cluster_index(); u < units; u += cluster_count()) {
+    for (int k = 0;; ++k) {
+      const int u = warp_unit_take(sc, ps, k, &g_err_linear_logp_bwd);
+      if (u < 0) break;
       if (!epilogue_acquire(ps, acc, acc_phase, &g_err_linear_logp_bwd)) break;
       int r0, v0;
       sc.tile_coords(u, 0, r0, v0);
@@ -198,7 +201,7 @@ extern "C" {
 
 size_t rlk_linear_logp_backward_workspace_size(int64_t N, int64_t V) {
   if (N < 0 || N >= (int64_t(1) << 31) || V < 1 || V >= (int64_t(1) << 31)) return 0;
-  return align_up((size_t)N * grad_ld(V) * 2, 256);
+  return align_up((size_t)N * grad_ld(V) * 2, 256) + 256;   // G, then the unit counter
 }
 
 rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
@@ -269,6 +272,12 @@ rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H, in
   a.grad = grad_logp;
   a.G = static_cast<uint16_t*>(workspace);
   a.ldG = grad_ld(V);
+  sc.counter = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) +
+                                      align_up((size_t)N * a.ldG * 2, 256));
+  if (cudaMemsetAsync(sc.counter, 0, sizeof(int), s) != cudaSuccess) {
+    cudaGetLastError();
+    return RLK_ERR_CUDA;
+  }
   const int64_t units = (int64_t)sc.order.rows * sc.order.cols;
   const int64_t clusters = dev.sm_count / 2;
   const int grid = 2 * (int)(units < clusters ? units : clusters);

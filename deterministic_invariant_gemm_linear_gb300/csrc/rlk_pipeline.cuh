@@ -61,6 +61,39 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                : "memory");
 }
+// Acquire at cluster scope: sees what the peer CTA released before arriving.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// Bounded like mbar_wait (abort flag, time limit, poll cap), acquiring at cluster scope.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort_flag, unsigned int* err) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((n & 31u) == 0u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitTimeoutNs || n > (1u << 30)) {
+        *abort_flag = 1;
+        atomicOr(err, kDevErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ void st_shared_cluster(uint32_t cluster_addr, int value) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(value) : "memory");
+}
+
 __device__ __forceinline__ void umma_pair_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -91,12 +124,26 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
                : "memory");
 }
 
+// Work units reach every role through a small ring that rank 0's scheduler
+// fills (in both CTAs) and that each consumer releases on rank 0's barrier.
+// A cluster's first unit is its own index and bypasses the ring, so the first
+// tiles start without waiting on the counter.
+constexpr int kUnitSlots = 4;
+// Consumers of each slot: rank 0's producer, MMA issuer and 4 epilogue warps;
+// rank 1's producer and 4 epilogue warps.
+constexpr int kUnitConsumers = 2 + 4 + 1 + 4;
+constexpr int kUnitDone = -1;      // no more units
+constexpr int kUnitAbort = -2;     // the CTA is winding down
+
 struct PipeBarriers {
   uint64_t full[kStages];    // used in rank 0 only: both CTAs' copies for a stage
   uint64_t empty[kStages];   // per CTA: the stage's shared memory may be refilled
   uint64_t acc_full[2];       // per CTA: accumulator b holds a finished tile
   uint64_t acc_empty[2];      // rank 0: both CTAs' epilogues released accumulator b
   uint64_t drained;           // rank 0: every issued MMA has completed
+  uint64_t unit_full[kUnitSlots];    // per CTA: slot k holds the next unit
+  uint64_t unit_empty[kUnitSlots];   // rank 0: every consumer has read slot k
+  int unit_id[kUnitSlots];           // per CTA copy of the ring
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -111,6 +158,10 @@ struct PipeSmem {
   __device__ __forceinline__ uint32_t acc_full(int b) const { return smem_u32(&bars->acc_full[b]); }
   __device__ __forceinline__ uint32_t acc_empty(int b) const {
     return smem_u32(&bars->acc_empty[b]);
+  }
+  __device__ __forceinline__ uint32_t unit_full(int k) const { return smem_u32(&bars->unit_full[k]); }
+  __device__ __forceinline__ uint32_t unit_empty(int k) const {
+    return smem_u32(&bars->unit_empty[k]);
   }
   __device__ __forceinline__ volatile int* abort_flag() const { return &bars->abort_flag; }
 };
@@ -139,6 +190,10 @@ __device__ __forceinline__ uint32_t pipe_setup(const PipeSmem& ps) {
       mbar_init(ps.acc_empty(b), 2 * (kEpilogueThreads / 32));
     }
     mbar_init(smem_u32(&ps.bars->drained), 1);
+    for (int k = 0; k < kUnitSlots; ++k) {
+      mbar_init(ps.unit_full(k), 1);
+      mbar_init(ps.unit_empty(k), kUnitConsumers);
+    }
     ps.bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -165,8 +220,89 @@ __device__ __forceinline__ void pipe_teardown(uint32_t tmem) {
   }
 }
 
+// Rank 0, warp 0, lane 1: hands out this cluster's units, in order, through the
+// ring.  With a counter (a zeroed int in the caller's workspace) each cluster
+// takes the next unit the moment it has room for it, so the units in flight
+// stay a compact, in-order window of the schedule: clusters cannot drift apart
+// over a long launch and evict each other's operand tiles from L2.  Without a
+// counter there is no ring: every role takes units c, c + C, c + 2C, ... of
+// cluster c directly.  Which cluster computes a unit never changes its
+// arithmetic.
+template <class Sched>
+__device__ __forceinline__ void scheduler_role(const Sched& sc, const PipeSmem& ps,
+                                               unsigned int* err) {
+  if (sc.counter == nullptr) return;   // every role computes the round-robin order itself
+  const int units = sc.num_units();
+  // Unit 0 of cluster c is unit c (every role knows it without the ring); the
+  // counter hands out units C, C + 1, ... from the second unit on, so ring
+  // position j carries the cluster's unit j + 1.
+  const int first_shared = (int)cluster_count();
+  for (int j = 0;; ++j) {
+    const int slot = j % kUnitSlots;
+    const uint32_t parity = (uint32_t)(j / kUnitSlots) & 1u;
+    if (!mbar_wait_cluster(ps.unit_empty(slot), parity ^ 1u, ps.abort_flag(), err)) return;
+    int u = first_shared + atomicAdd(sc.counter, 1);
+    if (u >= units) u = kUnitDone;
+    ps.bars->unit_id[slot] = u;
+    st_shared_cluster(mapa_shared(smem_u32(&ps.bars->unit_id[slot]), 1), u);
+    mbar_arrive(ps.unit_full(slot));
+    mbar_arrive_cluster(mapa_shared(ps.unit_full(slot), 1));
+    if (u == kUnitDone) return;
+  }
+}
+
+// Release slot `slot` after reading it (one arrival per consumer).  The arrival
+// carries no data, and the consumer has already used the value it read, so it
+// is relaxed: a release-ordered arrival from a thread with copies in flight
+// would stall that thread until they land.
+__device__ __forceinline__ void unit_release(const PipeSmem& ps, int slot) {
+  if (ps.rank == 0)
+    asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(ps.unit_empty(slot))
+                 : "memory");
+  else
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                     mapa_shared(ps.unit_empty(slot), 0))
+                 : "memory");
+}
+
+// The k-th unit of this cluster in the round-robin order (no counter).
+template <class Sched>
+__device__ __forceinline__ int unit_static(const Sched& sc, int k) {
+  const int u = (int)cluster_index() + k * (int)cluster_count();
+  return u < sc.num_units() ? u : kUnitDone;
+}
+
+// The k-th unit for a single-thread role: a unit id, kUnitDone or kUnitAbort.
+template <class Sched>
+__device__ __forceinline__ int unit_take(const Sched& sc, const PipeSmem& ps, int k,
+                                         unsigned int* err) {
+  if (sc.counter == nullptr || k == 0) return unit_static(sc, k);
+  const int slot = (k - 1) % kUnitSlots;
+  const uint32_t parity = (uint32_t)((k - 1) / kUnitSlots) & 1u;
+  if (!mbar_wait_cluster(ps.unit_full(slot), parity, ps.abort_flag(), err)) return kUnitAbort;
+  const int u = *reinterpret_cast<volatile int*>(&ps.bars->unit_id[slot]);
+  unit_release(ps, slot);
+  return u;
+}
+
+// The k-th unit for a whole warp (all lanes agree; lane 0 releases the slot).
+template <class Sched>
+__device__ __forceinline__ int warp_unit_take(const Sched& sc, const PipeSmem& ps, int k,
+                                              unsigned int* err) {
+  if (sc.counter == nullptr || k == 0) return unit_static(sc, k);
+  const int slot = (k - 1) % kUnitSlots;
+  const uint32_t parity = (uint32_t)((k - 1) / kUnitSlots) & 1u;
+  const bool ok = mbar_wait_cluster(ps.unit_full(slot), parity, ps.abort_flag(), err);
+  if (!__all_sync(0xffffffffu, ok)) return kUnitAbort;
+  const int u = *reinterpret_cast<volatile int*>(&ps.bars->unit_id[slot]);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) unit_release(ps, slot);
+  return u;
+}
+
 // Work description: a Schedule provides
-//   int  num_units() const;                    units are dealt to clusters round-robin
+//   int  num_units() const;                    units, handed out by scheduler_role
+//   int* counter;                              zeroed unit counter, or nullptr
 //   int  unit_tiles(int u) const;              accumulator tiles in unit u
 //   void tile_coords(int u, int i, int& a0, int& b0) const;
 //        a0 = first row of the pair's 256-row block of the left operand,
@@ -185,8 +321,12 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* ta, const CUten
   uint32_t phase = 0, issued = 0, last_parity = 0;
   bool run = true;
   const int32_t half = (int32_t)ps.rank * kHalfRows;
-  const int units = sc.num_units();
-  for (int u = cluster_index(); run && u < units; u += cluster_count()) {
+  for (int k = 0; run; ++k) {
+    const int u = unit_take(sc, ps, k, err);
+    if (u < 0) {
+      run = u != kUnitAbort;
+      break;
+    }
     const int nt = sc.unit_tiles(u);
     for (int i = 0; run && i < nt; ++i) {
       int a0, b0;
@@ -230,8 +370,9 @@ __device__ __forceinline__ void mma_role(const Sched& sc, const PipeSmem& ps, ui
   int stage = 0, acc = 0;
   uint32_t phase = 0, acc_phase = 0;
   bool run = true;
-  const int units = sc.num_units();
-  for (int u = cluster_index(); run && u < units; u += cluster_count()) {
+  for (int k = 0; run; ++k) {
+    const int u = unit_take(sc, ps, k, err);
+    if (u < 0) break;
     const int nt = sc.unit_tiles(u);
     for (int i = 0; run && i < nt; ++i) {
       if (!mbar_wait(ps.acc_empty(acc), acc_phase ^ 1u, ps.abort_flag(), err)) {

@@ -135,9 +135,10 @@ RLK_API rlk_status rlk_vocab_split_policy(int64_t V, int64_t* num_splits, int64_
 /*
  * Workspace bytes that rlk_linear_logp needs for exactly these operands:
  * N * S * 8 bytes of per-(row, split) online-softmax partials, N * 4 bytes for
- * the gathered target logits, plus a padded copy of hidden and/or weight when
- * that operand is misaligned (see "Alignment").  Each region starts on a
- * 256-byte boundary.  Returns 0 for invalid arguments.
+ * the gathered target logits, 256 bytes for the kernel's work-unit counter
+ * (zeroed by each call), plus a padded copy of hidden and/or weight when that
+ * operand is misaligned (see "Alignment").  Each region starts on a 256-byte
+ * boundary.  Returns 0 for invalid arguments.
  */
 RLK_API size_t rlk_linear_logp_workspace_size(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
                                       const void* weight, int64_t V, int64_t ld_weight);
@@ -211,7 +212,7 @@ RLK_API rlk_status rlk_linear_logp_combine(int64_t N, int64_t V, const int64_t* 
  * that loads the library holds until the process exits.  Nothing is allocated:
  * no cudaMalloc, no cudaFree, no allocating library routine.
  *  - Limit: the call needs N * S * 8 + N * 4 bytes (each rounded up to 256; S from
- *    rlk_vocab_split_policy(V)), plus a padded copy of any misaligned operand;
+ *    rlk_vocab_split_policy(V)) + 256, plus a padded copy of any misaligned operand;
  *    more than RLK_NOALLOC_SCRATCH_BYTES returns RLK_ERR_WORKSPACE and launches
  *    nothing.  (V = 151936: up to about 7,000 rows per call.)
  *  - The first call on each device looks up the array's device address (with that
@@ -253,7 +254,8 @@ RLK_API rlk_status rlk_linear_logp_noalloc(const void* hidden, int64_t N, int64_
  *  grad_bias     FP32 [V] or NULL to skip
  *  workspace     >= rlk_linear_logp_backward_workspace_size(N, V) bytes, 256-byte
  *                aligned.  After the call its first N * 8*ceil(V/8) * 2 bytes hold
- *                G as BF16 [N, 8*ceil(V/8)] (row pitch 8*ceil(V/8)).
+ *                G as BF16 [N, 8*ceil(V/8)] (row pitch 8*ceil(V/8)); the next 256
+ *                bytes hold the kernel's work-unit counter (zeroed by the call).
  * Determinism: every output is bitwise reproducible; a grad_hidden row depends
  * only on its own row's inputs (batch invariant), while grad_weight and
  * grad_bias sum over the rows of the call.  N == 0 writes zeros to grad_weight

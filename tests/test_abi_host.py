@@ -82,9 +82,10 @@ def test_vocab_split_policy_rejects(lib):
 def test_linear_logp_workspace_size(lib):
     f = lib.rlk_linear_logp_workspace_size
     # aligned operands: partials N*S*8 (256-aligned) + target logits N*4 (256-aligned)
+    # + a 256-byte unit counter
     N, H, V = 4096, 4096, 151936
     S = 594
-    want = -(-N * S * 8 // 256) * 256 + -(-N * 4 // 256) * 256
+    want = -(-N * S * 8 // 256) * 256 + -(-N * 4 // 256) * 256 + 256
     assert f(P16, N, H, H, P16, V, H) == want
     # odd pitch of hidden: a padded copy N x 8*ceil(H/8) bf16 is added
     base = f(P16, 10, 100, 104, P16, 300, 104)
@@ -97,8 +98,8 @@ def test_linear_logp_workspace_size(lib):
     assert f(P16, 10, 0, 1, P16, 10, 1) == 0
     assert f(P16, 10, 8, 4, P16, 10, 8) == 0
     assert f(P16, 10, 8, 8, P16, 0, 8) == 0
-    # N = 0 is valid and needs no partials
-    assert f(P16, 0, 8, 8, P16, 10, 8) == 0
+    # N = 0 is valid and needs no partials (only the counter region)
+    assert f(P16, 0, 8, 8, P16, 10, 8) == 256
 
 
 def test_linear_logp_validation(lib):
