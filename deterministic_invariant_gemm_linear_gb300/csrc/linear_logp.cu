@@ -37,7 +37,7 @@ namespace {
 
 struct LogpSched {
   Banded order;    // rows = 256-row blocks, cols = vocabulary splits
-  int* counter;    // zeroed unit counter in the workspace (units handed out in order)
+  int* counter;    // zeroed unit counter in the workspace (units in order), or null (round-robin)
   int S;           // vocabulary splits
   int vps;         // 256-id tiles per split
   int vtiles;      // 256-id tiles in the vocabulary
@@ -137,6 +137,10 @@ __device__ __forceinline__ void logp_chunk(const uint32_t (&r)[32], int vbase, i
 // tcgen05 loop; the CTA of rank r owns rows [256 * block + 128 r, +128).  Each
 // epilogue thread owns one row: for every 256-id tile of the split, in
 // ascending order, it folds the tile's logits into (m, s) 32 columns at a time.
+// R is the stage ring: RingFull, or RingThin when N <= 32 (every row in rank
+// 0's first 32); the MMA and the epilogue are the same for both, so a row's
+// bits do not depend on which ring computed it.
+template <class R>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     linear_logp_partials_kernel(const __grid_constant__ CUtensorMap tm_hidden,
                                      const __grid_constant__ CUtensorMap tm_weight, LogpSched sc,
@@ -149,15 +153,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_weight);
   }
   const uint32_t tmem = pipe_setup(ps);
+  using TA = OperandTile<false, R::kARows>;
   using THalf = OperandTile<false, kHalfRows>;
 
   if (warp == 0) {
-    if (lane == 0) producer_role<THalf, THalf>(&tm_hidden, &tm_weight, sc, ps, &g_err_linear_logp);
+    if (lane == 0) producer_role<TA, THalf, R>(&tm_hidden, &tm_weight, sc, ps, &g_err_linear_logp);
     if (lane == 1 && ps.rank == 0) scheduler_role(sc, ps, &g_err_linear_logp);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0 && ps.rank == 0)
-      mma_role<THalf, THalf>(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, false, false),
+      mma_role<TA, THalf, R>(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, false, false),
                               &g_err_linear_logp);
     __syncwarp();
   } else {
@@ -259,8 +264,12 @@ cudaError_t ensure_attrs(int dev) {
   std::lock_guard<std::mutex> lock(g_attr_mutex);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!g_attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(linear_logp_partials_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(linear_logp_partials_kernel<RingFull>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         RingFull::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(linear_logp_partials_kernel<RingThin>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, RingThin::kSmemBytes);
     if (e != cudaSuccess) return e;
     g_attr_set[dev] = true;
   }
@@ -371,10 +380,12 @@ rlk_status rlk_linear_logp_partials(const void* hidden, int64_t N, int64_t H, in
       return RLK_ERR_CUDA;
     w_src = ws + p.off_w;
   }
-  constexpr int kRowsPerUnit = kPairRows, kBoxRows = kHalfRows;
+  constexpr int kRowsPerUnit = kPairRows;
+  // At most 32 rows: the thin ring (rank 0 stages the 32 rows, 11 stages deep).
+  const bool thin = N <= RingThin::kARows;
   CUtensorMap tm_h, tm_w;
-  if (!encode_bf16_2d(&tm_h, h_src, H, N, p.ldh, kBK, kHalfRows) ||
-      !encode_bf16_2d(&tm_w, w_src, H, V, p.ldw, kBK, kBoxRows))
+  if (!encode_bf16_2d(&tm_h, h_src, H, N, p.ldh, kBK, thin ? RingThin::kARows : kHalfRows) ||
+      !encode_bf16_2d(&tm_w, w_src, H, V, p.ldw, kBK, kHalfRows))
     return RLK_ERR_CUDA;
 
   LogpSched sc;
@@ -382,11 +393,6 @@ rlk_status rlk_linear_logp_partials(const void* hidden, int64_t N, int64_t H, in
   sc.order.cols = (int)p.S;
   sc.order.band = band_rows(sc.order.rows, H, kRowsPerUnit);
   sc.rows_per_unit = kRowsPerUnit;
-  sc.counter = reinterpret_cast<int*>(ws + p.off_ctr);
-  if (cudaMemsetAsync(sc.counter, 0, sizeof(int), s) != cudaSuccess) {
-    cudaGetLastError();
-    return RLK_ERR_CUDA;
-  }
   sc.S = (int)p.S;
   sc.vps = (int)p.vps;
   sc.vtiles = (int)p.vtiles;
@@ -404,7 +410,20 @@ rlk_status rlk_linear_logp_partials(const void* hidden, int64_t N, int64_t H, in
   // One cluster of two CTAs per pair of SMs, persistent over the units.
   const int64_t clusters = dev.sm_count / 2;
   const int grid = 2 * (int)(units < clusters ? units : clusters);
-  linear_logp_partials_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_h, tm_w, sc, a);
+  sc.counter = nullptr;
+  if (ordered_units(units, clusters)) {
+    sc.counter = reinterpret_cast<int*>(ws + p.off_ctr);
+    if (cudaMemsetAsync(sc.counter, 0, sizeof(int), s) != cudaSuccess) {
+      cudaGetLastError();
+      return RLK_ERR_CUDA;
+    }
+  }
+  if (thin)
+    linear_logp_partials_kernel<RingThin>
+        <<<grid, kThreads, RingThin::kSmemBytes, s>>>(tm_h, tm_w, sc, a);
+  else
+    linear_logp_partials_kernel<RingFull>
+        <<<grid, kThreads, RingFull::kSmemBytes, s>>>(tm_h, tm_w, sc, a);
   return cudaGetLastError() == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
 }
 

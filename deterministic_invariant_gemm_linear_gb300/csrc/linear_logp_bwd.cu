@@ -35,7 +35,7 @@ namespace {
 
 struct GradSched {
   Banded order;    // rows = 256-row blocks (one per CTA pair), cols = 256-id vocabulary tiles
-  int* counter;    // zeroed unit counter in the workspace (units handed out in order)
+  int* counter;    // zeroed unit counter in the workspace (units in order), or null (round-robin)
   int nkb;         // 64-wide blocks of H
   __device__ __forceinline__ int num_units() const { return order.count(); }
   __device__ __forceinline__ int unit_tiles(int) const { return 1; }
@@ -272,15 +272,18 @@ rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H, in
   a.grad = grad_logp;
   a.G = static_cast<uint16_t*>(workspace);
   a.ldG = grad_ld(V);
-  sc.counter = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) +
-                                      align_up((size_t)N * a.ldG * 2, 256));
-  if (cudaMemsetAsync(sc.counter, 0, sizeof(int), s) != cudaSuccess) {
-    cudaGetLastError();
-    return RLK_ERR_CUDA;
-  }
   const int64_t units = (int64_t)sc.order.rows * sc.order.cols;
   const int64_t clusters = dev.sm_count / 2;
   const int grid = 2 * (int)(units < clusters ? units : clusters);
+  sc.counter = nullptr;
+  if (ordered_units(units, clusters)) {
+    sc.counter = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) +
+                                        align_up((size_t)N * a.ldG * 2, 256));
+    if (cudaMemsetAsync(sc.counter, 0, sizeof(int), s) != cudaSuccess) {
+      cudaGetLastError();
+      return RLK_ERR_CUDA;
+    }
+  }
   linear_logp_grad_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_h, tm_w, sc, a);
   if (cudaGetLastError() != cudaSuccess) return RLK_ERR_CUDA;
 

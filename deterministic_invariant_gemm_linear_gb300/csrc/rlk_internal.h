@@ -55,6 +55,16 @@ inline int band_rows(int64_t rows, int64_t K, int64_t rows_per_block = 128) {
   return (int)(b > 0 ? b : 1);
 }
 
+// Whether a persistent launch hands its units out in order from a counter in
+// the workspace (zeroed before the launch) or deals them round-robin.  Over
+// many rounds round-robin clusters drift apart and their operand tiles stop
+// sharing L2; a launch of a few rounds cannot drift far, and skips the zeroing.
+// Either way only which cluster computes a unit changes, never its arithmetic.
+constexpr int64_t kOrderedMinRounds = 8;
+inline bool ordered_units(int64_t units, int64_t clusters) {
+  return units > kOrderedMinRounds * clusters;
+}
+
 // Vocabulary split policy (function of V only).
 constexpr int64_t kVocabTile = 256;
 constexpr int64_t kMaxVocabSplits = 1024;

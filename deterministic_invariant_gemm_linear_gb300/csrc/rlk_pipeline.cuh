@@ -21,15 +21,50 @@
 
 namespace rlk {
 
-constexpr int kStages = 7;                            // shared-memory pipeline depth
-constexpr int kAStageBytes = kHalfRows * kBK * 2;     // 16 KiB: this CTA's left-operand half
-constexpr int kBStageBytes = kHalfRows * kBK * 2;     // 16 KiB: this CTA's right-operand half
-constexpr int kStageBytes = kAStageBytes + kBStageBytes;
-// Stage ring, alignment slack and the barrier block.
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 256;
-static_assert(kSmemBytes <= 232448, "exceeds the 227 KiB per-CTA shared memory limit");
-// One CTA per SM: a second resident CTA could not get TMEM columns.
-static_assert(kSmemBytes > 232448 / 2, "tcgen05 kernels must own their SM");
+// Dynamic shared memory: alignment slack, the barrier block, then the stage ring.
+constexpr int kSmemLimit = 232448;                    // 227 KiB per CTA
+constexpr int kBarrierBlockBytes = 1024;              // keeps the ring 1024-byte aligned
+constexpr int kMaxStages = 11;
+
+// The stage ring.  Each stage holds kARows rows of this CTA's left-operand half
+// and its 128 rows of the right-operand tile (64 reduction columns each), in two
+// areas: left-operand blocks of all stages first, then right-operand blocks.
+// kARows = 128 is the general ring.  kARows = 32 serves a left operand whose
+// valid rows all lie in rank 0's first 32: rank 0 stages only those, rank 1
+// none, and the smaller stages buy a deeper ring (more right-operand bytes in
+// flight).  The MMA still reads 128 rows per CTA; the rows past the staged ones
+// hold other data, which reaches only accumulator rows that nothing reads (row
+// i of a product depends on row i of the left operand alone).
+template <int kARows_>
+struct Ring {
+  static constexpr int kARows = kARows_;
+  static constexpr int kABytes = kARows * kBK * 2;                 // 16 KiB or 4 KiB
+  static constexpr int kBBytes = kHalfRows * kBK * 2;              // 16 KiB
+  static constexpr int kStages =
+      (kSmemLimit - 1024 - kBarrierBlockBytes) / (kABytes + kBBytes) < kMaxStages
+          ? (kSmemLimit - 1024 - kBarrierBlockBytes) / (kABytes + kBBytes)
+          : kMaxStages;
+  // Bytes rank 0's full barrier counts per stage (both CTAs' copies).
+  static constexpr uint32_t kTxBytes = kARows == kHalfRows ? 2u * (kABytes + kBBytes)
+                                                           : (uint32_t)kABytes + 2u * kBBytes;
+  static constexpr int kSmemBytes = 1024 + kBarrierBlockBytes + kStages * (kABytes + kBBytes);
+  static __device__ __forceinline__ uint32_t a_stage(uint32_t ring, int s) {
+    return ring + s * kABytes;
+  }
+  static __device__ __forceinline__ uint32_t b_stage(uint32_t ring, int s) {
+    return ring + kStages * kABytes + s * kBBytes;
+  }
+  static_assert(kARows == kHalfRows || kARows == 32, "general or thin ring");
+  static_assert(kSmemBytes <= kSmemLimit, "exceeds the 227 KiB per-CTA shared memory limit");
+  // One CTA per SM: a second resident CTA could not get TMEM columns.
+  static_assert(kSmemBytes > kSmemLimit / 2, "tcgen05 kernels must own their SM");
+  // The MMA reads 16 KiB of left operand from any stage's block: stay inside the ring.
+  static_assert(kStages * (kABytes + kBBytes) >= kHalfRows * kBK * 2 + (kStages - 1) * kABytes,
+                "left-operand reads leave the ring");
+};
+using RingFull = Ring<kHalfRows>;   // 7 stages x 32 KiB
+using RingThin = Ring<32>;          // 11 stages x 20 KiB
+constexpr int kSmemBytes = RingFull::kSmemBytes;
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -136,8 +171,8 @@ constexpr int kUnitDone = -1;      // no more units
 constexpr int kUnitAbort = -2;     // the CTA is winding down
 
 struct PipeBarriers {
-  uint64_t full[kStages];    // used in rank 0 only: both CTAs' copies for a stage
-  uint64_t empty[kStages];   // per CTA: the stage's shared memory may be refilled
+  uint64_t full[kMaxStages];    // used in rank 0 only: both CTAs' copies for a stage
+  uint64_t empty[kMaxStages];   // per CTA: the stage's shared memory may be refilled
   uint64_t acc_full[2];       // per CTA: accumulator b holds a finished tile
   uint64_t acc_empty[2];      // rank 0: both CTAs' epilogues released accumulator b
   uint64_t drained;           // rank 0: every issued MMA has completed
@@ -147,10 +182,10 @@ struct PipeBarriers {
   uint32_t tmem_base;
   int abort_flag;
 };
-static_assert(sizeof(PipeBarriers) <= 256, "barrier block overflows its reserved bytes");
+static_assert(sizeof(PipeBarriers) <= kBarrierBlockBytes, "barrier block overflows its bytes");
 
 struct PipeSmem {
-  uint32_t stages;
+  uint32_t stages;   // the ring (1024-byte aligned)
   PipeBarriers* bars;
   uint32_t rank;
   __device__ __forceinline__ uint32_t full(int s) const { return smem_u32(&bars->full[s]); }
@@ -170,8 +205,8 @@ __device__ __forceinline__ PipeSmem pipe_smem(uint8_t* raw) {
   const uint32_t base = smem_u32(raw);
   const uint32_t pad = (1024u - (base & 1023u)) & 1023u;
   PipeSmem p;
-  p.stages = base + pad;
-  p.bars = reinterpret_cast<PipeBarriers*>(raw + pad + kStages * kStageBytes);
+  p.bars = reinterpret_cast<PipeBarriers*>(raw + pad);
+  p.stages = base + pad + kBarrierBlockBytes;
   p.rank = cluster_rank();
   return p;
 }
@@ -181,7 +216,7 @@ __device__ __forceinline__ PipeSmem pipe_smem(uint8_t* raw) {
 __device__ __forceinline__ uint32_t pipe_setup(const PipeSmem& ps) {
   const int warp = threadIdx.x / 32;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(ps.full(s), 1);
       mbar_init(ps.empty(s), 1);
     }
@@ -312,11 +347,13 @@ __device__ __forceinline__ int warp_unit_take(const Sched& sc, const PipeSmem& p
 // from zero, so a tile's arithmetic depends only on its operand tiles, never on
 // the schedule, the grid or the row count.  TA / TB are the 128-row operand
 // halves (OperandTile<majorness, 128>).
-template <class TA, class TB, class Sched>
+template <class TA, class TB, class R = RingFull, class Sched>
 __device__ __forceinline__ void producer_role(const CUtensorMap* ta, const CUtensorMap* tb,
                                                const Sched& sc, const PipeSmem& ps,
                                                unsigned int* err) {
-  static_assert(TA::kBytes == kAStageBytes && TB::kBytes == kBStageBytes, "operand halves are 128 rows");
+  static_assert(TA::kBytes == R::kABytes && TB::kBytes == R::kBBytes, "operand blocks fit the ring");
+  constexpr int kStages = R::kStages;
+  const bool load_a = R::kARows == kHalfRows || ps.rank == 0;
   int stage = 0;
   uint32_t phase = 0, issued = 0, last_parity = 0;
   bool run = true;
@@ -336,11 +373,13 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* ta, const CUten
           run = false;
           break;
         }
-        if (ps.rank == 0) mbar_arrive_expect_tx(ps.full(stage), 2 * kStageBytes);
+        if (ps.rank == 0) mbar_arrive_expect_tx(ps.full(stage), R::kTxBytes);
         const uint32_t leader_full = mapa_shared(ps.full(stage), 0);
-        const uint32_t sa = ps.stages + stage * kStageBytes;
-        TA::template load<true>(sa, ta, leader_full, a0 + half, kb * kBK);
-        TB::template load<true>(sa + kAStageBytes, tb, leader_full, b0 + half, kb * kBK);
+        if (load_a)
+          TA::template load<true>(R::a_stage(ps.stages, stage), ta, leader_full, a0 + half,
+                                  kb * kBK);
+        TB::template load<true>(R::b_stage(ps.stages, stage), tb, leader_full, b0 + half,
+                                kb * kBK);
         issued |= 1u << stage;
         last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == kStages) {
@@ -364,9 +403,10 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* ta, const CUten
   }
 }
 
-template <class TA, class TB, class Sched>
+template <class TA, class TB, class R = RingFull, class Sched>
 __device__ __forceinline__ void mma_role(const Sched& sc, const PipeSmem& ps, uint32_t tmem,
                                           uint32_t idesc, unsigned int* err) {
+  constexpr int kStages = R::kStages;
   int stage = 0, acc = 0;
   uint32_t phase = 0, acc_phase = 0;
   bool run = true;
@@ -387,8 +427,8 @@ __device__ __forceinline__ void mma_role(const Sched& sc, const PipeSmem& ps, ui
           break;
         }
         tc_fence_after();
-        const uint32_t sa = ps.stages + stage * kStageBytes;
-        const uint32_t sb = sa + kAStageBytes;
+        const uint32_t sa = R::a_stage(ps.stages, stage);
+        const uint32_t sb = R::b_stage(ps.stages, stage);
 #pragma unroll
         for (int k = 0; k < kBK / kUmmaK; ++k)
           umma_pair_bf16(d, TA::desc(sa, k), TB::desc(sb, k), idesc, (kb | k) != 0 ? 1u : 0u);

@@ -136,7 +136,7 @@ RLK_API rlk_status rlk_vocab_split_policy(int64_t V, int64_t* num_splits, int64_
  * Workspace bytes that rlk_linear_logp needs for exactly these operands:
  * N * S * 8 bytes of per-(row, split) online-softmax partials, N * 4 bytes for
  * the gathered target logits, 256 bytes for the kernel's work-unit counter
- * (zeroed by each call), plus a padded copy of hidden and/or weight when that
+ * (zeroed by each call that deals more than 8 rounds of units), plus a padded copy of hidden and/or weight when that
  * operand is misaligned (see "Alignment").  Each region starts on a 256-byte
  * boundary.  Returns 0 for invalid arguments.
  */
@@ -255,7 +255,8 @@ RLK_API rlk_status rlk_linear_logp_noalloc(const void* hidden, int64_t N, int64_
  *  workspace     >= rlk_linear_logp_backward_workspace_size(N, V) bytes, 256-byte
  *                aligned.  After the call its first N * 8*ceil(V/8) * 2 bytes hold
  *                G as BF16 [N, 8*ceil(V/8)] (row pitch 8*ceil(V/8)); the next 256
- *                bytes hold the kernel's work-unit counter (zeroed by the call).
+ *                bytes hold the kernel's work-unit counter (zeroed by a call that
+ *                deals more than 8 rounds of units).
  * Determinism: every output is bitwise reproducible; a grad_hidden row depends
  * only on its own row's inputs (batch invariant), while grad_weight and
  * grad_bias sum over the rows of the call.  N == 0 writes zeros to grad_weight

@@ -120,3 +120,27 @@ def test_layouts(dev):
     assert_same(lp(hidden, wodd[:, :H], target, bias), ref, "odd weight pitch (staged)")
     t_strided = torch.stack([target, target], dim=1)[:, 0]           # stride 2
     assert_same(lp(hidden, weight, t_strided, bias), ref, "strided target")
+
+
+@pytest.mark.parametrize("n_small", [1, 17, 32])
+def test_thin_ring_matches_full_ring(dev, n_small):
+    """Calls of at most 32 rows stage only those rows (a deeper ring of smaller
+    stages); their bits equal the same rows inside larger calls (33 and 300 rows,
+    the general ring), for a ragged vocabulary with bias and a staged hidden."""
+    H, V = 2048, 32003
+    hidden, weight, bias, target = si.linear_logp_inputs(300, H, V, bias=True, seed=16, device=dev)
+    for start in (0, 5, 268):
+        rows = slice(start, start + n_small)
+        small = lp(hidden[rows], weight, target[rows], bias)
+        for big_n in (33, 300):
+            s0 = max(0, min(start, big_n - n_small))
+            h_big, t_big = hidden[:big_n].clone(), target[:big_n].clone()
+            h_big[s0:s0 + n_small], t_big[s0:s0 + n_small] = hidden[rows], target[rows]
+            big = lp(h_big, weight, t_big, bias)
+            assert_same(tuple(o[s0:s0 + n_small] for o in big), small,
+                        f"{n_small} rows at {start} vs a {big_n}-row call")
+    odd = torch.zeros(n_small, H + 1, dtype=torch.bfloat16, device=dev)
+    odd[:, :H] = hidden[:n_small]
+    assert_same(lp(odd[:, :H], weight, target[:n_small], bias),
+                lp(hidden[:n_small], weight, target[:n_small], bias), "thin ring, staged hidden")
+    assert rlk.device_error() == 0
