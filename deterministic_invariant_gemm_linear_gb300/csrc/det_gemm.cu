@@ -308,12 +308,23 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
   const int64_t units = num_mb * num_nb;
   const int64_t clusters = dev.sm_count / 2;
   const int grid = 2 * (int)(units < clusters ? units : clusters);
+  cudaError_t e = cudaErrorInvalidValue;
   switch (kind) {
-    case Kind::kFwd: det_gemm_kernel<false, true><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, sc, o); break;
-    case Kind::kDa: det_gemm_kernel<false, false><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, sc, o); break;
-    case Kind::kDb: det_gemm_kernel<true, true><<<grid, kThreads, kSmemBytes, s>>>(ta, tb, sc, o); break;
+    case Kind::kFwd:
+      e = launch_overlapped(det_gemm_kernel<false, true>, grid, kThreads, kSmemBytes, s, ta, tb, sc, o);
+      break;
+    case Kind::kDa:
+      e = launch_overlapped(det_gemm_kernel<false, false>, grid, kThreads, kSmemBytes, s, ta, tb, sc, o);
+      break;
+    case Kind::kDb:
+      e = launch_overlapped(det_gemm_kernel<true, true>, grid, kThreads, kSmemBytes, s, ta, tb, sc, o);
+      break;
   }
-  return cudaGetLastError() == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return RLK_ERR_CUDA;
+  }
+  return RLK_OK;
 }
 
 }  // namespace

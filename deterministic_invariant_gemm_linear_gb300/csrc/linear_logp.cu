@@ -232,6 +232,8 @@ __global__ void __launch_bounds__(256)
                                const int64_t* __restrict__ target, int64_t tstride, int N, int S,
                                int V, float* __restrict__ logp, float* __restrict__ lse,
                                float* __restrict__ zt_out) {
+  griddep_wait();   // the partials kernel has finished and its writes are visible
+  if (threadIdx.x == 0) griddep_launch_dependents();
   const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   if (row >= N) return;
@@ -418,13 +420,16 @@ rlk_status rlk_linear_logp_partials(const void* hidden, int64_t N, int64_t H, in
       return RLK_ERR_CUDA;
     }
   }
-  if (thin)
-    linear_logp_partials_kernel<RingThin>
-        <<<grid, kThreads, RingThin::kSmemBytes, s>>>(tm_h, tm_w, sc, a);
-  else
-    linear_logp_partials_kernel<RingFull>
-        <<<grid, kThreads, RingFull::kSmemBytes, s>>>(tm_h, tm_w, sc, a);
-  return cudaGetLastError() == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
+  const cudaError_t e =
+      thin ? launch_overlapped(linear_logp_partials_kernel<RingThin>, grid, kThreads,
+                               RingThin::kSmemBytes, s, tm_h, tm_w, sc, a)
+           : launch_overlapped(linear_logp_partials_kernel<RingFull>, grid, kThreads,
+                               RingFull::kSmemBytes, s, tm_h, tm_w, sc, a);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return RLK_ERR_CUDA;
+  }
+  return RLK_OK;
 }
 
 rlk_status rlk_linear_logp_combine(int64_t N, int64_t V, const int64_t* target,
@@ -451,10 +456,15 @@ rlk_status rlk_linear_logp_combine(int64_t N, int64_t V, const int64_t* target,
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);
   const int rows_per_block = 256 / 32;
   const int grid = (int)ceil_div(N, rows_per_block);
-  linear_logp_combine_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+  const cudaError_t e = launch_overlapped(
+      linear_logp_combine_kernel, grid, 256, 0, static_cast<cudaStream_t>(stream),
       reinterpret_cast<const float2*>(ws), reinterpret_cast<const float*>(ws + off_zt), target,
       target_stride, (int)N, (int)S, (int)V, logp, lse, target_logit);
-  return cudaGetLastError() == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return RLK_ERR_CUDA;
+  }
+  return RLK_OK;
 }
 
 rlk_status rlk_linear_logp(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,

@@ -148,6 +148,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(256)
     column_sum_bf16_kernel(const uint16_t* __restrict__ G, int N, int V, int64_t ldG,
                            float* __restrict__ out) {
+  griddep_wait();   // G is complete (the gradient kernels before this one have finished)
+  if (threadIdx.x == 0) griddep_launch_dependents();
   const int v = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
   if (v >= V) return;
   float s0 = 0.f, s1 = 0.f;
@@ -284,8 +286,11 @@ rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H, in
       return RLK_ERR_CUDA;
     }
   }
-  linear_logp_grad_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_h, tm_w, sc, a);
-  if (cudaGetLastError() != cudaSuccess) return RLK_ERR_CUDA;
+  if (launch_overlapped(linear_logp_grad_kernel, grid, kThreads, kSmemBytes, s, tm_h, tm_w, sc,
+                        a) != cudaSuccess) {
+    cudaGetLastError();
+    return RLK_ERR_CUDA;
+  }
 
   if (grad_hidden) {   // [N, H] = G [N, V] . W [V, H]
     st = rlk_det_gemm_fwd(a.G, N, V, a.ldG, weight, H, ld_weight, grad_hidden, grad_hidden_dtype,
@@ -300,8 +305,11 @@ rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H, in
   if (grad_bias) {
     const int threads = 256;
     const int grid_b = (int)ceil_div(ceil_div(V, 2), threads);
-    column_sum_bf16_kernel<<<grid_b, threads, 0, s>>>(a.G, (int)N, (int)V, a.ldG, grad_bias);
-    if (cudaGetLastError() != cudaSuccess) return RLK_ERR_CUDA;
+    if (launch_overlapped(column_sum_bf16_kernel, grid_b, threads, 0, s, a.G, (int)N, (int)V,
+                          a.ldG, grad_bias) != cudaSuccess) {
+      cudaGetLastError();
+      return RLK_ERR_CUDA;
+    }
   }
   return RLK_OK;
 }

@@ -46,6 +46,18 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+// Programmatic dependent launch.  griddep_wait blocks until the kernel before
+// this one in the stream has completed and its memory is visible (it returns at
+// once for an ordinary launch); griddep_launch_dependents lets the next kernel,
+// if launched with programmatic serialisation, start its own prologue.  Every
+// library kernel runs its prologue (barriers, TMEM, descriptor prefetch) and
+// waits before it reads or writes global memory; the tensor-core kernels signal
+// once their producer has run out of work, the short kernels right away.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

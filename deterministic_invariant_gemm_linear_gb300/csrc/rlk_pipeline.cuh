@@ -212,7 +212,8 @@ __device__ __forceinline__ PipeSmem pipe_smem(uint8_t* raw) {
 }
 
 // Barrier initialisation, collective TMEM allocation, then a cluster barrier
-// so that no CTA touches its peer's barriers before they exist.
+// so that no CTA touches its peer's barriers before they exist; then the wait
+// for the previous kernel in the stream (programmatic dependent launch).
 __device__ __forceinline__ uint32_t pipe_setup(const PipeSmem& ps) {
   const int warp = threadIdx.x / 32;
   if (threadIdx.x == 0) {
@@ -240,6 +241,8 @@ __device__ __forceinline__ uint32_t pipe_setup(const PipeSmem& ps) {
   __syncthreads();
   cluster_sync();
   tc_fence_after();
+  // The prologue above touched only this CTA's shared memory and TMEM.
+  griddep_wait();
   return ps.bars->tmem_base;
 }
 
@@ -389,6 +392,11 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* ta, const CUten
       }
     }
   }
+  // No more units for this CTA: the next kernel in the stream may start its
+  // prologue on the SMs this grid frees from here on (it waits for this grid
+  // to complete before it touches memory).  Signalling only now keeps its
+  // blocks from sitting resident beside the main loop.
+  griddep_launch_dependents();
   if (ps.rank == 0) {
     // Rank 0's full barriers count both CTAs' bytes: once they complete, every
     // copy of the pair has landed.
