@@ -225,6 +225,19 @@ def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
     assert rlk.device_error() == 0, "device error word set during the bench"
     part_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
     comb_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    warm = None
+    if flush is not None:
+        # the same steps with W left in L2 by the previous step (reported beside the cold numbers)
+        for k in range(K):
+            ev[k][0].record(stream)
+            call.partials()
+            ev[k][1].record(stream)
+            call.combine()
+            ev[k][2].record(stream)
+        torch.cuda.synchronize()
+        warm = {"partials_ms": float(np.mean([e[0].elapsed_time(e[1]) for e in ev])),
+                "combine_ms": float(np.mean([e[1].elapsed_time(e[2]) for e in ev])),
+                "note": "no flush between steps: W (%.1f MB) partly L2-resident" % (w_bytes / 1e6)}
     ms_step = t / K * 1e3
     tokens = w.N * world * K
     value = tokens / t
@@ -265,6 +278,7 @@ def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
         "frac_bf16_peak": flops * K / t_local / 1e12 / peak,
         "kernels_ms": {"linear_logp_partials": part_ms, "linear_logp_combine": comb_ms},
         "roofline": roof,
+        **({"l2_warm": warm} if warm is not None else {}),
         "clocks": clocks.summary(),
         "gpu_launches": 2 * K,
     }
@@ -457,6 +471,81 @@ def det_gemm_bench(args, dev, rank, world, peaks, peak_src):
     }
 
 
+def ablation_bench(args, dev, rank, world, peaks, peak_src):
+    """The throughput-mode ablation: the operator (V-only split) against the same
+    kernels with the occupancy-driven, N-dependent split count, whole calls
+    (partials + combine) timed in alternating blocks on the mid shape."""
+    import deterministic_invariant_gemm_linear_gb300 as rlk
+    w = si.MID
+    if args.rows:
+        w = si.LinearLogpWorkload(f"{w.name} (rows={args.rows})", N=args.rows, H=w.H, V=w.V,
+                                  bias=w.bias, target_mode=w.target_mode)
+    hidden, weight, bias, target = si.workload_inputs(w, seed=rank, device=dev)
+    s_inv = rlk.vocab_split_policy(w.V)[0]
+    s_tp = rlk.throughput_split_count(w.N, w.V)
+    calls = {"invariant": rlk.LinearLogpCall(hidden, weight, target, bias),
+             "throughput_mode": rlk.LinearLogpCall(hidden, weight, target, bias, num_splits=s_tp)}
+    for c in calls.values():
+        for _ in range(args.warmup):
+            c()
+    torch.cuda.synchronize()
+    K = args.steps
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if weight.numel() * 2 < (512 << 20) else None
+    ms = {k: [] for k in calls}
+    barrier(world)
+    with ClockSampler(dev.index) as clocks:
+        for _ in range(3):
+            for name, c in calls.items():
+                if flush is None:
+                    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    s.record(stream)
+                    for _ in range(K):
+                        c()
+                    e.record(stream)
+                    torch.cuda.synchronize()
+                    ms[name].append(s.elapsed_time(e) / K)
+                else:
+                    tot = 0.0
+                    for _ in range(K):
+                        flush.zero_()
+                        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        s.record(stream)
+                        c()
+                        e.record(stream)
+                        torch.cuda.synchronize()
+                        tot += s.elapsed_time(e)
+                    ms[name].append(tot / K)
+    assert rlk.device_error() == 0
+    med = {k: float(np.median(v)) for k, v in ms.items()}
+    t_inv = max_over_ranks(med["invariant"] / 1e3, world, dev)
+    flops = 2.0 * w.N * w.H * w.V
+    achieved = flops / t_inv / 1e12
+    return {
+        "metric": f"linear-logp throughput-mode ablation (N={w.N},H={w.H},V={w.V}): "
+                  "V-only split vs N-dependent split",
+        "value": w.N * world / t_inv, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": t_inv * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name}: N={w.N} H={w.H} V={w.V}, whole calls, 3 alternating "
+                               f"blocks of {K} per mode",
+                   "global_batch": w.N * world, "seq_len": None, "parallelism": f"replicas x{world}",
+                   "l2": "W streamed from HBM every call" if flush is None else
+                         "L2 flushed (256 MB write) before every call"},
+        "ablation": {"invariant": {"num_splits": s_inv, "ms_per_call": med["invariant"]},
+                     "throughput_mode": {"num_splits": s_tp, "ms_per_call": med["throughput_mode"]},
+                     "invariant_time_over_throughput_time":
+                         med["invariant"] / med["throughput_mode"],
+                     "blocks_ms": ms},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                     "kernel": "whole linear-logp call (partials + combine), V-only split",
+                     "peak_kind": f"{peak_src} burst bf16"},
+        "clocks": clocks.summary(),
+        "gpu_launches": 2 * 2 * 3 * K,
+    }
+
+
 def reference_arm(args):
     """The FP64 CPU oracle as the reference implementation, on a bounded sample.
 
@@ -513,7 +602,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="mid",
-                    choices=["mid", "large", "ragged", "det_gemm", "backward"])
+                    choices=["mid", "large", "ragged", "det_gemm", "backward", "ablation"])
     ap.add_argument("--impl", default="rlk", choices=["rlk", "reference"])
     ap.add_argument("--rows", type=int, default=0,
                     help="override the row count N of a linear-logp workload (profiling cases)")
@@ -537,6 +626,8 @@ def main():
         line = det_gemm_bench(args, dev, rank, world, peaks, src)
     elif args.workload == "backward":
         line = backward_bench(args, dev, rank, world, peaks, src)
+    elif args.workload == "ablation":
+        line = ablation_bench(args, dev, rank, world, peaks, src)
     else:
         line = linear_logp_bench(args, dev, rank, world, peaks, src)
     if rank == 0:

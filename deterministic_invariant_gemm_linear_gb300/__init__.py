@@ -61,6 +61,10 @@ SIGNATURES = {
     "rlk_linear_logp_combine": (_I, [_I64, _I64, _P, _I64, _P, _P, _P, _P, _SZ, _P]),
     "rlk_linear_logp_noalloc": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _P, _I64,
                                      _P, _P, _P, _P]),
+    "rlk_throughput_split_count": (_I, [_I64, _I64, ctypes.c_int32, ctypes.POINTER(_I64)]),
+    "rlk_linear_logp_splits_workspace_size": (_SZ, [_P, _I64, _I64, _I64, _P, _I64, _I64, _I64]),
+    "rlk_linear_logp_splits": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _P, _I64,
+                                    _P, _P, _P, _I64, _P, _SZ, _P]),
     "rlk_linear_logp_backward_workspace_size": (_SZ, [_I64, _I64]),
     "rlk_linear_logp_backward": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _P, _I64, _P, _P,
                                       _P, _I, _I64, _P, _I, _I64, _P, _P, _SZ, _P]),
@@ -162,13 +166,23 @@ def linear_logp_workspace(hidden2d, weight, ldh, ldw, N, H, V) -> torch.Tensor:
     return torch.empty(n, dtype=torch.uint8, device=hidden2d.device)
 
 
+def throughput_split_count(N: int, V: int, sm_count: int = 0) -> int:
+    """The occupancy-driven split count of the throughput-mode ablation (depends on N)."""
+    s = _I64()
+    _check(lib().rlk_throughput_split_count(N, V, sm_count, ctypes.byref(s)),
+           "rlk_throughput_split_count")
+    return s.value
+
+
 def linear_logp(hidden: torch.Tensor, weight: torch.Tensor, target: torch.Tensor,
                 bias: torch.Tensor | None = None, *, return_target_logit: bool = False,
-                stream=None):
+                stream=None, num_splits: int | None = None):
     """logp, lse (FP32, shaped like hidden's leading dims) [, target logit].
 
     hidden [..., H] bf16, weight [V, H] bf16, target [...] int64 (any strides,
     including an expanded zero-stride target), bias [V] fp32 or None.
+    num_splits (ablation only): an explicit vocabulary split count instead of
+    the V-only policy (rlk_linear_logp_splits); 0 means the V-only policy.
     """
     if hidden.requires_grad or weight.requires_grad or (bias is not None and bias.requires_grad):
         raise RuntimeError("linear_logp is forward-only: inputs that require grad are rejected")
@@ -199,10 +213,21 @@ def linear_logp(hidden: torch.Tensor, weight: torch.Tensor, target: torch.Tensor
     lse = torch.empty(N, dtype=torch.float32, device=dev)
     zt = torch.empty(N, dtype=torch.float32, device=dev) if return_target_logit else None
     with torch.cuda.device(dev):
-        ws = linear_logp_workspace(h2, w2, ldh, ldw, N, H, V)
-        st = lib().rlk_linear_logp(_ptr(h2), N, H, ldh, _ptr(w2), V, ldw, _ptr(bias), _ptr(t1),
-                                   tstride, _ptr(logp), _ptr(lse), _ptr(zt), _ptr(ws), ws.numel(),
-                                   _stream_ptr(stream))
+        if num_splits is None:
+            ws = linear_logp_workspace(h2, w2, ldh, ldw, N, H, V)
+            st = lib().rlk_linear_logp(_ptr(h2), N, H, ldh, _ptr(w2), V, ldw, _ptr(bias), _ptr(t1),
+                                       tstride, _ptr(logp), _ptr(lse), _ptr(zt), _ptr(ws),
+                                       ws.numel(), _stream_ptr(stream))
+        else:
+            n = lib().rlk_linear_logp_splits_workspace_size(_ptr(h2), N, H, ldh, _ptr(w2), V, ldw,
+                                                            num_splits)
+            if n == 0 and N > 0:
+                raise RlkError(2, "rlk_linear_logp_splits_workspace_size")
+            ws = torch.empty(n, dtype=torch.uint8, device=dev)
+            st = lib().rlk_linear_logp_splits(_ptr(h2), N, H, ldh, _ptr(w2), V, ldw, _ptr(bias),
+                                              _ptr(t1), tstride, _ptr(logp), _ptr(lse), _ptr(zt),
+                                              num_splits, _ptr(ws), ws.numel(),
+                                              _stream_ptr(stream))
     _check(st, "rlk_linear_logp")
     out = (logp.reshape(lead), lse.reshape(lead))
     if return_target_logit:
@@ -214,8 +239,10 @@ class LinearLogpCall:
     """A prepared linear-logp call on fixed tensors (outputs and workspace
     allocated once), runnable as the whole operator or as its two stages."""
 
-    def __init__(self, hidden, weight, target, bias=None, *, target_logit: bool = False):
+    def __init__(self, hidden, weight, target, bias=None, *, target_logit: bool = False,
+                 num_splits: int | None = None):
         _require_cuda(hidden, weight, target, bias)
+        self.num_splits = num_splits      # None: the operator; an int: the ablation entry point
         self.h, self.ldh = _matrix(hidden, "hidden")
         self.w, self.ldw = _matrix(weight, "weight")
         self.t = target.reshape(-1)
@@ -228,25 +255,46 @@ class LinearLogpCall:
         self.lse = torch.empty(self.N, dtype=torch.float32, device=dev)
         self.zt = torch.empty(self.N, dtype=torch.float32, device=dev) if target_logit else None
         with torch.cuda.device(dev):
-            self.ws = linear_logp_workspace(self.h, self.w, self.ldh, self.ldw, self.N, self.H, self.V)
+            if num_splits is None:
+                self.ws = linear_logp_workspace(self.h, self.w, self.ldh, self.ldw, self.N, self.H,
+                                                self.V)
+            else:
+                n = lib().rlk_linear_logp_splits_workspace_size(
+                    _ptr(self.h), self.N, self.H, self.ldh, _ptr(self.w), self.V, self.ldw,
+                    num_splits)
+                if n == 0 and self.N > 0:
+                    raise RlkError(2, "rlk_linear_logp_splits_workspace_size")
+                self.ws = torch.empty(n, dtype=torch.uint8, device=dev)
 
     def partials(self, stream=None):
+        if self.num_splits is not None:
+            raise RuntimeError("the two-stage calls use the V-only split")
         _check(lib().rlk_linear_logp_partials(
             _ptr(self.h), self.N, self.H, self.ldh, _ptr(self.w), self.V, self.ldw, _ptr(self.bias),
             _ptr(self.t), self.tstride, _ptr(self.ws), self.ws.numel(), _stream_ptr(stream)),
             "rlk_linear_logp_partials")
 
     def combine(self, stream=None):
+        if self.num_splits is not None:
+            raise RuntimeError("the two-stage calls use the V-only split")
         _check(lib().rlk_linear_logp_combine(
             self.N, self.V, _ptr(self.t), self.tstride, _ptr(self.logp), _ptr(self.lse),
             _ptr(self.zt), _ptr(self.ws), self.ws.numel(), _stream_ptr(stream)),
             "rlk_linear_logp_combine")
 
     def __call__(self, stream=None):
-        _check(lib().rlk_linear_logp(
-            _ptr(self.h), self.N, self.H, self.ldh, _ptr(self.w), self.V, self.ldw, _ptr(self.bias),
-            _ptr(self.t), self.tstride, _ptr(self.logp), _ptr(self.lse), _ptr(self.zt),
-            _ptr(self.ws), self.ws.numel(), _stream_ptr(stream)), "rlk_linear_logp")
+        if self.num_splits is None:
+            _check(lib().rlk_linear_logp(
+                _ptr(self.h), self.N, self.H, self.ldh, _ptr(self.w), self.V, self.ldw,
+                _ptr(self.bias), _ptr(self.t), self.tstride, _ptr(self.logp), _ptr(self.lse),
+                _ptr(self.zt), _ptr(self.ws), self.ws.numel(), _stream_ptr(stream)),
+                "rlk_linear_logp")
+        else:
+            _check(lib().rlk_linear_logp_splits(
+                _ptr(self.h), self.N, self.H, self.ldh, _ptr(self.w), self.V, self.ldw,
+                _ptr(self.bias), _ptr(self.t), self.tstride, _ptr(self.logp), _ptr(self.lse),
+                _ptr(self.zt), self.num_splits, _ptr(self.ws), self.ws.numel(),
+                _stream_ptr(stream)), "rlk_linear_logp_splits")
         return self.logp, self.lse
 
 

@@ -295,11 +295,25 @@ rlk_status check_shapes(int64_t N, int64_t H, int64_t ldh, int64_t V, int64_t ld
   return RLK_OK;
 }
 
+// Contiguous equal splits of the vocabulary tiles: splits_req = 0 takes the
+// V-only policy (rlk_vocab_split_policy); otherwise the tiles are cut into
+// ceil(vtiles / ceil(vtiles / splits_req)) splits (splits_req clamped to
+// [1, vtiles]).
+rlk_status split_plan(int64_t V, int64_t splits_req, int64_t* S, int64_t* vps, int64_t* vtiles) {
+  rlk_status st = rlk_vocab_split_policy(V, S, vps, vtiles);
+  if (st != RLK_OK || splits_req == 0) return st;
+  if (splits_req < 0) return RLK_ERR_SHAPE;
+  const int64_t want = splits_req < *vtiles ? splits_req : *vtiles;
+  *vps = ceil_div(*vtiles, want);
+  *S = ceil_div(*vtiles, *vps);
+  return RLK_OK;
+}
+
 rlk_status plan(const void* hidden, int64_t N, int64_t H, int64_t ldh, const void* weight,
-                int64_t V, int64_t ldw, LogpPlan* p) {
+                int64_t V, int64_t ldw, int64_t splits_req, LogpPlan* p) {
   rlk_status st = check_shapes(N, H, ldh, V, ldw);
   if (st != RLK_OK) return st;
-  st = rlk_vocab_split_policy(V, &p->S, &p->vps, &p->vtiles);
+  st = split_plan(V, splits_req, &p->S, &p->vps, &p->vtiles);
   if (st != RLK_OK) return st;
   p->stage_h = !tma_ready(hidden, ldh);
   p->stage_w = !tma_ready(weight, ldw);
@@ -335,22 +349,15 @@ uint32_t take_error_linear_logp() {
 
 using namespace rlk;
 
-extern "C" {
+namespace rlk {
+namespace {
 
-size_t rlk_linear_logp_workspace_size(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
-                                      const void* weight, int64_t V, int64_t ld_weight) {
+rlk_status partials_impl(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
+                         const void* weight, int64_t V, int64_t ld_weight, const float* bias,
+                         const int64_t* target, int64_t target_stride, int64_t splits_req,
+                         void* workspace, size_t workspace_bytes, void* stream) {
   LogpPlan p;
-  if (plan(hidden, N, H, ld_hidden, weight, V, ld_weight, &p) != RLK_OK) return 0;
-  return p.total;
-}
-
-rlk_status rlk_linear_logp_partials(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
-                                    const void* weight, int64_t V, int64_t ld_weight,
-                                    const float* bias, const int64_t* target,
-                                    int64_t target_stride, void* workspace,
-                                    size_t workspace_bytes, void* stream) {
-  LogpPlan p;
-  rlk_status st = plan(hidden, N, H, ld_hidden, weight, V, ld_weight, &p);
+  rlk_status st = plan(hidden, N, H, ld_hidden, weight, V, ld_weight, splits_req, &p);
   if (st != RLK_OK) return st;
   if (target_stride < 0) return RLK_ERR_SHAPE;
   if (N == 0) return RLK_OK;
@@ -432,10 +439,9 @@ rlk_status rlk_linear_logp_partials(const void* hidden, int64_t N, int64_t H, in
   return RLK_OK;
 }
 
-rlk_status rlk_linear_logp_combine(int64_t N, int64_t V, const int64_t* target,
-                                   int64_t target_stride, float* logp, float* lse,
-                                   float* target_logit, const void* workspace,
-                                   size_t workspace_bytes, void* stream) {
+rlk_status combine_impl(int64_t N, int64_t V, const int64_t* target, int64_t target_stride,
+                        float* logp, float* lse, float* target_logit, int64_t splits_req,
+                        const void* workspace, size_t workspace_bytes, void* stream) {
   if (N < 0 || N >= (int64_t(1) << 31) || V < 1 || V >= (int64_t(1) << 31) || target_stride < 0)
     return RLK_ERR_SHAPE;
   if (N == 0) return RLK_OK;
@@ -445,13 +451,14 @@ rlk_status rlk_linear_logp_combine(int64_t N, int64_t V, const int64_t* target,
       (reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(target_logit) & 3u))
     return RLK_ERR_ALIGN;
   int64_t S, vps, vt;
-  rlk_vocab_split_policy(V, &S, &vps, &vt);
+  rlk_status st = split_plan(V, splits_req, &S, &vps, &vt);
+  if (st != RLK_OK) return st;
   const size_t off_zt = align_up((size_t)N * S * sizeof(float2), 256);
   if ((reinterpret_cast<uintptr_t>(workspace) & 15u) ||
       workspace_bytes < off_zt + (size_t)N * sizeof(float))
     return RLK_ERR_WORKSPACE;
   DeviceInfo dev;
-  rlk_status st = device_ready(&dev);
+  st = device_ready(&dev);
   if (st != RLK_OK) return st;
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);
   const int rows_per_block = 256 / 32;
@@ -467,22 +474,98 @@ rlk_status rlk_linear_logp_combine(int64_t N, int64_t V, const int64_t* target,
   return RLK_OK;
 }
 
-rlk_status rlk_linear_logp(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
-                           const void* weight, int64_t V, int64_t ld_weight, const float* bias,
-                           const int64_t* target, int64_t target_stride, float* logp, float* lse,
-                           float* target_logit, void* workspace, size_t workspace_bytes,
-                           void* stream) {
+rlk_status linear_logp_impl(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
+                            const void* weight, int64_t V, int64_t ld_weight, const float* bias,
+                            const int64_t* target, int64_t target_stride, float* logp, float* lse,
+                            float* target_logit, int64_t splits_req, void* workspace,
+                            size_t workspace_bytes, void* stream) {
   // Validate everything the second stage needs before the first one launches.
   if (N > 0 && (!logp || !lse)) return RLK_ERR_NULL;
   if ((reinterpret_cast<uintptr_t>(logp) & 3u) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
       (reinterpret_cast<uintptr_t>(target_logit) & 3u))
     return RLK_ERR_ALIGN;
-  rlk_status st = rlk_linear_logp_partials(hidden, N, H, ld_hidden, weight, V, ld_weight, bias,
-                                           target, target_stride, workspace, workspace_bytes,
-                                           stream);
+  rlk_status st = partials_impl(hidden, N, H, ld_hidden, weight, V, ld_weight, bias, target,
+                                target_stride, splits_req, workspace, workspace_bytes, stream);
   if (st != RLK_OK) return st;
-  return rlk_linear_logp_combine(N, V, target, target_stride, logp, lse, target_logit, workspace,
-                                 workspace_bytes, stream);
+  return combine_impl(N, V, target, target_stride, logp, lse, target_logit, splits_req, workspace,
+                      workspace_bytes, stream);
+}
+
+}  // namespace
+}  // namespace rlk
+
+extern "C" {
+
+size_t rlk_linear_logp_workspace_size(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
+                                      const void* weight, int64_t V, int64_t ld_weight) {
+  LogpPlan p;
+  if (plan(hidden, N, H, ld_hidden, weight, V, ld_weight, 0, &p) != RLK_OK) return 0;
+  return p.total;
+}
+
+rlk_status rlk_linear_logp_partials(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
+                                    const void* weight, int64_t V, int64_t ld_weight,
+                                    const float* bias, const int64_t* target,
+                                    int64_t target_stride, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  return partials_impl(hidden, N, H, ld_hidden, weight, V, ld_weight, bias, target, target_stride,
+                       0, workspace, workspace_bytes, stream);
+}
+
+rlk_status rlk_linear_logp_combine(int64_t N, int64_t V, const int64_t* target,
+                                   int64_t target_stride, float* logp, float* lse,
+                                   float* target_logit, const void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  return combine_impl(N, V, target, target_stride, logp, lse, target_logit, 0, workspace,
+                      workspace_bytes, stream);
+}
+
+rlk_status rlk_linear_logp(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
+                           const void* weight, int64_t V, int64_t ld_weight, const float* bias,
+                           const int64_t* target, int64_t target_stride, float* logp, float* lse,
+                           float* target_logit, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  return linear_logp_impl(hidden, N, H, ld_hidden, weight, V, ld_weight, bias, target,
+                          target_stride, logp, lse, target_logit, 0, workspace, workspace_bytes,
+                          stream);
+}
+
+rlk_status rlk_throughput_split_count(int64_t N, int64_t V, int32_t sm_count,
+                                      int64_t* num_splits) {
+  if (!num_splits) return RLK_ERR_NULL;
+  if (N < 1 || N >= (int64_t(1) << 31) || V < 1 || V >= (int64_t(1) << 31) || sm_count < 0)
+    return RLK_ERR_SHAPE;
+  if (sm_count == 0) {
+    DeviceInfo dev;
+    const rlk_status st = device_ready(&dev);
+    if (st != RLK_OK) return st;
+    sm_count = dev.sm_count;
+  }
+  const int64_t vtiles = ceil_div(V, kVocabTile);
+  const int64_t row_blocks = ceil_div(N, 256);
+  const int64_t pairs = sm_count / 2 > 0 ? sm_count / 2 : 1;
+  const int64_t want = ceil_div(kOrderedMinRounds * pairs, row_blocks);
+  *num_splits = want < vtiles ? want : vtiles;
+  return RLK_OK;
+}
+
+size_t rlk_linear_logp_splits_workspace_size(const void* hidden, int64_t N, int64_t H,
+                                             int64_t ld_hidden, const void* weight, int64_t V,
+                                             int64_t ld_weight, int64_t num_splits) {
+  LogpPlan p;
+  if (plan(hidden, N, H, ld_hidden, weight, V, ld_weight, num_splits, &p) != RLK_OK) return 0;
+  return p.total;
+}
+
+rlk_status rlk_linear_logp_splits(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
+                                  const void* weight, int64_t V, int64_t ld_weight,
+                                  const float* bias, const int64_t* target, int64_t target_stride,
+                                  float* logp, float* lse, float* target_logit,
+                                  int64_t num_splits, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  return linear_logp_impl(hidden, N, H, ld_hidden, weight, V, ld_weight, bias, target,
+                          target_stride, logp, lse, target_logit, num_splits, workspace,
+                          workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -178,6 +178,49 @@ RLK_API rlk_status rlk_linear_logp(const void* hidden, int64_t N, int64_t H, int
                            void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Throughput-mode ablation (not batch invariant when num_splits depends on N).
+ *
+ * The RL-Kernel linear-logp page [P3 PR body, "Why this happens"] describes the
+ * project's earlier throughput scheduler: it picks the vocabulary split from N,
+ * V and the SM count, so one row may take a different FP32 merge path when the
+ * batch around it changes.  These entry points exist only to measure what the
+ * V-only policy costs against such a scheduler; rlk_linear_logp stays the
+ * operator.
+ *
+ * rlk_throughput_split_count: an occupancy-driven split count (the pages give
+ * no formula; this is the reading taken): enough splits that the (split,
+ * 256-row block) units number at least 8 per pair of SMs,
+ *     num_splits = min(ceil(V / 256), ceil(8 * floor(sm_count / 2) / ceil(N / 256))).
+ * sm_count = 0 queries the current device.  Host arithmetic only otherwise.
+ * Returns RLK_ERR_SHAPE for N < 1, V < 1, N or V >= 2^31 or sm_count < 0.
+ */
+RLK_API rlk_status rlk_throughput_split_count(int64_t N, int64_t V, int32_t sm_count,
+                                              int64_t* num_splits);
+
+/*
+ * rlk_linear_logp with an explicit split count: the 256-id tiles are cut into
+ * ceil(vtiles / vps) contiguous splits of vps = ceil(vtiles / num_splits) tiles
+ * (num_splits clamped to [1, vtiles]); num_splits = 0 selects the V-only policy
+ * and then equals rlk_linear_logp bit for bit.  Every other argument, the
+ * arithmetic within a split, the merge order and the error behaviour are those
+ * of rlk_linear_logp; the workspace must hold
+ * rlk_linear_logp_splits_workspace_size(..., num_splits) bytes.  Results are
+ * deterministic for a given num_splits; they are batch invariant only if the
+ * caller keeps num_splits fixed across batches.  RLK_ERR_SHAPE for num_splits < 0.
+ */
+RLK_API size_t rlk_linear_logp_splits_workspace_size(const void* hidden, int64_t N, int64_t H,
+                                                     int64_t ld_hidden, const void* weight,
+                                                     int64_t V, int64_t ld_weight,
+                                                     int64_t num_splits);
+RLK_API rlk_status rlk_linear_logp_splits(const void* hidden, int64_t N, int64_t H,
+                                          int64_t ld_hidden, const void* weight, int64_t V,
+                                          int64_t ld_weight, const float* bias,
+                                          const int64_t* target, int64_t target_stride,
+                                          float* logp, float* lse, float* target_logit,
+                                          int64_t num_splits, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+
+/*
  * First stage of rlk_linear_logp: one fused tensor-core kernel (projection
  * tiles + online-softmax epilogue) that writes the per-(row, split) partials
  * and the target logits into `workspace`.  Arguments as for rlk_linear_logp.

@@ -185,3 +185,34 @@ def test_binding_rejects_cpu_and_grad(lib):
         rlk.linear_logp(h.float().requires_grad_(), w, t)
     with pytest.raises(ValueError, match="CUDA"):
         rlk.det_gemm_fwd(h, w.T)
+
+
+def test_throughput_split_count(lib):
+    """Occupancy-driven split count of the ablation: min(vtiles, ceil(8 * pairs / row_blocks))."""
+    s = ctypes.c_int64()
+    f = lib.rlk_throughput_split_count
+    for N, V, sms, want in [(4096, 151936, 152, 38),      # 16 row blocks: ceil(608 / 16)
+                            (16384, 152064, 152, 10),     # 64 row blocks
+                            (17, 32003, 152, 126),        # one row block: every tile its own split
+                            (1, 151936, 152, 594),
+                            (256, 1024, 152, 4),          # capped at vtiles
+                            (100000, 151936, 152, 2),     # 391 row blocks: ceil(608 / 391)
+                            (200000, 151936, 152, 1),     # more row blocks than 8 * pairs
+                            (256, 151936, 1, 8)]:          # one SM still counts one pair
+        assert f(N, V, sms, ctypes.byref(s)) == 0, (N, V, sms)
+        assert s.value == want, (N, V, sms, s.value)
+    for bad in [(0, 10, 152), (10, 0, 152), (1 << 31, 10, 152), (10, 1 << 31, 152), (10, 10, -1)]:
+        assert f(*bad, ctypes.byref(s)) == 2
+    assert f(10, 10, 152, None) == 1
+
+
+def test_splits_workspace_size(lib):
+    f = lib.rlk_linear_logp_splits_workspace_size
+    g = lib.rlk_linear_logp_workspace_size
+    N, H, V = 4096, 4096, 151936
+    assert f(P16, N, H, H, P16, V, H, 0) == g(P16, N, H, H, P16, V, H)
+    assert f(P16, N, H, H, P16, V, H, 594) == g(P16, N, H, H, P16, V, H)
+    for req, S in [(38, 38), (1, 1), (5000, 594), (100, 99)]:   # vps = ceil(594/req), S = ceil(594/vps)
+        want = -(-N * S * 8 // 256) * 256 + -(-N * 4 // 256) * 256 + 256
+        assert f(P16, N, H, H, P16, V, H, req) == want, (req, S)
+    assert f(P16, N, H, H, P16, V, H, -1) == 0
