@@ -177,3 +177,44 @@ def test_zero_rows(dev):
     weight = torch.zeros(10, 256, dtype=torch.bfloat16, device=dev)
     lp, ls = rlk.linear_logp(hidden, weight, torch.empty(0, dtype=torch.int64, device=dev))
     assert lp.numel() == 0 and ls.numel() == 0
+
+
+def test_two_tile_splits(dev, orc):
+    """V > 262,144: the V-only policy puts two 256-id tiles in each split (vps = 2), so
+    each unit carries (m, s) across a tile boundary.  Targets sit on split and tile
+    edges; chunked calls reproduce the full call's bits."""
+    N, H, V = 300, 256, 300007
+    S, vps, vt = rlk.vocab_split_policy(V)
+    assert (S, vps, vt) == (586, 2, 1172)
+    hidden, weight, bias, target = si.linear_logp_inputs(N, H, V, bias=True, seed=31)
+    edges = [0, 255, 256, 511, 512, 1023, 1024, 299519, 299520, V - 1, 150000, 150016]
+    for i, e in enumerate(edges):
+        target[i * 23] = e
+    hd, wd, bd, td = hidden.to(dev), weight.to(dev), bias.to(dev), target.to(dev)
+    logp, lse, zt = rlk.linear_logp(hd, wd, td, bd, return_target_logit=True)
+    torch.cuda.synchronize()
+    rows = sorted(set(sample_rows(N, 24, seed=5)) | {i * 23 for i in range(len(edges))})
+    rlp, rls, rzt = oracle_rows(orc, hidden[rows], weight, target[rows], bias)
+    assert_logp_close(logp.cpu().numpy()[rows], lse.cpu().numpy()[rows], rlp, rls, "vps=2")
+    assert np.abs(zt.cpu().numpy()[rows] - rzt).max() <= 1e-4
+    for chunk in (1, 7, 129):
+        parts = [rlk.linear_logp(hd[s:s + chunk], wd, td[s:s + chunk], bd) for s in range(0, N, chunk)]
+        assert torch.equal(torch.cat([p[0] for p in parts]), logp)
+        assert torch.equal(torch.cat([p[1] for p in parts]), lse)
+    assert rlk.device_error() == 0
+
+
+def test_long_hidden(dev, orc):
+    """H = 65,536: 1,024 reduction blocks of 64 per tile.  A logit's FP32
+    accumulation error grows with H (about sqrt(H) * 2^-24 * sum|x w|, ~2.5e-3
+    here), so the target logit is held to the operator's 1e-3 rather than the
+    1e-4 the moderate-H tests use."""
+    N, H, V = 200, 65536, 1000
+    hidden, weight, bias, target = si.linear_logp_inputs(N, H, V, bias=True, seed=32)
+    lp, ls, zt = run(dev, hidden, weight, target, bias)
+    rows = sample_rows(N, 16, seed=6, must=(0, 127, 128, N - 1))
+    rlp, rls, rzt = oracle_rows(orc, hidden[rows], weight, target[rows], bias)
+    assert_logp_close(lp[rows], ls[rows], rlp, rls, "H=65536")
+    assert np.abs(zt[rows] - rzt).max() <= LOGP_ATOL
+    one = rlk.linear_logp(hidden[7:8].to(dev), weight.to(dev), target[7:8].to(dev), bias.to(dev))
+    assert float(one[0]) == float(lp[7]) and float(one[1]) == float(ls[7])
