@@ -46,7 +46,7 @@ def load_peaks():
 
 
 # ---------------------------------------------------------------- measured traffic
-KERNEL_SOURCES = ["rlk_device.cuh", "rlk_pipeline.cuh", "linear_logp.cu", "det_gemm.cu", "common.cu"]
+KERNEL_SOURCES = ["rlk_device.cuh", "rlk_pipeline.cuh", "rlk_solo.cuh", "linear_logp.cu", "det_gemm.cu", "common.cu"]
 # (linear_logp_bwd.cu is not hashed: it launches none of the kernels whose traffic is recorded)
 
 

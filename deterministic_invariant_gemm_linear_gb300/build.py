@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "librlk.so")
 
 SOURCES = ["common.cu", "linear_logp.cu", "linear_logp_bwd.cu", "det_gemm.cu"]
-HEADERS = [os.path.join(CSRC, h) for h in ("rlk_device.cuh", "rlk_pipeline.cuh", "rlk_internal.h")]
+HEADERS = [os.path.join(CSRC, h) for h in ("rlk_device.cuh", "rlk_pipeline.cuh", "rlk_solo.cuh", "rlk_internal.h")]
 HEADERS.append(os.path.join(INCLUDE, "rlk.h"))
 
 NVCC_FLAGS = [

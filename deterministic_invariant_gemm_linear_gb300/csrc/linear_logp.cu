@@ -7,7 +7,9 @@
 //
 // Stage 1 (linear_logp_partials_kernel): the 2-SM tcgen05 main loop (a cluster
 // of two CTAs, M=256 x N=256 per MMA) computes 256 x 256 FP32 logit tiles, each
-// CTA holding its 128 rows in TMEM; the epilogue keeps, per row and per vocabulary split,
+// CTA holding its 128 rows in TMEM; calls of at most 128 rows run instead on
+// the one-CTA loop (linear_logp_solo_kernel, M=128 x N=256 per MMA, one unit
+// per CTA), which gives the same bits.  The epilogue keeps, per row and per vocabulary split,
 // an online maximum m and sum of exponentials s over the split's tiles in
 // ascending vocabulary order, and captures the target logit.  Work unit =
 // (vocabulary split j, 256-row block), dealt in L2-sized bands of row blocks so
@@ -28,6 +30,7 @@
 #include "rlk.h"
 #include "rlk_internal.h"
 #include "rlk_pipeline.cuh"
+#include "rlk_solo.cuh"
 
 namespace rlk {
 
@@ -133,14 +136,67 @@ __device__ __forceinline__ void logp_chunk(const uint32_t (&r)[32], int vbase, i
   m = mn;
 }
 
+// Epilogue warps (2..5) of both loops: each thread owns one row (TMEM lane) of
+// the CTA's 128 accumulator rows; for every 256-id tile of the unit's split, in
+// ascending order, it folds the tile's logits into (m, s) 32 columns at a time,
+// then writes the split's partial.  kSolo: the one-CTA loop (128-row blocks,
+// round-robin units, local release); else the 2-SM loop (256-row blocks over
+// the pair, units from the ring, release on rank 0's barrier).  The arithmetic
+// is the same code either way.
+template <bool kSolo>
+__device__ __forceinline__ void logp_epilogue(const LogpSched& sc, const LogpArgs& args,
+                                              const PipeSmem& ps, uint32_t tmem) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int q = warp & 3;
+  const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+  int acc = 0;
+  uint32_t acc_phase = 0;
+  bool run = true;
+  for (int k = 0; run; ++k) {
+    const int u = kSolo ? solo_unit(sc, k) : warp_unit_take(sc, ps, k, &g_err_linear_logp);
+    if (u < 0) break;
+    const int j = sc.split_of(u);
+    const int row = sc.rb_of(u) * sc.rows_per_unit + (kSolo ? 0 : (int)ps.rank * kHalfRows) +
+                    q * 32 + lane;
+    const bool valid = row < args.N;
+    const int64_t tgt = valid ? __ldg(args.target + (int64_t)row * args.tstride) : -1;
+    float m = -INFINITY, s = 0.f, zt = 0.f;
+    bool have_zt = false;
+    const int t0 = sc.first_tile(u), nt = sc.unit_tiles(u);
+    for (int i = 0; i < nt; ++i) {
+      if (!epilogue_acquire(ps, acc, acc_phase, &g_err_linear_logp)) {
+        run = false;
+        break;
+      }
+      const int v0 = (t0 + i) * kBN;
+      const uint32_t taddr = tmem + acc * kAccCols + lane_off;
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        const int vbase = v0 + c * 32;
+        if (vbase >= args.V) break;          // uniform: depends on the tile only
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(taddr + c * 32, r);
+        tmem_wait_ld();
+        logp_chunk(r, vbase, args.V, args.bias, tgt, m, s, have_zt, zt);
+      }
+      if (kSolo)
+        solo_release(ps, acc);
+      else
+        epilogue_release(ps, acc);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (!run) break;
+    if (valid) {
+      args.ws_ms[(int64_t)row * sc.S + j] = make_float2(m, s);
+      if (have_zt) args.ws_zt[row] = zt;
+    }
+  }
+}
+
 // A cluster of two CTAs computes a unit = (split j, 256-row block) on the 2-SM
-// tcgen05 loop; the CTA of rank r owns rows [256 * block + 128 r, +128).  Each
-// epilogue thread owns one row: for every 256-id tile of the split, in
-// ascending order, it folds the tile's logits into (m, s) 32 columns at a time.
-// R is the stage ring: RingFull, or RingThin when N <= 32 (every row in rank
-// 0's first 32); the MMA and the epilogue are the same for both, so a row's
-// bits do not depend on which ring computed it.
-template <class R>
+// tcgen05 loop; the CTA of rank r owns rows [256 * block + 128 r, +128).
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     linear_logp_partials_kernel(const __grid_constant__ CUtensorMap tm_hidden,
                                      const __grid_constant__ CUtensorMap tm_weight, LogpSched sc,
@@ -153,63 +209,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_weight);
   }
   const uint32_t tmem = pipe_setup(ps);
-  using TA = OperandTile<false, R::kARows>;
   using THalf = OperandTile<false, kHalfRows>;
 
   if (warp == 0) {
-    if (lane == 0) producer_role<TA, THalf, R>(&tm_hidden, &tm_weight, sc, ps, &g_err_linear_logp);
+    if (lane == 0) producer_role<THalf, THalf>(&tm_hidden, &tm_weight, sc, ps, &g_err_linear_logp);
     if (lane == 1 && ps.rank == 0) scheduler_role(sc, ps, &g_err_linear_logp);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0 && ps.rank == 0)
-      mma_role<TA, THalf, R>(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, false, false),
+      mma_role<THalf, THalf>(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, false, false),
                               &g_err_linear_logp);
     __syncwarp();
   } else {
-    const int q = warp & 3;
-    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    bool run = true;
-    for (int k = 0; run; ++k) {
-      const int u = warp_unit_take(sc, ps, k, &g_err_linear_logp);
-      if (u < 0) break;
-      const int j = sc.split_of(u);
-      const int row = sc.rb_of(u) * kPairRows + (int)ps.rank * kHalfRows + q * 32 + lane;
-      const bool valid = row < args.N;
-      const int64_t tgt = valid ? __ldg(args.target + (int64_t)row * args.tstride) : -1;
-      float m = -INFINITY, s = 0.f, zt = 0.f;
-      bool have_zt = false;
-      const int t0 = sc.first_tile(u), nt = sc.unit_tiles(u);
-      for (int i = 0; i < nt; ++i) {
-        if (!epilogue_acquire(ps, acc, acc_phase, &g_err_linear_logp)) {
-          run = false;
-          break;
-        }
-        const int v0 = (t0 + i) * kBN;
-        const uint32_t taddr = tmem + acc * kAccCols + lane_off;
-#pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-          const int vbase = v0 + c * 32;
-          if (vbase >= args.V) break;          // uniform: depends on the tile only
-          uint32_t r[32];
-          __syncwarp();
-          tmem_ld32(taddr + c * 32, r);
-          tmem_wait_ld();
-          logp_chunk(r, vbase, args.V, args.bias, tgt, m, s, have_zt, zt);
-        }
-        epilogue_release(ps, acc);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
-      }
-      if (!run) break;
-      if (valid) {
-        args.ws_ms[(int64_t)row * sc.S + j] = make_float2(m, s);
-        if (have_zt) args.ws_zt[row] = zt;
-      }
-    }
+    logp_epilogue<false>(sc, args, ps, tmem);
   }
   pipe_teardown(tmem);
+}
+
+// One CTA per unit = (split j, 128-row block) on the one-CTA loop, for calls of
+// at most 128 rows (a single row block).  R: SoloThin when N <= 32, else
+// SoloFull.
+template <class R>
+__global__ void __launch_bounds__(kThreads, 1)
+    linear_logp_solo_kernel(const __grid_constant__ CUtensorMap tm_hidden,
+                            const __grid_constant__ CUtensorMap tm_weight, LogpSched sc,
+                            LogpArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  const PipeSmem ps = pipe_smem(smem_raw);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tm_hidden);
+    tma_prefetch_desc(&tm_weight);
+  }
+  const uint32_t tmem = solo_setup(ps);
+  using TA = OperandTile<false, R::kARows>;
+  using TB = OperandTile<false, kBN>;
+
+  if (warp == 0) {
+    if (lane == 0) solo_producer<TA, TB, R>(&tm_hidden, &tm_weight, sc, ps, &g_err_linear_logp);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0)
+      solo_mma<TA, TB, R>(sc, ps, tmem, idesc_bf16_f32(kHalfRows, kBN, false, false),
+                          &g_err_linear_logp);
+    __syncwarp();
+  } else {
+    logp_epilogue<true>(sc, args, ps, tmem);
+  }
+  solo_teardown(tmem);
 }
 
 // (m, s) pair merge with explicit roundings, so merge(a, b) == merge(b, a) bitwise.
@@ -266,12 +313,15 @@ cudaError_t ensure_attrs(int dev) {
   std::lock_guard<std::mutex> lock(g_attr_mutex);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!g_attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(linear_logp_partials_kernel<RingFull>,
+    cudaError_t e = cudaFuncSetAttribute(linear_logp_partials_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         RingFull::kSmemBytes);
+                                         PairRing::kSmemBytes);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(linear_logp_partials_kernel<RingThin>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, RingThin::kSmemBytes);
+    e = cudaFuncSetAttribute(linear_logp_solo_kernel<SoloFull>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, SoloFull::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(linear_logp_solo_kernel<SoloThin>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, SoloThin::kSmemBytes);
     if (e != cudaSuccess) return e;
     g_attr_set[dev] = true;
   }
@@ -389,12 +439,15 @@ rlk_status partials_impl(const void* hidden, int64_t N, int64_t H, int64_t ld_hi
       return RLK_ERR_CUDA;
     w_src = ws + p.off_w;
   }
-  constexpr int kRowsPerUnit = kPairRows;
-  // At most 32 rows: the thin ring (rank 0 stages the 32 rows, 11 stages deep).
-  const bool thin = N <= RingThin::kARows;
+  // At most 128 rows (one 128-row block): the one-CTA loop, one unit per CTA;
+  // otherwise the 2-SM loop over 256-row blocks.  At most 32 rows: the thin
+  // rings (only 32 hidden rows staged per stage).
+  const bool solo = N <= kHalfRows;
+  const bool thin = N <= 32;
+  const int kRowsPerUnit = solo ? kHalfRows : kPairRows;
   CUtensorMap tm_h, tm_w;
-  if (!encode_bf16_2d(&tm_h, h_src, H, N, p.ldh, kBK, thin ? RingThin::kARows : kHalfRows) ||
-      !encode_bf16_2d(&tm_w, w_src, H, V, p.ldw, kBK, kHalfRows))
+  if (!encode_bf16_2d(&tm_h, h_src, H, N, p.ldh, kBK, thin ? 32 : kHalfRows) ||
+      !encode_bf16_2d(&tm_w, w_src, H, V, p.ldw, kBK, solo ? kBN : kHalfRows))
     return RLK_ERR_CUDA;
 
   LogpSched sc;
@@ -416,6 +469,20 @@ rlk_status partials_impl(const void* hidden, int64_t N, int64_t H, int64_t ld_hi
   a.ws_zt = reinterpret_cast<float*>(ws + p.off_zt);
   const int64_t units = (int64_t)sc.order.rows * sc.S;
   if (units >= (int64_t(1) << 31)) return RLK_ERR_SHAPE;
+  if (solo) {
+    sc.counter = nullptr;      // round-robin: at most ceil(1024 / #SMs) rounds
+    const int grid = (int)(units < dev.sm_count ? units : dev.sm_count);
+    const cudaError_t e =
+        thin ? launch_overlapped(linear_logp_solo_kernel<SoloThin>, grid, kThreads,
+                                 SoloThin::kSmemBytes, s, tm_h, tm_w, sc, a)
+             : launch_overlapped(linear_logp_solo_kernel<SoloFull>, grid, kThreads,
+                                 SoloFull::kSmemBytes, s, tm_h, tm_w, sc, a);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return RLK_ERR_CUDA;
+    }
+    return RLK_OK;
+  }
   // One cluster of two CTAs per pair of SMs, persistent over the units.
   const int64_t clusters = dev.sm_count / 2;
   const int grid = 2 * (int)(units < clusters ? units : clusters);
@@ -427,11 +494,8 @@ rlk_status partials_impl(const void* hidden, int64_t N, int64_t H, int64_t ld_hi
       return RLK_ERR_CUDA;
     }
   }
-  const cudaError_t e =
-      thin ? launch_overlapped(linear_logp_partials_kernel<RingThin>, grid, kThreads,
-                               RingThin::kSmemBytes, s, tm_h, tm_w, sc, a)
-           : launch_overlapped(linear_logp_partials_kernel<RingFull>, grid, kThreads,
-                               RingFull::kSmemBytes, s, tm_h, tm_w, sc, a);
+  const cudaError_t e = launch_overlapped(linear_logp_partials_kernel, grid, kThreads,
+                                         PairRing::kSmemBytes, s, tm_h, tm_w, sc, a);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return RLK_ERR_CUDA;

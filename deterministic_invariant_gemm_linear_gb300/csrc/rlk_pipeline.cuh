@@ -26,27 +26,19 @@ constexpr int kSmemLimit = 232448;                    // 227 KiB per CTA
 constexpr int kBarrierBlockBytes = 1024;              // keeps the ring 1024-byte aligned
 constexpr int kMaxStages = 11;
 
-// The stage ring.  Each stage holds kARows rows of this CTA's left-operand half
-// and its 128 rows of the right-operand tile (64 reduction columns each), in two
-// areas: left-operand blocks of all stages first, then right-operand blocks.
-// kARows = 128 is the general ring.  kARows = 32 serves a left operand whose
-// valid rows all lie in rank 0's first 32: rank 0 stages only those, rank 1
-// none, and the smaller stages buy a deeper ring (more right-operand bytes in
-// flight).  The MMA still reads 128 rows per CTA; the rows past the staged ones
-// hold other data, which reaches only accumulator rows that nothing reads (row
-// i of a product depends on row i of the left operand alone).
-template <int kARows_>
-struct Ring {
-  static constexpr int kARows = kARows_;
-  static constexpr int kABytes = kARows * kBK * 2;                 // 16 KiB or 4 KiB
+// The stage ring: each stage holds this CTA's 128 rows of the left operand and
+// its 128 rows of the right-operand tile (64 reduction columns each, 16 KiB
+// apiece), in two areas: left-operand blocks of all stages first, then the
+// right-operand blocks.
+struct PairRing {
+  static constexpr int kABytes = kHalfRows * kBK * 2;              // 16 KiB
   static constexpr int kBBytes = kHalfRows * kBK * 2;              // 16 KiB
   static constexpr int kStages =
       (kSmemLimit - 1024 - kBarrierBlockBytes) / (kABytes + kBBytes) < kMaxStages
           ? (kSmemLimit - 1024 - kBarrierBlockBytes) / (kABytes + kBBytes)
-          : kMaxStages;
+          : kMaxStages;                                             // 7
   // Bytes rank 0's full barrier counts per stage (both CTAs' copies).
-  static constexpr uint32_t kTxBytes = kARows == kHalfRows ? 2u * (kABytes + kBBytes)
-                                                           : (uint32_t)kABytes + 2u * kBBytes;
+  static constexpr uint32_t kTxBytes = 2u * (kABytes + kBBytes);
   static constexpr int kSmemBytes = 1024 + kBarrierBlockBytes + kStages * (kABytes + kBBytes);
   static __device__ __forceinline__ uint32_t a_stage(uint32_t ring, int s) {
     return ring + s * kABytes;
@@ -54,17 +46,11 @@ struct Ring {
   static __device__ __forceinline__ uint32_t b_stage(uint32_t ring, int s) {
     return ring + kStages * kABytes + s * kBBytes;
   }
-  static_assert(kARows == kHalfRows || kARows == 32, "general or thin ring");
   static_assert(kSmemBytes <= kSmemLimit, "exceeds the 227 KiB per-CTA shared memory limit");
   // One CTA per SM: a second resident CTA could not get TMEM columns.
   static_assert(kSmemBytes > kSmemLimit / 2, "tcgen05 kernels must own their SM");
-  // The MMA reads 16 KiB of left operand from any stage's block: stay inside the ring.
-  static_assert(kStages * (kABytes + kBBytes) >= kHalfRows * kBK * 2 + (kStages - 1) * kABytes,
-                "left-operand reads leave the ring");
 };
-using RingFull = Ring<kHalfRows>;   // 7 stages x 32 KiB
-using RingThin = Ring<32>;          // 11 stages x 20 KiB
-constexpr int kSmemBytes = RingFull::kSmemBytes;
+constexpr int kSmemBytes = PairRing::kSmemBytes;
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -350,13 +336,13 @@ __device__ __forceinline__ int warp_unit_take(const Sched& sc, const PipeSmem& p
 // from zero, so a tile's arithmetic depends only on its operand tiles, never on
 // the schedule, the grid or the row count.  TA / TB are the 128-row operand
 // halves (OperandTile<majorness, 128>).
-template <class TA, class TB, class R = RingFull, class Sched>
+template <class TA, class TB, class Sched>
 __device__ __forceinline__ void producer_role(const CUtensorMap* ta, const CUtensorMap* tb,
                                                const Sched& sc, const PipeSmem& ps,
                                                unsigned int* err) {
-  static_assert(TA::kBytes == R::kABytes && TB::kBytes == R::kBBytes, "operand blocks fit the ring");
+  using R = PairRing;
+  static_assert(TA::kBytes == R::kABytes && TB::kBytes == R::kBBytes, "operand halves are 128 rows");
   constexpr int kStages = R::kStages;
-  const bool load_a = R::kARows == kHalfRows || ps.rank == 0;
   int stage = 0;
   uint32_t phase = 0, issued = 0, last_parity = 0;
   bool run = true;
@@ -378,9 +364,8 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* ta, const CUten
         }
         if (ps.rank == 0) mbar_arrive_expect_tx(ps.full(stage), R::kTxBytes);
         const uint32_t leader_full = mapa_shared(ps.full(stage), 0);
-        if (load_a)
-          TA::template load<true>(R::a_stage(ps.stages, stage), ta, leader_full, a0 + half,
-                                  kb * kBK);
+        TA::template load<true>(R::a_stage(ps.stages, stage), ta, leader_full, a0 + half,
+                                kb * kBK);
         TB::template load<true>(R::b_stage(ps.stages, stage), tb, leader_full, b0 + half,
                                 kb * kBK);
         issued |= 1u << stage;
@@ -411,9 +396,10 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* ta, const CUten
   }
 }
 
-template <class TA, class TB, class R = RingFull, class Sched>
+template <class TA, class TB, class Sched>
 __device__ __forceinline__ void mma_role(const Sched& sc, const PipeSmem& ps, uint32_t tmem,
                                           uint32_t idesc, unsigned int* err) {
+  using R = PairRing;
   constexpr int kStages = R::kStages;
   int stage = 0, acc = 0;
   uint32_t phase = 0, acc_phase = 0;

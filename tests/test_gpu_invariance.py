@@ -122,17 +122,21 @@ def test_layouts(dev):
     assert_same(lp(hidden, weight, t_strided, bias), ref, "strided target")
 
 
-@pytest.mark.parametrize("n_small", [1, 17, 32])
-def test_thin_ring_matches_full_ring(dev, n_small):
-    """Calls of at most 32 rows stage only those rows (a deeper ring of smaller
-    stages); their bits equal the same rows inside larger calls (33 and 300 rows,
-    the general ring), for a ragged vocabulary with bias and a staged hidden."""
+@pytest.mark.parametrize("n_small", [1, 17, 32, 100, 128])
+def test_small_call_loops_match_the_pair_loop(dev, n_small):
+    """Calls of at most 128 rows run on the one-CTA loop (M=128 per CTA; at most
+    32 rows: a thin ring staging only those rows); larger calls on the 2-SM loop
+    (M=256 over a pair).  A row's bits are the same in all of them: the rows of a
+    small call equal the same rows inside 33-, 129- and 300-row calls, for a
+    ragged vocabulary with bias, and with a staged (odd-pitch) hidden."""
     H, V = 2048, 32003
     hidden, weight, bias, target = si.linear_logp_inputs(300, H, V, bias=True, seed=16, device=dev)
-    for start in (0, 5, 268):
+    for start in (0, 5, 172):
         rows = slice(start, start + n_small)
         small = lp(hidden[rows], weight, target[rows], bias)
-        for big_n in (33, 300):
+        for big_n in (33, 129, 300):
+            if big_n <= n_small:
+                continue
             s0 = max(0, min(start, big_n - n_small))
             h_big, t_big = hidden[:big_n].clone(), target[:big_n].clone()
             h_big[s0:s0 + n_small], t_big[s0:s0 + n_small] = hidden[rows], target[rows]
@@ -142,5 +146,5 @@ def test_thin_ring_matches_full_ring(dev, n_small):
     odd = torch.zeros(n_small, H + 1, dtype=torch.bfloat16, device=dev)
     odd[:, :H] = hidden[:n_small]
     assert_same(lp(odd[:, :H], weight, target[:n_small], bias),
-                lp(hidden[:n_small], weight, target[:n_small], bias), "thin ring, staged hidden")
+                lp(hidden[:n_small], weight, target[:n_small], bias), "small call, staged hidden")
     assert rlk.device_error() == 0
