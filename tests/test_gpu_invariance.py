@@ -148,3 +148,18 @@ def test_small_call_loops_match_the_pair_loop(dev, n_small):
     assert_same(lp(odd[:, :H], weight, target[:n_small], bias),
                 lp(hidden[:n_small], weight, target[:n_small], bias), "small call, staged hidden")
     assert rlk.device_error() == 0
+
+
+@pytest.mark.parametrize("N", [17, 300])
+def test_bias_alignment_paths(dev, N):
+    """A 16-byte-aligned bias is read four floats at a time, any other one float at a
+    time; both add the same FP32 values, so the bits agree (one-CTA and 2-SM loops)."""
+    H, V = 1024, 32003
+    hidden, weight, bias, target = si.linear_logp_inputs(N, H, V, bias=True, seed=17, device=dev)
+    assert bias.data_ptr() % 16 == 0
+    store = torch.empty(V + 4, dtype=torch.float32, device=dev)
+    store[1:V + 1] = bias
+    shifted = store[1:V + 1]
+    assert shifted.data_ptr() % 16 == 4
+    assert_same(lp(hidden, weight, target, shifted), lp(hidden, weight, target, bias),
+                "bias read one float at a time vs four at a time")
