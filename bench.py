@@ -161,6 +161,22 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- CPU oracle leg
+def oracle_gemm_tflops(A, B, dC, rows: int):
+    """Time the FP64 oracle's fwd, dA and dB on `rows` output rows each (host cores)."""
+    import oracle
+    orc = oracle.load()
+    cores = orc.max_threads()
+    a, b, d = si.bf16_bits(A), si.bf16_bits(B), si.bf16_bits(dC)
+    r = np.arange(rows, dtype=np.int64)
+    t0 = time.perf_counter()
+    orc.gemm_fwd(a, b, rows=r, threads=cores)
+    orc.gemm_da(d, b, rows=r, threads=cores)
+    orc.gemm_db(a, d, rows=r, threads=cores)
+    dt = time.perf_counter() - t0
+    flop = 2.0 * rows * (B.shape[1] * A.shape[1] + dC.shape[1] * B.shape[0] + dC.shape[1] * A.shape[0])
+    return flop / dt / 1e12, dt, cores
+
+
 def oracle_tokens_per_s(hidden, weight, target, bias, rows: int):
     """Time the FP64 oracle on `rows` rows of the workload (host cores)."""
     import oracle
@@ -407,7 +423,7 @@ def backward_bench(args, dev, rank, world, peaks, peak_src):
             "grad_hidden det_gemm_fwd": t_dh / K * 1e3, "grad_weight det_gemm_db": t_dw / K * 1e3}
     peak = peaks["bf16_tflops"]
     achieved = flops * K / t_local / 1e12
-    return {
+    line = {
         "metric": f"linear-logp backward TFLOP/s (N={N},H={H},V={V}; grad_hidden + grad_weight)",
         "value": flops * world * K / t / 1e12, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": t / K * 1e3, "higher_is_better": True,
@@ -424,6 +440,20 @@ def backward_bench(args, dev, rank, world, peaks, peak_src):
         "clocks": clocks.summary(),
         "gpu_launches": 3 * K,
     }
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+        orc = oracle.load()
+        rows = orc.max_threads()
+        hb, wb = si.bf16_bits(hidden[:rows]), si.bf16_bits(weight)
+        t0 = time.perf_counter()
+        orc.linear_logp_backward(hb, wb, target[:rows].cpu().numpy(), g[:rows].cpu().numpy(),
+                                 threads=rows)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": 3 * 2.0 * rows * H * V / dt / 1e12, "unit": "TFLOP/s",
+                                "cores": rows, "kind": "oracle",
+                                "sample": f"{rows} rows of the backward (G by definition in FP64, "
+                                          f"then float64 products), full V and H, {dt:.2f} s wall"}
+    return line
 
 
 def det_gemm_bench(args, dev, rank, world, peaks, peak_src):
@@ -472,7 +502,7 @@ def det_gemm_bench(args, dev, rank, world, peaks, peak_src):
     torch.cuda.synchronize()
     cublas = flop / (c0.elapsed_time(c1) / 10 / 1e3) / 1e12
     best = min(ms, key=ms.get)
-    return {
+    line = {
         "metric": "det_gemm fwd+da+db TFLOP/s (M=N=K=4096, BF16 in/out, FP32 accumulate)",
         "value": 3 * flop * world * K / t / 1e12, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": t / K * 1e3, "higher_is_better": True,
@@ -493,6 +523,36 @@ def det_gemm_bench(args, dev, rank, world, peaks, peak_src):
         "clocks": clocks.summary(),
         "gpu_launches": 3 * K,
     }
+    # ---- e2e: host buffers (pinned) in, all three results out, copies timed
+    if not args.no_e2e:
+        Ah, Bh, dCh = (x.cpu().pin_memory() for x in (A, B, dC))
+        outs = [torch.empty(M, N, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+        E = max(3, min(K, 10))
+        for i in range(E + 2):
+            if i == 2:
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            A.copy_(Ah, non_blocking=True)
+            B.copy_(Bh, non_blocking=True)
+            dC.copy_(dCh, non_blocking=True)
+            for o, (_, f) in zip(outs, ops):
+                o.copy_(f(), non_blocking=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        te = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
+        line["e2e"] = {"value": 3 * flop * world * E / te / 1e12, "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": 3 * M * K_ * 2, "d2h_bytes_per_step": 3 * M * N * 2,
+                       "ms_per_step": te / E * 1e3}
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+        rows = 2 * oracle.load().max_threads()
+        tf, dt, cores = oracle_gemm_tflops(A, B, dC, rows)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                "sample": f"{rows} output rows of each of fwd, dA and dB at 4096^3, "
+                                          f"FP64, {dt:.2f} s wall"}
+    return line
 
 
 def ablation_bench(args, dev, rank, world, peaks, peak_src):
