@@ -51,6 +51,7 @@ struct GradArgs {
   int N, V;
   int64_t tstride;
   const float* bias;
+  bool bias_vec4;       // bias is 16-byte aligned: whole chunks read it 4 floats at a time
   const int64_t* target;
   const float* lse;
   const float* grad;
@@ -112,12 +113,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
         tmem_ld32(taddr + c * 32, r);
         tmem_wait_ld();
+        float bv[32];
+        if (a.bias != nullptr && a.bias_vec4 && vbase + 32 <= a.V) {
+          const float4* b4 = reinterpret_cast<const float4*>(a.bias + vbase);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 b = __ldg(b4 + i);
+            bv[4 * i] = b.x;
+            bv[4 * i + 1] = b.y;
+            bv[4 * i + 2] = b.z;
+            bv[4 * i + 3] = b.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            bv[i] = (a.bias != nullptr && vbase + i < a.V) ? __ldg(a.bias + vbase + i) : 0.f;
+        }
         float G[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int v = vbase + i;
           float z = __uint_as_float(r[i]);
-          if (a.bias != nullptr && v < a.V) z = __fadd_rn(z, __ldg(a.bias + v));
+          if (a.bias != nullptr && v < a.V) z = __fadd_rn(z, bv[i]);
           const float p = ex2_approx(__fmul_rn(__fsub_rn(z, L), kLog2e));
           const float onehot = (int64_t)v == t ? 1.f : 0.f;
           G[i] = (live && v < a.V) ? __fmul_rn(g, __fsub_rn(onehot, p)) : 0.f;
@@ -269,6 +286,7 @@ rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H, in
   a.V = (int)V;
   a.tstride = target_stride;
   a.bias = bias;
+  a.bias_vec4 = (reinterpret_cast<uintptr_t>(bias) & 15u) == 0;
   a.target = target;
   a.lse = lse;
   a.grad = grad_logp;

@@ -145,8 +145,12 @@ def test_small_call_loops_match_the_pair_loop(dev, n_small):
                         f"{n_small} rows at {start} vs a {big_n}-row call")
     odd = torch.zeros(n_small, H + 1, dtype=torch.bfloat16, device=dev)
     odd[:, :H] = hidden[:n_small]
-    assert_same(lp(odd[:, :H], weight, target[:n_small], bias),
-                lp(hidden[:n_small], weight, target[:n_small], bias), "small call, staged hidden")
+    ref = lp(hidden[:n_small], weight, target[:n_small], bias)
+    assert_same(lp(odd[:, :H], weight, target[:n_small], bias), ref, "small call, staged hidden")
+    wodd = torch.zeros(V, H + 3, dtype=torch.bfloat16, device=dev)
+    wodd[:, :H] = weight
+    assert_same(lp(hidden[:n_small], wodd[:, :H], target[:n_small], bias), ref,
+                "small call, staged weight")
     assert rlk.device_error() == 0
 
 

@@ -120,3 +120,20 @@ def test_backward_zero_rows(dev):
                                           torch.empty(0, device=dev), torch.empty(0, device=dev),
                                           torch.zeros(50, device=dev), out_dtype=torch.float32)
     assert dh.numel() == 0 and bool((dw == 0).all()) and bool((db == 0).all())
+
+
+def test_backward_bias_alignment_paths(dev):
+    """An aligned bias is read four floats at a time, any other one float at a time:
+    G and all three gradients agree bit for bit."""
+    N, H, V = 300, 512, 5003
+    hidden, weight, b, target = si.linear_logp_inputs(N, H, V, bias=True, seed=41, device=dev)
+    g = torch.randn(N, generator=torch.Generator(device=dev).manual_seed(42), device=dev)
+    _, lse = rlk.linear_logp(hidden, weight, target, b)
+    store = torch.empty(V + 4, dtype=torch.float32, device=dev)
+    store[1:V + 1] = b
+    shifted = store[1:V + 1]
+    assert b.data_ptr() % 16 == 0 and shifted.data_ptr() % 16 == 4
+    ref = rlk.linear_logp_backward(hidden, weight, target, lse, g, b, return_grad_logits=True)
+    got = rlk.linear_logp_backward(hidden, weight, target, lse, g, shifted, return_grad_logits=True)
+    for x, y in zip(ref, got):
+        assert torch.equal(x, y)
