@@ -82,3 +82,21 @@ def test_n_dependent_count_changes_bits(dev):
     # record, do not require: how many sampled rows changed lse bits
     print(f"throughput mode: {differ} of {len(rows)} sampled rows changed lse bits "
           f"between N=1 (S={s_one}) and N={w.N} (S={s_full})")
+
+
+@pytest.mark.parametrize("splits", [1, 7])
+def test_small_call_multi_tile_units(dev, orc, splits):
+    """17 rows run on the one-CTA loop; with 1 or 7 splits each unit folds many
+    256-id tiles (594 or 85) into its (m, s)."""
+    w = si.MID
+    hidden, weight, bias, target = si.workload_inputs(w, seed=24, device=dev)
+    hidden, target = hidden[:17].contiguous(), target[:17].contiguous()
+    got = run(hidden, weight, target, bias, splits)
+    for a, b in zip(got, run(hidden, weight, target, bias, splits)):
+        assert torch.equal(a, b)
+    rlp, rls, rzt = orc.linear_logp(si.bf16_bits(hidden), si.bf16_bits(weight),
+                                    target.cpu().numpy(), None)
+    lp, ls, zt = (t.cpu().numpy() for t in got)
+    assert_logp_close(lp, ls, rlp, rls, f"17 rows, splits={splits}")
+    assert np.abs(zt - rzt).max() <= 1e-4
+    assert rlk.device_error() == 0
