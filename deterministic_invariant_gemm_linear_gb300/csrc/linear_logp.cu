@@ -12,8 +12,9 @@
 // per CTA), which gives the same bits.  The epilogue keeps, per row and per vocabulary split,
 // an online maximum m and sum of exponentials s over the split's tiles in
 // ascending vocabulary order, and captures the target logit.  Work unit =
-// (vocabulary split j, 256-row block), dealt in L2-sized bands of row blocks so
-// that the clusters running at the same time share hidden and W tiles in L2.
+// (vocabulary split j, 256-row block) — 128-row on the one-CTA loop — dealt in
+// L2-sized bands of row blocks so that the clusters running at the same time
+// share hidden and W tiles in L2.
 //
 // Stage 2 (linear_logp_combine_kernel): one warp per row merges the row's S
 // partials in a fixed order (lane l takes splits l, l+32, ... ascending, then a
@@ -61,7 +62,7 @@ struct LogpSched {
     const int t0 = first_tile(u);
     return min(vps, vtiles - t0);
   }
-  int rows_per_unit;   // 256: the rows of a CTA pair
+  int rows_per_unit;   // 256 (a CTA pair's rows) or 128 (one CTA's, the one-CTA loop)
   __device__ __forceinline__ void tile_coords(int u, int i, int& a0, int& b0) const {
     a0 = rb_of(u) * rows_per_unit;
     b0 = (first_tile(u) + i) * kBN;
