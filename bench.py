@@ -247,7 +247,7 @@ def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
     assert rlk.device_error() == 0, "device error word set during the bench"
     part_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
     comb_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
-    warm = None
+    warm = whole = None
     if flush is not None:
         # the same steps with W left in L2 by the previous step (reported beside the cold numbers)
         for k in range(K):
@@ -260,6 +260,17 @@ def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
         warm = {"partials_ms": float(np.mean([e[0].elapsed_time(e[1]) for e in ev])),
                 "combine_ms": float(np.mean([e[1].elapsed_time(e[2]) for e in ev])),
                 "note": "no flush between steps: W (%.1f MB) partly L2-resident" % (w_bytes / 1e6)}
+        # whole calls (partials + combine, no event between them: the combine's launch
+        # overlaps the partials kernel's tail), L2 flushed before each as in the timed region
+        for k in range(K):
+            flush.zero_()
+            ev[k][0].record(stream)
+            call()
+            ev[k][2].record(stream)
+        torch.cuda.synchronize()
+        whole = {"ms": float(np.mean([e[0].elapsed_time(e[2]) for e in ev])),
+                 "note": "partials + combine with no event between them (the combine's launch "
+                         "overlaps the partials tail), L2 flushed before each call"}
     ms_step = t / K * 1e3
     tokens = w.N * world * K
     value = tokens / t
@@ -303,6 +314,7 @@ def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
         "kernels_ms": {"linear_logp_partials": part_ms, "linear_logp_combine": comb_ms},
         "roofline": roof,
         **({"l2_warm": warm} if warm is not None else {}),
+        **({"whole_call": whole} if whole is not None else {}),
         "clocks": clocks.summary(),
         "gpu_launches": 2 * K,
     }
