@@ -212,7 +212,7 @@ rlk_status rlk_selftest_bounded_wait(uint32_t timeout_us, void* stream) {
 rlk_status rlk_vocab_split_policy(int64_t V, int64_t* num_splits, int64_t* vtiles_per_split,
                                   int64_t* num_vtiles) {
   if (!num_splits || !vtiles_per_split || !num_vtiles) return RLK_ERR_NULL;
-  if (V < 1 || V >= (int64_t(1) << 31)) return RLK_ERR_SHAPE;
+  if (V < 1 || V >= rlk::kMaxExtent) return RLK_ERR_SHAPE;
   const int64_t vt = rlk::ceil_div(V, rlk::kVocabTile);
   const int64_t vps = rlk::ceil_div(vt, rlk::kMaxVocabSplits);
   *num_vtiles = vt;

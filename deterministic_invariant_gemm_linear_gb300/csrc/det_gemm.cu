@@ -208,7 +208,7 @@ void plan_operand(Operand& o, size_t& off) {
 
 rlk_status check_operand(const Operand& o, bool allow_fp32) {
   if (!dtype_ok(o.dtype) || (o.dtype == RLK_FP32 && !allow_fp32)) return RLK_ERR_DTYPE;
-  if (o.rows < 0 || o.rows >= kDimLimit || o.cols < 1 || o.cols >= kDimLimit) return RLK_ERR_SHAPE;
+  if (o.rows < 0 || o.rows >= kMaxExtent || o.cols < 1 || o.cols >= kMaxExtent) return RLK_ERR_SHAPE;
   if (o.ld < o.cols || o.ld >= kLdLimit) return RLK_ERR_SHAPE;
   return RLK_OK;
 }

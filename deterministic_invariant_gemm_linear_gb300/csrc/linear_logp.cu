@@ -350,9 +350,9 @@ struct LogpPlan {
 };
 
 rlk_status check_shapes(int64_t N, int64_t H, int64_t ldh, int64_t V, int64_t ldw) {
-  if (N < 0 || N >= (int64_t(1) << 31)) return RLK_ERR_SHAPE;
+  if (N < 0 || N >= kMaxExtent) return RLK_ERR_SHAPE;
   if (H < 1 || H >= (int64_t(1) << 20)) return RLK_ERR_SHAPE;
-  if (V < 1 || V >= (int64_t(1) << 31)) return RLK_ERR_SHAPE;
+  if (V < 1 || V >= kMaxExtent) return RLK_ERR_SHAPE;
   if (ldh < H || ldw < H) return RLK_ERR_SHAPE;
   if (ldh >= (int64_t(1) << 36) || ldw >= (int64_t(1) << 36)) return RLK_ERR_SHAPE;
   return RLK_OK;
@@ -378,6 +378,8 @@ rlk_status plan(const void* hidden, int64_t N, int64_t H, int64_t ldh, const voi
   if (st != RLK_OK) return st;
   st = split_plan(V, splits_req, &p->S, &p->vps, &p->vtiles);
   if (st != RLK_OK) return st;
+  // (split, row block) units are numbered in an int
+  if (ceil_div(N, kPairRows) * p->S >= (int64_t(1) << 31)) return RLK_ERR_SHAPE;
   p->stage_h = !tma_ready(hidden, ldh);
   p->stage_w = !tma_ready(weight, ldw);
   p->ldh = p->stage_h ? staged_ld(H) : ldh;
@@ -481,8 +483,7 @@ rlk_status partials_impl(const void* hidden, int64_t N, int64_t H, int64_t ld_hi
   a.target = target;
   a.ws_ms = reinterpret_cast<float2*>(ws);
   a.ws_zt = reinterpret_cast<float*>(ws + p.off_zt);
-  const int64_t units = (int64_t)sc.order.rows * sc.S;
-  if (units >= (int64_t(1) << 31)) return RLK_ERR_SHAPE;
+  const int64_t units = (int64_t)sc.order.rows * sc.S;   // < 2^31: checked by plan()
   if (solo) {
     sc.counter = nullptr;      // round-robin: at most ceil(1024 / #SMs) rounds
     const int grid = (int)(units < dev.sm_count ? units : dev.sm_count);
@@ -520,7 +521,7 @@ rlk_status partials_impl(const void* hidden, int64_t N, int64_t H, int64_t ld_hi
 rlk_status combine_impl(int64_t N, int64_t V, const int64_t* target, int64_t target_stride,
                         float* logp, float* lse, float* target_logit, int64_t splits_req,
                         const void* workspace, size_t workspace_bytes, void* stream) {
-  if (N < 0 || N >= (int64_t(1) << 31) || V < 1 || V >= (int64_t(1) << 31) || target_stride < 0)
+  if (N < 0 || N >= kMaxExtent || V < 1 || V >= kMaxExtent || target_stride < 0)
     return RLK_ERR_SHAPE;
   if (N == 0) return RLK_OK;
   if (!target || !logp || !lse) return RLK_ERR_NULL;
@@ -611,7 +612,7 @@ rlk_status rlk_linear_logp(const void* hidden, int64_t N, int64_t H, int64_t ld_
 rlk_status rlk_throughput_split_count(int64_t N, int64_t V, int32_t sm_count,
                                       int64_t* num_splits) {
   if (!num_splits) return RLK_ERR_NULL;
-  if (N < 1 || N >= (int64_t(1) << 31) || V < 1 || V >= (int64_t(1) << 31) || sm_count < 0)
+  if (N < 1 || N >= kMaxExtent || V < 1 || V >= kMaxExtent || sm_count < 0)
     return RLK_ERR_SHAPE;
   if (sm_count == 0) {
     DeviceInfo dev;

@@ -219,7 +219,7 @@ using namespace rlk;
 extern "C" {
 
 size_t rlk_linear_logp_backward_workspace_size(int64_t N, int64_t V) {
-  if (N < 0 || N >= (int64_t(1) << 31) || V < 1 || V >= (int64_t(1) << 31)) return 0;
+  if (N < 0 || N >= kMaxExtent || V < 1 || V >= kMaxExtent) return 0;
   return align_up((size_t)N * grad_ld(V) * 2, 256) + 256;   // G, then the unit counter
 }
 
@@ -231,8 +231,8 @@ rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H, in
                                     int64_t ld_grad_hidden, void* grad_weight,
                                     int grad_weight_dtype, int64_t ld_grad_weight, float* grad_bias,
                                     void* workspace, size_t workspace_bytes, void* stream) {
-  if (N < 0 || N >= (int64_t(1) << 31) || H < 1 || H >= (int64_t(1) << 20) || V < 1 ||
-      V >= (int64_t(1) << 31) || ld_hidden < H || ld_weight < H || target_stride < 0 ||
+  if (N < 0 || N >= kMaxExtent || H < 1 || H >= (int64_t(1) << 20) || V < 1 ||
+      V >= kMaxExtent || ld_hidden < H || ld_weight < H || target_stride < 0 ||
       ld_hidden >= (int64_t(1) << 36) || ld_weight >= (int64_t(1) << 36))
     return RLK_ERR_SHAPE;
   if (grad_hidden && ld_grad_hidden < H) return RLK_ERR_SHAPE;

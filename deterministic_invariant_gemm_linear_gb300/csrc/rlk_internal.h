@@ -43,6 +43,11 @@ cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// Largest accepted row / column / vocabulary extent (exclusive): kernels index
+// rows and ids in 32-bit ints, and the last index of a 256-wide block (and a
+// 32-wide chunk's end) must stay below 2^31.
+constexpr int64_t kMaxExtent = (int64_t(1) << 31) - 256;
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

@@ -127,7 +127,7 @@ RLK_API rlk_status rlk_selftest_bounded_wait(uint32_t timeout_us, void* stream);
  * than 1024:
  *     vtiles_per_split = ceil(vtiles / 1024),  S = ceil(vtiles / vtiles_per_split).
  * Split j covers vocabulary ids [j * vps * 256, min((j + 1) * vps * 256, V)).
- * Host-only; needs no device.  Returns RLK_ERR_SHAPE for V < 1 or V >= 2^31.
+ * Host-only; needs no device.  Returns RLK_ERR_SHAPE for V < 1 or V >= 2^31 - 256.
  */
 RLK_API rlk_status rlk_vocab_split_policy(int64_t V, int64_t* num_splits, int64_t* vtiles_per_split,
                                   int64_t* num_vtiles);
@@ -157,7 +157,8 @@ RLK_API size_t rlk_linear_logp_workspace_size(const void* hidden, int64_t N, int
  *                entered the log-sum-exp
  *  workspace     >= rlk_linear_logp_workspace_size(...) bytes, 16-byte aligned
  *
- * Shapes: 0 <= N < 2^31, 1 <= H < 2^20, 1 <= V < 2^31.  A target outside
+ * Shapes: 0 <= N < 2^31 - 256, 1 <= H < 2^20, 1 <= V < 2^31 - 256 (the kernels
+ * index rows and ids in 32-bit ints).  A target outside
  * [0, V) yields logp = NaN (and target_logit = NaN) for that row; lse is
  * still valid; nothing is read out of bounds.
  *
@@ -192,7 +193,7 @@ RLK_API rlk_status rlk_linear_logp(const void* hidden, int64_t N, int64_t H, int
  * 256-row block) units number at least 8 per pair of SMs,
  *     num_splits = min(ceil(V / 256), ceil(8 * floor(sm_count / 2) / ceil(N / 256))).
  * sm_count = 0 queries the current device.  Host arithmetic only otherwise.
- * Returns RLK_ERR_SHAPE for N < 1, V < 1, N or V >= 2^31 or sm_count < 0.
+ * Returns RLK_ERR_SHAPE for N < 1, V < 1, N or V >= 2^31 - 256 or sm_count < 0.
  */
 RLK_API rlk_status rlk_throughput_split_count(int64_t N, int64_t V, int32_t sm_count,
                                               int64_t* num_splits);
@@ -330,7 +331,7 @@ RLK_API rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64
  * A batched operand [b, M, K] is passed flattened as [b * M, K] (a leading
  * shape is a row count), so fwd and dA are bitwise equal per row whatever the
  * batching, and dB sums over all b * M rows in ascending order.
- * Shapes: 0 <= M < 2^31 and 1 <= K, N < 2^31 (M is the row count of A / dC,
+ * Shapes: 0 <= M < 2^31 - 256 and 1 <= K, N < 2^31 - 256 (M is the row count of A / dC,
  * K the column count of A and row count of B, N the column count of B / dC).
  * Leading dimensions >= the column count of their matrix.
  */

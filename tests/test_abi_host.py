@@ -47,7 +47,7 @@ def test_status_strings_and_version(lib):
 
 
 @pytest.mark.parametrize("V", [1, 2, 255, 256, 257, 1024, 32003, 151936, 152064, 262144, 262145,
-                               1 << 20, (1 << 31) - 1])
+                               1 << 20, (1 << 31) - 257])
 def test_vocab_split_policy(lib, V):
     S, vps, vt = rlk.vocab_split_policy(V)
     assert vt == -(-V // 256)
@@ -216,3 +216,24 @@ def test_splits_workspace_size(lib):
         want = -(-N * S * 8 // 256) * 256 + -(-N * 4 // 256) * 256 + 256
         assert f(P16, N, H, H, P16, V, H, req) == want, (req, S)
     assert f(P16, N, H, H, P16, V, H, -1) == 0
+
+
+def test_extent_limits(lib):
+    """Row, column and vocabulary extents stay below 2^31 - 256 (the kernels index
+    them in 32-bit ints); shape errors come before any other check."""
+    lim = (1 << 31) - 256
+    s, v, t = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    assert lib.rlk_vocab_split_policy(lim, ctypes.byref(s), ctypes.byref(v), ctypes.byref(t)) == 2
+    assert lib.rlk_vocab_split_policy(lim - 1, ctypes.byref(s), ctypes.byref(v), ctypes.byref(t)) == 0
+    assert t.value == -(-(lim - 1) // 256) and s.value * v.value >= t.value
+    ws = ctypes.c_void_p(0x20000)
+    f = lib.rlk_linear_logp
+    assert f(P16, lim, 8, 8, P16, 10, 8, NULL, P16, 1, P16, P16, NULL, ws, 1 << 20, NULL) == 2
+    assert f(P16, 4, 8, 8, P16, lim, 8, NULL, P16, 1, P16, P16, NULL, ws, 1 << 20, NULL) == 2
+    assert lib.rlk_linear_logp_workspace_size(P16, lim, 8, 8, P16, 10, 8) == 0
+    # (split, row block) units must number below 2^31: 2^29 rows x 1024 splits do not
+    assert lib.rlk_linear_logp_workspace_size(P16, 1 << 29, 8, 8, P16, 1 << 18, 8) == 0
+    assert lib.rlk_throughput_split_count(lim, 10, 152, ctypes.byref(s)) == 2
+    fwd = lib.rlk_det_gemm_fwd
+    assert fwd(P16, lim, 8, 8, P16, 8, 8, P16, 0, 8, ws, 0, NULL) == 2
+    assert fwd(P16, 4, 8, 8, P16, lim, lim, P16, 0, lim, ws, 0, NULL) == 2
