@@ -1,5 +1,6 @@
 // The warp-specialised, persistent 2-SM (cta_group::2) tcgen05 main loop shared
-// by every tensor-core kernel of the library.
+// by the library's tensor-core kernels (linear-logp calls of at most 128 rows
+// use the one-CTA variant in rlk_solo.cuh instead).
 //
 // A cluster of two CTAs on two SMs computes one 256 x 256 FP32 accumulator
 // tile per MMA chain: rank r holds rows [128 r, 128 r + 128) of the left
@@ -24,7 +25,7 @@ namespace rlk {
 // Dynamic shared memory: alignment slack, the barrier block, then the stage ring.
 constexpr int kSmemLimit = 232448;                    // 227 KiB per CTA
 constexpr int kBarrierBlockBytes = 1024;              // keeps the ring 1024-byte aligned
-constexpr int kMaxStages = 11;
+constexpr int kMaxStages = 11;                        // barrier slots; the rings use at most 7
 
 // The stage ring: each stage holds this CTA's 128 rows of the left operand and
 // its 128 rows of the right-operand tile (64 reduction columns each, 16 KiB
