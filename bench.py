@@ -203,7 +203,7 @@ def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
     if args.workload == "ragged":
         w = si.ragged(args.rows or 17)
     else:
-        w = {"mid": si.MID, "large": si.LARGE}[args.workload]
+        w = {"mid": si.MID, "large": si.LARGE, "tiny": si.TINY}[args.workload]
     if args.rows and args.workload != "ragged":
         w = si.LinearLogpWorkload(f"{w.name} (rows={args.rows})", N=args.rows, H=w.H, V=w.V,
                                   bias=w.bias, target_mode=w.target_mode)
@@ -706,7 +706,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="mid",
-                    choices=["mid", "large", "ragged", "det_gemm", "backward", "ablation"])
+                    choices=["mid", "large", "tiny", "ragged", "det_gemm", "backward", "ablation"])
     ap.add_argument("--impl", default="rlk", choices=["rlk", "reference"])
     ap.add_argument("--rows", type=int, default=0,
                     help="override the row count N of a linear-logp workload (profiling cases)")
