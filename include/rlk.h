@@ -163,8 +163,9 @@ RLK_API size_t rlk_linear_logp_workspace_size(const void* hidden, int64_t N, int
  * still valid; nothing is read out of bounds.
  *
  * Arithmetic (fixed; depends on V and H only): FP32 accumulation over H in
- * ascending blocks of 64 (tensor cores, M=256 x N=256 x K=16 per instruction
- * over a pair of SMs); per 256-id tile
+ * ascending blocks of 64 (tensor cores, K=16 per instruction: M=256 x N=256
+ * over a pair of SMs, or M=128 x N=256 on one SM for calls of at most 128
+ * rows, which give the same bits per element); per 256-id tile
  * and per row an online max / sum-of-exponentials in ascending vocabulary
  * order; S = rlk_vocab_split_policy(V) partials per row merged in a fixed
  * order (lane j%32 ascending, then a fixed xor-butterfly).  Each row's bits
