@@ -84,3 +84,32 @@ def test_backward_and_det_gemm_graph_replay(dev):
         for a, b in zip(outs, eager):
             assert torch.equal(a, b)
     assert rlk.device_error() == 0
+
+
+@pytest.mark.parametrize("N", [17, 1000])
+def test_calls_see_inputs_written_just_before(dev, N):
+    """Each library kernel may start while the previous kernel in the stream is
+    finishing (programmatic dependent launch) and waits for it before touching
+    memory: a torch kernel that rewrites the inputs right before every call, with
+    no synchronisation in between, is always seen."""
+    H, V = 1024, 20000
+    hidden, weight, bias, target = si.linear_logp_inputs(N, H, V, bias=True, seed=56, device=dev)
+    A, B, _ = si.det_gemm_inputs(N, H, 768, seed=57, device=dev)
+    want = {}
+    for sign in (1.0, -1.0):
+        want[sign] = (rlk.linear_logp(hidden * sign, weight, target, bias),
+                      rlk.det_gemm_fwd(A * sign, B, out_dtype=torch.float32))
+    torch.cuda.synchronize()
+    got = []
+    sign = 1.0
+    for _ in range(8):
+        hidden.mul_(-1.0)            # torch kernels, immediately followed by the library's
+        A.mul_(-1.0)
+        sign = -sign
+        got.append((sign, rlk.linear_logp(hidden, weight, target, bias),
+                    rlk.det_gemm_fwd(A, B, out_dtype=torch.float32)))
+    torch.cuda.synchronize()
+    for sign, lp, c in got:
+        (wl, wc) = want[sign]
+        assert torch.equal(lp[0], wl[0]) and torch.equal(lp[1], wl[1]) and torch.equal(c, wc)
+    assert rlk.device_error() == 0
