@@ -245,8 +245,11 @@ def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
         t_local = sum(e[0].elapsed_time(e[2]) for e in ev) / 1e3
     t = max_over_ranks(t_local, world, dev)
     assert rlk.device_error() == 0, "device error word set during the bench"
-    part_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
-    comb_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
+    part_all = [e[0].elapsed_time(e[1]) for e in ev]
+    comb_all = [e[1].elapsed_time(e[2]) for e in ev]
+    part_ms, comb_ms = float(np.mean(part_all)), float(np.mean(comb_all))
+    step_stats = {"partials_median_ms": float(np.median(part_all)), "partials_best_ms": float(min(part_all)),
+                  "combine_median_ms": float(np.median(comb_all)), "combine_best_ms": float(min(comb_all))}
     warm = whole = None
     if flush is not None:
         # the same steps with W left in L2 by the previous step (reported beside the cold numbers)
@@ -312,6 +315,7 @@ def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
         "tflops": flops * world * K / t / 1e12,
         "frac_bf16_peak": flops * K / t_local / 1e12 / peak,
         "kernels_ms": {"linear_logp_partials": part_ms, "linear_logp_combine": comb_ms},
+        "kernels_step_stats": step_stats,
         "roofline": roof,
         **({"l2_warm": warm} if warm is not None else {}),
         **({"whole_call": whole} if whole is not None else {}),
