@@ -108,22 +108,78 @@ def max_over_ranks(x: float, world: int, device) -> float:
 
 
 # ---------------------------------------------------------------- clocks
+# NVML clock-event reason bits (nvml.h): read only, never set.
+_NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+class _Nvml:
+    """Read-only NVML queries through ctypes (the driver's libnvidia-ml): the SM
+    clock, its maximum, the power draw and the active clock-event reasons."""
+
+    def __init__(self, device: torch.device):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        ok = False
+        try:   # match the CUDA device to its NVML handle by PCI bus id
+            p = torch.cuda.get_device_properties(device)
+            bus = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0".encode()
+            ok = self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(self.h)) == 0
+        except (AttributeError, TypeError):
+            ok = False
+        if not ok and self.lib.nvmlDeviceGetHandleByIndex_v2(
+                ctypes.c_uint(device.index or 0), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle for the device")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        v = ctypes.c_uint()
+        self.max_mhz = float(v.value) if self.lib.nvmlDeviceGetMaxClockInfo(
+            self.h, 1, ctypes.byref(v)) == 0 else None
+
+    def sample(self):
+        c = self.c
+        clk, mw, rs = c.c_uint(), c.c_uint(), c.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, c.byref(clk)) != 0:   # NVML_CLOCK_SM
+            return None
+        power = mw.value / 1e3 if self.lib.nvmlDeviceGetPowerUsage(self.h, c.byref(mw)) == 0 else None
+        reasons = rs.value if self.reasons_fn(self.h, c.byref(rs)) == 0 else 0
+        return float(clk.value), power, reasons
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+    """SM clock / throttle-reason samples taken while the timed region runs: NVML
+    every ~2 ms from a thread of this process (read-only queries), else
+    nvidia-smi every 50 ms."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
-        self.index = index
+    def __init__(self, device):
+        self.device = device if isinstance(device, torch.device) else torch.device("cuda", device)
         self.proc = None
+        self.nvml = None
         self.lines = []
+        self.samples = []
+        self.stop = threading.Event()
+        self.thread = None
 
     def __enter__(self):
         try:
+            self.nvml = _Nvml(self.device)
+        except (OSError, AttributeError):
+            self.nvml = None
+        if self.nvml is not None:
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return self
+        try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                ["nvidia-smi", "-i", str(self.device.index or 0), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
@@ -132,20 +188,41 @@ class ClockSampler:
             self.proc = None
         return self
 
+    def _poll(self):
+        while not self.stop.is_set():
+            s = self.nvml.sample()
+            if s is not None:
+                self.samples.append(s)
+            self.stop.wait(0.002)
+
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
     def __exit__(self, *exc):
+        self.stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self.thread is not None:
             self.thread.join(timeout=2)
 
     def summary(self):
+        if self.nvml is not None:
+            if not self.samples:
+                return None
+            sm = [x[0] for x in self.samples]
+            reasons = set()
+            for _, _, r in self.samples:
+                reasons.update(n for bit, n in _NVML_REASONS.items() if r & bit)
+            pw = [x[1] for x in self.samples if x[1] is not None]
+            return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": self.nvml.max_mhz,
+                    "sm_mhz_min": min(sm), "sm_mhz_max": max(sm), "reasons": sorted(reasons),
+                    "samples": len(sm), "power_w_max": max(pw) if pw else None,
+                    "source": "NVML in-process, ~2 ms period"}
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.lines:
@@ -163,7 +240,27 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvidia-smi, 50 ms period"}
+
+
+# Dense BF16 tensor-core rate per SM per clock on this architecture: one
+# M=128 x N=256 x K=16 MMA (1,048,576 FLOP) per 128 cycles, i.e. 8192 FLOP/clk
+# (the nominal 2.25 PFLOP/s over 152 SMs corresponds to ~1.81 GHz).
+BF16_FLOP_PER_SM_CLK = 8192
+
+
+def per_clock(achieved_tflops: float, clocks, device) -> dict:
+    """The achieved rate normalised by the SM clock sampled during the timed region."""
+    if not clocks or not clocks.get("sm_mhz"):
+        return {}
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    mhz = clocks["sm_mhz"]
+    ceiling = sms * BF16_FLOP_PER_SM_CLK * mhz * 1e6 / 1e12
+    return {"tflops_per_ghz": achieved_tflops / (mhz / 1e3),
+            "per_clock_ceiling_tflops": ceiling,
+            "per_clock_frac": achieved_tflops / ceiling,
+            "per_clock_note": f"{sms} SMs x {BF16_FLOP_PER_SM_CLK} dense BF16 FLOP/clk x median "
+                              f"{mhz:.0f} MHz under load"}
 
 
 # ---------------------------------------------------------------- CPU oracle leg
@@ -226,7 +323,7 @@ def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
     end = torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(dev.index) as clocks:
+    with ClockSampler(dev) as clocks:
         start.record(stream)
         for k in range(K):
             if flush is not None:
@@ -322,6 +419,8 @@ def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
         "clocks": clocks.summary(),
         "gpu_launches": 2 * K,
     }
+    if roof["bound"] == "tensor":
+        roof.update(per_clock(roof["achieved"], line["clocks"], dev))
     # ---- e2e through the public API with host buffers (pinned), copies timed.
     # Inputs are double-buffered: step k+1's host-to-device copies run on a copy
     # stream while step k's kernels run, and every step still copies all of its
@@ -436,7 +535,7 @@ def backward_bench(args, dev, rank, world, peaks, peak_src):
         return s.elapsed_time(e) / 1e3
 
     barrier(world)
-    with ClockSampler(dev.index) as clocks:
+    with ClockSampler(dev) as clocks:
         t_local = timed(step)
     t = max_over_ranks(t_local, world, dev)
     t_dh, t_dw = timed(gemm_dh), timed(gemm_dw)
@@ -464,6 +563,7 @@ def backward_bench(args, dev, rank, world, peaks, peak_src):
         "clocks": clocks.summary(),
         "gpu_launches": 3 * K,
     }
+    line["roofline"].update(per_clock(line["roofline"]["achieved"], line["clocks"], dev))
     if rank == 0 and world == 1 and not args.no_cpu:
         import oracle
         orc = oracle.load()
@@ -497,7 +597,7 @@ def det_gemm_bench(args, dev, rank, world, peaks, peak_src):
     per = {n: [] for n, _ in ops}
     total = 0.0
     barrier(world)
-    with ClockSampler(dev.index) as clocks:
+    with ClockSampler(dev) as clocks:
         for _ in range(K):
             flush.zero_()
             s = torch.cuda.Event(enable_timing=True)
@@ -547,6 +647,7 @@ def det_gemm_bench(args, dev, rank, world, peaks, peak_src):
         "clocks": clocks.summary(),
         "gpu_launches": 3 * K,
     }
+    line["roofline"].update(per_clock(line["roofline"]["achieved"], line["clocks"], dev))
     # ---- e2e: host buffers (pinned) in, all three results out, copies timed.  Two
     # input / output sets alternate: a step's host-to-device copies (h2d stream)
     # and the previous step's device-to-host copies (d2h stream) overlap the
@@ -642,7 +743,7 @@ def ablation_bench(args, dev, rank, world, peaks, peak_src):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if weight.numel() * 2 < (512 << 20) else None
     ms = {k: [] for k in calls}
     barrier(world)
-    with ClockSampler(dev.index) as clocks:
+    with ClockSampler(dev) as clocks:
         for _ in range(3):
             for name, c in calls.items():
                 if flush is None:

@@ -66,6 +66,7 @@ SIGNATURES = {
     "rlk_linear_logp_splits": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _P, _I64,
                                     _P, _P, _P, _I64, _P, _SZ, _P]),
     "rlk_linear_logp_backward_workspace_size": (_SZ, [_I64, _I64]),
+    "rlk_linear_logp_backward_workspace_size_for": (_SZ, [_P, _I64, _I64, _I64, _P, _I64, _I64]),
     "rlk_linear_logp_backward": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _P, _I64, _P, _P,
                                       _P, _I, _I64, _P, _I, _I64, _P, _P, _SZ, _P]),
     "rlk_det_gemm_workspace_size": (_SZ, [_I, _P, _I, _I64, _I64, _I64, _P, _I, _I64, _I64, _I64]),
@@ -327,8 +328,10 @@ def linear_logp_backward(hidden: torch.Tensor, weight: torch.Tensor, target: tor
     gw = torch.empty(V, H, dtype=out_dtype, device=dev) if grad_weight else None
     gb = torch.empty(V, dtype=torch.float32, device=dev) if grad_bias else None
     with torch.cuda.device(dev):
-        n = lib().rlk_linear_logp_backward_workspace_size(N, V)
-        ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+        n = lib().rlk_linear_logp_backward_workspace_size_for(_ptr(h2), N, H, ldh, _ptr(w2), V, ldw)
+        if n == 0:
+            raise RlkError(2, "rlk_linear_logp_backward_workspace_size_for")
+        ws = torch.empty(n, dtype=torch.uint8, device=dev)
         dt = _DT[out_dtype]
         _check(lib().rlk_linear_logp_backward(
             _ptr(h2), N, H, ldh, _ptr(w2), V, ldw, _ptr(bias), _ptr(t1), tstride, _ptr(l1), _ptr(g1),

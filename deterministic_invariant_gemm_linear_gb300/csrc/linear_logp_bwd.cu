@@ -199,6 +199,50 @@ cudaError_t ensure_attrs(int dev) {
 
 inline int64_t grad_ld(int64_t V) { return ceil_div(V, 8) * 8; }
 
+constexpr int64_t kLdLimit = int64_t(1) << 36;
+constexpr int64_t kUnitLimit = int64_t(1) << 31;
+
+// Workspace plan of the backward (each region 256-byte aligned):
+// [G: N x ldG BF16][unit counter][padded copy of hidden][padded copy of W].
+// hidden / W are copied (zero padded) only when TMA cannot read them in place;
+// the copies hold the same values, so the results are bitwise the same.
+struct BwdPlan {
+  int64_t ldG = 0;
+  bool stage_h = false, stage_w = false;
+  int64_t ldh = 0, ldw = 0;      // pitches the kernels read
+  size_t off_ctr = 0, off_h = 0, off_w = 0, total = 0;
+};
+
+rlk_status bwd_plan(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
+                    const void* weight, int64_t V, int64_t ld_weight, BwdPlan* p) {
+  if (N < 0 || N >= kMaxExtent || H < 1 || H >= (int64_t(1) << 20) || V < 1 ||
+      V >= kMaxExtent || ld_hidden < H || ld_weight < H || ld_hidden >= kLdLimit ||
+      ld_weight >= kLdLimit)
+    return RLK_ERR_SHAPE;
+  // work-unit counts of the G kernel and of the two products, numbered in ints
+  const int64_t rb = ceil_div(N, kPairRows), vt = ceil_div(V, kBN), hb = ceil_div(H, kBN);
+  if (rb * vt >= kUnitLimit || rb * hb >= kUnitLimit || vt * hb >= kUnitLimit)
+    return RLK_ERR_SHAPE;
+  p->ldG = grad_ld(V);
+  p->stage_h = N > 0 && !tma_ready(hidden, ld_hidden);
+  p->stage_w = N > 0 && !tma_ready(weight, ld_weight);
+  p->ldh = p->stage_h ? staged_ld(H) : ld_hidden;
+  p->ldw = p->stage_w ? staged_ld(H) : ld_weight;
+  size_t off = align_up((size_t)N * p->ldG * 2, 256);
+  p->off_ctr = off;
+  off += 256;
+  p->off_h = off;
+  if (p->stage_h) off = align_up(off + (size_t)N * p->ldh * 2, 256);
+  p->off_w = off;
+  if (p->stage_w) off = align_up(off + (size_t)V * p->ldw * 2, 256);
+  p->total = off;
+  return RLK_OK;
+}
+
+inline bool aligned_to(const void* p, size_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
 }  // namespace
 
 uint32_t take_error_linear_logp_bwd() {
@@ -223,6 +267,14 @@ size_t rlk_linear_logp_backward_workspace_size(int64_t N, int64_t V) {
   return align_up((size_t)N * grad_ld(V) * 2, 256) + 256;   // G, then the unit counter
 }
 
+size_t rlk_linear_logp_backward_workspace_size_for(const void* hidden, int64_t N, int64_t H,
+                                                   int64_t ld_hidden, const void* weight,
+                                                   int64_t V, int64_t ld_weight) {
+  BwdPlan p;
+  if (bwd_plan(hidden, N, H, ld_hidden, weight, V, ld_weight, &p) != RLK_OK) return 0;
+  return p.total;
+}
+
 rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
                                     const void* weight, int64_t V, int64_t ld_weight,
                                     const float* bias, const int64_t* target,
@@ -231,74 +283,91 @@ rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H, in
                                     int64_t ld_grad_hidden, void* grad_weight,
                                     int grad_weight_dtype, int64_t ld_grad_weight, float* grad_bias,
                                     void* workspace, size_t workspace_bytes, void* stream) {
-  if (N < 0 || N >= kMaxExtent || H < 1 || H >= (int64_t(1) << 20) || V < 1 ||
-      V >= kMaxExtent || ld_hidden < H || ld_weight < H || target_stride < 0 ||
-      ld_hidden >= (int64_t(1) << 36) || ld_weight >= (int64_t(1) << 36))
-    return RLK_ERR_SHAPE;
-  if (grad_hidden && ld_grad_hidden < H) return RLK_ERR_SHAPE;
-  if (grad_weight && ld_grad_weight < H) return RLK_ERR_SHAPE;
+  // ---- every check, including those of the products below, before the first launch
+  BwdPlan p;
+  rlk_status st = bwd_plan(hidden, N, H, ld_hidden, weight, V, ld_weight, &p);
+  if (st != RLK_OK) return st;
+  if (target_stride < 0) return RLK_ERR_SHAPE;
+  if (grad_hidden && (ld_grad_hidden < H || ld_grad_hidden >= kLdLimit)) return RLK_ERR_SHAPE;
+  if (grad_weight && (ld_grad_weight < H || ld_grad_weight >= kLdLimit)) return RLK_ERR_SHAPE;
   if ((grad_hidden && grad_hidden_dtype != RLK_BF16 && grad_hidden_dtype != RLK_FP32) ||
       (grad_weight && grad_weight_dtype != RLK_BF16 && grad_weight_dtype != RLK_FP32))
     return RLK_ERR_DTYPE;
-  const size_t need = rlk_linear_logp_backward_workspace_size(N, V);
+  const size_t es_h = grad_hidden_dtype == RLK_FP32 ? 4 : 2;
+  const size_t es_w = grad_weight_dtype == RLK_FP32 ? 4 : 2;
+  if ((grad_hidden && !aligned_to(grad_hidden, es_h)) ||
+      (grad_weight && !aligned_to(grad_weight, es_w)) || !aligned_to(grad_bias, 4))
+    return RLK_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (N == 0) {
     // No rows: grad_hidden is empty; grad_weight and grad_bias are the empty sums.
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (!grad_weight && !grad_bias) return RLK_OK;
     DeviceInfo dev;
-    rlk_status st = device_ready(&dev);
+    st = device_ready(&dev);
     if (st != RLK_OK) return st;
-    if (grad_weight) {
-      const size_t es = grad_weight_dtype == RLK_FP32 ? 4 : 2;
-      if (cudaMemset2DAsync(grad_weight, ld_grad_weight * es, 0, H * es, V, s) != cudaSuccess)
-        return RLK_ERR_CUDA;
-    }
-    if (grad_bias && cudaMemsetAsync(grad_bias, 0, V * sizeof(float), s) != cudaSuccess)
+    if (grad_weight &&
+        cudaMemset2DAsync(grad_weight, ld_grad_weight * es_w, 0, H * es_w, V, s) != cudaSuccess) {
+      cudaGetLastError();
       return RLK_ERR_CUDA;
+    }
+    if (grad_bias && cudaMemsetAsync(grad_bias, 0, V * sizeof(float), s) != cudaSuccess) {
+      cudaGetLastError();
+      return RLK_ERR_CUDA;
+    }
     return RLK_OK;
   }
   if (!hidden || !weight || !target || !lse || !grad_logp) return RLK_ERR_NULL;
-  if (!tma_ready(hidden, ld_hidden) || !tma_ready(weight, ld_weight)) return RLK_ERR_ALIGN;
-  if ((reinterpret_cast<uintptr_t>(target) & 7u) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
-      (reinterpret_cast<uintptr_t>(grad_logp) & 3u) || (reinterpret_cast<uintptr_t>(bias) & 3u) ||
-      (reinterpret_cast<uintptr_t>(grad_bias) & 3u))
+  if (!aligned_to(hidden, 2) || !aligned_to(weight, 2) || !aligned_to(target, 8) ||
+      !aligned_to(lse, 4) || !aligned_to(grad_logp, 4) || !aligned_to(bias, 4))
     return RLK_ERR_ALIGN;
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+  if (!workspace || !aligned_to(workspace, 256) || workspace_bytes < p.total)
     return RLK_ERR_WORKSPACE;
   DeviceInfo dev;
-  rlk_status st = device_ready(&dev);
+  st = device_ready(&dev);
   if (st != RLK_OK) return st;
   if (ensure_attrs(dev.device) != cudaSuccess) return RLK_ERR_CUDA;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
 
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const void* h_src = hidden;
+  const void* w_src = weight;
   CUtensorMap tm_h, tm_w;
-  if (!encode_bf16_2d(&tm_h, hidden, H, N, ld_hidden, kBK, kHalfRows) ||
-      !encode_bf16_2d(&tm_w, weight, H, V, ld_weight, kBK, kHalfRows))
+  // The tensor maps only describe addresses; encoding them launches nothing.
+  if (p.stage_h) h_src = ws + p.off_h;
+  if (p.stage_w) w_src = ws + p.off_w;
+  if (!encode_bf16_2d(&tm_h, h_src, H, N, p.ldh, kBK, kHalfRows) ||
+      !encode_bf16_2d(&tm_w, w_src, H, V, p.ldw, kBK, kHalfRows))
     return RLK_ERR_CUDA;
+  if (p.stage_h &&
+      launch_stage_bf16(static_cast<const uint16_t*>(hidden), N, H, ld_hidden,
+                        reinterpret_cast<uint16_t*>(ws + p.off_h), p.ldh, s) != cudaSuccess)
+    return RLK_ERR_CUDA;
+  if (p.stage_w &&
+      launch_stage_bf16(static_cast<const uint16_t*>(weight), V, H, ld_weight,
+                        reinterpret_cast<uint16_t*>(ws + p.off_w), p.ldw, s) != cudaSuccess)
+    return RLK_ERR_CUDA;
+
   GradSched sc;
   sc.order.rows = (int)ceil_div(N, kPairRows);
   sc.order.cols = (int)ceil_div(V, kBN);
   sc.order.band = band_rows(sc.order.rows, H, kPairRows);
   sc.nkb = (int)ceil_div(H, kBK);
-  if ((int64_t)sc.order.rows * sc.order.cols >= (int64_t(1) << 31)) return RLK_ERR_SHAPE;
   GradArgs a;
   a.N = (int)N;
   a.V = (int)V;
   a.tstride = target_stride;
   a.bias = bias;
-  a.bias_vec4 = (reinterpret_cast<uintptr_t>(bias) & 15u) == 0;
+  a.bias_vec4 = aligned_to(bias, 16);
   a.target = target;
   a.lse = lse;
   a.grad = grad_logp;
-  a.G = static_cast<uint16_t*>(workspace);
-  a.ldG = grad_ld(V);
+  a.G = reinterpret_cast<uint16_t*>(ws);
+  a.ldG = p.ldG;
   const int64_t units = (int64_t)sc.order.rows * sc.order.cols;
   const int64_t clusters = dev.sm_count / 2;
   const int grid = 2 * (int)(units < clusters ? units : clusters);
   sc.counter = nullptr;
   if (ordered_units(units, clusters)) {
-    sc.counter = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) +
-                                        align_up((size_t)N * a.ldG * 2, 256));
+    sc.counter = reinterpret_cast<int*>(ws + p.off_ctr);
     if (cudaMemsetAsync(sc.counter, 0, sizeof(int), s) != cudaSuccess) {
       cudaGetLastError();
       return RLK_ERR_CUDA;
@@ -310,13 +379,15 @@ rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H, in
     return RLK_ERR_CUDA;
   }
 
+  // The products read G and the (possibly staged) operands, all TMA-ready, so
+  // they need no workspace and every argument they check was checked above.
   if (grad_hidden) {   // [N, H] = G [N, V] . W [V, H]
-    st = rlk_det_gemm_fwd(a.G, N, V, a.ldG, weight, H, ld_weight, grad_hidden, grad_hidden_dtype,
+    st = rlk_det_gemm_fwd(a.G, N, V, a.ldG, w_src, H, p.ldw, grad_hidden, grad_hidden_dtype,
                           ld_grad_hidden, nullptr, 0, stream);
     if (st != RLK_OK) return st;
   }
   if (grad_weight) {   // [V, H] = G^T . hidden
-    st = rlk_det_gemm_db(a.G, N, V, a.ldG, hidden, RLK_BF16, H, ld_hidden, grad_weight,
+    st = rlk_det_gemm_db(a.G, N, V, a.ldG, h_src, RLK_BF16, H, p.ldh, grad_weight,
                          grad_weight_dtype, ld_grad_weight, nullptr, 0, stream);
     if (st != RLK_OK) return st;
   }

@@ -261,8 +261,9 @@ RLK_API rlk_status rlk_linear_logp_combine(int64_t N, int64_t V, const int64_t* 
  *    more than RLK_NOALLOC_SCRATCH_BYTES returns RLK_ERR_WORKSPACE and launches
  *    nothing.  (V = 151936: up to about 7,000 rows per call.)
  *  - The first call on each device looks up the array's device address (with that
- *    device current) and caches it; make that first call before any stream
- *    capture.
+ *    device current) and caches it for as long as the same CUDA context stays
+ *    current (a new context, e.g. after cudaDeviceReset, repeats the lookup); make
+ *    that first call, in each context, before any stream capture.
  *  - Every call on a device shares the array and leaves its contents behind; no
  *    part of it needs to start at zero.  Calls whose GPU work overlaps (two streams
  *    without ordering between them) race on it: order them.
@@ -288,26 +289,36 @@ RLK_API rlk_status rlk_linear_logp_noalloc(const void* hidden, int64_t N, int64_
  * FP32 accumulation (the products are rlk_det_gemm_fwd and rlk_det_gemm_db).
  * A row whose target is outside [0, V) contributes zero gradient.
  *
- *  hidden, weight, bias, target, target_stride  as for rlk_linear_logp; hidden
- *                and weight must be 16-byte aligned with a pitch that is a
- *                multiple of 8 elements (else RLK_ERR_ALIGN)
+ *  hidden, weight, bias, target, target_stride  as for rlk_linear_logp (a
+ *                misaligned hidden or weight is copied into the workspace first,
+ *                as in the forward; bit-identical results)
  *  lse           FP32 [N], the forward's lse for these inputs
  *  grad_logp     FP32 [N]
  *  grad_hidden   [N, H] in grad_hidden_dtype (RLK_BF16 / RLK_FP32), pitch
  *                ld_grad_hidden; NULL to skip
  *  grad_weight   [V, H] in grad_weight_dtype, pitch ld_grad_weight; NULL to skip
  *  grad_bias     FP32 [V] or NULL to skip
- *  workspace     >= rlk_linear_logp_backward_workspace_size(N, V) bytes, 256-byte
- *                aligned.  After the call its first N * 8*ceil(V/8) * 2 bytes hold
- *                G as BF16 [N, 8*ceil(V/8)] (row pitch 8*ceil(V/8)); the next 256
- *                bytes hold the kernel's work-unit counter (zeroed by a call that
- *                deals more than 8 rounds of units).
+ *  workspace     >= rlk_linear_logp_backward_workspace_size_for(...) bytes
+ *                (rlk_linear_logp_backward_workspace_size(N, V) suffices when hidden
+ *                and weight are 16-byte aligned with a pitch that is a multiple of 8
+ *                elements), 256-byte aligned.  After the call its first
+ *                N * 8*ceil(V/8) * 2 bytes hold G as BF16 [N, 8*ceil(V/8)] (row pitch
+ *                8*ceil(V/8)); the next 256 bytes hold the kernel's work-unit counter
+ *                (zeroed by a call that deals more than 8 rounds of units), then the
+ *                padded copies of a misaligned hidden / weight.
+ * Errors: every argument, including the output pointers, pitches and dtypes that
+ * the two products check, is validated before the first launch; on an error
+ * nothing is launched and no output or workspace byte is touched.
  * Determinism: every output is bitwise reproducible; a grad_hidden row depends
  * only on its own row's inputs (batch invariant), while grad_weight and
  * grad_bias sum over the rows of the call.  N == 0 writes zeros to grad_weight
  * and grad_bias.
  */
 RLK_API size_t rlk_linear_logp_backward_workspace_size(int64_t N, int64_t V);
+RLK_API size_t rlk_linear_logp_backward_workspace_size_for(const void* hidden, int64_t N,
+                                                           int64_t H, int64_t ld_hidden,
+                                                           const void* weight, int64_t V,
+                                                           int64_t ld_weight);
 RLK_API rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H,
                                             int64_t ld_hidden, const void* weight, int64_t V,
                                             int64_t ld_weight, const float* bias,

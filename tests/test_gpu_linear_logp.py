@@ -106,9 +106,12 @@ def test_integer_logits_bit_exact(dev, orc):
     lp, ls, zt = run(dev, hidden, weight, target)
     rlp, rls, rzt = oracle_rows(orc, hidden, weight, target, None)
     assert np.array_equal(zt.astype(np.float64), rzt)
-    # lse is large here (logits up to a few hundred); compare in relative terms too
-    assert np.abs(ls - rls).max() <= LOGP_ATOL * max(1.0, np.abs(rls).max() / 100)
-    assert np.abs(lp - rlp).max() <= LOGP_ATOL * max(1.0, np.abs(rls).max() / 100)
+    # lse reaches a few hundred here, but the bound stays the absolute 1e-3: the
+    # maximum is an exact integer and log s < log V, so FP32 loses about one ulp
+    # of lse (~3e-5 at 400)
+    assert np.abs(rls).max() > 100.0
+    assert np.abs(ls - rls).max() <= LOGP_ATOL
+    assert np.abs(lp - rlp).max() <= LOGP_ATOL
 
 
 def test_invariants_on_gpu(dev):

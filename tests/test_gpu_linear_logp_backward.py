@@ -170,3 +170,102 @@ def test_backward_mid_parity_sampled(dev, orc):
     hd = dec_bf16(si.bf16_bits(hidden))
     assert rel_fro(dw[vs].cpu().double().numpy(), Gcols.T @ hd) <= 1e-5
     assert rlk.device_error() == 0
+
+
+def test_backward_full_vocabulary_grad_weight_vs_oracle(dev, orc):
+    """grad_weight at the full mid vocabulary (V = 151,936, H = 4096) tied back to
+    the FP64 oracle end to end: N = 256 rows, the oracle's G by definition on
+    every row, and sampled vocabulary rows of grad_weight = G^T . hidden (the
+    tile edges 0 / 255 / 256, the last id, and ids that some row targets) against
+    the exact product, within the end-to-end 1e-2 relative Frobenius bound (the
+    BF16 rounding of G dominates); the same rows within 1e-5 of the float64
+    product of the GPU's own G."""
+    w = si.MID
+    N = 256
+    hidden, weight, b, target = si.workload_inputs(w, seed=9, device=dev)
+    hidden, target = hidden[:N].contiguous(), target[:N].contiguous()
+    g = torch.randn(N, generator=torch.Generator(device=dev).manual_seed(10), device=dev)
+    dh, dw, _, G = _backward(hidden, weight, target, g, b, torch.float32)
+    torch.cuda.synchronize()
+    hb, wb = si.bf16_bits(hidden), si.bf16_bits(weight)
+    tgt = target.cpu().numpy()
+    ref_G = orc.grad_logits(hb, wb, tgt, g.cpu().double().numpy())          # [N, V]
+    vs = np.array(sorted({0, 1, 255, 256, 75968, w.V - 1, int(tgt[0]), int(tgt[1]),
+                          int(tgt[N - 1])}), dtype=np.int64)
+    hd = dec_bf16(hb)
+    got = dw[vs].cpu().double().numpy()
+    assert rel_fro(got, ref_G[:, vs].T @ hd) <= 1e-2
+    for i, v in enumerate(vs):                        # row by row as well
+        assert rel_fro(got[i], ref_G[:, v] @ hd) <= 1e-2, f"vocabulary row {v}"
+    Gcols = dec_bf16(si.bf16_bits(G[:, vs].contiguous()))
+    assert rel_fro(got, Gcols.T @ hd) <= 1e-5
+    # G itself on every row: one BF16 ulp of the exact value (+ the FP32 error of exp)
+    Gg = dec_bf16(si.bf16_bits(G))
+    slack = 1e-5 * np.abs(g.cpu().double().numpy())[:, None]
+    assert np.all(np.abs(Gg - ref_G) <= bf16_ulp(ref_G) + slack)
+    assert rlk.device_error() == 0
+
+
+def test_backward_layouts_staged_operands(dev):
+    """A wider-pitch view, an odd-pitch (staged) hidden and an odd-pitch (staged)
+    weight give the same G and gradients bit for bit as contiguous operands."""
+    N, H, V = 300, 1000, 5003
+    hidden, weight, b, target, g = _case(N, H, V, True, seed=43, dev=dev)
+    _, lse = rlk.linear_logp(hidden, weight, target, b)
+
+    def bwd(h, w):
+        return rlk.linear_logp_backward(h, w, target, lse, g, b, out_dtype=torch.float32,
+                                        return_grad_logits=True)
+
+    ref = bwd(hidden, weight)
+    for name, pad_h, pad_w in (("wide pitch", 64, 0), ("odd hidden pitch", 1, 0),
+                               ("odd weight pitch", 0, 3), ("both odd", 5, 7)):
+        h = torch.zeros(N, H + pad_h, dtype=torch.bfloat16, device=dev)
+        h[:, :H] = hidden
+        w = torch.zeros(V, H + pad_w, dtype=torch.bfloat16, device=dev)
+        w[:, :H] = weight
+        got = bwd(h[:, :H], w[:, :H])
+        for x, y, what in zip(ref, got, ("grad_hidden", "grad_weight", "grad_bias", "G")):
+            assert torch.equal(x, y), f"{name}: {what} bits differ"
+    # a hidden whose base is 2 bytes past a 16-byte boundary is staged as well
+    store = torch.zeros(N * H + 8, dtype=torch.bfloat16, device=dev)
+    shifted = store[1:1 + N * H].view(N, H)
+    shifted.copy_(hidden)
+    assert shifted.data_ptr() % 16 == 2
+    got = bwd(shifted, weight)
+    for x, y in zip(ref, got):
+        assert torch.equal(x, y)
+    assert rlk.device_error() == 0
+
+
+def test_backward_fails_closed_on_a_misaligned_output(dev):
+    """An FP32 grad_weight that is not 4-byte aligned is refused before anything
+    launches: grad_hidden and the workspace keep every byte."""
+    import ctypes
+    N, H, V = 64, 256, 1000
+    hidden, weight, b, target, g = _case(N, H, V, False, seed=44, dev=dev)
+    _, lse = rlk.linear_logp(hidden, weight, target, b)
+    lib = rlk.lib()
+    n = lib.rlk_linear_logp_backward_workspace_size_for(rlk._ptr(hidden), N, H, H, rlk._ptr(weight),
+                                                        V, H)
+    ws = torch.full((n,), 0x5A, dtype=torch.uint8, device=dev)
+    gh = torch.full((N, H), -7.0, device=dev)
+    gw_store = torch.zeros(V * H + 4, dtype=torch.float32, device=dev)
+    bad_gw = ctypes.c_void_p(gw_store.data_ptr() + 2)
+    torch.cuda.synchronize()
+    st = lib.rlk_linear_logp_backward(
+        rlk._ptr(hidden), N, H, H, rlk._ptr(weight), V, H, None, rlk._ptr(target), 1,
+        rlk._ptr(lse), rlk._ptr(g), rlk._ptr(gh), rlk.RLK_FP32, H, bad_gw, rlk.RLK_FP32, H, None,
+        rlk._ptr(ws), n, rlk._stream_ptr(None))
+    assert st == 4                                                     # RLK_ERR_ALIGN
+    torch.cuda.synchronize()
+    assert bool((gh == -7.0).all()) and bool((ws == 0x5A).all()) and bool((gw_store == 0).all())
+    # a grad_hidden pitch below H is refused the same way
+    st = lib.rlk_linear_logp_backward(
+        rlk._ptr(hidden), N, H, H, rlk._ptr(weight), V, H, None, rlk._ptr(target), 1,
+        rlk._ptr(lse), rlk._ptr(g), rlk._ptr(gh), rlk.RLK_FP32, H - 1, None, rlk.RLK_FP32, H, None,
+        rlk._ptr(ws), n, rlk._stream_ptr(None))
+    assert st == 2                                                     # RLK_ERR_SHAPE
+    torch.cuda.synchronize()
+    assert bool((gh == -7.0).all()) and bool((ws == 0x5A).all())
+    assert rlk.device_error() == 0
