@@ -62,6 +62,14 @@ SIGNATURES = {
     "rlk_linear_logp_noalloc": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _P, _I64,
                                      _P, _P, _P, _P]),
     "rlk_throughput_split_count": (_I, [_I64, _I64, ctypes.c_int32, ctypes.POINTER(_I64)]),
+    "rlk_vocab_shard_range": (_I, [_I64, _I64, _I64, ctypes.POINTER(_I64), ctypes.POINTER(_I64),
+                                   ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
+    "rlk_linear_logp_shard_workspace_size": (_SZ, [_P, _I64, _I64, _I64, _P, _I64, _I64, _I64,
+                                                   _I64]),
+    "rlk_linear_logp_shard_partials": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _I64, _I64, _P,
+                                            _P, _I64, _P, _I64, _P, _P, _SZ, _P]),
+    "rlk_linear_logp_combine_shards": (_I, [_I64, _I64, _P, _I64, _I64, _P, _P, _I64, _I64, _P,
+                                            _I64, _P, _P, _P, _P]),
     "rlk_linear_logp_splits_workspace_size": (_SZ, [_P, _I64, _I64, _I64, _P, _I64, _I64, _I64]),
     "rlk_linear_logp_splits": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _P, _I64,
                                     _P, _P, _P, _I64, _P, _SZ, _P]),
@@ -297,6 +305,138 @@ class LinearLogpCall:
                 _ptr(self.zt), self.num_splits, _ptr(self.ws), self.ws.numel(),
                 _stream_ptr(stream)), "rlk_linear_logp_splits")
         return self.logp, self.lse
+
+
+# ------------------------------------------------------------ vocabulary shards
+def vocab_shard_range(V: int, num_shards: int, shard: int):
+    """(split_begin, split_end, v_begin, v_end) of shard `shard` in the balanced
+    partition of the V-only splits into num_shards contiguous runs."""
+    out = [_I64() for _ in range(4)]
+    _check(lib().rlk_vocab_shard_range(V, num_shards, shard, *[ctypes.byref(x) for x in out]),
+           "rlk_vocab_shard_range")
+    return tuple(x.value for x in out)
+
+
+def linear_logp_shard_partials(hidden: torch.Tensor, weight_shard: torch.Tensor,
+                               target: torch.Tensor, V: int, split_begin: int, split_end: int,
+                               bias_shard: torch.Tensor | None = None, *, ld_partials: int = 0,
+                               stream=None):
+    """Partials of one vocabulary shard: (partials [N, ld, 2] fp32 with the shard's
+    (m, s) pairs in its first split_end - split_begin columns, target logits [N]
+    fp32, NaN for rows whose target the shard does not hold).
+
+    weight_shard [v_end - v_begin, H] bf16 holds the weight rows of the shard's
+    vocabulary ids, bias_shard the matching bias entries; V is the whole
+    vocabulary; target holds global ids.
+    """
+    _require_cuda(hidden, weight_shard, target, bias_shard)
+    h2, ldh = _matrix(hidden.reshape(-1, hidden.size(-1)), "hidden")
+    w2, ldw = _matrix(weight_shard, "weight_shard")
+    N, H = h2.shape
+    t1 = target.reshape(-1)
+    tstride = t1.stride(0) if N > 1 else 1
+    n = split_end - split_begin
+    ld = max(ld_partials, n, 1)
+    if bias_shard is not None:
+        bias_shard = bias_shard.contiguous()
+    dev = hidden.device
+    partials = torch.empty(N, ld, 2, dtype=torch.float32, device=dev)
+    zt = torch.full((N,), float("nan"), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        nb = lib().rlk_linear_logp_shard_workspace_size(_ptr(h2), N, H, ldh, _ptr(w2), V,
+                                                        split_begin, split_end, ldw)
+        if nb == 0:
+            raise RlkError(2, "rlk_linear_logp_shard_workspace_size")
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        _check(lib().rlk_linear_logp_shard_partials(
+            _ptr(h2), N, H, ldh, _ptr(w2), V, split_begin, split_end, ldw, _ptr(bias_shard),
+            _ptr(t1), tstride, _ptr(partials), ld, _ptr(zt), _ptr(ws), nb, _stream_ptr(stream)),
+            "rlk_linear_logp_shard_partials")
+    return partials, zt
+
+
+def linear_logp_combine_shards(partials: torch.Tensor, target_logits: torch.Tensor,
+                               split_offsets, target: torch.Tensor, V: int, *,
+                               return_target_logit: bool = False, stream=None):
+    """The fixed-order merge over gathered shard outputs.
+
+    partials [R, N, ld, 2] fp32 (shard q's pairs in its first
+    split_offsets[q+1] - split_offsets[q] columns), target_logits [R, N] fp32,
+    split_offsets R + 1 split indices (0 .. S).  Returns logp, lse [, target logit],
+    bitwise equal to linear_logp on the whole vocabulary.
+    """
+    _require_cuda(partials, target_logits, target)
+    if partials.dim() != 4 or partials.size(-1) != 2 or partials.dtype != torch.float32:
+        raise ValueError("partials must be a float32 [R, N, ld, 2] tensor")
+    partials = partials.contiguous()
+    target_logits = target_logits.contiguous()
+    R, N, ld, _ = partials.shape
+    offs = (ctypes.c_int64 * (R + 1))(*[int(x) for x in split_offsets])
+    if len(split_offsets) != R + 1:
+        raise ValueError("split_offsets needs one entry per shard plus one")
+    t1 = target.reshape(-1)
+    tstride = t1.stride(0) if N > 1 else 1
+    dev = partials.device
+    logp = torch.empty(N, dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    zt = torch.empty(N, dtype=torch.float32, device=dev) if return_target_logit else None
+    with torch.cuda.device(dev):
+        _check(lib().rlk_linear_logp_combine_shards(
+            N, V, _ptr(t1), tstride, R, offs, _ptr(partials), ld, N * ld, _ptr(target_logits), N,
+            _ptr(logp), _ptr(lse), _ptr(zt), _stream_ptr(stream)), "rlk_linear_logp_combine_shards")
+    return (logp, lse, zt) if return_target_logit else (logp, lse)
+
+
+def exchange_shard_partials(partials: torch.Tensor, target_logit: torch.Tensor, group=None):
+    """All-gather every rank's shard output: ([R, N, ld, 2], [R, N]) in rank order.
+
+    Every rank passes partials padded to the same [N, ld, 2] (the widest shard).
+    With the NCCL backend the device tensors are exchanged directly; with gloo the
+    tensors travel through host copies and come back on the caller's device.
+    """
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    dev = partials.device
+    via_host = dist.get_backend(group) != "nccl"
+    p = partials.contiguous()
+    z = target_logit.contiguous()
+    if via_host:
+        p, z = p.cpu(), z.cpu()
+    ps = [torch.empty_like(p) for _ in range(world)]
+    zs = [torch.empty_like(z) for _ in range(world)]
+    dist.all_gather(ps, p, group=group)
+    dist.all_gather(zs, z, group=group)
+    return torch.stack(ps).to(dev), torch.stack(zs).to(dev)
+
+
+def vocab_parallel_linear_logp(hidden: torch.Tensor, weight_shard: torch.Tensor,
+                               target: torch.Tensor, V: int,
+                               bias_shard: torch.Tensor | None = None, *, group=None,
+                               return_target_logit: bool = False):
+    """linear_logp with the vocabulary divided between the ranks of `group`.
+
+    Rank q holds the weight rows (and bias entries) of its balanced shard,
+    vocab_shard_range(V, world, q); every rank passes the same hidden and target.
+    Each rank computes its shard's partials, the ranks exchange them
+    (exchange_shard_partials), and every rank merges all of them in the fixed
+    order: the results equal single-device linear_logp bit for bit.
+    """
+    import torch.distributed as dist
+    world, rank = dist.get_world_size(group), dist.get_rank(group)
+    ranges = [vocab_shard_range(V, world, q) for q in range(world)]
+    j0, j1, v0, v1 = ranges[rank]
+    if weight_shard.size(0) != v1 - v0:
+        raise ValueError(f"rank {rank} holds vocabulary ids [{v0}, {v1}): weight_shard needs "
+                         f"{v1 - v0} rows, got {weight_shard.size(0)}")
+    widest = max(r[1] - r[0] for r in ranges)
+    partials, zt = linear_logp_shard_partials(hidden, weight_shard, target, V, j0, j1, bias_shard,
+                                              ld_partials=widest)
+    gp, gz = exchange_shard_partials(partials, zt, group)
+    offsets = [r[0] for r in ranges] + [ranges[-1][1]]
+    out = linear_logp_combine_shards(gp, gz, offsets, target, V,
+                                     return_target_logit=return_target_logit)
+    lead = hidden.shape[:-1]
+    return tuple(o.reshape(lead) for o in out)
 
 
 def linear_logp_backward(hidden: torch.Tensor, weight: torch.Tensor, target: torch.Tensor,

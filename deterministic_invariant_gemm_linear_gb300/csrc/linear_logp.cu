@@ -40,11 +40,12 @@ __device__ unsigned int g_err_linear_logp = 0;
 namespace {
 
 struct LogpSched {
-  Banded order;    // rows = 256-row blocks, cols = vocabulary splits
+  Banded order;    // rows = 256-row blocks, cols = this call's vocabulary splits
   int* counter;    // zeroed unit counter in the workspace (units in order), or null (round-robin)
-  int S;           // vocabulary splits
+  int S;           // vocabulary splits in this call (all S, or a shard's run of them)
   int vps;         // 256-id tiles per split
-  int vtiles;      // 256-id tiles in the vocabulary
+  int vtiles;      // 256-id tiles of the weight rows this call reads
+  int tile0;       // global index of the first of those tiles (0 unless a vocabulary shard)
   int nkb;         // 64-wide blocks of H
   __device__ __forceinline__ int num_units() const { return order.count(); }
   __device__ __forceinline__ int split_of(int u) const {
@@ -70,13 +71,15 @@ struct LogpSched {
 };
 
 struct LogpArgs {
-  int N, V;
+  int N, V;                   // V: the whole vocabulary (ids past it are masked)
+  int v_off;                  // first vocabulary id of the weight rows read (shard start, or 0)
   int64_t tstride;
-  const float* bias;          // [V] or null
+  const float* bias;          // [weight rows read] (bias[v - v_off]) or null
   bool bias_vec4;             // bias is 16-byte aligned: whole chunks read it 4 floats at a time
   const int64_t* target;
-  float2* ws_ms;              // [N][S]: (m, s) per row and split
-  float* ws_zt;               // [N]: target logit
+  float2* ws_ms;              // [N][ld_ms]: (m, s) per row and split of this call
+  int64_t ld_ms;
+  float* ws_zt;               // [N]: target logit (rows whose target lies in this call's ids)
 };
 
 // One 32-column chunk of a row: bias, vocabulary-tail mask, target capture and
@@ -84,6 +87,7 @@ struct LogpArgs {
 // is 2^((z - m) * log2(e)) with z - m formed first, so the running maximum's own
 // term is exactly 2^0 = 1: s >= 1 always, hence lse >= max logit and logp <= 0
 // hold exactly in FP32.
+// `bias` points at the chunk's first id (or is null).
 __device__ __forceinline__ void logp_chunk(const uint32_t (&r)[32], int vbase, int V,
                                            const float* bias, bool bias_vec4, int64_t tgt,
                                            float& m, float& s, bool& have_zt, float& zt) {
@@ -93,7 +97,7 @@ __device__ __forceinline__ void logp_chunk(const uint32_t (&r)[32], int vbase, i
   if (bias != nullptr) {
     if (vbase + 32 <= V && bias_vec4) {
       // every lane reads the same 128 bytes: 8 vector loads instead of 32 scalar ones
-      const float4* b4 = reinterpret_cast<const float4*>(bias + vbase);
+      const float4* b4 = reinterpret_cast<const float4*>(bias);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float4 b = __ldg(b4 + i);
@@ -104,11 +108,11 @@ __device__ __forceinline__ void logp_chunk(const uint32_t (&r)[32], int vbase, i
       }
     } else if (vbase + 32 <= V) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) z[i] = __fadd_rn(z[i], __ldg(bias + vbase + i));
+      for (int i = 0; i < 32; ++i) z[i] = __fadd_rn(z[i], __ldg(bias + i));
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i)
-        if (vbase + i < V) z[i] = __fadd_rn(z[i], __ldg(bias + vbase + i));
+        if (vbase + i < V) z[i] = __fadd_rn(z[i], __ldg(bias + i));
     }
   }
   if (vbase + 32 > V) {
@@ -181,7 +185,7 @@ __device__ __forceinline__ void logp_epilogue(const LogpSched& sc, const LogpArg
         run = false;
         break;
       }
-      const int v0 = (t0 + i) * kBN;
+      const int v0 = (sc.tile0 + t0 + i) * kBN;   // global vocabulary id of the tile
       const uint32_t taddr = tmem + acc * kAccCols + lane_off;
 #pragma unroll 1
       for (int c = 0; c < kBN / 32; ++c) {
@@ -191,7 +195,8 @@ __device__ __forceinline__ void logp_epilogue(const LogpSched& sc, const LogpArg
         __syncwarp();
         tmem_ld32(taddr + c * 32, r);
         tmem_wait_ld();
-        logp_chunk(r, vbase, args.V, args.bias, args.bias_vec4, tgt, m, s, have_zt, zt);
+        const float* bias = args.bias ? args.bias + (vbase - args.v_off) : nullptr;
+        logp_chunk(r, vbase, args.V, bias, args.bias_vec4, tgt, m, s, have_zt, zt);
       }
       if (kSolo)
         solo_release(ps, acc);
@@ -202,7 +207,7 @@ __device__ __forceinline__ void logp_epilogue(const LogpSched& sc, const LogpArg
     }
     if (!run) break;
     if (valid) {
-      args.ws_ms[(int64_t)row * sc.S + j] = make_float2(m, s);
+      args.ws_ms[(int64_t)row * args.ld_ms + j] = make_float2(m, s);
       if (have_zt) args.ws_zt[row] = zt;
     }
   }
@@ -287,20 +292,57 @@ __device__ __forceinline__ void merge_ms(float& M, float& s, float m2, float s2)
   M = Mn;
 }
 
+// Where the merge reads a row's S partials and its target logit.
+// One [N][S] block of (m, s) partials and one [N] array of target logits (one GPU).
+struct ContiguousPartials {
+  const float2* ms;
+  const float* zt;
+  int S;
+  __device__ __forceinline__ float2 at(int row, int j) const { return ms[(int64_t)row * S + j]; }
+  __device__ __forceinline__ float target_logit(int row, int64_t) const { return zt[row]; }
+};
+
+// Partials gathered from vocabulary shards: shard q holds splits [off[q], off[q+1])
+// as an [N][ld] block at ms + q * shard_stride, and target logits at
+// zt + q * zt_stride for the rows whose target lies in its ids.
+constexpr int kMaxShards = 64;
+struct ShardedPartials {
+  const float2* ms;
+  int64_t ld, shard_stride;
+  const float* zt;
+  int64_t zt_stride;
+  int vps;
+  int off[kMaxShards + 1];
+  __device__ __forceinline__ int shard_of(int j) const {   // j < off[last] = S
+    int q = 0;
+    while (j >= off[q + 1]) ++q;
+    return q;
+  }
+  __device__ __forceinline__ float2 at(int row, int j) const {
+    const int q = shard_of(j);
+    return ms[q * shard_stride + (int64_t)row * ld + (j - off[q])];
+  }
+  __device__ __forceinline__ float target_logit(int row, int64_t t) const {
+    const int q = shard_of((int)(t / kBN) / vps);
+    return zt[q * zt_stride + row];
+  }
+};
+
+// One warp per row: the same fixed order whatever the source of the partials,
+// so a row's bits depend only on its partial values.
+template <class Src>
 __global__ void __launch_bounds__(256)
-    linear_logp_combine_kernel(const float2* __restrict__ ws_ms, const float* __restrict__ ws_zt,
-                               const int64_t* __restrict__ target, int64_t tstride, int N, int S,
-                               int V, float* __restrict__ logp, float* __restrict__ lse,
+    linear_logp_combine_kernel(Src src, const int64_t* __restrict__ target, int64_t tstride, int N,
+                               int S, int V, float* __restrict__ logp, float* __restrict__ lse,
                                float* __restrict__ zt_out) {
   griddep_wait();   // the partials kernel has finished and its writes are visible
   if (threadIdx.x == 0) griddep_launch_dependents();
   const int row = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   if (row >= N) return;
-  const float2* p = ws_ms + (int64_t)row * S;
   float M = -INFINITY, s = 0.f;
   for (int j = lane; j < S; j += 32) {
-    const float2 v = p[j];
+    const float2 v = src.at(row, j);
     merge_ms(M, s, v.x, v.y);
   }
 #pragma unroll
@@ -312,7 +354,7 @@ __global__ void __launch_bounds__(256)
   if (lane == 0) {
     const float L = __fadd_rn(M, logf(s));
     const int64_t t = __ldg(target + (int64_t)row * tstride);
-    const float z = (t >= 0 && t < V) ? ws_zt[row] : __int_as_float(0x7fc00000);
+    const float z = (t >= 0 && t < V) ? src.target_logit(row, t) : __int_as_float(0x7fc00000);
     lse[row] = L;
     logp[row] = __fsub_rn(z, L);
     if (zt_out) zt_out[row] = z;
@@ -417,73 +459,81 @@ using namespace rlk;
 namespace rlk {
 namespace {
 
-rlk_status partials_impl(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
-                         const void* weight, int64_t V, int64_t ld_weight, const float* bias,
-                         const int64_t* target, int64_t target_stride, int64_t splits_req,
-                         void* workspace, size_t workspace_bytes, void* stream) {
-  LogpPlan p;
-  rlk_status st = plan(hidden, N, H, ld_hidden, weight, V, ld_weight, splits_req, &p);
-  if (st != RLK_OK) return st;
-  if (target_stride < 0) return RLK_ERR_SHAPE;
-  if (N == 0) return RLK_OK;
-  if (!hidden || !weight || !target) return RLK_ERR_NULL;
-  if (!workspace) return RLK_ERR_WORKSPACE;
-  if ((reinterpret_cast<uintptr_t>(hidden) & 1u) || (reinterpret_cast<uintptr_t>(weight) & 1u) ||
-      (reinterpret_cast<uintptr_t>(target) & 7u) || (reinterpret_cast<uintptr_t>(bias) & 3u))
-    return RLK_ERR_ALIGN;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 15u) || workspace_bytes < p.total)
-    return RLK_ERR_WORKSPACE;
-  DeviceInfo dev;
-  st = device_ready(&dev);
-  if (st != RLK_OK) return st;
-  if (ensure_attrs(dev.device) != cudaSuccess) return RLK_ERR_CUDA;
+// One launch of the partials kernel over the weight rows of splits [j0, j1) of
+// the vocabulary policy: the whole vocabulary (j0 = 0, j1 = S) or a shard of it.
+// The caller has validated every argument; this stages misaligned operands,
+// encodes the tensor maps and launches.
+struct PartialsLaunch {
+  const void* hidden;
+  int64_t N, H, ld_hidden;
+  bool stage_h;
+  int64_t ldh;                 // pitch the kernel reads
+  uint16_t* h_stage;           // padded copy of hidden (when stage_h)
+  const void* weight;          // rows: vocabulary ids [v_off, v_off + w_rows)
+  int64_t w_rows, ld_weight;
+  bool stage_w;
+  int64_t ldw;
+  uint16_t* w_stage;
+  int64_t V, vps, j0, j1, v_off;
+  const float* bias;           // [w_rows] or null
+  const int64_t* target;
+  int64_t tstride;
+  float2* ms;                  // [N][ld_ms]
+  int64_t ld_ms;
+  float* zt;                   // [N]
+  int* counter;                // 256-byte slot for the unit counter
+};
 
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const void* h_src = hidden;
-  const void* w_src = weight;
-  if (p.stage_h) {
-    if (launch_stage_bf16(static_cast<const uint16_t*>(hidden), N, H, ld_hidden,
-                          reinterpret_cast<uint16_t*>(ws + p.off_h), p.ldh, s) != cudaSuccess)
+rlk_status launch_partials(const PartialsLaunch& L, const DeviceInfo& dev, cudaStream_t s) {
+  if (ensure_attrs(dev.device) != cudaSuccess) return RLK_ERR_CUDA;
+  const void* h_src = L.hidden;
+  const void* w_src = L.weight;
+  if (L.stage_h) {
+    if (launch_stage_bf16(static_cast<const uint16_t*>(L.hidden), L.N, L.H, L.ld_hidden, L.h_stage,
+                          L.ldh, s) != cudaSuccess)
       return RLK_ERR_CUDA;
-    h_src = ws + p.off_h;
+    h_src = L.h_stage;
   }
-  if (p.stage_w) {
-    if (launch_stage_bf16(static_cast<const uint16_t*>(weight), V, H, ld_weight,
-                          reinterpret_cast<uint16_t*>(ws + p.off_w), p.ldw, s) != cudaSuccess)
+  if (L.stage_w) {
+    if (launch_stage_bf16(static_cast<const uint16_t*>(L.weight), L.w_rows, L.H, L.ld_weight,
+                          L.w_stage, L.ldw, s) != cudaSuccess)
       return RLK_ERR_CUDA;
-    w_src = ws + p.off_w;
+    w_src = L.w_stage;
   }
   // At most 128 rows (one 128-row block): the one-CTA loop, one unit per CTA;
   // otherwise the 2-SM loop over 256-row blocks.  At most 32 rows: the thin
   // rings (only 32 hidden rows staged per stage).
-  const bool solo = N <= kHalfRows;
-  const bool thin = N <= 32;
+  const bool solo = L.N <= kHalfRows;
+  const bool thin = L.N <= 32;
   const int kRowsPerUnit = solo ? kHalfRows : kPairRows;
   CUtensorMap tm_h, tm_w;
-  if (!encode_bf16_2d(&tm_h, h_src, H, N, p.ldh, kBK, thin ? 32 : kHalfRows) ||
-      !encode_bf16_2d(&tm_w, w_src, H, V, p.ldw, kBK, solo ? kBN : kHalfRows))
+  if (!encode_bf16_2d(&tm_h, h_src, L.H, L.N, L.ldh, kBK, thin ? 32 : kHalfRows) ||
+      !encode_bf16_2d(&tm_w, w_src, L.H, L.w_rows, L.ldw, kBK, solo ? kBN : kHalfRows))
     return RLK_ERR_CUDA;
 
   LogpSched sc;
-  sc.order.rows = (int)ceil_div(N, kRowsPerUnit);
-  sc.order.cols = (int)p.S;
-  sc.order.band = band_rows(sc.order.rows, H, kRowsPerUnit);
+  const int64_t splits = L.j1 - L.j0;
+  sc.order.rows = (int)ceil_div(L.N, kRowsPerUnit);
+  sc.order.cols = (int)splits;
+  sc.order.band = band_rows(sc.order.rows, L.H, kRowsPerUnit);
   sc.rows_per_unit = kRowsPerUnit;
-  sc.S = (int)p.S;
-  sc.vps = (int)p.vps;
-  sc.vtiles = (int)p.vtiles;
-  sc.nkb = (int)ceil_div(H, kBK);
+  sc.S = (int)splits;
+  sc.vps = (int)L.vps;
+  sc.vtiles = (int)ceil_div(L.w_rows, kBN);
+  sc.tile0 = (int)(L.j0 * L.vps);
+  sc.nkb = (int)ceil_div(L.H, kBK);
   LogpArgs a;
-  a.N = (int)N;
-  a.V = (int)V;
-  a.tstride = target_stride;
-  a.bias = bias;
-  a.bias_vec4 = (reinterpret_cast<uintptr_t>(bias) & 15u) == 0;
-  a.target = target;
-  a.ws_ms = reinterpret_cast<float2*>(ws);
-  a.ws_zt = reinterpret_cast<float*>(ws + p.off_zt);
-  const int64_t units = (int64_t)sc.order.rows * sc.S;   // < 2^31: checked by plan()
+  a.N = (int)L.N;
+  a.V = (int)L.V;
+  a.v_off = (int)L.v_off;
+  a.ld_ms = L.ld_ms;
+  a.tstride = L.tstride;
+  a.bias = L.bias;
+  a.bias_vec4 = (reinterpret_cast<uintptr_t>(L.bias) & 15u) == 0;
+  a.target = L.target;
+  a.ws_ms = L.ms;
+  a.ws_zt = L.zt;
+  const int64_t units = (int64_t)sc.order.rows * sc.S;   // < 2^31: checked by the caller
   if (solo) {
     sc.counter = nullptr;      // round-robin: at most ceil(1024 / #SMs) rounds
     const int grid = (int)(units < dev.sm_count ? units : dev.sm_count);
@@ -503,7 +553,7 @@ rlk_status partials_impl(const void* hidden, int64_t N, int64_t H, int64_t ld_hi
   const int grid = 2 * (int)(units < clusters ? units : clusters);
   sc.counter = nullptr;
   if (ordered_units(units, clusters)) {
-    sc.counter = reinterpret_cast<int*>(ws + p.off_ctr);
+    sc.counter = L.counter;
     if (cudaMemsetAsync(sc.counter, 0, sizeof(int), s) != cudaSuccess) {
       cudaGetLastError();
       return RLK_ERR_CUDA;
@@ -516,6 +566,55 @@ rlk_status partials_impl(const void* hidden, int64_t N, int64_t H, int64_t ld_hi
     return RLK_ERR_CUDA;
   }
   return RLK_OK;
+}
+
+rlk_status partials_impl(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
+                         const void* weight, int64_t V, int64_t ld_weight, const float* bias,
+                         const int64_t* target, int64_t target_stride, int64_t splits_req,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  LogpPlan p;
+  rlk_status st = plan(hidden, N, H, ld_hidden, weight, V, ld_weight, splits_req, &p);
+  if (st != RLK_OK) return st;
+  if (target_stride < 0) return RLK_ERR_SHAPE;
+  if (N == 0) return RLK_OK;
+  if (!hidden || !weight || !target) return RLK_ERR_NULL;
+  if (!workspace) return RLK_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(hidden) & 1u) || (reinterpret_cast<uintptr_t>(weight) & 1u) ||
+      (reinterpret_cast<uintptr_t>(target) & 7u) || (reinterpret_cast<uintptr_t>(bias) & 3u))
+    return RLK_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 15u) || workspace_bytes < p.total)
+    return RLK_ERR_WORKSPACE;
+  DeviceInfo dev;
+  st = device_ready(&dev);
+  if (st != RLK_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  PartialsLaunch L;
+  L.hidden = hidden;
+  L.N = N;
+  L.H = H;
+  L.ld_hidden = ld_hidden;
+  L.stage_h = p.stage_h;
+  L.ldh = p.ldh;
+  L.h_stage = reinterpret_cast<uint16_t*>(ws + p.off_h);
+  L.weight = weight;
+  L.w_rows = V;
+  L.ld_weight = ld_weight;
+  L.stage_w = p.stage_w;
+  L.ldw = p.ldw;
+  L.w_stage = reinterpret_cast<uint16_t*>(ws + p.off_w);
+  L.V = V;
+  L.vps = p.vps;
+  L.j0 = 0;
+  L.j1 = p.S;
+  L.v_off = 0;
+  L.bias = bias;
+  L.target = target;
+  L.tstride = target_stride;
+  L.ms = reinterpret_cast<float2*>(ws);
+  L.ld_ms = p.S;
+  L.zt = reinterpret_cast<float*>(ws + p.off_zt);
+  L.counter = reinterpret_cast<int*>(ws + p.off_ctr);
+  return launch_partials(L, dev, static_cast<cudaStream_t>(stream));
 }
 
 rlk_status combine_impl(int64_t N, int64_t V, const int64_t* target, int64_t target_stride,
@@ -542,10 +641,161 @@ rlk_status combine_impl(int64_t N, int64_t V, const int64_t* target, int64_t tar
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);
   const int rows_per_block = 256 / 32;
   const int grid = (int)ceil_div(N, rows_per_block);
+  ContiguousPartials src;
+  src.ms = reinterpret_cast<const float2*>(ws);
+  src.zt = reinterpret_cast<const float*>(ws + off_zt);
+  src.S = (int)S;
   const cudaError_t e = launch_overlapped(
-      linear_logp_combine_kernel, grid, 256, 0, static_cast<cudaStream_t>(stream),
-      reinterpret_cast<const float2*>(ws), reinterpret_cast<const float*>(ws + off_zt), target,
-      target_stride, (int)N, (int)S, (int)V, logp, lse, target_logit);
+      linear_logp_combine_kernel<ContiguousPartials>, grid, 256, 0,
+      static_cast<cudaStream_t>(stream), src, target, target_stride, (int)N, (int)S, (int)V, logp,
+      lse, target_logit);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return RLK_ERR_CUDA;
+  }
+  return RLK_OK;
+}
+
+// ---- vocabulary shards ("feat(linear-logp)...", author notes: V -> split count
+// -> contiguous ranges -> ordered merge).  A shard is a contiguous run of whole
+// splits [j0, j1) of the V-only policy, i.e. the weight rows of vocabulary ids
+// [v_begin, v_end); its partials are the ones the whole-vocabulary call computes
+// for those splits, bit for bit, because every split is computed from the same
+// tiles in the same order.
+struct ShardPlan {
+  int64_t S = 0, vps = 0, vtiles = 0;
+  int64_t v_begin = 0, v_end = 0;
+  bool stage_h = false, stage_w = false;
+  int64_t ldh = 0, ldw = 0;
+  size_t off_h = 0, off_w = 0, total = 0;     // [counter 256][staged hidden][staged W]
+};
+
+rlk_status shard_plan(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
+                      const void* weight, int64_t V, int64_t j0, int64_t j1, int64_t ld_weight,
+                      ShardPlan* p) {
+  rlk_status st = rlk_vocab_split_policy(V, &p->S, &p->vps, &p->vtiles);
+  if (st != RLK_OK) return st;
+  if (j0 < 0 || j1 < j0 || j1 > p->S) return RLK_ERR_SHAPE;
+  p->v_begin = j0 * p->vps * kVocabTile;
+  p->v_end = j1 * p->vps * kVocabTile < V ? j1 * p->vps * kVocabTile : V;
+  const int64_t rows = p->v_end - p->v_begin;
+  st = check_shapes(N, H, ld_hidden, rows > 0 ? rows : 1, ld_weight);
+  if (st != RLK_OK) return st;
+  if (ceil_div(N, kPairRows) * (j1 - j0) >= (int64_t(1) << 31)) return RLK_ERR_SHAPE;
+  const bool work = N > 0 && rows > 0;
+  p->stage_h = work && !tma_ready(hidden, ld_hidden);
+  p->stage_w = work && !tma_ready(weight, ld_weight);
+  p->ldh = p->stage_h ? staged_ld(H) : ld_hidden;
+  p->ldw = p->stage_w ? staged_ld(H) : ld_weight;
+  size_t off = 256;
+  p->off_h = off;
+  if (p->stage_h) off = align_up(off + (size_t)N * p->ldh * 2, 256);
+  p->off_w = off;
+  if (p->stage_w) off = align_up(off + (size_t)rows * p->ldw * 2, 256);
+  p->total = off;
+  return RLK_OK;
+}
+
+rlk_status shard_partials_impl(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
+                               const void* weight, int64_t V, int64_t j0, int64_t j1,
+                               int64_t ld_weight, const float* bias, const int64_t* target,
+                               int64_t target_stride, float* partials, int64_t ld_partials,
+                               float* target_logit, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  ShardPlan p;
+  rlk_status st = shard_plan(hidden, N, H, ld_hidden, weight, V, j0, j1, ld_weight, &p);
+  if (st != RLK_OK) return st;
+  if (target_stride < 0 || ld_partials < j1 - j0 || ld_partials >= (int64_t(1) << 31))
+    return RLK_ERR_SHAPE;
+  if (N == 0 || j0 == j1) return RLK_OK;
+  if (!hidden || !weight || !target || !partials || !target_logit) return RLK_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(hidden) & 1u) || (reinterpret_cast<uintptr_t>(weight) & 1u) ||
+      (reinterpret_cast<uintptr_t>(target) & 7u) || (reinterpret_cast<uintptr_t>(bias) & 3u) ||
+      (reinterpret_cast<uintptr_t>(partials) & 7u) ||
+      (reinterpret_cast<uintptr_t>(target_logit) & 3u))
+    return RLK_ERR_ALIGN;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 15u) || workspace_bytes < p.total)
+    return RLK_ERR_WORKSPACE;
+  DeviceInfo dev;
+  st = device_ready(&dev);
+  if (st != RLK_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  PartialsLaunch L;
+  L.hidden = hidden;
+  L.N = N;
+  L.H = H;
+  L.ld_hidden = ld_hidden;
+  L.stage_h = p.stage_h;
+  L.ldh = p.ldh;
+  L.h_stage = reinterpret_cast<uint16_t*>(ws + p.off_h);
+  L.weight = weight;
+  L.w_rows = p.v_end - p.v_begin;
+  L.ld_weight = ld_weight;
+  L.stage_w = p.stage_w;
+  L.ldw = p.ldw;
+  L.w_stage = reinterpret_cast<uint16_t*>(ws + p.off_w);
+  L.V = V;
+  L.vps = p.vps;
+  L.j0 = j0;
+  L.j1 = j1;
+  L.v_off = p.v_begin;
+  L.bias = bias;
+  L.target = target;
+  L.tstride = target_stride;
+  L.ms = reinterpret_cast<float2*>(partials);
+  L.ld_ms = ld_partials;
+  L.zt = target_logit;
+  L.counter = reinterpret_cast<int*>(ws);
+  return launch_partials(L, dev, static_cast<cudaStream_t>(stream));
+}
+
+rlk_status combine_shards_impl(int64_t N, int64_t V, const int64_t* target, int64_t target_stride,
+                               int64_t num_shards, const int64_t* split_offsets,
+                               const float* partials, int64_t ld_partials, int64_t shard_stride,
+                               const float* target_logits, int64_t zt_stride, float* logp,
+                               float* lse, float* target_logit, void* stream) {
+  int64_t S, vps, vt;
+  rlk_status st = rlk_vocab_split_policy(V, &S, &vps, &vt);
+  if (st != RLK_OK) return st;
+  if (N < 0 || N >= kMaxExtent || target_stride < 0 || num_shards < 1 ||
+      num_shards > kMaxShards)
+    return RLK_ERR_SHAPE;
+  if (!split_offsets) return RLK_ERR_NULL;
+  ShardedPartials src;
+  if (split_offsets[0] != 0 || split_offsets[num_shards] != S) return RLK_ERR_SHAPE;
+  int64_t widest = 0;
+  for (int64_t q = 0; q < num_shards; ++q) {
+    const int64_t n = split_offsets[q + 1] - split_offsets[q];
+    if (n < 0) return RLK_ERR_SHAPE;
+    widest = n > widest ? n : widest;
+  }
+  for (int64_t q = 0; q <= num_shards; ++q) src.off[q] = (int)split_offsets[q];
+  // Unused slots repeat S, so a search for the shard of a split stops in range.
+  for (int64_t q = num_shards + 1; q <= kMaxShards; ++q) src.off[q] = (int)S;
+  if (ld_partials < widest || ld_partials >= (int64_t(1) << 31)) return RLK_ERR_SHAPE;
+  if (N > 0 && (num_shards > 1 && (shard_stride < N * ld_partials || zt_stride < N)))
+    return RLK_ERR_SHAPE;
+  if (shard_stride < 0 || zt_stride < 0) return RLK_ERR_SHAPE;
+  if (N == 0) return RLK_OK;
+  if (!target || !partials || !target_logits || !logp || !lse) return RLK_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(target) & 7u) || (reinterpret_cast<uintptr_t>(partials) & 7u) ||
+      (reinterpret_cast<uintptr_t>(target_logits) & 3u) ||
+      (reinterpret_cast<uintptr_t>(logp) & 3u) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(target_logit) & 3u))
+    return RLK_ERR_ALIGN;
+  DeviceInfo dev;
+  st = device_ready(&dev);
+  if (st != RLK_OK) return st;
+  src.ms = reinterpret_cast<const float2*>(partials);
+  src.ld = ld_partials;
+  src.shard_stride = shard_stride;
+  src.zt = target_logits;
+  src.zt_stride = zt_stride;
+  src.vps = (int)vps;
+  const int grid = (int)ceil_div(N, 256 / 32);
+  const cudaError_t e = launch_overlapped(
+      linear_logp_combine_kernel<ShardedPartials>, grid, 256, 0, static_cast<cudaStream_t>(stream),
+      src, target, target_stride, (int)N, (int)S, (int)V, logp, lse, target_logit);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return RLK_ERR_CUDA;
@@ -628,6 +878,60 @@ rlk_status rlk_throughput_split_count(int64_t N, int64_t V, int32_t sm_count,
   return RLK_OK;
 }
 
+rlk_status rlk_vocab_shard_range(int64_t V, int64_t num_shards, int64_t shard,
+                                 int64_t* split_begin, int64_t* split_end, int64_t* v_begin,
+                                 int64_t* v_end) {
+  if (!split_begin || !split_end || !v_begin || !v_end) return RLK_ERR_NULL;
+  int64_t S, vps, vt;
+  const rlk_status st = rlk_vocab_split_policy(V, &S, &vps, &vt);
+  if (st != RLK_OK) return st;
+  if (num_shards < 1 || num_shards > kMaxShards || shard < 0 || shard >= num_shards)
+    return RLK_ERR_SHAPE;
+  const int64_t j0 = shard * S / num_shards, j1 = (shard + 1) * S / num_shards;
+  const int64_t span = vps * kVocabTile;
+  *split_begin = j0;
+  *split_end = j1;
+  *v_begin = j0 * span < V ? j0 * span : V;
+  *v_end = j1 * span < V ? j1 * span : V;
+  return RLK_OK;
+}
+
+size_t rlk_linear_logp_shard_workspace_size(const void* hidden, int64_t N, int64_t H,
+                                            int64_t ld_hidden, const void* weight_shard,
+                                            int64_t V, int64_t split_begin, int64_t split_end,
+                                            int64_t ld_weight) {
+  ShardPlan p;
+  if (shard_plan(hidden, N, H, ld_hidden, weight_shard, V, split_begin, split_end, ld_weight,
+                 &p) != RLK_OK)
+    return 0;
+  return p.total;
+}
+
+rlk_status rlk_linear_logp_shard_partials(const void* hidden, int64_t N, int64_t H,
+                                          int64_t ld_hidden, const void* weight_shard, int64_t V,
+                                          int64_t split_begin, int64_t split_end,
+                                          int64_t ld_weight, const float* bias_shard,
+                                          const int64_t* target, int64_t target_stride,
+                                          float* partials, int64_t ld_partials,
+                                          float* target_logit, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
+  return shard_partials_impl(hidden, N, H, ld_hidden, weight_shard, V, split_begin, split_end,
+                             ld_weight, bias_shard, target, target_stride, partials, ld_partials,
+                             target_logit, workspace, workspace_bytes, stream);
+}
+
+rlk_status rlk_linear_logp_combine_shards(int64_t N, int64_t V, const int64_t* target,
+                                          int64_t target_stride, int64_t num_shards,
+                                          const int64_t* split_offsets, const float* partials,
+                                          int64_t ld_partials, int64_t shard_stride,
+                                          const float* target_logits, int64_t zt_stride,
+                                          float* logp, float* lse, float* target_logit,
+                                          void* stream) {
+  return combine_shards_impl(N, V, target, target_stride, num_shards, split_offsets, partials,
+                             ld_partials, shard_stride, target_logits, zt_stride, logp, lse,
+                             target_logit, stream);
+}
+
 size_t rlk_linear_logp_splits_workspace_size(const void* hidden, int64_t N, int64_t H,
                                              int64_t ld_hidden, const void* weight, int64_t V,
                                              int64_t ld_weight, int64_t num_splits) {
@@ -673,23 +977,78 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;   // 32 MiB per device
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+constexpr int kNoAllocMaxDevices = 64;
+
+// The cached device address of g_noalloc_scratch, per device, tagged with the
+// unique id of the CUDA context it was looked up in: after cudaDeviceReset (or
+// any release and re-creation of the primary context) the library's module is
+// loaded again at a new address, so an address is reused only while the context
+// that produced it is still the current one.
+struct NoAllocSlot {
+  unsigned long long ctx_id;
+  void* ptr;
+};
 std::mutex g_noalloc_mutex;
-void* g_noalloc_ptr[64];     // device address of g_noalloc_scratch, per device
+NoAllocSlot g_noalloc_slot[kNoAllocMaxDevices];
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+// Id of the context current on this thread (called with g_noalloc_mutex held).
+rlk_status current_context_id(unsigned long long* id) {
+  if (!g_ctx_get_current || !g_ctx_get_id) {
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) !=
+            cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) !=
+            cudaSuccess ||
+        q2 != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return RLK_ERR_CUDA;
+    }
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+    g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f2);
+  }
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) return RLK_ERR_CUDA;
+  if (ctx == nullptr) {
+    // No context is current on this thread yet: the symbol lookup below makes
+    // the device's primary context current (it allocates nothing).
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return RLK_ERR_CUDA;
+    }
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return RLK_ERR_CUDA;
+  }
+  return g_ctx_get_id(ctx, id) == CUDA_SUCCESS ? RLK_OK : RLK_ERR_CUDA;
+}
 
 // Host code cannot use g_noalloc_scratch's name as an address (on the host it
-// names a stand-in object); the device address is looked up once per device,
-// with that device current, and cached.
+// names a stand-in object); the device address is looked up with the device
+// current and cached until the current context changes.
 rlk_status noalloc_scratch(int dev, void** out) {
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return RLK_ERR_UNSUPPORTED_DEVICE;
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (!g_noalloc_ptr[dev]) {
+  unsigned long long id = 0;
+  rlk_status st = current_context_id(&id);
+  if (st != RLK_OK) return st;
+  NoAllocSlot& slot = g_noalloc_slot[dev];
+  if (slot.ptr == nullptr || slot.ctx_id != id) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
       cudaGetLastError();
       return RLK_ERR_CUDA;
     }
-    g_noalloc_ptr[dev] = p;
+    slot.ptr = p;
+    slot.ctx_id = id;
   }
-  *out = g_noalloc_ptr[dev];
+  *out = slot.ptr;
   return RLK_OK;
 }
 

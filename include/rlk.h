@@ -244,6 +244,92 @@ RLK_API rlk_status rlk_linear_logp_combine(int64_t N, int64_t V, const int64_t* 
                                    float* target_logit, const void* workspace,
                                    size_t workspace_bytes, void* stream);
 
+/* ---- Vocabulary-parallel linear-logp ------------------------------------
+ * The page's split policy [P3 author notes: V -> split count -> contiguous
+ * ranges -> ordered merge] lets the vocabulary be divided between devices at
+ * split boundaries: a shard is a contiguous run of whole splits
+ * [split_begin, split_end) of rlk_vocab_split_policy(V), i.e. the weight rows of
+ * vocabulary ids [v_begin, v_end) with v_begin = split_begin * vps * 256 and
+ * v_end = min(split_end * vps * 256, V).  Each shard computes the (m, s)
+ * partials of its splits (bit for bit those the whole-vocabulary call computes)
+ * and the target logits of the rows whose target it holds; after the partials
+ * are exchanged, rlk_linear_logp_combine_shards merges every row's S partials in
+ * the same fixed order as rlk_linear_logp, so logp, lse and the target logit
+ * equal the one-device results bit for bit.
+ */
+
+/*
+ * A balanced partition into num_shards (1 .. 64) shards: shard q gets splits
+ * [floor(q S / num_shards), floor((q + 1) S / num_shards)) (empty when
+ * num_shards > S) and the vocabulary ids they cover.  Host-only.
+ * RLK_ERR_SHAPE for V out of range, num_shards outside [1, 64] or shard outside
+ * [0, num_shards).
+ */
+RLK_API rlk_status rlk_vocab_shard_range(int64_t V, int64_t num_shards, int64_t shard,
+                                         int64_t* split_begin, int64_t* split_end,
+                                         int64_t* v_begin, int64_t* v_end);
+
+/*
+ * Workspace bytes of rlk_linear_logp_shard_partials: 256 bytes for the kernel's
+ * work-unit counter plus padded copies of a misaligned hidden / weight shard.
+ * Returns 0 for invalid arguments.
+ */
+RLK_API size_t rlk_linear_logp_shard_workspace_size(const void* hidden, int64_t N, int64_t H,
+                                                    int64_t ld_hidden, const void* weight_shard,
+                                                    int64_t V, int64_t split_begin,
+                                                    int64_t split_end, int64_t ld_weight);
+
+/*
+ * Partials of one vocabulary shard.
+ *  hidden        BF16 [N, H] (ld_hidden), as for rlk_linear_logp
+ *  weight_shard  BF16 [v_end - v_begin, H] (ld_weight): rows v_begin .. v_end - 1 of
+ *                the lm-head weight
+ *  V             the WHOLE vocabulary size (it fixes the split policy)
+ *  split_begin, split_end   0 <= split_begin <= split_end <= S
+ *  bias_shard    FP32 [v_end - v_begin] (bias[v_begin ..]) or NULL
+ *  target        int64 global ids, target[r * target_stride]
+ *  partials      FP32 output: for row r and local split i (0 <= i < split_end -
+ *                split_begin) the pair (m, s) at partials[2 (r ld_partials + i)];
+ *                ld_partials >= split_end - split_begin (in pairs), 8-byte aligned
+ *  target_logit  FP32 [N] output: written for the rows whose target lies in
+ *                [v_begin, v_end) (the logit exactly as it entered the partials);
+ *                every other entry is left untouched
+ * N == 0 or an empty shard is a no-op.  Errors as for rlk_linear_logp.
+ */
+RLK_API rlk_status rlk_linear_logp_shard_partials(const void* hidden, int64_t N, int64_t H,
+                                                  int64_t ld_hidden, const void* weight_shard,
+                                                  int64_t V, int64_t split_begin,
+                                                  int64_t split_end, int64_t ld_weight,
+                                                  const float* bias_shard, const int64_t* target,
+                                                  int64_t target_stride, float* partials,
+                                                  int64_t ld_partials, float* target_logit,
+                                                  void* workspace, size_t workspace_bytes,
+                                                  void* stream);
+
+/*
+ * The fixed-order merge over gathered shard partials.
+ *  split_offsets  HOST array of num_shards + 1 (1 .. 64 shards) split indices:
+ *                 0 = split_offsets[0] <= ... <= split_offsets[num_shards] = S;
+ *                 shard q holds splits [split_offsets[q], split_offsets[q + 1])
+ *  partials       shard q's pair for row r and local split i at
+ *                 partials[2 (q shard_stride + r ld_partials + i)] (shard_stride and
+ *                 ld_partials in pairs; shard_stride >= N ld_partials when
+ *                 num_shards > 1), e.g. an all-gather of every shard's output
+ *  target_logits  shard q's target logits at target_logits[q zt_stride + r]
+ *                 (zt_stride >= N when num_shards > 1); row r's value is taken
+ *                 from the shard that holds its target
+ *  target, target_stride, logp, lse, target_logit  as for rlk_linear_logp_combine
+ * Output bits equal rlk_linear_logp's for the same rows.
+ */
+RLK_API rlk_status rlk_linear_logp_combine_shards(int64_t N, int64_t V, const int64_t* target,
+                                                  int64_t target_stride, int64_t num_shards,
+                                                  const int64_t* split_offsets,
+                                                  const float* partials, int64_t ld_partials,
+                                                  int64_t shard_stride,
+                                                  const float* target_logits, int64_t zt_stride,
+                                                  float* logp, float* lse, float* target_logit,
+                                                  void* stream);
+
 /*
  * rlk_linear_logp without a workspace argument, for callers that cannot
  * allocate device memory where they call it: a plugin inside a host framework
