@@ -122,19 +122,20 @@ def test_layouts(dev):
     assert_same(lp(hidden, weight, t_strided, bias), ref, "strided target")
 
 
-@pytest.mark.parametrize("n_small", [1, 17, 32, 100, 128])
+@pytest.mark.parametrize("n_small", [1, 17, 32, 100, 128, 129, 200, 255, 256])
 def test_small_call_loops_match_the_pair_loop(dev, n_small):
     """Calls of at most 128 rows run on the one-CTA loop (M=128 per CTA; at most
     32 rows: a thin ring staging only those rows); larger calls on the 2-SM loop
-    (M=256 over a pair).  A row's bits are the same in all of them: the rows of a
-    small call equal the same rows inside 33-, 129- and 300-row calls, for a
-    ragged vocabulary with bias, and with a staged (odd-pitch) hidden."""
+    (M=256 over a pair, rows split between the pair's CTAs).  A row's bits are the
+    same in all of them: the rows of a small call equal the same rows inside 33-,
+    129-, 257- and 300-row calls (other row blocks and pair halves), for a ragged
+    vocabulary with bias, and with a staged (odd-pitch) hidden or weight."""
     H, V = 2048, 32003
     hidden, weight, bias, target = si.linear_logp_inputs(300, H, V, bias=True, seed=16, device=dev)
-    for start in (0, 5, 172):
+    for start in (0, 5, 44):
         rows = slice(start, start + n_small)
         small = lp(hidden[rows], weight, target[rows], bias)
-        for big_n in (33, 129, 300):
+        for big_n in (33, 129, 257, 300):
             if big_n <= n_small:
                 continue
             s0 = max(0, min(start, big_n - n_small))
