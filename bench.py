@@ -430,6 +430,8 @@ def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
     }
     if roof["bound"] == "tensor":
         roof.update(per_clock(roof["achieved"], line["clocks"], dev))
+    if args.phases:
+        line["phases"] = phase_breakdown(rlk, call, flush, K, stream, alg_bytes, peaks)
     # ---- e2e through the public API with host buffers (pinned), copies timed.
     # Inputs are double-buffered: step k+1's host-to-device copies run on a copy
     # stream while step k's kernels run, and every step still copies all of its
@@ -494,6 +496,42 @@ def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
                                 "sample": f"{rows} rows of the {w.name} workload (full V, full H), "
                                           f"FP64, {dt:.2f} s wall"}
     return line
+
+
+def phase_breakdown(rlk, call, flush, K, stream, alg_bytes, peaks):
+    """Where a partials launch spends its time, from the debug build's per-CTA phase
+    trace (%globaltimer): for K single launches (L2 flushed first when the weight
+    fits in it), the times of each phase relative to the first CTA's entry, as the
+    median over CTAs and the latest CTA, then the median over launches."""
+    if not rlk.is_debug_build():
+        raise SystemExit("--phases reads the debug build's trace: run with RLK_LIBRARY=debug")
+    names = ["entry", "setup_done", "first_stage_landed", "last_accumulator_complete",
+             "last_partials_written", "exit"]
+    per = []
+    for _ in range(K):
+        if flush is not None:
+            flush_l2(flush)
+        rlk.debug_trace()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call.partials()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        tr = rlk.debug_trace().astype(np.int64)
+        used = tr[tr[:, 4] > 0]
+        t0 = used[:, 0].min()
+        row = {"event_us": e0.elapsed_time(e1) * 1e3, "ctas": int(len(used))}
+        for f, n in enumerate(names):
+            v = used[:, f]
+            v = v[v > 0] - t0
+            row[f"{n}_median_us"] = float(np.median(v)) / 1e3
+            row[f"{n}_last_us"] = float(v.max()) / 1e3
+        per.append(row)
+    out = {k: float(np.median([r[k] for r in per])) for k in per[0]}
+    out["hbm_floor_us"] = alg_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6
+    out["note"] = ("debug build (store checks on); times from the first CTA's entry; "
+                   "event_us - exit_last_us = launch latency and event overhead")
+    return out
 
 
 def backward_bench(args, dev, rank, world, peaks, peak_src):
@@ -804,6 +842,61 @@ def ablation_bench(args, dev, rank, world, peaks, peak_src):
     }
 
 
+def h2d_bench(args, dev, rank, world, peaks, peak_src):
+    """The host link the end-to-end legs copy through: pinned host <-> device copies of
+    the mid weight's size (1.245 GB), as one copy and split over 2..16 streams, timed
+    with CUDA events (best of `steps` repetitions after `warmup`)."""
+    nbytes = 151936 * 4096 * 2
+    host = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    host.fill_(1)
+    devbuf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    res = {}
+
+    def timed(fn, streams):
+        best = float("inf")
+        main = torch.cuda.current_stream()
+        for i in range(args.warmup + args.steps):
+            torch.cuda.synchronize()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(main)
+            for st in streams:
+                st.wait_event(s)
+            fn()
+            for st in streams:
+                main.wait_stream(st)
+            e.record(main)
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                best = min(best, s.elapsed_time(e) / 1e3)
+        return nbytes / best / 1e9
+
+    with ClockSampler(dev) as clocks:
+        for name, direction in (("h2d", 0), ("d2h", 1)):
+            for n in (1, 2, 4, 8, 16):
+                streams = [torch.cuda.Stream(device=dev) for _ in range(n)]
+                chunk = -(-nbytes // n)
+
+                def run():
+                    for k, st in enumerate(streams):
+                        lo, hi = k * chunk, min(nbytes, (k + 1) * chunk)
+                        with torch.cuda.stream(st):
+                            if direction == 0:
+                                devbuf[lo:hi].copy_(host[lo:hi], non_blocking=True)
+                            else:
+                                host[lo:hi].copy_(devbuf[lo:hi], non_blocking=True)
+                res[f"{name}_{n}_streams_gbs"] = timed(run, streams)
+    best_h2d = max(v for k, v in res.items() if k.startswith("h2d"))
+    return {
+        "metric": "pinned host-to-device copy GB/s (1.245 GB, the mid weight's size)",
+        "value": best_h2d, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": nbytes / best_h2d / 1e6, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": "host link: one pinned 1.245 GB buffer copied whole or split over "
+                               "2-16 streams, each direction; best of steps after warmup"},
+        "copies": res, "clocks": clocks.summary(), "gpu_launches": 0,
+    }
+
+
 def reference_arm(args):
     """The FP64 CPU oracle as the reference implementation, on a bounded sample.
 
@@ -860,12 +953,15 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="mid",
-                    choices=["mid", "large", "tiny", "ragged", "det_gemm", "backward", "ablation"])
+                    choices=["mid", "large", "tiny", "ragged", "det_gemm", "backward", "ablation", "h2d"])
     ap.add_argument("--impl", default="rlk", choices=["rlk", "reference"])
     ap.add_argument("--rows", type=int, default=0,
                     help="override the row count N of a linear-logp workload (profiling cases)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--phases", action="store_true",
+                    help="linear-logp: per-phase breakdown of the partials kernel from the debug "
+                         "build's trace (needs RLK_LIBRARY=debug)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
@@ -886,6 +982,8 @@ def main():
         line = backward_bench(args, dev, rank, world, peaks, src)
     elif args.workload == "ablation":
         line = ablation_bench(args, dev, rank, world, peaks, src)
+    elif args.workload == "h2d":
+        line = h2d_bench(args, dev, rank, world, peaks, src)
     else:
         line = linear_logp_bench(args, dev, rank, world, peaks, src)
     if rank == 0:

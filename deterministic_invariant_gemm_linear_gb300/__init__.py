@@ -25,7 +25,10 @@ import os
 import torch
 
 _PKG_DIR = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG_DIR, "librlk.so")
+# RLK_LIBRARY=debug selects the debug build (store checks, phase trace) of the
+# same library; anything else, or unset, the release build.
+LIB_PATH = os.path.join(_PKG_DIR, "librlk_debug.so" if os.environ.get("RLK_LIBRARY") == "debug"
+                        else "librlk.so")
 
 RLK_OK = 0
 RLK_BF16, RLK_FP32 = 0, 1
@@ -33,7 +36,10 @@ RLK_GEMM_FWD, RLK_GEMM_DA, RLK_GEMM_DB = 0, 1, 2
 RLK_GEMM_LINEAR_FWD, RLK_GEMM_LINEAR_DX, RLK_GEMM_LINEAR_DW, RLK_GEMM_FWD_ACCUM = 3, 4, 5, 6
 STATUS_NAMES = {0: "RLK_OK", 1: "RLK_ERR_NULL", 2: "RLK_ERR_SHAPE", 3: "RLK_ERR_DTYPE",
                 4: "RLK_ERR_ALIGN", 5: "RLK_ERR_WORKSPACE", 6: "RLK_ERR_UNSUPPORTED_DEVICE",
-                7: "RLK_ERR_CUDA", 8: "RLK_ERR_TIMEOUT"}
+                7: "RLK_ERR_CUDA", 8: "RLK_ERR_TIMEOUT", 9: "RLK_ERR_BOUNDS",
+                10: "RLK_ERR_NOT_DEBUG_BUILD"}
+RLK_DEVERR_TIMEOUT, RLK_DEVERR_BOUNDS = 0x1, 0x2
+TRACE_FIELDS, TRACE_MAX_CTAS = 6, 1024
 
 
 class RlkError(RuntimeError):
@@ -51,6 +57,9 @@ SIGNATURES = {
     "rlk_device_check": (_I, []),
     "rlk_get_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "rlk_selftest_bounded_wait": (_I, [ctypes.c_uint32, _P]),
+    "rlk_is_debug_build": (_I, []),
+    "rlk_selftest_store_check": (_I, [_P]),
+    "rlk_debug_trace_read": (_I, [_P, _I64, ctypes.POINTER(_I64)]),
     "rlk_vocab_split_policy": (_I, [_I64, ctypes.POINTER(_I64), ctypes.POINTER(_I64),
                                     ctypes.POINTER(_I64)]),
     "rlk_linear_logp_workspace_size": (_SZ, [_P, _I64, _I64, _I64, _P, _I64, _I64]),
@@ -86,6 +95,14 @@ SIGNATURES = {
     "rlk_det_linear_fwd": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _I, _I64, _P, _SZ, _P]),
     "rlk_det_linear_dx": (_I, [_P, _I, _I64, _I64, _I64, _P, _I64, _I64, _P, _I, _I64, _P, _SZ, _P]),
     "rlk_det_linear_dw": (_I, [_P, _I, _I64, _I64, _I64, _P, _I64, _I64, _P, _I, _I64, _P, _SZ, _P]),
+    "rlk_det_gemm_backward_workspace_size": (_SZ, [_P, _I, _I64, _I64, _I64, _P, _I64, _I64, _P,
+                                                   _I64]),
+    "rlk_det_gemm_backward": (_I, [_P, _I, _I64, _I64, _I64, _P, _I64, _I64, _P, _I64, _P, _I,
+                                   _I64, _P, _I, _I64, _P, _SZ, _P]),
+    "rlk_det_linear_backward_workspace_size": (_SZ, [_P, _I, _I64, _I64, _I64, _P, _I64, _I64, _P,
+                                                     _I64]),
+    "rlk_det_linear_backward": (_I, [_P, _I, _I64, _I64, _I64, _P, _I64, _I64, _P, _I64, _P, _I,
+                                     _I64, _P, _I, _I64, _P, _SZ, _P]),
 }
 
 _LIB = None
@@ -133,9 +150,24 @@ def device_error(stream=None) -> int:
     """Reads and clears the library's device error word (synchronises the stream)."""
     flags = ctypes.c_uint32(0)
     st = lib().rlk_get_device_error(_stream_ptr(stream), ctypes.byref(flags))
-    if st not in (RLK_OK, 8):
+    if st not in (RLK_OK, 8, 9):
         _check(st, "rlk_get_device_error")
     return flags.value
+
+
+def is_debug_build() -> bool:
+    return bool(lib().rlk_is_debug_build())
+
+
+def debug_trace(max_ctas: int = TRACE_MAX_CTAS):
+    """Debug build: the linear-logp kernels' per-CTA phase timestamps (ns) since the
+    last read, as a list of TRACE_FIELDS-tuples indexed by CTA (then cleared)."""
+    import numpy as np
+    out = np.zeros((max_ctas, TRACE_FIELDS), dtype=np.uint64)
+    n = _I64()
+    _check(lib().rlk_debug_trace_read(out.ctypes.data_as(ctypes.c_void_p), max_ctas,
+                                      ctypes.byref(n)), "rlk_debug_trace_read")
+    return out[:n.value]
 
 
 def _stream_ptr(stream):
@@ -627,3 +659,49 @@ def det_linear_dw(dY: torch.Tensor, X: torch.Tensor, out_dtype=torch.bfloat16, *
                                        _DT[out_dtype], K, _ptr(ws), n, _stream_ptr(stream)),
                "rlk_det_linear_dw")
     return dW
+
+
+def _two_grads(fn, size_fn, g, x, w, out_shapes, out_dtype, want, stream):
+    g2, ldg = _matrix(_flatten_rows(g), "grad")
+    x2, ldx = _matrix(_flatten_rows(x), "x")
+    w2, ldw = _matrix(w, "w")
+    M, N = g2.shape
+    K = x2.size(1)
+    dev = g.device
+    outs = [torch.empty(*shp, dtype=out_dtype, device=dev) if want[i] else None
+            for i, shp in enumerate(out_shapes(M, N, K))]
+    gdt = _DT[g2.dtype]
+    with torch.cuda.device(dev):
+        n = size_fn(_ptr(g2), gdt, M, N, ldg, _ptr(x2), K, ldx, _ptr(w2), ldw)
+        ws = torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+        dt = _DT[out_dtype]
+        lds = [o.size(1) if o is not None else 1 for o in outs]
+        _check(fn(_ptr(g2), gdt, M, N, ldg, _ptr(x2), K, ldx, _ptr(w2), ldw, _ptr(outs[0]), dt,
+                  lds[0], _ptr(outs[1]), dt, lds[1], _ptr(ws), n, _stream_ptr(stream)),
+               fn.__name__)
+    return tuple(outs)
+
+
+def det_gemm_backward(dC: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                      out_dtype=torch.bfloat16, *, grad_a: bool = True, grad_b: bool = True,
+                      stream=None):
+    """(dA = dC . B^T, dB = A^T . dC) for C = A . B, from one dC (bf16 or fp32; an fp32
+    dC is rounded to bf16 once and shared by both products).  Bitwise equal to
+    det_gemm_da and det_gemm_db."""
+    _require_cuda(dC, A, B)
+    lib_ = lib()
+    return _two_grads(lib_.rlk_det_gemm_backward, lib_.rlk_det_gemm_backward_workspace_size, dC, A,
+                      B, lambda M, N, K: ((M, K), (K, N)), out_dtype, (grad_a, grad_b),
+                      stream)
+
+
+def det_linear_backward(dY: torch.Tensor, X: torch.Tensor, W: torch.Tensor,
+                        out_dtype=torch.bfloat16, *, grad_x: bool = True, grad_w: bool = True,
+                        stream=None):
+    """(dX = dY . W, dW = dY^T . X) for Y = X . W^T with W [N, K], from one dY (an fp32 dY
+    is rounded to bf16 once).  Bitwise equal to det_linear_dx and det_linear_dw."""
+    _require_cuda(dY, X, W)
+    lib_ = lib()
+    return _two_grads(lib_.rlk_det_linear_backward, lib_.rlk_det_linear_backward_workspace_size, dY,
+                      X, W, lambda M, N, K: ((M, K), (N, K)), out_dtype, (grad_x, grad_w),
+                      stream)

@@ -91,7 +91,8 @@ __global__ void stage_bf16_kernel(const uint16_t* __restrict__ src, int64_t rows
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = i / ld_dst, c = i - r * ld_dst;
-    dst[i] = c < cols ? src[r * ld_src + c] : (uint16_t)0;
+    if (RLK_STORE_OK(i >= 0 && i < rows * ld_dst, &g_err_common))
+      dst[i] = c < cols ? src[r * ld_src + c] : (uint16_t)0;
   }
 }
 
@@ -106,7 +107,7 @@ __global__ void cast_f32_bf16_kernel(const float* __restrict__ src, int64_t rows
       __nv_bfloat16 b = __float2bfloat16_rn(src[r * ld_src + c]);
       v = *reinterpret_cast<uint16_t*>(&b);
     }
-    dst[i] = v;
+    if (RLK_STORE_OK(i >= 0 && i < rows * ld_dst, &g_err_common)) dst[i] = v;
   }
 }
 
@@ -145,6 +146,13 @@ __global__ void selftest_wait_kernel(uint64_t timeout_ns) {
   }
 }
 
+// Debug builds only: one thread declares a store outside its buffer through the
+// debug store check, which records kDevErrBounds and skips the store (no memory
+// is written at all).
+__global__ void selftest_store_check_kernel(unsigned int* never_written) {
+  if (threadIdx.x == 0 && RLK_STORE_OK(false, &g_err_common)) *never_written = 1u;
+}
+
 uint32_t take_error_common() {
   unsigned int v = 0, zero = 0;
   if (cudaMemcpyFromSymbol(&v, g_err_common, sizeof v) != cudaSuccess) {
@@ -173,6 +181,10 @@ const char* rlk_status_string(int status) {
       return "RLK_ERR_UNSUPPORTED_DEVICE: no CUDA device, or the device is not sm_103";
     case RLK_ERR_CUDA: return "RLK_ERR_CUDA: the CUDA runtime rejected a call";
     case RLK_ERR_TIMEOUT: return "RLK_ERR_TIMEOUT: a kernel wait expired";
+    case RLK_ERR_BOUNDS:
+      return "RLK_ERR_BOUNDS: a debug-build kernel skipped a store outside its buffer";
+    case RLK_ERR_NOT_DEBUG_BUILD:
+      return "RLK_ERR_NOT_DEBUG_BUILD: the call needs the debug build of the library";
     default: return "RLK_ERR_UNKNOWN";
   }
 }
@@ -196,7 +208,8 @@ rlk_status rlk_get_device_error(void* stream, uint32_t* flags) {
   }
   *flags = rlk::take_error_linear_logp() | rlk::take_error_det_gemm() | rlk::take_error_common() |
            rlk::take_error_linear_logp_bwd();
-  return *flags ? RLK_ERR_TIMEOUT : RLK_OK;
+  if (*flags & RLK_DEVERR_TIMEOUT) return RLK_ERR_TIMEOUT;
+  return *flags ? RLK_ERR_BOUNDS : RLK_OK;
 }
 
 rlk_status rlk_selftest_bounded_wait(uint32_t timeout_us, void* stream) {
@@ -207,6 +220,27 @@ rlk_status rlk_selftest_bounded_wait(uint32_t timeout_us, void* stream) {
   rlk::selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
       (uint64_t)timeout_us * 1000u);
   return cudaGetLastError() == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
+}
+
+int rlk_is_debug_build(void) {
+#ifdef RLK_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+rlk_status rlk_selftest_store_check(void* stream) {
+#ifdef RLK_DEBUG
+  rlk::DeviceInfo info;
+  rlk_status st = rlk::device_ready(&info);
+  if (st != RLK_OK) return st;
+  rlk::selftest_store_check_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(nullptr);
+  return cudaGetLastError() == cudaSuccess ? RLK_OK : RLK_ERR_CUDA;
+#else
+  (void)stream;
+  return RLK_ERR_NOT_DEBUG_BUILD;
+#endif
 }
 
 rlk_status rlk_vocab_split_policy(int64_t V, int64_t* num_splits, int64_t* vtiles_per_split,

@@ -55,6 +55,11 @@ struct GemmOut {
 
 __device__ __forceinline__ void store_chunk(const GemmOut& o, int row, int col0,
                                             const uint32_t (&r)[32]) {
+  // the chunk's 32 columns (clipped to N) lie in row `row` of the M x ldc output
+  if (!RLK_STORE_OK(row >= 0 && row < o.M && col0 >= 0 &&
+                        (int64_t)min(col0 + 32, o.N) <= o.ldc,
+                    &g_err_det_gemm))
+    return;
   const bool full = o.vec_ok && col0 + 32 <= o.N;
   if (o.fp32) {
     float* dst = static_cast<float*>(o.C) + (int64_t)row * o.ldc + col0;
@@ -327,6 +332,94 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
   return RLK_OK;
 }
 
+// Checks an output of a product before anything launches (the checks run_gemm
+// makes on it), so that a two-product call fails closed.
+rlk_status check_output(int64_t rows, int64_t cols, const void* C, int c_dtype, int64_t ldc) {
+  if (!dtype_ok(c_dtype)) return RLK_ERR_DTYPE;
+  if (ldc < cols || ldc >= kLdLimit) return RLK_ERR_SHAPE;
+  if (ceil_div(rows, kPairRows) * ceil_div(cols, kBN) >= kDimLimit) return RLK_ERR_SHAPE;
+  if (rows > 0 && !C) return RLK_ERR_NULL;
+  if (!ptr_aligned(C, esize(c_dtype))) return RLK_ERR_ALIGN;
+  return RLK_OK;
+}
+
+// Both products of a backward from one gradient g [M, N]: out1 = g . r1 (kind k1)
+// and out2 = (the kDb product of) x2 and g, with g staged (an FP32 g rounded to
+// BF16, or a misaligned BF16 g copied) once into the workspace and shared.
+// Workspace: [g staged][r1 staged][x2 staged], each 256-byte aligned.
+struct TwoProducts {
+  Operand g, r1, x2;
+  size_t total = 0;
+};
+
+rlk_status plan_two(TwoProducts& t) {
+  rlk_status st;
+  if ((st = check_operand(t.g, true)) != RLK_OK || (st = check_operand(t.r1, false)) != RLK_OK ||
+      (st = check_operand(t.x2, false)) != RLK_OK)
+    return st;
+  size_t off = 0;
+  plan_operand(t.g, off);
+  plan_operand(t.r1, off);
+  plan_operand(t.x2, off);
+  t.total = off;
+  return RLK_OK;
+}
+
+// Runs out1 = kind1(g, r1) [rows1 x cols1, reduced over red1] and
+// out2 = kDb(x2, g) [rows2 x cols2, reduced over M] after validating everything.
+rlk_status run_two(TwoProducts t, Kind kind1, int64_t rows1, int64_t cols1, int64_t red1,
+                   void* out1, int dt1, int64_t ld1, bool db_x2_is_left, int64_t rows2,
+                   int64_t cols2, void* out2, int dt2, int64_t ld2, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  rlk_status st;
+  if (out1 && (st = check_output(rows1, cols1, out1, dt1, ld1)) != RLK_OK) return st;
+  if (out2 && (st = check_output(rows2, cols2, out2, dt2, ld2)) != RLK_OK) return st;
+  if (!out1 && !out2) return RLK_OK;
+  const int64_t M = t.g.rows;
+  if (M > 0 && (!t.g.ptr || (out1 && !t.r1.ptr) || (out2 && !t.x2.ptr))) return RLK_ERR_NULL;
+  if (!ptr_aligned(t.g.ptr, esize(t.g.dtype)) || !ptr_aligned(t.r1.ptr, 2) ||
+      !ptr_aligned(t.x2.ptr, 2))
+    return RLK_ERR_ALIGN;
+  if (t.total > 0 && (!workspace || !ptr_aligned(workspace, 16) || workspace_bytes < t.total))
+    return RLK_ERR_WORKSPACE;
+  DeviceInfo dev;
+  if ((st = device_ready(&dev)) != RLK_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M == 0) {   // out1 has no rows; out2 is the empty sum
+    if (out2 && cudaMemset2DAsync(out2, ld2 * esize(dt2), 0, cols2 * esize(dt2), rows2, s) !=
+                    cudaSuccess) {
+      cudaGetLastError();
+      return RLK_ERR_CUDA;
+    }
+    return RLK_OK;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  // Stage each operand that a product will read at most once (g once for both);
+  // the products then read BF16, TMA-ready copies and need no workspace.
+  const bool use[3] = {true, out1 != nullptr, out2 != nullptr};
+  Operand ops[3] = {t.g, t.r1, t.x2};
+  for (int i = 0; i < 3; ++i) {
+    if (!use[i]) continue;
+    const void* p = ops[i].ptr;
+    if ((st = materialise(ops[i], ws, s, &p)) != RLK_OK) return st;
+    const int64_t ld = ops[i].staged ? ops[i].eff_ld : ops[i].ld;
+    ops[i] = Operand{p, RLK_BF16, ops[i].rows, ops[i].cols, ld};
+  }
+  if (out1) {
+    st = run_gemm(kind1, ops[0], ops[1], rows1, cols1, red1, out1, dt1, ld1, nullptr, 0, stream);
+    if (st != RLK_OK) return st;
+  }
+  if (out2) {
+    st = db_x2_is_left
+             ? run_gemm(Kind::kDb, ops[2], ops[0], rows2, cols2, M, out2, dt2, ld2, nullptr, 0,
+                        stream)
+             : run_gemm(Kind::kDb, ops[0], ops[2], rows2, cols2, M, out2, dt2, ld2, nullptr, 0,
+                        stream);
+    if (st != RLK_OK) return st;
+  }
+  return RLK_OK;
+}
+
 }  // namespace
 
 uint32_t take_error_det_gemm() {
@@ -441,6 +534,50 @@ rlk_status rlk_det_linear_dw(const void* dY, int dy_dtype, int64_t M, int64_t N,
   // dW [N,K] = dY^T . X: the dB configuration with the gradient as the left operand.
   return run_gemm(Kind::kDb, a, b, N, K, M, dW, out_dtype, lddw, workspace, workspace_bytes,
                   stream);
+}
+
+size_t rlk_det_gemm_backward_workspace_size(const void* dC, int dc_dtype, int64_t M, int64_t N,
+                                            int64_t lddc, const void* A, int64_t K, int64_t lda,
+                                            const void* B, int64_t ldb) {
+  TwoProducts t{{dC, dc_dtype, M, N, lddc}, {B, RLK_BF16, K, N, ldb}, {A, RLK_BF16, M, K, lda}};
+  if (K < 1 || plan_two(t) != RLK_OK) return 0;
+  return t.total;
+}
+
+rlk_status rlk_det_gemm_backward(const void* dC, int dc_dtype, int64_t M, int64_t N,
+                                 int64_t lddc, const void* A, int64_t K, int64_t lda,
+                                 const void* B, int64_t ldb, void* dA, int da_dtype, int64_t ldda,
+                                 void* dB, int db_dtype, int64_t lddb, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  TwoProducts t{{dC, dc_dtype, M, N, lddc}, {B, RLK_BF16, K, N, ldb}, {A, RLK_BF16, M, K, lda}};
+  if (K < 1) return RLK_ERR_SHAPE;
+  rlk_status st = plan_two(t);
+  if (st != RLK_OK) return st;
+  // dA [M, K] = dC . B^T (the dA configuration); dB [K, N] = A^T . dC
+  return run_two(t, Kind::kDa, M, K, N, dA, da_dtype, ldda, /*db_x2_is_left=*/true, K, N, dB,
+                 db_dtype, lddb, workspace, workspace_bytes, stream);
+}
+
+size_t rlk_det_linear_backward_workspace_size(const void* dY, int dy_dtype, int64_t M,
+                                             int64_t N, int64_t lddy, const void* X, int64_t K,
+                                             int64_t ldx, const void* W, int64_t ldw) {
+  TwoProducts t{{dY, dy_dtype, M, N, lddy}, {W, RLK_BF16, N, K, ldw}, {X, RLK_BF16, M, K, ldx}};
+  if (K < 1 || plan_two(t) != RLK_OK) return 0;
+  return t.total;
+}
+
+rlk_status rlk_det_linear_backward(const void* dY, int dy_dtype, int64_t M, int64_t N,
+                                   int64_t lddy, const void* X, int64_t K, int64_t ldx,
+                                   const void* W, int64_t ldw, void* dX, int dx_dtype,
+                                   int64_t lddx, void* dW, int dw_dtype, int64_t lddw,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  TwoProducts t{{dY, dy_dtype, M, N, lddy}, {W, RLK_BF16, N, K, ldw}, {X, RLK_BF16, M, K, ldx}};
+  if (K < 1) return RLK_ERR_SHAPE;
+  rlk_status st = plan_two(t);
+  if (st != RLK_OK) return st;
+  // dX [M, K] = dY . W (the forward configuration); dW [N, K] = dY^T . X (dY on the left)
+  return run_two(t, Kind::kFwd, M, K, N, dX, dx_dtype, lddx, /*db_x2_is_left=*/false, N, K, dW,
+                 dw_dtype, lddw, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -185,6 +185,7 @@ __device__ __forceinline__ void logp_epilogue(const LogpSched& sc, const LogpArg
         run = false;
         break;
       }
+      if (threadIdx.x == 64) RLK_TRACE(3);     // an accumulator is complete
       const int v0 = (sc.tile0 + t0 + i) * kBN;   // global vocabulary id of the tile
       const uint32_t taddr = tmem + acc * kAccCols + lane_off;
 #pragma unroll 1
@@ -207,9 +208,12 @@ __device__ __forceinline__ void logp_epilogue(const LogpSched& sc, const LogpArg
     }
     if (!run) break;
     if (valid) {
-      args.ws_ms[(int64_t)row * args.ld_ms + j] = make_float2(m, s);
-      if (have_zt) args.ws_zt[row] = zt;
+      if (RLK_STORE_OK(row >= 0 && row < args.N && j >= 0 && j < args.ld_ms, &g_err_linear_logp))
+        args.ws_ms[(int64_t)row * args.ld_ms + j] = make_float2(m, s);
+      if (have_zt && RLK_STORE_OK(row >= 0 && row < args.N, &g_err_linear_logp))
+        args.ws_zt[row] = zt;
     }
+    if (threadIdx.x == 64) RLK_TRACE(4);       // the unit's partials are written
   }
 }
 
@@ -220,6 +224,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                      const __grid_constant__ CUtensorMap tm_weight, LogpSched sc,
                                      LogpArgs args) {
   extern __shared__ uint8_t smem_raw[];
+  if (threadIdx.x == 0) RLK_TRACE(0);
   const PipeSmem ps = pipe_smem(smem_raw);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
@@ -227,6 +232,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_weight);
   }
   const uint32_t tmem = pipe_setup(ps);
+  if (threadIdx.x == 0) RLK_TRACE(1);
   using THalf = OperandTile<false, kHalfRows>;
 
   if (warp == 0) {
@@ -242,6 +248,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     logp_epilogue<false>(sc, args, ps, tmem);
   }
   pipe_teardown(tmem);
+  if (threadIdx.x == 0) RLK_TRACE(5);
 }
 
 // One CTA per unit = (split j, 128-row block) on the one-CTA loop, for calls of
@@ -253,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const __grid_constant__ CUtensorMap tm_weight, LogpSched sc,
                             LogpArgs args) {
   extern __shared__ uint8_t smem_raw[];
+  if (threadIdx.x == 0) RLK_TRACE(0);
   const PipeSmem ps = pipe_smem(smem_raw);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
@@ -260,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_weight);
   }
   const uint32_t tmem = solo_setup(ps);
+  if (threadIdx.x == 0) RLK_TRACE(1);
   using TA = OperandTile<false, R::kARows>;
   using TB = OperandTile<false, kBN>;
 
@@ -275,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     logp_epilogue<true>(sc, args, ps, tmem);
   }
   solo_teardown(tmem);
+  if (threadIdx.x == 0) RLK_TRACE(5);
 }
 
 // (m, s) pair merge with explicit roundings, so merge(a, b) == merge(b, a) bitwise.
@@ -351,7 +361,7 @@ __global__ void __launch_bounds__(256)
     const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
     merge_ms(M, s, m2, s2);
   }
-  if (lane == 0) {
+  if (lane == 0 && RLK_STORE_OK(row >= 0 && row < N, &g_err_linear_logp)) {
     const float L = __fadd_rn(M, logf(s));
     const int64_t t = __ldg(target + (int64_t)row * tstride);
     const float z = (t >= 0 && t < V) ? src.target_logit(row, t) : __int_as_float(0x7fc00000);
@@ -440,6 +450,35 @@ rlk_status plan(const void* hidden, int64_t N, int64_t H, int64_t ldh, const voi
 }
 
 }  // namespace
+
+static_assert(kTraceFields == RLK_TRACE_FIELDS && kTraceCtas == RLK_TRACE_MAX_CTAS,
+              "the trace table matches its description in rlk.h");
+
+rlk_status read_trace(uint64_t* out, int64_t max_ctas, int64_t* n_ctas) {
+#ifdef RLK_DEBUG
+  if (!out || !n_ctas) return RLK_ERR_NULL;
+  if (max_ctas < 0) return RLK_ERR_SHAPE;
+  DeviceInfo dev;
+  rlk_status st = device_ready(&dev);
+  if (st != RLK_OK) return st;
+  const int64_t n = max_ctas < kTraceCtas ? max_ctas : kTraceCtas;
+  static unsigned long long zeros[kTraceCtas * kTraceFields];
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      (n > 0 && cudaMemcpyFromSymbol(out, g_trace, n * kTraceFields * sizeof(uint64_t)) !=
+                    cudaSuccess) ||
+      cudaMemcpyToSymbol(g_trace, zeros, sizeof zeros) != cudaSuccess) {
+    cudaGetLastError();
+    return RLK_ERR_CUDA;
+  }
+  *n_ctas = n;
+  return RLK_OK;
+#else
+  (void)out;
+  (void)max_ctas;
+  (void)n_ctas;
+  return RLK_ERR_NOT_DEBUG_BUILD;
+#endif
+}
 
 uint32_t take_error_linear_logp() {
   unsigned int v = 0, zero = 0;
@@ -857,6 +896,10 @@ rlk_status rlk_linear_logp(const void* hidden, int64_t N, int64_t H, int64_t ld_
   return linear_logp_impl(hidden, N, H, ld_hidden, weight, V, ld_weight, bias, target,
                           target_stride, logp, lse, target_logit, 0, workspace, workspace_bytes,
                           stream);
+}
+
+rlk_status rlk_debug_trace_read(uint64_t* out, int64_t max_ctas, int64_t* n_ctas) {
+  return read_trace(out, max_ctas, n_ctas);
 }
 
 rlk_status rlk_throughput_split_count(int64_t N, int64_t V, int32_t sm_count,

@@ -149,7 +149,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           uint4* dst = reinterpret_cast<uint4*>(a.G + (int64_t)row * a.ldG + vbase);
 #pragma unroll
           for (int k = 0; k < 4; ++k)   // 8 columns per store; groups past V stay within ldG
-            if (vbase + 8 * k < a.V)
+            if (vbase + 8 * k < a.V &&
+                RLK_STORE_OK(row >= 0 && row < a.N && vbase + 8 * k + 8 <= a.ldG,
+                             &g_err_linear_logp_bwd))
               dst[k] = make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
         }
       }
@@ -178,8 +180,8 @@ __global__ void __launch_bounds__(256)
     s0 = __fadd_rn(s0, __uint_as_float(w << 16));
     s1 = __fadd_rn(s1, __uint_as_float(w & 0xffff0000u));
   }
-  out[v] = s0;
-  if (v + 1 < V) out[v + 1] = s1;
+  if (RLK_STORE_OK(v >= 0 && v < V, &g_err_linear_logp_bwd)) out[v] = s0;
+  if (v + 1 < V && RLK_STORE_OK(v + 1 < V, &g_err_linear_logp_bwd)) out[v + 1] = s1;
 }
 
 std::mutex g_attr_mutex;

@@ -30,6 +30,39 @@ constexpr int kEpilogueThreads = 128;
 // raises the device error word and makes the CTA wind down.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;   // 2 s
 constexpr uint32_t kDevErrTimeout = 0x1u;
+constexpr uint32_t kDevErrBounds = 0x2u;
+
+// Store checks of the debug build (-DRLK_DEBUG): every global store first tests
+// its index against the extent of the buffer it writes; a store outside raises
+// kDevErrBounds in the error word and is skipped (nothing traps).  Release builds
+// compile the test away.
+#ifdef RLK_DEBUG
+__device__ __forceinline__ bool store_in_bounds(bool ok, unsigned int* err) {
+  if (!ok) atomicOr(err, kDevErrBounds);
+  return ok;
+}
+#define RLK_STORE_OK(cond, err) (::rlk::store_in_bounds((cond), (err)))
+#else
+#define RLK_STORE_OK(cond, err) true
+#endif
+
+__device__ __forceinline__ uint64_t globaltimer_ns();
+
+// Phase timestamps of the debug build: field f of this CTA's record takes the
+// current %globaltimer (a later mark of the same field overwrites it).  Each
+// translation unit has its own table; the linear-logp one is read back by
+// rlk_debug_trace_read.  Release builds compile the marks away.
+constexpr int kTraceFields = 6;
+constexpr int kTraceCtas = 1024;
+#ifdef RLK_DEBUG
+static __device__ unsigned long long g_trace[kTraceCtas * kTraceFields];
+__device__ __forceinline__ void trace_mark(int field) {
+  if (blockIdx.x < kTraceCtas) g_trace[blockIdx.x * kTraceFields + field] = globaltimer_ns();
+}
+#define RLK_TRACE(field) ::rlk::trace_mark(field)
+#else
+#define RLK_TRACE(field) ((void)0)
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -421,6 +421,7 @@ __device__ __forceinline__ void mma_role(const Sched& sc, const PipeSmem& ps, ui
           run = false;
           break;
         }
+        if (k == 0 && i == 0 && kb == 0) RLK_TRACE(2);   // the CTA's first stage has landed
         tc_fence_after();
         const uint32_t sa = R::a_stage(ps.stages, stage);
         const uint32_t sb = R::b_stage(ps.stages, stage);

@@ -76,7 +76,9 @@ typedef enum rlk_status {
     RLK_ERR_WORKSPACE = 5,          /* workspace NULL or smaller than required          */
     RLK_ERR_UNSUPPORTED_DEVICE = 6, /* no CUDA device, or the device is not sm_103      */
     RLK_ERR_CUDA = 7,               /* the CUDA runtime rejected a launch or query      */
-    RLK_ERR_TIMEOUT = 8             /* a kernel's bounded wait expired (device error)   */
+    RLK_ERR_TIMEOUT = 8,            /* a kernel's bounded wait expired (device error)   */
+    RLK_ERR_BOUNDS = 9,             /* debug build: a kernel skipped an out-of-bounds store */
+    RLK_ERR_NOT_DEBUG_BUILD = 10    /* the call exists only in the debug build          */
 } rlk_status;
 
 typedef enum rlk_dtype {
@@ -86,6 +88,9 @@ typedef enum rlk_dtype {
 
 /* Device error-word bits reported by rlk_get_device_error. */
 #define RLK_DEVERR_TIMEOUT 0x1u     /* an mbarrier wait gave up after its time limit   */
+#define RLK_DEVERR_BOUNDS 0x2u      /* debug build (librlk_debug.so, compiled with
+                                       -DRLK_DEBUG): a global store's index fell outside
+                                       the buffer it writes; the store was skipped      */
 
 /* Human-readable name of a status code (static storage, never NULL). */
 RLK_API const char* rlk_status_string(int status);
@@ -100,7 +105,8 @@ RLK_API rlk_status rlk_device_check(void);
 /*
  * Reads and clears the device error word after synchronising `stream`.
  * *flags receives the OR of RLK_DEVERR_* bits raised by kernels since the last
- * call (0 when nothing went wrong).  Returns RLK_ERR_TIMEOUT when a bit was set.
+ * call (0 when nothing went wrong).  Returns RLK_ERR_TIMEOUT when the timeout
+ * bit was set, else RLK_ERR_BOUNDS when the bounds bit was set, else RLK_OK.
  */
 RLK_API rlk_status rlk_get_device_error(void* stream, uint32_t* flags);
 
@@ -114,6 +120,39 @@ RLK_API rlk_status rlk_get_device_error(void* stream, uint32_t* flags);
  * Returns RLK_ERR_SHAPE for a limit out of range.
  */
 RLK_API rlk_status rlk_selftest_bounded_wait(uint32_t timeout_us, void* stream);
+
+/*
+ * Debug build.  The library is also built as librlk_debug.so with -DRLK_DEBUG
+ * (same ABI, same arithmetic and output bits): there every kernel tests each
+ * global store's index against the extent of the buffer it writes; a store
+ * outside is skipped and raises RLK_DEVERR_BOUNDS (nothing traps), and the
+ * linear-logp kernels record per-CTA phase timestamps (rlk_debug_trace_read).
+ * rlk_is_debug_build returns 1 in that build, 0 in librlk.so.
+ */
+RLK_API int rlk_is_debug_build(void);
+
+/*
+ * Debug build: launches one thread that declares a store outside its buffer
+ * through the store check; the store is skipped (no memory is written) and
+ * RLK_DEVERR_BOUNDS is raised, so rlk_get_device_error then returns
+ * RLK_ERR_BOUNDS.  librlk.so returns RLK_ERR_NOT_DEBUG_BUILD and launches nothing.
+ */
+RLK_API rlk_status rlk_selftest_store_check(void* stream);
+
+/*
+ * Debug build: copies the phase timestamps (%globaltimer, ns) that the linear-logp
+ * partials kernels recorded since the last read, then clears them.  out receives
+ * max_ctas records of RLK_TRACE_FIELDS uint64 values, indexed by CTA (block)
+ * index: [0] CTA entry, [1] set-up done (barriers, TMEM, wait for the previous
+ * kernel), [2] first operand stage landed (seen by the MMA issuer), [3] last MMA of
+ * the CTA complete (accumulator handed to the epilogue), [4] last partial
+ * written (epilogue), [5] CTA exit; 0 = not recorded.  *n_ctas receives the
+ * number of records kept (at most RLK_TRACE_MAX_CTAS).  librlk.so returns
+ * RLK_ERR_NOT_DEBUG_BUILD.
+ */
+#define RLK_TRACE_FIELDS 6
+#define RLK_TRACE_MAX_CTAS 1024
+RLK_API rlk_status rlk_debug_trace_read(uint64_t* out, int64_t max_ctas, int64_t* n_ctas);
 
 /* ===================================================================== *
  *  Fused linear log-probability                                  [P3]  *
@@ -494,6 +533,27 @@ RLK_API rlk_status rlk_det_gemm_db(const void* A, int64_t M, int64_t K, int64_t 
                            void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Both gradients of C = A . B from one dC                  [P1 Summary; review comment]
+ *   dA[M, K] = dC . B^T   and   dB[K, N] = A^T . dC
+ * bitwise equal to rlk_det_gemm_da and rlk_det_gemm_db on the same arguments, but
+ * an FP32 dC (the gradient of an FP32-output forward) is rounded to BF16 once, into
+ * the workspace, and both products read that copy (likewise a misaligned dC is
+ * copied once).  dA or dB may be NULL to skip it.  Every argument of both products
+ * is validated before the first launch.  M == 0: dA is empty, dB is written with
+ * zeros.  workspace >= rlk_det_gemm_backward_workspace_size(...) bytes (0 when
+ * nothing needs staging), 16-byte aligned.
+ */
+RLK_API size_t rlk_det_gemm_backward_workspace_size(const void* dC, int dc_dtype, int64_t M,
+                                                    int64_t N, int64_t lddc, const void* A,
+                                                    int64_t K, int64_t lda, const void* B,
+                                                    int64_t ldb);
+RLK_API rlk_status rlk_det_gemm_backward(const void* dC, int dc_dtype, int64_t M, int64_t N,
+                                         int64_t lddc, const void* A, int64_t K, int64_t lda,
+                                         const void* B, int64_t ldb, void* dA, int da_dtype,
+                                         int64_t ldda, void* dB, int db_dtype, int64_t lddb,
+                                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * C[M, N] += A[M, K] . B[K, N] with C in FP32 — the accumulate-into-FP32 forward
  * [P1 Implementation: forward_accum_fp32].  Reading taken: the product is formed
  * exactly as by rlk_det_gemm_fwd (same tiles, same ascending K order) and the
@@ -530,6 +590,22 @@ RLK_API rlk_status rlk_det_linear_dw(const void* dY, int dy_dtype, int64_t M, in
                                     int64_t lddy, const void* X, int64_t K, int64_t ldx, void* dW,
                                     int out_dtype, int64_t lddw, void* workspace,
                                     size_t workspace_bytes, void* stream);
+
+/*
+ * Both gradients of Y = X . W^T (W stored [N, K]) from one dY:
+ *   dX[M, K] = dY . W   and   dW[N, K] = dY^T . X
+ * bitwise equal to rlk_det_linear_dx and rlk_det_linear_dw, with an FP32 dY rounded
+ * to BF16 once and shared; the rest as for rlk_det_gemm_backward.
+ */
+RLK_API size_t rlk_det_linear_backward_workspace_size(const void* dY, int dy_dtype, int64_t M,
+                                                      int64_t N, int64_t lddy, const void* X,
+                                                      int64_t K, int64_t ldx, const void* W,
+                                                      int64_t ldw);
+RLK_API rlk_status rlk_det_linear_backward(const void* dY, int dy_dtype, int64_t M, int64_t N,
+                                           int64_t lddy, const void* X, int64_t K, int64_t ldx,
+                                           const void* W, int64_t ldw, void* dX, int dx_dtype,
+                                           int64_t lddx, void* dW, int dw_dtype, int64_t lddw,
+                                           void* workspace, size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -237,3 +237,26 @@ def test_extent_limits(lib):
     fwd = lib.rlk_det_gemm_fwd
     assert fwd(P16, lim, 8, 8, P16, 8, 8, P16, 0, 8, ws, 0, NULL) == 2
     assert fwd(P16, 4, 8, 8, P16, lim, lim, P16, 0, lim, ws, 0, NULL) == 2
+
+
+def test_two_product_backward_validates_before_any_device_use(lib):
+    """rlk_det_gemm_backward / rlk_det_linear_backward check both products' outputs
+    before anything launches (fail closed): fake pointers, no device touched."""
+    f = lib.rlk_det_gemm_backward
+    M, N, K = 64, 96, 32
+    # dA misaligned for FP32, dB fine
+    assert f(P16, 1, M, N, N, P16, K, K, P16, N, ctypes.c_void_p(0x10002), 1, K, P16, 1, N,
+             P16, 1 << 20, None) == 4
+    # dB pitch below its column count
+    assert f(P16, 1, M, N, N, P16, K, K, P16, N, P16, 1, K, P16, 1, N - 1, P16, 1 << 20, None) == 2
+    # an unknown output dtype
+    assert f(P16, 1, M, N, N, P16, K, K, P16, N, P16, 7, K, None, 1, N, P16, 1 << 20, None) == 3
+    # K = 0
+    assert f(P16, 1, M, N, N, P16, 0, 1, P16, N, P16, 1, 1, P16, 1, N, P16, 1 << 20, None) == 2
+    g = lib.rlk_det_linear_backward
+    assert g(P16, 0, M, N, N, P16, K, K, P16, K, P16, 0, K - 1, None, 0, K, P16, 1 << 20, None) == 2
+    # workspace sizes: an FP32 dC is staged once (M x 8 ceil(N/8) BF16), 0 when nothing is staged
+    ws = lib.rlk_det_gemm_backward_workspace_size
+    assert ws(P16, 1, M, N, N, P16, K, K, P16, N) == M * N * 2
+    assert ws(P16, 0, M, N, N, P16, K, K, P16, N) == 0
+    assert ws(P16, 1, M, N, N, P16, 0, 1, P16, N) == 0          # invalid: K = 0

@@ -90,7 +90,12 @@ def test_4096_parity_sampled(dev, orc, op):
     assert torch.equal(c16, c32.to(torch.bfloat16))
     # ... and within one BF16 ulp of the exact result's rounding
     g = dec_bf16(si.bf16_bits(c16)[rows])
-    bf16_within_one_ulp(g, ref, orc.f64_to_bf16_rne(ref), abs_terms(op, x, y, rows), 4096)
+    n, strict, cancelled, beyond, worst = bf16_within_one_ulp(
+        g, ref, orc.f64_to_bf16_rne(ref), abs_terms(op, x, y, rows), 4096)
+    print(f"BF16 classes det_gemm {op} 4096^3, {len(rows)} rows: entries={n} strict={strict} "
+          f"cancellation-bound={cancelled} beyond one ulp={beyond} (all cancellation-bound) "
+          f"worst strict |gpu - RNE(exact)| = {worst:.3f} ulp")
+    assert n == ref.size and strict + cancelled == n
     assert rlk.device_error() == 0
 
 
@@ -206,3 +211,34 @@ def test_db_empty_reduction_is_zero(dev):
     dC = torch.empty(0, 40, dtype=torch.bfloat16, device=dev)
     out = rlk.det_gemm_db(A, dC, out_dtype=torch.float32)
     assert out.shape == (24, 40) and bool((out == 0).all())
+
+
+@pytest.mark.parametrize("dc_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("shape", [(300, 200, 520), (1000, 1000, 1000), (33, 33, 33), (0, 64, 96)])
+def test_two_product_backward_equals_separate_calls(dev, dc_dtype, shape):
+    """rlk_det_gemm_backward (one shared BF16 rounding of an FP32 dC) and
+    rlk_det_linear_backward give exactly the bits of the separate dA / dB (dX / dW)
+    calls, with aligned and staged (odd-pitch) operands, and with M = 0 (empty dA,
+    zero dB)."""
+    M, K, N = shape
+    A, B, dC = si.det_gemm_inputs(max(M, 1), K, N, seed=M + K + N, device=dev, dc_dtype=dc_dtype)
+    A, dC = A[:M], dC[:M]
+    for out in (torch.float32, torch.bfloat16):
+        dA, dB = rlk.det_gemm_backward(dC, A, B, out)
+        assert torch.equal(dA, rlk.det_gemm_da(dC, B, out))
+        assert torch.equal(dB, rlk.det_gemm_db(A, dC, out))
+        W = B.T.contiguous()                                   # [N, K]
+        dX, dW = rlk.det_linear_backward(dC, A, W, out)
+        assert torch.equal(dX, rlk.det_linear_dx(dC, W, out))
+        assert torch.equal(dW, rlk.det_linear_dw(dC, A, out))
+    if M > 0:
+        odd = torch.zeros(M, K + 3, dtype=torch.bfloat16, device=dev)
+        odd[:, :K] = A
+        dA2, dB2 = rlk.det_gemm_backward(dC, odd[:, :K], B, torch.float32)
+        assert torch.equal(dA2, rlk.det_gemm_da(dC, B, torch.float32))
+        assert torch.equal(dB2, rlk.det_gemm_db(A, dC, torch.float32))
+        only_b = rlk.det_gemm_backward(dC, A, B, torch.float32, grad_a=False)
+        assert only_b[0] is None and torch.equal(only_b[1], dB2)
+    else:
+        assert bool((rlk.det_gemm_backward(dC, A, B, torch.float32)[1] == 0).all())
+    assert rlk.device_error() == 0

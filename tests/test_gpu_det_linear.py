@@ -73,7 +73,10 @@ def test_linear_parity_sampled(dev, orc):
             terms = np.abs(dec_bf16(dYb)[r]) @ np.abs(W.cpu().double().numpy())
         else:
             terms = np.abs(dec_bf16(dYb)).T[r] @ np.abs(X.cpu().double().numpy())
-        bf16_within_one_ulp(dec_bf16(si.bf16_bits(out16)[r]), ref, orc.f64_to_bf16_rne(ref), terms, red)
+        n, strict, cancelled, beyond, worst = bf16_within_one_ulp(
+            dec_bf16(si.bf16_bits(out16)[r]), ref, orc.f64_to_bf16_rne(ref), terms, red)
+        print(f"BF16 classes det_linear {name}: entries={n} strict={strict} "
+              f"cancellation-bound={cancelled} beyond one ulp={beyond} worst strict={worst:.3f} ulp")
     assert rlk.device_error() == 0
 
 
