@@ -433,60 +433,12 @@ def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
     if args.phases:
         line["phases"] = phase_breakdown(rlk, call, flush, K, stream, alg_bytes, peaks)
     # ---- e2e through the public API with host buffers (pinned), copies timed.
-    # Inputs are double-buffered: step k+1's host-to-device copies run on a copy
-    # stream while step k's kernels run, and every step still copies all of its
-    # inputs inside the timed region.
     if not args.no_e2e:
-        hh = hidden.cpu().pin_memory()
-        wh = weight.cpu().pin_memory()
-        th = target.cpu().pin_memory()
-        bh = None if bias is None else bias.cpu().pin_memory()
-        sets = [(hidden, weight, target, bias, call)]
-        h2, w2, t2 = torch.empty_like(hidden), torch.empty_like(weight), torch.empty_like(target)
-        b2 = None if bias is None else torch.empty_like(bias)
-        sets.append((h2, w2, t2, b2, rlk.LinearLogpCall(h2, w2, t2, b2)))
-        outs = [(torch.empty(w.N, dtype=torch.float32).pin_memory(),
-                 torch.empty(w.N, dtype=torch.float32).pin_memory()) for _ in range(2)]
-        copy_stream = torch.cuda.Stream(device=dev)
-        ready = [torch.cuda.Event() for _ in range(2)]
-        free = [None, None]
-        E = max(3, min(K, 20))
-        for i in range(E + 2):
-            b = i % 2
-            hd, wd, td, bd, c = sets[b]
-            if i == 2:
-                torch.cuda.synchronize()
-                barrier(world)
-                e0 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                copy_stream.wait_event(e0)
-            if free[b] is not None:
-                copy_stream.wait_event(free[b])      # the kernels that last read set b are done
-            with torch.cuda.stream(copy_stream):
-                hd.copy_(hh, non_blocking=True)
-                wd.copy_(wh, non_blocking=True)
-                td.copy_(th, non_blocking=True)
-                if bd is not None:
-                    bd.copy_(bh, non_blocking=True)
-            ready[b].record(copy_stream)
-            stream.wait_event(ready[b])
-            c()
-            free[b] = torch.cuda.Event()
-            free[b].record(stream)
-            outs[b][0].copy_(c.logp, non_blocking=True)
-            outs[b][1].copy_(c.lse, non_blocking=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        te = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
-        assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
-        h2d = hh.numel() * 2 + wh.numel() * 2 + th.numel() * 8 + (0 if bh is None else bh.numel() * 4)
-        line["e2e"] = {"value": w.N * world * E / te, "unit": "tokens/s",
-                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 8 * w.N,
-                       "ms_per_step": te / E * 1e3,
-                       "h2d_gbs": h2d * E / te / 1e9,
-                       "pipelining": "inputs double-buffered; a step's host-to-device copies (copy "
-                                     "stream) overlap the previous step's kernels"}
+        line["e2e"] = e2e_linear_logp(w, hidden, weight, target, bias, call, dev, world, K, stream,
+                                      copy_weight=False)
+        line["e2e_weight_copied_each_step"] = e2e_linear_logp(w, hidden, weight, target, bias,
+                                                              call, dev, world, K, stream,
+                                                              copy_weight=True)
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
     if rank == 0 and world == 1 and not args.no_cpu:
         import oracle
@@ -496,6 +448,74 @@ def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
                                 "sample": f"{rows} rows of the {w.name} workload (full V, full H), "
                                           f"FP64, {dt:.2f} s wall"}
     return line
+
+
+def e2e_linear_logp(w, hidden, weight, target, bias, call, dev, world, K, stream, copy_weight):
+    """Tokens/s through the public binding with host buffers: every step copies its
+    activations (hidden, targets) from pinned host memory and reads logp and lse
+    back; the lm-head weight (and bias) is model state uploaded once before the
+    timed region (copy_weight=False) or, as a bound, copied every step too.
+    Two buffer sets alternate, so a step's host-to-device copies (copy stream)
+    overlap the previous step's kernels; every step still moves all its bytes
+    inside the timed region."""
+    import deterministic_invariant_gemm_linear_gb300 as rlk
+    hh = hidden.cpu().pin_memory()
+    th = target.cpu().pin_memory()
+    wh = weight.cpu().pin_memory() if copy_weight else None
+    bh = bias.cpu().pin_memory() if (copy_weight and bias is not None) else None
+    sets = [(hidden, weight, target, bias, call)]
+    h2, t2 = torch.empty_like(hidden), torch.empty_like(target)
+    w2 = torch.empty_like(weight) if copy_weight else weight
+    b2 = (torch.empty_like(bias) if (copy_weight and bias is not None) else bias)
+    sets.append((h2, w2, t2, b2, rlk.LinearLogpCall(h2, w2, t2, b2)))
+    outs = [(torch.empty(w.N, dtype=torch.float32).pin_memory(),
+             torch.empty(w.N, dtype=torch.float32).pin_memory()) for _ in range(2)]
+    copy_stream = torch.cuda.Stream(device=dev)
+    ready = [torch.cuda.Event() for _ in range(2)]
+    free = [None, None]
+    E = max(3, min(K, 20))
+    for i in range(E + 2):
+        b = i % 2
+        hd, wd, td, bd, c = sets[b]
+        if i == 2:
+            torch.cuda.synchronize()
+            barrier(world)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            copy_stream.wait_event(e0)
+        if free[b] is not None:
+            copy_stream.wait_event(free[b])      # the kernels that last read set b are done
+        with torch.cuda.stream(copy_stream):
+            hd.copy_(hh, non_blocking=True)
+            td.copy_(th, non_blocking=True)
+            if copy_weight:
+                wd.copy_(wh, non_blocking=True)
+                if bd is not None:
+                    bd.copy_(bh, non_blocking=True)
+        ready[b].record(copy_stream)
+        stream.wait_event(ready[b])
+        c()
+        free[b] = torch.cuda.Event()
+        free[b].record(stream)
+        outs[b][0].copy_(c.logp, non_blocking=True)
+        outs[b][1].copy_(c.lse, non_blocking=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    te = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    h2d = hh.numel() * 2 + th.numel() * 8
+    if copy_weight:
+        h2d += wh.numel() * 2 + (0 if bh is None else bh.numel() * 4)
+    return {"value": w.N * world * E / te, "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 8 * w.N,
+            "ms_per_step": te / E * 1e3, "h2d_gbs": h2d * E / te / 1e9,
+            "inputs": ("hidden + targets copied host-to-device every step, logp + lse read back; "
+                       "the lm-head weight" + (" and bias" if bias is not None else "") +
+                       (" copied every step as well" if copy_weight else
+                        " is model state, uploaded once before the timed region")),
+            "pipelining": "two buffer sets; a step's host-to-device copies (copy stream) overlap "
+                          "the previous step's kernels"}
 
 
 def phase_breakdown(rlk, call, flush, K, stream, alg_bytes, peaks):
