@@ -13,7 +13,8 @@
 //   dA       dC [M,N] K-major,                       B [K,N] K-major (N is reduced)
 //   dB       A [M,K] MN-major (output rows = K),      dC [M,N] MN-major (M is reduced)
 // Output tiles are 256 x 256 per CTA pair (2-SM tcgen05 loop, M=256 x N=256 x
-// K=16 per MMA), the reduction runs over blocks of 64 in ascending order, each tile's accumulation starts from zero, and there is no
+// K=16 per MMA; 256 x 128 for outputs too small to fill the SM pairs), the
+// reduction runs over blocks of 64 in ascending order, each tile's accumulation starts from zero, and there is no
 // split of the reduction: every output bit is a function of its own row of the
 // left operand and column of the right operand only.
 #include <mutex>
@@ -31,16 +32,17 @@ __device__ unsigned int g_err_det_gemm = 0;
 namespace {
 
 struct GemmSched {
-  Banded order; // rows = 256-row output blocks (one per CTA pair), cols = 256-column blocks
+  Banded order; // rows = 256-row output blocks (one per CTA pair), cols = tile_n-column blocks
   int* counter; // nullptr: cluster c takes units c, c + C, ... (a few rounds at most sizes)
   int nkb;      // 64-wide reduction blocks
+  int tile_n;   // output columns per tile: 256, or 128 when that fills the last wave better
   __device__ __forceinline__ int num_units() const { return order.count(); }
   __device__ __forceinline__ int unit_tiles(int) const { return 1; }
   __device__ __forceinline__ void tile_coords(int u, int, int& a0, int& b0) const {
     int mb, nb;
     order.unit(u, mb, nb);
     a0 = mb * kPairRows;
-    b0 = nb * kBN;
+    b0 = nb * tile_n;
   }
 };
 
@@ -108,10 +110,12 @@ __device__ __forceinline__ void store_chunk(const GemmOut& o, int row, int col0,
   }
 }
 
-// One 256 x 256 output tile per CTA pair (2-SM loop): rank r stages rows
-// [a0 + 128 r, +128) of the left operand and rows / columns [b0 + 128 r, +128) of
-// the right operand, and stores its own 128 output rows.
-template <bool kAMN, bool kBMN>
+// One 256 x kTileN output tile per CTA pair (2-SM loop): rank r stages rows
+// [a0 + 128 r, +128) of the left operand and rows / columns [b0 + kTileN/2 r,
+// +kTileN/2) of the right operand, and stores its own 128 output rows.  Every
+// output element sums the same 16-wide products over the same ascending 64-wide
+// blocks whatever the tile width, so both widths give the same bits (tested).
+template <bool kAMN, bool kBMN, int kTileN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     det_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     GemmSched sc, GemmOut out) {
@@ -123,16 +127,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_b);
   }
   const uint32_t tmem = pipe_setup(ps);
+  using R = PairRingT<kTileN / 2>;
   using TA = OperandTile<kAMN, kHalfRows>;
-  using TB = OperandTile<kBMN, kHalfRows>;
+  using TB = OperandTile<kBMN, kTileN / 2>;
 
   if (warp == 0) {
-    if (lane == 0) producer_role<TA, TB>(&tm_a, &tm_b, sc, ps, &g_err_det_gemm);
+    if (lane == 0) producer_role<TA, TB, GemmSched, R>(&tm_a, &tm_b, sc, ps, &g_err_det_gemm);
     if (lane == 1 && ps.rank == 0) scheduler_role(sc, ps, &g_err_det_gemm);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0 && ps.rank == 0)
-      mma_role<TA, TB>(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, kAMN, kBMN), &g_err_det_gemm);
+      mma_role<TA, TB, GemmSched, R>(sc, ps, tmem, idesc_bf16_f32(kPairRows, kTileN, kAMN, kBMN),
+                                     &g_err_det_gemm);
     __syncwarp();
   } else {
     const int q = warp & 3;
@@ -148,7 +154,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int row = m0 + (int)ps.rank * kHalfRows + q * 32 + lane;
       const uint32_t taddr = tmem + acc * kAccCols + lane_off;
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
+      for (int c = 0; c < kTileN / 32; ++c) {
         const int col0 = n0 + c * 32;
         if (col0 >= out.N) break;               // uniform: depends on the tile only
         uint32_t r[32];
@@ -168,23 +174,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 std::mutex g_attr_mutex;
 bool g_attr_set[64];
 
-template <bool kAMN, bool kBMN>
+template <bool kAMN, bool kBMN, int kTileN>
 cudaError_t set_attr() {
-  return cudaFuncSetAttribute(det_gemm_kernel<kAMN, kBMN>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  return cudaFuncSetAttribute(det_gemm_kernel<kAMN, kBMN, kTileN>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              PairRingT<kTileN / 2>::kSmemBytes);
 }
 
 cudaError_t ensure_attrs(int dev) {
   std::lock_guard<std::mutex> lock(g_attr_mutex);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!g_attr_set[dev]) {
-    cudaError_t e = set_attr<false, true>();
-    if (e == cudaSuccess) e = set_attr<false, false>();
-    if (e == cudaSuccess) e = set_attr<true, true>();
+    cudaError_t e = set_attr<false, true, 256>();
+    if (e == cudaSuccess) e = set_attr<false, false, 256>();
+    if (e == cudaSuccess) e = set_attr<true, true, 256>();
+    if (e == cudaSuccess) e = set_attr<false, true, 128>();
+    if (e == cudaSuccess) e = set_attr<false, false, 128>();
+    if (e == cudaSuccess) e = set_attr<true, true, 128>();
     if (e != cudaSuccess) return e;
     g_attr_set[dev] = true;
   }
   return cudaSuccess;
+}
+
+// Output tile width, from the output's extents and the number of CTA pairs
+// only: 256 columns, or 128 when even twice as many 128-wide tiles fit in one
+// wave of pairs.  A 128-wide tile takes about 0.89 of a 256-wide tile's time
+// (measured on GB300), so narrow tiles pay off only where wide ones would leave
+// at least half the pairs idle (1000^3: 15.0 vs 17 - 19 us); at 4096^3 uniform
+// narrow tiles took 135.8 us against 86.7 us.  Bits are the same either way.
+int choose_tile_n(int64_t out_rows, int64_t out_cols, int64_t clusters) {
+  const int64_t wide = ceil_div(out_rows, kPairRows) * ceil_div(out_cols, kBN);
+  return 2 * wide <= clusters ? kBN / 2 : kBN;
 }
 
 inline bool dtype_ok(int d) { return d == RLK_BF16 || d == RLK_FP32; }
@@ -245,8 +266,9 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
   if (!dtype_ok(c_dtype)) return RLK_ERR_DTYPE;
   if (accum && c_dtype != RLK_FP32) return RLK_ERR_DTYPE;
   if (ldc < out_cols || ldc >= kLdLimit) return RLK_ERR_SHAPE;
-  const int64_t num_mb = ceil_div(out_rows, kPairRows), num_nb = ceil_div(out_cols, kBN);
-  if (num_mb * num_nb >= kDimLimit) return RLK_ERR_SHAPE;
+  // units are numbered in ints (checked for the narrower, more numerous tiles)
+  const int64_t num_mb = ceil_div(out_rows, kPairRows);
+  if (num_mb * ceil_div(out_cols, kBN / 2) >= kDimLimit) return RLK_ERR_SHAPE;
   size_t off = 0;
   plan_operand(x, off);
   plan_operand(y, off);
@@ -277,7 +299,11 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
   if ((st = materialise(x, ws, s, &xp)) != RLK_OK) return st;
   if ((st = materialise(y, ws, s, &yp)) != RLK_OK) return st;
 
-  // Tensor maps: {contiguous extent, row count}, pitch, box (128-row halves per CTA).
+  const int64_t clusters = dev.sm_count / 2;
+  const int tile_n = choose_tile_n(out_rows, out_cols, clusters);
+  const int64_t num_nb = ceil_div(out_cols, tile_n);
+  // Tensor maps: {contiguous extent, row count}, pitch, box (per CTA: 128 left-operand
+  // rows, tile_n / 2 right-operand rows or columns).
   CUtensorMap ta, tb;
   bool ok = false;
   switch (kind) {
@@ -287,7 +313,7 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
       break;
     case Kind::kDa:    // dC [M,N] K-major; B [K,N] K-major (N reduced)
       ok = encode_bf16_2d(&ta, xp, x.cols, x.rows, x.eff_ld, kBK, kHalfRows) &&
-           encode_bf16_2d(&tb, yp, y.cols, y.rows, y.eff_ld, kBK, kHalfRows);
+           encode_bf16_2d(&tb, yp, y.cols, y.rows, y.eff_ld, kBK, tile_n / 2);
       break;
     case Kind::kDb:    // A [M,K] MN-major; dC [M,N] MN-major (M reduced)
       ok = encode_bf16_2d(&ta, xp, x.cols, x.rows, x.eff_ld, 64, kBK) &&
@@ -302,6 +328,7 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
   sc.order.band = band_rows(num_mb, red, kPairRows);
   sc.counter = nullptr;
   sc.nkb = (int)ceil_div(red, kBK);
+  sc.tile_n = tile_n;
   GemmOut o;
   o.M = (int)out_rows;
   o.N = (int)out_cols;
@@ -311,18 +338,22 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
   o.accum = accum ? 1 : 0;
   o.vec_ok = ptr_aligned(C, 16) && ((ldc * esize(c_dtype)) % 16) == 0;
   const int64_t units = num_mb * num_nb;
-  const int64_t clusters = dev.sm_count / 2;
   const int grid = 2 * (int)(units < clusters ? units : clusters);
+  constexpr int kWide = PairRingT<kHalfRows>::kSmemBytes, kNarrow = PairRingT<kHalfRows / 2>::kSmemBytes;
+  const bool wide = tile_n == 256;
   cudaError_t e = cudaErrorInvalidValue;
   switch (kind) {
     case Kind::kFwd:
-      e = launch_overlapped(det_gemm_kernel<false, true>, grid, kThreads, kSmemBytes, s, ta, tb, sc, o);
+      e = wide ? launch_overlapped(det_gemm_kernel<false, true, 256>, grid, kThreads, kWide, s, ta, tb, sc, o)
+               : launch_overlapped(det_gemm_kernel<false, true, 128>, grid, kThreads, kNarrow, s, ta, tb, sc, o);
       break;
     case Kind::kDa:
-      e = launch_overlapped(det_gemm_kernel<false, false>, grid, kThreads, kSmemBytes, s, ta, tb, sc, o);
+      e = wide ? launch_overlapped(det_gemm_kernel<false, false, 256>, grid, kThreads, kWide, s, ta, tb, sc, o)
+               : launch_overlapped(det_gemm_kernel<false, false, 128>, grid, kThreads, kNarrow, s, ta, tb, sc, o);
       break;
     case Kind::kDb:
-      e = launch_overlapped(det_gemm_kernel<true, true>, grid, kThreads, kSmemBytes, s, ta, tb, sc, o);
+      e = wide ? launch_overlapped(det_gemm_kernel<true, true, 256>, grid, kThreads, kWide, s, ta, tb, sc, o)
+               : launch_overlapped(det_gemm_kernel<true, true, 128>, grid, kThreads, kNarrow, s, ta, tb, sc, o);
       break;
   }
   if (e != cudaSuccess) {
@@ -337,7 +368,7 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
 rlk_status check_output(int64_t rows, int64_t cols, const void* C, int c_dtype, int64_t ldc) {
   if (!dtype_ok(c_dtype)) return RLK_ERR_DTYPE;
   if (ldc < cols || ldc >= kLdLimit) return RLK_ERR_SHAPE;
-  if (ceil_div(rows, kPairRows) * ceil_div(cols, kBN) >= kDimLimit) return RLK_ERR_SHAPE;
+  if (ceil_div(rows, kPairRows) * ceil_div(cols, kBN / 2) >= kDimLimit) return RLK_ERR_SHAPE;
   if (rows > 0 && !C) return RLK_ERR_NULL;
   if (!ptr_aligned(C, esize(c_dtype))) return RLK_ERR_ALIGN;
   return RLK_OK;

@@ -222,7 +222,8 @@ rlk_status bwd_plan(const void* hidden, int64_t N, int64_t H, int64_t ld_hidden,
       ld_weight >= kLdLimit)
     return RLK_ERR_SHAPE;
   // work-unit counts of the G kernel and of the two products, numbered in ints
-  const int64_t rb = ceil_div(N, kPairRows), vt = ceil_div(V, kBN), hb = ceil_div(H, kBN);
+  // (the products are checked for their narrower, 128-column tiles)
+  const int64_t rb = ceil_div(N, kPairRows), vt = ceil_div(V, kBN), hb = ceil_div(H, kBN / 2);
   if (rb * vt >= kUnitLimit || rb * hb >= kUnitLimit || vt * hb >= kUnitLimit)
     return RLK_ERR_SHAPE;
   p->ldG = grad_ld(V);

@@ -28,12 +28,15 @@ constexpr int kBarrierBlockBytes = 1024;              // keeps the ring 1024-byt
 constexpr int kMaxStages = 11;                        // barrier slots; the rings use at most 7
 
 // The stage ring: each stage holds this CTA's 128 rows of the left operand and
-// its 128 rows of the right-operand tile (64 reduction columns each, 16 KiB
-// apiece), in two areas: left-operand blocks of all stages first, then the
-// right-operand blocks.
-struct PairRing {
+// its kBHalf rows of the right-operand tile (half of the tile's 2 kBHalf
+// columns; 64 reduction columns each, 16 KiB apiece for 256-wide tiles), in two
+// areas: left-operand blocks of all stages first, then the right-operand blocks.
+template <int kBHalf_>
+struct PairRingT {
+  static constexpr int kBHalf = kBHalf_;
+  static constexpr int kTileN = 2 * kBHalf;                         // MMA N
   static constexpr int kABytes = kHalfRows * kBK * 2;              // 16 KiB
-  static constexpr int kBBytes = kHalfRows * kBK * 2;              // 16 KiB
+  static constexpr int kBBytes = kBHalf * kBK * 2;                 // 16 or 8 KiB
   static constexpr int kStages =
       (kSmemLimit - 1024 - kBarrierBlockBytes) / (kABytes + kBBytes) < kMaxStages
           ? (kSmemLimit - 1024 - kBarrierBlockBytes) / (kABytes + kBBytes)
@@ -50,7 +53,9 @@ struct PairRing {
   static_assert(kSmemBytes <= kSmemLimit, "exceeds the 227 KiB per-CTA shared memory limit");
   // One CTA per SM: a second resident CTA could not get TMEM columns.
   static_assert(kSmemBytes > kSmemLimit / 2, "tcgen05 kernels must own their SM");
+  static_assert(kBHalf == kHalfRows || kBHalf == kHalfRows / 2, "256- or 128-wide tiles");
 };
+using PairRing = PairRingT<kHalfRows>;                              // 256 x 256 tiles, 7 stages
 constexpr int kSmemBytes = PairRing::kSmemBytes;
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -337,17 +342,17 @@ __device__ __forceinline__ int warp_unit_take(const Sched& sc, const PipeSmem& p
 // from zero, so a tile's arithmetic depends only on its operand tiles, never on
 // the schedule, the grid or the row count.  TA / TB are the 128-row operand
 // halves (OperandTile<majorness, 128>).
-template <class TA, class TB, class Sched>
+template <class TA, class TB, class Sched, class R = PairRing>
 __device__ __forceinline__ void producer_role(const CUtensorMap* ta, const CUtensorMap* tb,
                                                const Sched& sc, const PipeSmem& ps,
                                                unsigned int* err) {
-  using R = PairRing;
-  static_assert(TA::kBytes == R::kABytes && TB::kBytes == R::kBBytes, "operand halves are 128 rows");
+  static_assert(TA::kBytes == R::kABytes && TB::kBytes == R::kBBytes, "operand halves fit the ring");
   constexpr int kStages = R::kStages;
   int stage = 0;
   uint32_t phase = 0, issued = 0, last_parity = 0;
   bool run = true;
-  const int32_t half = (int32_t)ps.rank * kHalfRows;
+  const int32_t half = (int32_t)ps.rank * kHalfRows;         // this CTA's left-operand rows
+  const int32_t half_b = (int32_t)ps.rank * R::kBHalf;       // and right-operand rows
   for (int k = 0; run; ++k) {
     const int u = unit_take(sc, ps, k, err);
     if (u < 0) {
@@ -367,7 +372,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* ta, const CUten
         const uint32_t leader_full = mapa_shared(ps.full(stage), 0);
         TA::template load<true>(R::a_stage(ps.stages, stage), ta, leader_full, a0 + half,
                                 kb * kBK);
-        TB::template load<true>(R::b_stage(ps.stages, stage), tb, leader_full, b0 + half,
+        TB::template load<true>(R::b_stage(ps.stages, stage), tb, leader_full, b0 + half_b,
                                 kb * kBK);
         issued |= 1u << stage;
         last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -397,10 +402,9 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* ta, const CUten
   }
 }
 
-template <class TA, class TB, class Sched>
+template <class TA, class TB, class Sched, class R = PairRing>
 __device__ __forceinline__ void mma_role(const Sched& sc, const PipeSmem& ps, uint32_t tmem,
                                           uint32_t idesc, unsigned int* err) {
-  using R = PairRing;
   constexpr int kStages = R::kStages;
   int stage = 0, acc = 0;
   uint32_t phase = 0, acc_phase = 0;

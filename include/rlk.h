@@ -463,7 +463,9 @@ RLK_API rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64
  * blocks of 64 (16 per tensor-core instruction) with no split of the
  * reduction, no atomics and no data-dependent order, so every output is
  * bitwise reproducible.  Output tiles are 256 x 256 (one per pair of SMs, M=256 x
- * N=256 x K=16 per tensor-core instruction) whatever the problem size.
+ * N=256 x K=16 per tensor-core instruction), or 256 x 128 (N=128) when the
+ * 256-wide tiles would leave at least half of the SM pairs idle; each output
+ * element is the same sum either way, so the width never changes a bit.
  * Outputs are BF16 (round to nearest even from the FP32 accumulator) or FP32.
  * A batched operand [b, M, K] is passed flattened as [b * M, K] (a leading
  * shape is a row count), so fwd and dA are bitwise equal per row whatever the

@@ -242,3 +242,23 @@ def test_two_product_backward_equals_separate_calls(dev, dc_dtype, shape):
     else:
         assert bool((rlk.det_gemm_backward(dC, A, B, torch.float32)[1] == 0).all())
     assert rlk.device_error() == 0
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_tile_widths_give_the_same_bits(dev, out_dtype):
+    """Outputs whose 256-wide tiles would leave at least half the CTA pairs idle use
+    128-wide tiles.  A 256-row chunk of a 4096-row product (8 wide tiles: narrow
+    tiles) must equal the same rows of the full product (128 wide tiles: wide)
+    bit for bit, for the forward (MN-major right operand) and dA (K-major)."""
+    M, K, N = 4096, 1024, 2048
+    A, B, dC = si.det_gemm_inputs(M, K, N, seed=12, device=dev)
+    full_f = rlk.det_gemm_fwd(A, B, out_dtype)
+    full_a = rlk.det_gemm_da(dC, B, out_dtype)
+    for r0 in (0, 256, 3840):
+        rows = slice(r0, r0 + 256)
+        assert torch.equal(rlk.det_gemm_fwd(A[rows], B, out_dtype), full_f[rows])
+        assert torch.equal(rlk.det_gemm_da(dC[rows], B, out_dtype), full_a[rows])
+    # a ragged narrow case: 33 rows x 2000 columns against the same rows of 4096
+    assert torch.equal(rlk.det_gemm_fwd(A[100:133], B[:, :2000], out_dtype),
+                       rlk.det_gemm_fwd(A, B[:, :2000], out_dtype)[100:133])
+    assert rlk.device_error() == 0
