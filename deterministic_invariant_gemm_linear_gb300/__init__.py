@@ -403,9 +403,11 @@ def linear_logp_combine_shards(partials: torch.Tensor, target_logits: torch.Tens
     partials = partials.contiguous()
     target_logits = target_logits.contiguous()
     R, N, ld, _ = partials.shape
-    offs = (ctypes.c_int64 * (R + 1))(*[int(x) for x in split_offsets])
     if len(split_offsets) != R + 1:
         raise ValueError("split_offsets needs one entry per shard plus one")
+    if tuple(target_logits.shape) != (R, N):
+        raise ValueError("target_logits must be [R, N] like the partials' first two dims")
+    offs = (ctypes.c_int64 * (R + 1))(*[int(x) for x in split_offsets])
     t1 = target.reshape(-1)
     tstride = t1.stride(0) if N > 1 else 1
     dev = partials.device
