@@ -115,7 +115,7 @@ _NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slow
 
 class _Nvml:
     """Read-only NVML queries through ctypes (the driver's libnvidia-ml): the SM
-    clock, its maximum, the power draw and the active clock-event reasons."""
+    clock, its maximum and the active clock-event reasons."""
 
     def __init__(self, device: torch.device):
         import ctypes
@@ -142,12 +142,11 @@ class _Nvml:
 
     def sample(self):
         c = self.c
-        clk, mw, rs = c.c_uint(), c.c_uint(), c.c_ulonglong()
+        clk, rs = c.c_uint(), c.c_ulonglong()
         if self.lib.nvmlDeviceGetClockInfo(self.h, 1, c.byref(clk)) != 0:   # NVML_CLOCK_SM
             return None
-        power = mw.value / 1e3 if self.lib.nvmlDeviceGetPowerUsage(self.h, c.byref(mw)) == 0 else None
         reasons = rs.value if self.reasons_fn(self.h, c.byref(rs)) == 0 else 0
-        return float(clk.value), power, reasons
+        return float(clk.value), reasons
 
 
 class ClockSampler:
@@ -216,13 +215,11 @@ class ClockSampler:
                 return None
             sm = [x[0] for x in self.samples]
             reasons = set()
-            for _, _, r in self.samples:
+            for _, r in self.samples:
                 reasons.update(n for bit, n in _NVML_REASONS.items() if r & bit)
-            pw = [x[1] for x in self.samples if x[1] is not None]
             return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": self.nvml.max_mhz,
                     "sm_mhz_min": min(sm), "sm_mhz_max": max(sm), "reasons": sorted(reasons),
-                    "samples": len(sm), "power_w_max": max(pw) if pw else None,
-                    "source": "NVML in-process, ~2 ms period"}
+                    "samples": len(sm), "source": "NVML in-process, ~2 ms period"}
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.lines:

@@ -68,7 +68,7 @@ def test_mid_parity_sampled(dev, orc):
     hidden, weight, bias, target = si.workload_inputs(w, seed=0, device=dev)
     logp, lse, zt = rlk.linear_logp(hidden, weight, target, bias, return_target_logit=True)
     torch.cuda.synchronize()
-    rows = sample_rows(w.N, 512, seed=1, must=(511, 512, 2047, 2048, 4095))
+    rows = sample_rows(w.N, 1024, seed=1, must=(511, 512, 2047, 2048, 4095))
     rlp, rls, rzt = oracle_rows(orc, hidden[rows], weight, target[rows], bias)
     assert_logp_close(logp.cpu().numpy()[rows], lse.cpu().numpy()[rows], rlp, rls, "mid")
     assert np.abs(zt.cpu().numpy()[rows] - rzt).max() <= 1e-4
@@ -87,7 +87,7 @@ def test_large_parity_sampled(dev, orc):
     assert logp.shape == w.lead_shape
     logp, lse, zt = logp.reshape(-1), lse.reshape(-1), zt.reshape(-1)
     id0 = torch.nonzero(target == 0).flatten().cpu().numpy()[:100]
-    rows = sample_rows(w.N, 400, seed=2, must=tuple(int(i) for i in id0) + (2047, 2048, 16383))
+    rows = sample_rows(w.N, 920, seed=2, must=tuple(int(i) for i in id0) + (2047, 2048, 16383))
     assert int((target[rows] == 0).sum()) >= 100
     rlp, rls, rzt = oracle_rows(orc, hidden[rows], weight, target[rows], bias)
     assert_logp_close(logp.cpu().numpy()[rows], lse.cpu().numpy()[rows], rlp, rls, "large")
