@@ -17,6 +17,7 @@ slowest rank's time is reported.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import math
 import os
@@ -689,6 +690,26 @@ def det_gemm_bench(args, dev, rank, world, peaks, peak_src):
     c1.record(stream)
     torch.cuda.synchronize()
     cublas = flop / (c0.elapsed_time(c1) / 10 / 1e3) / 1e12
+    # the linear layout (weight [N, K]) and the two-product backward, same sizes, as context
+    W = B.T.contiguous()
+    dC32 = dC.float()
+    extra = [("linear_fwd", lambda: rlk.det_linear(A, W)), ("linear_dx", lambda: rlk.det_linear_dx(dC, W)),
+             ("linear_dw", lambda: rlk.det_linear_dw(dC, A)),
+             ("backward_da_db_fp32_dC", lambda: rlk.det_gemm_backward(dC32, A, B)),
+             ("da_then_db_fp32_dC", lambda: (rlk.det_gemm_da(dC32, B), rlk.det_gemm_db(A, dC32)))]
+    extra_ms = {}
+    for name, f in extra:
+        f()
+        ts = []
+        for _ in range(max(3, min(K, 10))):
+            flush_l2(flush)
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            f()
+            s1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(s0.elapsed_time(s1))
+        extra_ms[name] = float(np.median(ts))
     best = min(ms, key=ms.get)
     line = {
         "metric": "det_gemm fwd+da+db TFLOP/s (M=N=K=4096, BF16 in/out, FP32 accumulate)",
@@ -708,6 +729,7 @@ def det_gemm_bench(args, dev, rank, world, peaks, peak_src):
                                     f"{2 * (M * K_ + K_ * N) + 2 * M * N} bytes (bf16 out)",
                      "peak_kind": f"{peak_src} burst bf16"},
         "cublas_bf16_tflops_context": cublas,
+        "other_entry_points_ms_median": extra_ms,
         "clocks": clocks.summary(),
         "gpu_launches": 3 * K,
     }
@@ -914,6 +936,110 @@ def h2d_bench(args, dev, rank, world, peaks, peak_src):
     }
 
 
+def shards_bench(args, dev, rank, world, peaks, peak_src):
+    """The vocabulary-parallel path on one GPU: the mid workload's vocabulary cut into
+    --shards balanced runs of whole splits, each shard's partials computed from its
+    own weight rows (one launch per shard, back to back), then the fixed-order merge
+    over the gathered partials; against the one-call operator on the same inputs.
+    The exchange between GPUs (an all-gather of N*S*8 + 4*N bytes per rank) has no
+    second GPU to go to here and is not timed."""
+    import deterministic_invariant_gemm_linear_gb300 as rlk
+    w = si.MID
+    R = args.shards
+    hidden, weight, bias, target = si.workload_inputs(w, seed=rank, device=dev)
+    S = rlk.vocab_split_policy(w.V)[0]
+    ranges = [rlk.vocab_shard_range(w.V, R, q) for q in range(R)]
+    widest = max(r[1] - r[0] for r in ranges)
+    shards = [weight[v0:v1].contiguous() for _, _, v0, v1 in ranges]
+    offsets = [r[0] for r in ranges] + [S]
+    lib, P, sp = rlk.lib(), rlk._ptr, rlk._stream_ptr(None)
+    N, H, V = w.N, w.H, w.V
+    parts = torch.empty(R, N, widest, 2, dtype=torch.float32, device=dev)
+    zts = torch.full((R, N), float("nan"), dtype=torch.float32, device=dev)
+    wss = []
+    for (j0, j1, v0, v1), ws_ in zip(ranges, shards):
+        n = lib.rlk_linear_logp_shard_workspace_size(P(hidden), N, H, H, P(ws_), V, j0, j1, H)
+        wss.append(torch.empty(n, dtype=torch.uint8, device=dev))
+    logp = torch.empty(N, device=dev)
+    lse = torch.empty(N, device=dev)
+    offs = (ctypes.c_int64 * (R + 1))(*offsets)
+
+    def shard(q):
+        j0, j1, v0, v1 = ranges[q]
+        rlk._check(lib.rlk_linear_logp_shard_partials(
+            P(hidden), N, H, H, P(shards[q]), V, j0, j1, H, None, P(target), 1, P(parts[q]), widest,
+            P(zts[q]), P(wss[q]), wss[q].numel(), sp), "rlk_linear_logp_shard_partials")
+
+    def merge():
+        rlk._check(lib.rlk_linear_logp_combine_shards(
+            N, V, P(target), 1, R, offs, P(parts), widest, N * widest, P(zts), N, P(logp), P(lse),
+            None, sp), "rlk_linear_logp_combine_shards")
+
+    one = rlk.LinearLogpCall(hidden, weight, target, bias)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        for q in range(R):
+            shard(q)
+        merge()
+        one()
+    torch.cuda.synchronize()
+    assert torch.equal(logp, one.logp) and torch.equal(lse, one.lse), "shards must equal one call"
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(R + 2)] for _ in range(K)]
+    barrier(world)
+    with ClockSampler(dev) as clocks:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for k in range(K):
+            ev[k][0].record(stream)
+            for q in range(R):
+                shard(q)
+                ev[k][q + 1].record(stream)
+            merge()
+            ev[k][R + 1].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    t = max_over_ranks(start.elapsed_time(end) / 1e3, world, dev)
+    shard_ms = [float(np.mean([e[q].elapsed_time(e[q + 1]) for e in ev])) for q in range(R)]
+    merge_ms = float(np.mean([e[R].elapsed_time(e[R + 1]) for e in ev]))
+    o0, o1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    o0.record(stream)
+    for _ in range(K):
+        one()
+    o1.record(stream)
+    torch.cuda.synchronize()
+    one_ms = o0.elapsed_time(o1) / K
+    assert rlk.device_error() == 0
+    flops = 2.0 * N * H * V
+    q_big = max(range(R), key=lambda q: ranges[q][3] - ranges[q][2])
+    vq = ranges[q_big][3] - ranges[q_big][2]
+    achieved = 2.0 * N * H * vq / (shard_ms[q_big] / 1e3) / 1e12
+    line = {
+        "metric": f"vocabulary-parallel linear-logp on one GPU ({R} shards back to back + merge; "
+                  f"N={N},H={H},V={V})",
+        "value": N * world * K / t, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": t / K * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name}: N={N} H={H} V={V}, {R} balanced shards of whole splits",
+                   "shards": [{"splits": [j0, j1], "ids": [v0, v1]} for j0, j1, v0, v1 in ranges],
+                   "l2": f"inputs larger than L2: W {V * H * 2 / 1e9:.3f} GB streamed per step"},
+        "kernels_ms": {"shard_partials": shard_ms, "combine_shards": merge_ms},
+        "one_call_ms": one_ms,
+        "shards_over_one_call": (sum(shard_ms) + merge_ms) / one_ms,
+        "bitwise_equal_to_one_call": True,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                     "kernel": f"linear_logp_partials_kernel on shard {q_big} ({vq} ids)",
+                     "algorithmic": f"2*N*H*V_shard = {2.0 * N * H * vq:.4g} FLOP per launch",
+                     "peak_kind": f"{peak_src} burst bf16"},
+        "exchange": f"not timed (one GPU): {N * S * 8 + 4 * N} bytes gathered per step in total",
+        "clocks": clocks.summary(),
+        "gpu_launches": (R + 1) * K,
+    }
+    line["roofline"].update(per_clock(achieved, line["clocks"], dev))
+    return line
+
+
 def reference_arm(args):
     """The FP64 CPU oracle as the reference implementation, on a bounded sample.
 
@@ -970,10 +1096,12 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="mid",
-                    choices=["mid", "large", "tiny", "ragged", "det_gemm", "backward", "ablation", "h2d"])
+                    choices=["mid", "large", "tiny", "ragged", "det_gemm", "backward", "ablation", "h2d",
+                             "shards"])
     ap.add_argument("--impl", default="rlk", choices=["rlk", "reference"])
     ap.add_argument("--rows", type=int, default=0,
                     help="override the row count N of a linear-logp workload (profiling cases)")
+    ap.add_argument("--shards", type=int, default=2, help="--workload shards: number of shards")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--phases", action="store_true",
@@ -1001,6 +1129,8 @@ def main():
         line = ablation_bench(args, dev, rank, world, peaks, src)
     elif args.workload == "h2d":
         line = h2d_bench(args, dev, rank, world, peaks, src)
+    elif args.workload == "shards":
+        line = shards_bench(args, dev, rank, world, peaks, src)
     else:
         line = linear_logp_bench(args, dev, rank, world, peaks, src)
     if rank == 0:

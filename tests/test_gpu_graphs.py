@@ -113,3 +113,51 @@ def test_calls_see_inputs_written_just_before(dev, N):
         (wl, wc) = want[sign]
         assert torch.equal(lp[0], wl[0]) and torch.equal(lp[1], wl[1]) and torch.equal(c, wc)
     assert rlk.device_error() == 0
+
+
+def test_vocabulary_shards_and_two_product_backward_graph_replay(dev):
+    """Shard partials (two shards, one staged through its workspace), the merge over
+    the gathered shards, and the two-product det_gemm backward with an FP32 dC
+    (one shared BF16 rounding) captured in one graph replay with the eager bits."""
+    N, H, V = 300, 1002, 32003                      # pitch 1002: hidden and W shards staged
+    hidden, weight, bias, target = si.linear_logp_inputs(N, H, V, bias=True, seed=57, device=dev)
+    S, vps, _ = rlk.vocab_split_policy(V)
+    cut = 50
+    offsets = [0, cut, S]
+    v_cut = cut * vps * 256
+    shards = [(weight[:v_cut].contiguous(), bias[:v_cut].contiguous(), 0, cut),
+              (weight[v_cut:].contiguous(), bias[v_cut:].contiguous(), cut, S)]
+    A, B, dC = si.det_gemm_inputs(520, 300, 264, seed=58, device=dev, dc_dtype=torch.float32)
+
+    def run():
+        parts, zts = [], []
+        for w_, b_, j0, j1 in shards:
+            p, z = rlk.linear_logp_shard_partials(hidden, w_, target, V, j0, j1, b_,
+                                                  ld_partials=S - cut)
+            parts.append(p)
+            zts.append(z)
+        out = rlk.linear_logp_combine_shards(torch.stack(parts), torch.stack(zts), offsets, target,
+                                             V, return_target_logit=True)
+        return out + rlk.det_gemm_backward(dC, A, B, torch.float32)
+
+    eager = [t.clone() for t in run()]
+    ref = rlk.linear_logp(hidden, weight, target, bias, return_target_logit=True)
+    for a, b in zip(eager[:3], ref):
+        assert torch.equal(a, b)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        run()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        outs = run()
+    for _ in range(2):
+        for t in outs:
+            t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(outs, eager):
+            assert torch.equal(a, b)
+    assert rlk.device_error() == 0
