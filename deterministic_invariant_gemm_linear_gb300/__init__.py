@@ -92,6 +92,7 @@ SIGNATURES = {
     "rlk_det_gemm_db": (_I, [_P, _I64, _I64, _I64, _P, _I, _I64, _I64, _P, _I, _I64, _P, _SZ, _P]),
     "rlk_det_gemm_fwd_accum_fp32": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _I64, _P, _SZ,
                                          _P]),
+    "rlk_sum_partials_ordered": (_I, [_P, _I64, _I64, _I64, _I64, _I64, _P, _I, _I64, _P]),
     "rlk_det_linear_fwd": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _I, _I64, _P, _SZ, _P]),
     "rlk_det_linear_dx": (_I, [_P, _I, _I64, _I64, _I64, _P, _I64, _I64, _P, _I, _I64, _P, _SZ, _P]),
     "rlk_det_linear_dw": (_I, [_P, _I, _I64, _I64, _I64, _P, _I64, _I64, _P, _I, _I64, _P, _SZ, _P]),
@@ -421,6 +422,21 @@ def linear_logp_combine_shards(partials: torch.Tensor, target_logits: torch.Tens
     return (logp, lse, zt) if return_target_logit else (logp, lse)
 
 
+def _all_gather(t: torch.Tensor, group=None) -> torch.Tensor:
+    """Every rank's equally shaped tensor, stacked in rank order on t's device.
+    With the NCCL backend device tensors are exchanged directly; with gloo they
+    travel through host copies."""
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    dev = t.device
+    x = t.contiguous()
+    if dist.get_backend(group) != "nccl":
+        x = x.cpu()
+    parts = [torch.empty_like(x) for _ in range(world)]
+    dist.all_gather(parts, x, group=group)
+    return torch.stack(parts).to(dev)
+
+
 def exchange_shard_partials(partials: torch.Tensor, target_logit: torch.Tensor, group=None):
     """All-gather every rank's shard output: ([R, N, ld, 2], [R, N]) in rank order.
 
@@ -428,19 +444,34 @@ def exchange_shard_partials(partials: torch.Tensor, target_logit: torch.Tensor, 
     With the NCCL backend the device tensors are exchanged directly; with gloo the
     tensors travel through host copies and come back on the caller's device.
     """
-    import torch.distributed as dist
-    world = dist.get_world_size(group)
-    dev = partials.device
-    via_host = dist.get_backend(group) != "nccl"
-    p = partials.contiguous()
-    z = target_logit.contiguous()
-    if via_host:
-        p, z = p.cpu(), z.cpu()
-    ps = [torch.empty_like(p) for _ in range(world)]
-    zs = [torch.empty_like(z) for _ in range(world)]
-    dist.all_gather(ps, p, group=group)
-    dist.all_gather(zs, z, group=group)
-    return torch.stack(ps).to(dev), torch.stack(zs).to(dev)
+    return _all_gather(partials, group), _all_gather(target_logit, group)
+
+
+def sum_partials_ordered(parts: torch.Tensor, out_dtype=torch.float32, *, stream=None):
+    """out = parts[0] + parts[1] + ... (FP32, ascending part order) for parts [P, rows, cols]
+    fp32, written as out_dtype (bf16 rounds to nearest even)."""
+    _require_cuda(parts)
+    if parts.dim() != 3 or parts.dtype != torch.float32:
+        raise ValueError("parts must be a float32 [P, rows, cols] tensor")
+    parts = parts.contiguous()
+    P, rows, cols = parts.shape
+    out = torch.empty(rows, cols, dtype=out_dtype, device=parts.device)
+    with torch.cuda.device(parts.device):
+        _check(lib().rlk_sum_partials_ordered(_ptr(parts), P, rows, cols, cols, rows * cols,
+                                              _ptr(out), _DT[out_dtype], cols, _stream_ptr(stream)),
+               "rlk_sum_partials_ordered")
+    return out
+
+
+def det_gemm_db_row_sharded(A_local: torch.Tensor, dC_local: torch.Tensor,
+                            out_dtype=torch.bfloat16, *, group=None):
+    """dB = A^T . dC when the rows of A and dC are divided between the ranks of `group`:
+    each rank forms its FP32 partial product (det_gemm_db over its own rows), the ranks
+    all-gather the partials, and every rank adds them in rank order
+    (sum_partials_ordered).  The result is the same bits on every rank and run to
+    run; it depends on the row partition, not on the exchange."""
+    local = det_gemm_db(A_local, dC_local, out_dtype=torch.float32)
+    return sum_partials_ordered(_all_gather(local, group), out_dtype)
 
 
 def vocab_parallel_linear_logp(hidden: torch.Tensor, weight_shard: torch.Tensor,

@@ -171,6 +171,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   pipe_teardown(tmem);
 }
 
+// out[r, c] = part_0[r, c] + part_1[r, c] + ... + part_{P-1}[r, c], added in FP32
+// (round to nearest) in ascending part order, written as FP32 or BF16 (round to
+// nearest even).  Consecutive threads take consecutive columns, so every part's
+// row is read coalesced.
+__global__ void __launch_bounds__(256)
+    ordered_sum_kernel(const float* __restrict__ parts, int64_t P, int64_t rows, int64_t cols,
+                       int64_t ld_in, int64_t part_stride, void* __restrict__ out, int out_fp32,
+                       int64_t ld_out) {
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  const int64_t total = rows * cols;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / cols, c = i - r * cols;
+    const float* p = parts + r * ld_in + c;
+    float acc = __ldg(p);
+    for (int64_t q = 1; q < P; ++q) acc = __fadd_rn(acc, __ldg(p + q * part_stride));
+    if (!RLK_STORE_OK(r < rows && c < cols && c < ld_out, &g_err_det_gemm)) continue;
+    if (out_fp32) {
+      static_cast<float*>(out)[r * ld_out + c] = acc;
+    } else {
+      static_cast<__nv_bfloat16*>(out)[r * ld_out + c] = __float2bfloat16_rn(acc);
+    }
+  }
+}
+
 std::mutex g_attr_mutex;
 bool g_attr_set[64];
 
@@ -609,6 +635,31 @@ rlk_status rlk_det_linear_backward(const void* dY, int dy_dtype, int64_t M, int6
   // dX [M, K] = dY . W (the forward configuration); dW [N, K] = dY^T . X (dY on the left)
   return run_two(t, Kind::kFwd, M, K, N, dX, dx_dtype, lddx, /*db_x2_is_left=*/false, N, K, dW,
                  dw_dtype, lddw, workspace, workspace_bytes, stream);
+}
+
+rlk_status rlk_sum_partials_ordered(const float* partials, int64_t num_parts, int64_t rows,
+                                    int64_t cols, int64_t ld_partial, int64_t part_stride,
+                                    void* out, int out_dtype, int64_t ld_out, void* stream) {
+  if (!dtype_ok(out_dtype)) return RLK_ERR_DTYPE;
+  if (num_parts < 1 || num_parts >= kDimLimit || rows < 0 || rows >= kMaxExtent || cols < 1 ||
+      cols >= kMaxExtent || ld_partial < cols || ld_partial >= kLdLimit || ld_out < cols ||
+      ld_out >= kLdLimit || part_stride < 0 || (num_parts > 1 && part_stride < rows * ld_partial))
+    return RLK_ERR_SHAPE;
+  if (rows == 0) return RLK_OK;
+  if (!partials || !out) return RLK_ERR_NULL;
+  if (!ptr_aligned(partials, 4) || !ptr_aligned(out, esize(out_dtype))) return RLK_ERR_ALIGN;
+  DeviceInfo dev;
+  rlk_status st = device_ready(&dev);
+  if (st != RLK_OK) return st;
+  const int64_t blocks = ceil_div(rows * cols, 256);
+  const int grid = (int)(blocks < 8 * (int64_t)dev.sm_count ? blocks : 8 * (int64_t)dev.sm_count);
+  if (launch_overlapped(ordered_sum_kernel, grid, 256, 0, static_cast<cudaStream_t>(stream),
+                        partials, num_parts, rows, cols, ld_partial, part_stride, out,
+                        out_dtype == RLK_FP32 ? 1 : 0, ld_out) != cudaSuccess) {
+    cudaGetLastError();
+    return RLK_ERR_CUDA;
+  }
+  return RLK_OK;
 }
 
 }  // extern "C"

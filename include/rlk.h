@@ -556,6 +556,26 @@ RLK_API rlk_status rlk_det_gemm_backward(const void* dC, int dc_dtype, int64_t M
                                          void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Fixed-order sum of per-device partial results: the cross-device step of a dB
+ * whose rows are divided between devices, where each device's partial product is
+ * gathered and the parts are added in a fixed device order (a ring all-reduce
+ * would add them in an order that depends on the ring):
+ *   out[r, c] = part_0[r, c] + part_1[r, c] + ... + part_{P-1}[r, c]
+ * added in FP32 (round to nearest) in ascending part order and written as FP32
+ * or BF16 (round to nearest even).  Part p starts at partials + p * part_stride
+ * (elements, >= rows * ld_partial when P > 1), row pitch ld_partial; out has
+ * pitch ld_out and must not overlap the partials.  The result is bitwise
+ * reproducible and the same on every device that runs it on the same gathered
+ * partials; it depends on how the rows were divided (the order of the sum), so
+ * it may differ in the last bits from one rlk_det_gemm_db over all rows.
+ * rows == 0 is a no-op.  P must be >= 1.
+ */
+RLK_API rlk_status rlk_sum_partials_ordered(const float* partials, int64_t num_parts,
+                                            int64_t rows, int64_t cols, int64_t ld_partial,
+                                            int64_t part_stride, void* out, int out_dtype,
+                                            int64_t ld_out, void* stream);
+
+/*
  * C[M, N] += A[M, K] . B[K, N] with C in FP32 — the accumulate-into-FP32 forward
  * [P1 Implementation: forward_accum_fp32].  Reading taken: the product is formed
  * exactly as by rlk_det_gemm_fwd (same tiles, same ascending K order) and the

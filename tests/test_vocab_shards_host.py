@@ -138,3 +138,13 @@ def test_exchange_gathers_in_rank_order_world2():
     for rank in range(world):
         gp, gz = out[rank]
         assert gp == want_p and gz == want_z
+
+
+def test_ordered_sum_validates_before_any_device_use(lib):
+    f = lib.rlk_sum_partials_ordered
+    assert f(P16, 0, 4, 4, 4, 16, P16, 1, 4, None) == 2          # no parts
+    assert f(P16, 2, 4, 4, 4, 15, P16, 1, 4, None) == 2          # parts overlap
+    assert f(P16, 2, 4, 4, 3, 16, P16, 1, 4, None) == 2          # pitch below the columns
+    assert f(P16, 2, 4, 4, 4, 16, P16, 5, 4, None) == 3          # unknown dtype
+    assert f(ctypes.c_void_p(0x10002), 2, 4, 4, 4, 16, P16, 1, 4, None) == 4
+    assert f(P16, 2, 0, 4, 4, 0, P16, 1, 4, None) == 0           # no rows: nothing to do
