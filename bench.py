@@ -47,18 +47,24 @@ def load_peaks():
 
 
 # ---------------------------------------------------------------- measured traffic
-KERNEL_SOURCES = ["rlk_device.cuh", "rlk_pipeline.cuh", "rlk_solo.cuh", "linear_logp.cu", "det_gemm.cu", "common.cu"]
-# (linear_logp_bwd.cu is not hashed: it launches none of the kernels whose traffic is recorded)
+# The source files each recorded kernel is built from (its translation unit and the
+# headers that define its loops, schedule and launch).
+_COMMON = ["rlk_device.cuh", "rlk_pipeline.cuh", "rlk_internal.h", "common.cu"]
+KERNEL_SOURCES = {
+    "linear_logp_partials_kernel": _COMMON + ["rlk_solo.cuh", "linear_logp.cu"],
+    "linear_logp_solo_kernel": _COMMON + ["rlk_solo.cuh", "linear_logp.cu"],
+    "det_gemm_kernel": _COMMON + ["det_gemm.cu"],
+}
 
 
-def kernel_sources_sha256() -> str:
-    """Hash of the kernel sources' code: comments and whitespace are dropped, so
-    editing a comment does not invalidate the recorded captures."""
+def kernel_sources_sha256(kernel: str) -> str:
+    """Hash of the code of the files `kernel` is built from: comments and whitespace
+    are dropped, so editing a comment does not invalidate the recorded captures."""
     import hashlib
     import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "deterministic_invariant_gemm_linear_gb300", "csrc")
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, name)) as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
@@ -69,12 +75,12 @@ def kernel_sources_sha256() -> str:
 
 def measured_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu capture, or None when there is
-    none for this kernel / workload or the kernel sources changed since."""
+    none for this kernel / workload or the kernel's sources changed since."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     rec = json.load(open(p)).get(f"{kernel}@{workload}")
-    if not rec or rec.get("sources_sha256") != kernel_sources_sha256():
+    if not rec or rec.get("sources_sha256") != kernel_sources_sha256(kernel):
         return None
     return rec["dram_bytes_per_launch"]
 
