@@ -197,6 +197,207 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// ---- Two products in one launch --------------------------------------------
+// The linear-logp backward needs grad_hidden = G . W (the forward configuration,
+// a few very long tiles: K = V) and grad_weight = G^T . hidden (the dB
+// configuration, many short tiles).  Run apart, the long product leaves most SM
+// pairs idle in its last wave.  Here both products' 256 x 256 tiles form one
+// unit list, the product with the longer reduction first, handed out in order
+// from one counter, so the short tiles fill the pairs the long ones leave idle.  Each tile is computed
+// exactly as by det_gemm_kernel (same operands, same ascending reduction), so
+// the outputs are the same bits as the two separate launches.
+struct DualSched {
+  Banded order1, order2;   // output blocks of product 1 and product 2
+  int two_first;           // 1: product 2's units come first (its reduction is longer)
+  int* counter;            // zeroed unit counter (ordered hand-out)
+  int nkb1, nkb2;          // 64-wide reduction blocks of each product
+  __device__ __forceinline__ int num_units() const { return order1.count() + order2.count(); }
+  __device__ __forceinline__ int unit_tiles(int) const { return 1; }
+  __device__ __forceinline__ bool second(int u) const {
+    return two_first ? u < order2.count() : u >= order1.count();
+  }
+  __device__ __forceinline__ int unit_nkb(int u) const { return second(u) ? nkb2 : nkb1; }
+  __device__ __forceinline__ void tile_coords(int u, int, int& a0, int& b0) const {
+    int mb, nb;
+    if (second(u))
+      order2.unit(two_first ? u : u - order1.count(), mb, nb);
+    else
+      order1.unit(two_first ? u - order2.count() : u, mb, nb);
+    a0 = mb * kPairRows;
+    b0 = nb * kBN;
+  }
+};
+
+// The TMA producer of the two-product loop (see producer_role): the unit's
+// product selects the tensor maps and the operand layouts.
+template <class TA1, class TB1, class TA2, class TB2>
+__device__ __forceinline__ void dual_producer(const CUtensorMap* ta1, const CUtensorMap* tb1,
+                                              const CUtensorMap* ta2, const CUtensorMap* tb2,
+                                              const DualSched& sc, const PipeSmem& ps,
+                                              unsigned int* err) {
+  using R = PairRing;
+  static_assert(TA1::kBytes == R::kABytes && TB1::kBytes == R::kBBytes &&
+                    TA2::kBytes == R::kABytes && TB2::kBytes == R::kBBytes,
+                "operand halves fit the ring");
+  constexpr int kStages = R::kStages;
+  int stage = 0;
+  uint32_t phase = 0, issued = 0, last_parity = 0;
+  bool run = true;
+  const int32_t half = (int32_t)ps.rank * kHalfRows;
+  for (int k = 0; run; ++k) {
+    const int u = unit_take(sc, ps, k, err);
+    if (u < 0) {
+      run = u != kUnitAbort;
+      break;
+    }
+    const bool two = sc.second(u);
+    const int nkb = sc.unit_nkb(u);
+    int a0, b0;
+    sc.tile_coords(u, 0, a0, b0);
+    for (int kb = 0; kb < nkb; ++kb) {
+      if (!mbar_wait(ps.empty(stage), phase ^ 1u, ps.abort_flag(), err)) {
+        run = false;
+        break;
+      }
+      if (ps.rank == 0) mbar_arrive_expect_tx(ps.full(stage), R::kTxBytes);
+      const uint32_t leader_full = mapa_shared(ps.full(stage), 0);
+      const uint32_t sa = R::a_stage(ps.stages, stage), sb = R::b_stage(ps.stages, stage);
+      if (two) {
+        TA2::template load<true>(sa, ta2, leader_full, a0 + half, kb * kBK);
+        TB2::template load<true>(sb, tb2, leader_full, b0 + half, kb * kBK);
+      } else {
+        TA1::template load<true>(sa, ta1, leader_full, a0 + half, kb * kBK);
+        TB1::template load<true>(sb, tb1, leader_full, b0 + half, kb * kBK);
+      }
+      issued |= 1u << stage;
+      last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  griddep_launch_dependents();
+  if (ps.rank == 0) {
+    for (int s = 0; s < kStages; ++s)
+      if ((issued >> s) & 1u) mbar_wait_drain(ps.full(s), (last_parity >> s) & 1u, err);
+  } else if (!run) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 1000000ull) {
+    }
+  }
+}
+
+// The MMA issuer of the two-product loop (see mma_role).
+template <class TA1, class TB1, class TA2, class TB2>
+__device__ __forceinline__ void dual_mma(const DualSched& sc, const PipeSmem& ps, uint32_t tmem,
+                                         uint32_t idesc1, uint32_t idesc2, unsigned int* err) {
+  using R = PairRing;
+  constexpr int kStages = R::kStages;
+  int stage = 0, acc = 0;
+  uint32_t phase = 0, acc_phase = 0;
+  bool run = true;
+  for (int k = 0; run; ++k) {
+    const int u = unit_take(sc, ps, k, err);
+    if (u < 0) break;
+    const bool two = sc.second(u);
+    const int nkb = sc.unit_nkb(u);
+    if (!mbar_wait(ps.acc_empty(acc), acc_phase ^ 1u, ps.abort_flag(), err)) break;
+    tc_fence_after();
+    const uint32_t d = tmem + acc * kAccCols;
+    for (int kb = 0; kb < nkb; ++kb) {
+      if (!mbar_wait(ps.full(stage), phase, ps.abort_flag(), err)) {
+        run = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sa = R::a_stage(ps.stages, stage), sb = R::b_stage(ps.stages, stage);
+#pragma unroll
+      for (int j = 0; j < kBK / kUmmaK; ++j) {
+        if (two)
+          umma_pair_bf16(d, TA2::desc(sa, j), TB2::desc(sb, j), idesc2, (kb | j) != 0 ? 1u : 0u);
+        else
+          umma_pair_bf16(d, TA1::desc(sa, j), TB1::desc(sb, j), idesc1, (kb | j) != 0 ? 1u : 0u);
+      }
+      umma_pair_commit(ps.empty(stage), 0x3);
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!run) break;
+    umma_pair_commit(ps.acc_full(acc), 0x3);
+    acc ^= 1;
+    if (acc == 0) acc_phase ^= 1u;
+  }
+  umma_pair_commit(smem_u32(&ps.bars->drained), 0x1);
+  mbar_wait_drain(smem_u32(&ps.bars->drained), 0, err);
+}
+
+// Product 1: out1 = A1 . B1 in the forward configuration (A1 K-major, B1 MN-major);
+// product 2: out2 = A2^T . B2 in the dB configuration (both MN-major).
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    det_gemm_fwd_db_kernel(const __grid_constant__ CUtensorMap tm_a1,
+                           const __grid_constant__ CUtensorMap tm_b1,
+                           const __grid_constant__ CUtensorMap tm_a2,
+                           const __grid_constant__ CUtensorMap tm_b2, DualSched sc, GemmOut out1,
+                           GemmOut out2) {
+  extern __shared__ uint8_t smem_raw[];
+  const PipeSmem ps = pipe_smem(smem_raw);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tm_a1);
+    tma_prefetch_desc(&tm_b1);
+    tma_prefetch_desc(&tm_a2);
+    tma_prefetch_desc(&tm_b2);
+  }
+  const uint32_t tmem = pipe_setup(ps);
+  using TA1 = OperandTile<false, kHalfRows>;
+  using TB1 = OperandTile<true, kHalfRows>;
+  using TA2 = OperandTile<true, kHalfRows>;
+  using TB2 = OperandTile<true, kHalfRows>;
+  if (warp == 0) {
+    if (lane == 0)
+      dual_producer<TA1, TB1, TA2, TB2>(&tm_a1, &tm_b1, &tm_a2, &tm_b2, sc, ps, &g_err_det_gemm);
+    if (lane == 1 && ps.rank == 0) scheduler_role(sc, ps, &g_err_det_gemm);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && ps.rank == 0)
+      dual_mma<TA1, TB1, TA2, TB2>(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, false, true),
+                                   idesc_bf16_f32(kPairRows, kBN, true, true), &g_err_det_gemm);
+    __syncwarp();
+  } else {
+    const int q = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int k = 0;; ++k) {
+      const int u = warp_unit_take(sc, ps, k, &g_err_det_gemm);
+      if (u < 0) break;
+      if (!epilogue_acquire(ps, acc, acc_phase, &g_err_det_gemm)) break;
+      const GemmOut& out = sc.second(u) ? out2 : out1;
+      int m0, n0;
+      sc.tile_coords(u, 0, m0, n0);
+      const int row = m0 + (int)ps.rank * kHalfRows + q * 32 + lane;
+      const uint32_t taddr = tmem + acc * kAccCols + lane_off;
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        const int col0 = n0 + c * 32;
+        if (col0 >= out.N) break;               // uniform: depends on the tile only
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(taddr + c * 32, r);
+        tmem_wait_ld();
+        if (row < out.M) store_chunk(out, row, col0, r);
+      }
+      epilogue_release(ps, acc);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+  pipe_teardown(tmem);
+}
+
 std::mutex g_attr_mutex;
 bool g_attr_set[64];
 
@@ -217,6 +418,9 @@ cudaError_t ensure_attrs(int dev) {
     if (e == cudaSuccess) e = set_attr<false, true, 128>();
     if (e == cudaSuccess) e = set_attr<false, false, 128>();
     if (e == cudaSuccess) e = set_attr<true, true, 128>();
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(det_gemm_fwd_db_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemBytes);
     if (e != cudaSuccess) return e;
     g_attr_set[dev] = true;
   }
@@ -478,6 +682,56 @@ rlk_status run_two(TwoProducts t, Kind kind1, int64_t rows1, int64_t cols1, int6
 }
 
 }  // namespace
+
+rlk_status launch_fwd_and_db(const void* G, int64_t N, int64_t V, int64_t ldG, const void* W,
+                             int64_t H, int64_t ldw, void* out1, int dt1, int64_t ld1,
+                             const void* hidden, int64_t ldh, void* out2, int dt2, int64_t ld2,
+                             int* counter, cudaStream_t s) {
+  DeviceInfo dev;
+  rlk_status st = device_ready(&dev);
+  if (st != RLK_OK) return st;
+  if (ensure_attrs(dev.device) != cudaSuccess) return RLK_ERR_CUDA;
+  CUtensorMap ta1, tb1, ta2, tb2;
+  // product 1: [N, H] = G [N, V] (K-major) . W [V, H] (MN-major)
+  // product 2: [V, H] = G^T (G read MN-major, N reduced) . hidden [N, H] (MN-major)
+  if (!encode_bf16_2d(&ta1, G, V, N, ldG, kBK, kHalfRows) ||
+      !encode_bf16_2d(&tb1, W, H, V, ldw, 64, kBK) || !encode_bf16_2d(&ta2, G, V, N, ldG, 64, kBK) ||
+      !encode_bf16_2d(&tb2, hidden, H, N, ldh, 64, kBK))
+    return RLK_ERR_CUDA;
+  DualSched sc;
+  sc.order1.rows = (int)ceil_div(N, kPairRows);
+  sc.order1.cols = (int)ceil_div(H, kBN);
+  sc.order1.band = band_rows(sc.order1.rows, V, kPairRows);
+  sc.order2.rows = (int)ceil_div(V, kPairRows);
+  sc.order2.cols = (int)ceil_div(H, kBN);
+  sc.order2.band = band_rows(sc.order2.rows, N, kPairRows);
+  sc.nkb1 = (int)ceil_div(V, kBK);
+  sc.nkb2 = (int)ceil_div(N, kBK);
+  sc.two_first = sc.nkb2 > sc.nkb1 ? 1 : 0;
+  sc.counter = counter;
+  auto make_out = [](int64_t M, int64_t Ncols, void* C, int dt, int64_t ld) {
+    GemmOut o;
+    o.M = (int)M;
+    o.N = (int)Ncols;
+    o.C = C;
+    o.ldc = ld;
+    o.fp32 = dt == RLK_FP32;
+    o.accum = 0;
+    o.vec_ok = ptr_aligned(C, 16) && ((ld * esize(dt)) % 16) == 0;
+    return o;
+  };
+  const GemmOut o1 = make_out(N, H, out1, dt1, ld1), o2 = make_out(V, H, out2, dt2, ld2);
+  const int64_t units = (int64_t)sc.order1.rows * sc.order1.cols + (int64_t)sc.order2.rows * sc.order2.cols;
+  const int64_t clusters = dev.sm_count / 2;
+  const int grid = 2 * (int)(units < clusters ? units : clusters);
+  if (cudaMemsetAsync(counter, 0, sizeof(int), s) != cudaSuccess ||
+      launch_overlapped(det_gemm_fwd_db_kernel, grid, kThreads, kSmemBytes, s, ta1, tb1, ta2, tb2,
+                        sc, o1, o2) != cudaSuccess) {
+    cudaGetLastError();
+    return RLK_ERR_CUDA;
+  }
+  return RLK_OK;
+}
 
 uint32_t take_error_det_gemm() {
   unsigned int v = 0, zero = 0;

@@ -384,12 +384,17 @@ rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H, in
 
   // The products read G and the (possibly staged) operands, all TMA-ready, so
   // they need no workspace and every argument they check was checked above.
-  if (grad_hidden) {   // [N, H] = G [N, V] . W [V, H]
+  // Both requested: one launch over both products' tiles (same bits as two).
+  if (grad_hidden && grad_weight) {
+    st = launch_fwd_and_db(a.G, N, V, a.ldG, w_src, H, p.ldw, grad_hidden, grad_hidden_dtype,
+                           ld_grad_hidden, h_src, p.ldh, grad_weight, grad_weight_dtype,
+                           ld_grad_weight, reinterpret_cast<int*>(ws + p.off_ctr), s);
+    if (st != RLK_OK) return st;
+  } else if (grad_hidden) {   // [N, H] = G [N, V] . W [V, H]
     st = rlk_det_gemm_fwd(a.G, N, V, a.ldG, w_src, H, p.ldw, grad_hidden, grad_hidden_dtype,
                           ld_grad_hidden, nullptr, 0, stream);
     if (st != RLK_OK) return st;
-  }
-  if (grad_weight) {   // [V, H] = G^T . hidden
+  } else if (grad_weight) {   // [V, H] = G^T . hidden
     st = rlk_det_gemm_db(a.G, N, V, a.ldG, h_src, RLK_BF16, H, p.ldh, grad_weight,
                          grad_weight_dtype, ld_grad_weight, nullptr, 0, stream);
     if (st != RLK_OK) return st;

@@ -93,6 +93,16 @@ inline bool ordered_units(int64_t units, int64_t clusters) {
 constexpr int64_t kVocabTile = 256;
 constexpr int64_t kMaxVocabSplits = 1024;
 
+// grad_hidden-style and grad_weight-style products of one BF16 G in one launch
+// (det_gemm.cu): out1 [N, H] = G [N, V] . W [V, H] and out2 [V, H] = G^T . hidden
+// [N, H], with every tile computed as by rlk_det_gemm_fwd / rlk_det_gemm_db (same
+// bits).  All operands TMA-ready and all arguments validated by the caller;
+// `counter` is a 4-byte slot of device memory the launch zeroes and uses.
+rlk_status launch_fwd_and_db(const void* G, int64_t N, int64_t V, int64_t ldG, const void* W,
+                             int64_t H, int64_t ldw, void* out1, int dt1, int64_t ld1,
+                             const void* hidden, int64_t ldh, void* out2, int dt2, int64_t ld2,
+                             int* counter, cudaStream_t s);
+
 // Per-translation-unit device error words: read-and-clear after a stream sync.
 uint32_t take_error_linear_logp();
 uint32_t take_error_det_gemm();
