@@ -264,7 +264,10 @@ def per_clock(achieved_tflops: float, clocks, device) -> dict:
             "per_clock_ceiling_tflops": ceiling,
             "per_clock_frac": achieved_tflops / ceiling,
             "per_clock_note": f"{sms} SMs x {BF16_FLOP_PER_SM_CLK} dense BF16 FLOP/clk x median "
-                              f"{mhz:.0f} MHz under load"}
+                              f"{mhz:.0f} MHz as NVML reports it; the SMs' own cycle counters read "
+                              "8-20% lower under tensor load (profiles/"
+                              "linear_logp_partials_effective_clock.md), so this understates the "
+                              "work per actual cycle"}
 
 
 # ---------------------------------------------------------------- CPU oracle leg
@@ -545,13 +548,31 @@ def phase_breakdown(rlk, call, flush, K, stream, alg_bytes, peaks):
         used = tr[tr[:, 4] > 0]
         t0 = used[:, 0].min()
         row = {"event_us": e0.elapsed_time(e1) * 1e3, "ctas": int(len(used))}
+        # the clock each CTA ran at: SM cycles between entry and exit over the elapsed ns
+        cyc = used[:, 7] - used[:, 6]
+        ns = used[:, 5] - used[:, 0]
+        ok = (cyc > 0) & (ns > 0)
+        row["sm_clock_mhz_median"] = float(np.median(cyc[ok] / ns[ok])) * 1e3 if ok.any() else None
         for f, n in enumerate(names):
             v = used[:, f]
             v = v[v > 0] - t0
             row[f"{n}_median_us"] = float(np.median(v)) / 1e3
             row[f"{n}_last_us"] = float(v.max()) / 1e3
         per.append(row)
-    out = {k: float(np.median([r[k] for r in per])) for k in per[0]}
+    out = {k: float(np.median([r[k] for r in per if r[k] is not None])) for k in per[0]}
+    # the clock under load: the last of K launches run back to back
+    rlk.debug_trace()
+    for _ in range(K):
+        if flush is not None:
+            flush_l2(flush)
+        call.partials()
+    torch.cuda.synchronize()
+    tr = rlk.debug_trace().astype(np.int64)
+    used = tr[tr[:, 4] > 0]
+    cyc, ns = used[:, 7] - used[:, 6], used[:, 5] - used[:, 0]
+    ok = (cyc > 0) & (ns > 0)
+    out["sm_clock_mhz_under_load"] = float(np.median(cyc[ok] / ns[ok])) * 1e3 if ok.any() else None
+    out["span_under_load_us"] = float(used[:, 5].max() - used[:, 0].min()) / 1e3
     out["hbm_floor_us"] = alg_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6
     out["note"] = ("debug build (store checks on); times from the first CTA's entry; "
                    "event_us - exit_last_us = launch latency and event overhead")

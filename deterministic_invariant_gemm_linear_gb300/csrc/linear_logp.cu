@@ -224,7 +224,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                      const __grid_constant__ CUtensorMap tm_weight, LogpSched sc,
                                      LogpArgs args) {
   extern __shared__ uint8_t smem_raw[];
-  if (threadIdx.x == 0) RLK_TRACE(0);
+  if (threadIdx.x == 0) {
+    RLK_TRACE(0);
+    RLK_TRACE_CYCLES(6);
+  }
   const PipeSmem ps = pipe_smem(smem_raw);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
@@ -248,7 +251,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     logp_epilogue<false>(sc, args, ps, tmem);
   }
   pipe_teardown(tmem);
-  if (threadIdx.x == 0) RLK_TRACE(5);
+  if (threadIdx.x == 0) {
+    RLK_TRACE_CYCLES(7);
+    RLK_TRACE(5);
+  }
 }
 
 // One CTA per unit = (split j, 128-row block) on the one-CTA loop, for calls of
@@ -260,7 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const __grid_constant__ CUtensorMap tm_weight, LogpSched sc,
                             LogpArgs args) {
   extern __shared__ uint8_t smem_raw[];
-  if (threadIdx.x == 0) RLK_TRACE(0);
+  if (threadIdx.x == 0) {
+    RLK_TRACE(0);
+    RLK_TRACE_CYCLES(6);
+  }
   const PipeSmem ps = pipe_smem(smem_raw);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
@@ -284,7 +293,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     logp_epilogue<true>(sc, args, ps, tmem);
   }
   solo_teardown(tmem);
-  if (threadIdx.x == 0) RLK_TRACE(5);
+  if (threadIdx.x == 0) {
+    RLK_TRACE_CYCLES(7);
+    RLK_TRACE(5);
+  }
 }
 
 // (m, s) pair merge with explicit roundings, so merge(a, b) == merge(b, a) bitwise.

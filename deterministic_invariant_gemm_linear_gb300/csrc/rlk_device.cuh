@@ -52,16 +52,23 @@ __device__ __forceinline__ uint64_t globaltimer_ns();
 // current %globaltimer (a later mark of the same field overwrites it).  Each
 // translation unit has its own table; the linear-logp one is read back by
 // rlk_debug_trace_read.  Release builds compile the marks away.
-constexpr int kTraceFields = 6;
+// Fields 6 and 7 hold the SM's cycle counter (clock64) at entry and exit, so that
+// cycles / elapsed ns gives the clock the CTA actually ran at.
+constexpr int kTraceFields = 8;
 constexpr int kTraceCtas = 1024;
 #ifdef RLK_DEBUG
 static __device__ unsigned long long g_trace[kTraceCtas * kTraceFields];
 __device__ __forceinline__ void trace_mark(int field) {
   if (blockIdx.x < kTraceCtas) g_trace[blockIdx.x * kTraceFields + field] = globaltimer_ns();
 }
+__device__ __forceinline__ void trace_cycles(int field) {
+  if (blockIdx.x < kTraceCtas) g_trace[blockIdx.x * kTraceFields + field] = clock64();
+}
 #define RLK_TRACE(field) ::rlk::trace_mark(field)
+#define RLK_TRACE_CYCLES(field) ::rlk::trace_cycles(field)
 #else
 #define RLK_TRACE(field) ((void)0)
+#define RLK_TRACE_CYCLES(field) ((void)0)
 #endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

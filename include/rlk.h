@@ -146,11 +146,12 @@ RLK_API rlk_status rlk_selftest_store_check(void* stream);
  * index: [0] CTA entry, [1] set-up done (barriers, TMEM, wait for the previous
  * kernel), [2] first operand stage landed (seen by the MMA issuer), [3] last MMA of
  * the CTA complete (accumulator handed to the epilogue), [4] last partial
- * written (epilogue), [5] CTA exit; 0 = not recorded.  *n_ctas receives the
+ * written (epilogue), [5] CTA exit; then the SM's cycle counter at [6] entry and
+ * [7] exit (cycles, not ns); 0 = not recorded.  *n_ctas receives the
  * number of records kept (at most RLK_TRACE_MAX_CTAS).  librlk.so returns
  * RLK_ERR_NOT_DEBUG_BUILD.
  */
-#define RLK_TRACE_FIELDS 6
+#define RLK_TRACE_FIELDS 8
 #define RLK_TRACE_MAX_CTAS 1024
 RLK_API rlk_status rlk_debug_trace_read(uint64_t* out, int64_t max_ctas, int64_t* n_ctas);
 

@@ -63,7 +63,8 @@ for N in (17, 300):
     tr = rlk.debug_trace().astype(np.int64)
     used = tr[tr[:, 4] > 0]
     # the fields a CTA recorded (the second CTA of a pair issues no MMAs: no field 2)
-    ordered.append([int(len(used)), all(bool(np.all(np.diff(r[r > 0]) >= 0)) for r in used)])
+    times = used[:, :6]                             # fields 6 and 7 are cycle counts
+    ordered.append([int(len(used)), all(bool(np.all(np.diff(r[r > 0]) >= 0)) for r in times)])
 res["trace"] = ordered
 res["final_word"] = rlk.device_error()
 print(json.dumps(res))
