@@ -636,8 +636,14 @@ def backward_bench(args, dev, rank, world, peaks, peak_src):
     flop_one = 2.0 * N * H * V
     flops = 3 * flop_one
     t_g = t_h_only - t_dh
+    # the library runs both products in one launch when the longer-reduction one
+    # fills at most half of the SM pairs, else as two launches
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    long_tiles = -(-min(N, V) // 256) * -(-H // 256)
+    one_launch = 2 * long_tiles <= sms // 2
     part = {"grad_logits_kernel (by difference)": t_g / K * 1e3,
-            "grad_hidden + grad_weight, one launch (by difference)": (t_local - t_g) / K * 1e3,
+            "grad_hidden + grad_weight (by difference; " + ("one launch)" if one_launch else
+                                                           "two launches)"): (t_local - t_g) / K * 1e3,
             "grad_hidden det_gemm_fwd alone": t_dh / K * 1e3,
             "grad_weight det_gemm_db alone": t_dw / K * 1e3}
     peak = peaks["bf16_tflops"]
@@ -653,11 +659,12 @@ def backward_bench(args, dev, rank, world, peaks, peak_src):
         "kernels_ms": part,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": None,
-                     "kernel": "whole backward step (2 tensor-core launches: G, then both products in one)",
+                     "kernel": "whole backward step (G kernel, then the two products: " +
+                               ("one launch)" if one_launch else "two launches)"),
                      "algorithmic": f"3 x 2*N*H*V = {flops:.4g} FLOP per step",
                      "peak_kind": f"{peak_src} burst bf16"},
         "clocks": clocks.summary(),
-        "gpu_launches": 2 * K,
+        "gpu_launches": (2 if one_launch else 3) * K,
     }
     line["roofline"].update(per_clock(line["roofline"]["achieved"], line["clocks"], dev))
     if rank == 0 and world == 1 and not args.no_cpu:

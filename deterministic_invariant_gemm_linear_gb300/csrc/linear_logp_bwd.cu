@@ -384,20 +384,31 @@ rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H, in
 
   // The products read G and the (possibly staged) operands, all TMA-ready, so
   // they need no workspace and every argument they check was checked above.
-  // Both requested: one launch over both products' tiles (same bits as two).
-  if (grad_hidden && grad_weight) {
+  // Both requested and the longer-reduction product's 256 x 256 tiles fill at
+  // most half of the SM pairs: one launch over both products' tiles, so the
+  // short tiles use the pairs the long ones leave idle (same bits as two
+  // launches).  Measured on GB300 at H = 4096, V = 151,936: N = 512 1.37 vs
+  // 1.67 ms; with a wave or more of long tiles the two products running side by
+  // side were 3 - 4% slower (N = 1024, 2048) or level (N = 4096), so there they
+  // stay apart.
+  const int64_t long_tiles = ceil_div(V >= N ? N : V, kPairRows) * ceil_div(H, kBN);
+  const bool one_launch = 2 * long_tiles <= dev.sm_count / 2;
+  if (grad_hidden && grad_weight && one_launch) {
     st = launch_fwd_and_db(a.G, N, V, a.ldG, w_src, H, p.ldw, grad_hidden, grad_hidden_dtype,
                            ld_grad_hidden, h_src, p.ldh, grad_weight, grad_weight_dtype,
                            ld_grad_weight, reinterpret_cast<int*>(ws + p.off_ctr), s);
     if (st != RLK_OK) return st;
-  } else if (grad_hidden) {   // [N, H] = G [N, V] . W [V, H]
-    st = rlk_det_gemm_fwd(a.G, N, V, a.ldG, w_src, H, p.ldw, grad_hidden, grad_hidden_dtype,
-                          ld_grad_hidden, nullptr, 0, stream);
-    if (st != RLK_OK) return st;
-  } else if (grad_weight) {   // [V, H] = G^T . hidden
-    st = rlk_det_gemm_db(a.G, N, V, a.ldG, h_src, RLK_BF16, H, p.ldh, grad_weight,
-                         grad_weight_dtype, ld_grad_weight, nullptr, 0, stream);
-    if (st != RLK_OK) return st;
+  } else {
+    if (grad_hidden) {   // [N, H] = G [N, V] . W [V, H]
+      st = rlk_det_gemm_fwd(a.G, N, V, a.ldG, w_src, H, p.ldw, grad_hidden, grad_hidden_dtype,
+                            ld_grad_hidden, nullptr, 0, stream);
+      if (st != RLK_OK) return st;
+    }
+    if (grad_weight) {   // [V, H] = G^T . hidden
+      st = rlk_det_gemm_db(a.G, N, V, a.ldG, h_src, RLK_BF16, H, p.ldh, grad_weight,
+                           grad_weight_dtype, ld_grad_weight, nullptr, 0, stream);
+      if (st != RLK_OK) return st;
+    }
   }
   if (grad_bias) {
     const int threads = 256;

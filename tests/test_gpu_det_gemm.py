@@ -262,3 +262,20 @@ def test_tile_widths_give_the_same_bits(dev, out_dtype):
     assert torch.equal(rlk.det_gemm_fwd(A[100:133], B[:, :2000], out_dtype),
                        rlk.det_gemm_fwd(A, B[:, :2000], out_dtype)[100:133])
     assert rlk.device_error() == 0
+
+
+def test_two_product_backward_matches_the_oracle(dev, orc):
+    """dA and dB from one FP32 dC (one shared BF16 rounding) against the FP64 oracle
+    on the BF16 rounding of dC: relative Frobenius <= 1e-5 on sampled rows."""
+    M, K, N = 1000, 768, 640
+    A, B, dC = si.det_gemm_inputs(M, K, N, seed=72, device=dev, dc_dtype=torch.float32)
+    dA, dB = rlk.det_gemm_backward(dC, A, B, torch.float32)
+    torch.cuda.synchronize()
+    d16 = orc.f32_to_bf16_rne(dC.cpu().numpy())
+    ra = sample_rows(M, 24, seed=73)
+    rb = sample_rows(K, 24, seed=74)
+    ref_a = orc.gemm_da(d16, si.bf16_bits(B), rows=ra)
+    ref_b = orc.gemm_db(si.bf16_bits(A), d16, rows=rb)
+    assert rel_fro(dA.cpu().numpy()[ra].astype(np.float64), ref_a) <= GEMM_FP32_REL_FRO
+    assert rel_fro(dB.cpu().numpy()[rb].astype(np.float64), ref_b) <= GEMM_FP32_REL_FRO
+    assert rlk.device_error() == 0

@@ -161,3 +161,20 @@ def test_two_ranks_exchange_through_gloo(dev, N, H, V):
             got = torch.load(os.path.join(d, f"rank{r}.pt"))
             for x, y in zip(ref, got):
                 assert bits_equal(x, y), f"rank {r}"
+
+
+def test_merged_shards_match_the_oracle(dev, orc):
+    """The merged shards against the FP64 oracle directly (|delta| <= 1e-3 on logp and
+    lse, target logit within 1e-4), V = 300,007 (two 256-id tiles per split), three
+    uneven shards, bias, every row."""
+    from helpers import assert_logp_close
+    N, H, V = 200, 512, 300007
+    hidden, weight, b, target = si.linear_logp_inputs(N, H, V, bias=True, seed=71, device=dev)
+    S = rlk.vocab_split_policy(V)[0]
+    logp, lse, zt = run_shards(hidden, weight, target, b, V, [0, 3, 401, S])
+    torch.cuda.synchronize()
+    rlp, rls, rzt = orc.linear_logp(si.bf16_bits(hidden), si.bf16_bits(weight),
+                                    target.cpu().numpy(), b.cpu().numpy())
+    assert_logp_close(logp.cpu().numpy(), lse.cpu().numpy(), rlp, rls, "merged shards")
+    assert float((zt.cpu().double() - torch.from_numpy(rzt)).abs().max()) <= 1e-4
+    assert rlk.device_error() == 0
