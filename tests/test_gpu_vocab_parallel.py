@@ -178,3 +178,21 @@ def test_merged_shards_match_the_oracle(dev, orc):
     assert_logp_close(logp.cpu().numpy(), lse.cpu().numpy(), rlp, rls, "merged shards")
     assert float((zt.cpu().double() - torch.from_numpy(rzt)).abs().max()) <= 1e-4
     assert rlk.device_error() == 0
+
+
+def test_shard_partials_are_batch_invariant(dev):
+    """A shard's partials for a chunk of rows equal the same rows of the shard's
+    partials for the whole batch (1-, 7- and 129-row chunks; one-CTA and 2-SM loops)."""
+    N, H, V = 300, 1024, 151936
+    hidden, weight, b, target = si.linear_logp_inputs(N, H, V, bias=True, seed=75, device=dev)
+    j0, j1 = 100, 250
+    v0, v1 = j0 * 256, j1 * 256
+    w, bb = weight[v0:v1].contiguous(), b[v0:v1].contiguous()
+    full_p, full_z = rlk.linear_logp_shard_partials(hidden, w, target, V, j0, j1, bb)
+    for chunk in (1, 7, 129):
+        for s0 in range(0, N, chunk * 11):
+            rows = slice(s0, min(N, s0 + chunk))
+            p, z = rlk.linear_logp_shard_partials(hidden[rows], w, target[rows], V, j0, j1, bb)
+            assert bits_equal(p, full_p[rows]), f"chunk {chunk} at {s0}"
+            assert bits_equal(z, full_z[rows])
+    assert rlk.device_error() == 0
