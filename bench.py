@@ -1078,6 +1078,76 @@ def shards_bench(args, dev, rank, world, peaks, peak_src):
     return line
 
 
+def secondary_measurements(dev, peaks, steps: int = 10):
+    """Compact measurements of the other workloads, carried by the default line so that
+    they are recorded in the same run: partials kernel times (CUDA events on the
+    launching stream, L2 flushed before each launch when the weight fits in it) for
+    ragged N=17 / 255 and the large workload, the whole tiny call, det_gemm fwd / dA /
+    dB at 4096^3 (L2 flushed) and the mid backward step."""
+    import deterministic_invariant_gemm_linear_gb300 as rlk
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = {}
+
+    def timed(fn, cold):
+        ts = []
+        with ClockSampler(dev) as clocks:
+            for i in range(3 + steps):
+                if cold:
+                    flush_l2(flush)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                if i >= 3:
+                    ts.append(e0.elapsed_time(e1))
+        sm = (clocks.summary() or {}).get("sm_mhz")
+        return float(np.median(ts)), float(np.min(ts)), sm
+
+    for name, w in (("ragged_N17", si.ragged(17)), ("ragged_N255", si.ragged(255)), ("large", si.LARGE),
+                    ("tiny", si.TINY)):
+        hidden, weight, bias, target = si.workload_inputs(w, seed=0, device=dev)
+        call = rlk.LinearLogpCall(hidden, weight, target, bias)
+        cold = weight.numel() * 2 < (512 << 20)
+        med, best, mhz = timed(call if name == "tiny" else call.partials, cold)
+        S = rlk.vocab_split_policy(w.V)[0]
+        alg = 2 * w.V * w.H + 2 * w.N * w.H + 8 * w.N + 8 * w.N * S + 4 * w.N + (4 * w.V if w.bias else 0)
+        flops = 2.0 * w.N * w.H * w.V
+        rec = {"what": ("whole call" if name == "tiny" else "partials kernel") +
+                       (", L2 flushed (write + read) before each" if cold else ", W streamed from HBM"),
+               "ms_median": med, "ms_best": best, "sm_mhz": mhz}
+        if name.startswith("ragged"):
+            rec["hbm_frac"] = alg / (med / 1e3) / 1e9 / peaks["hbm_gbs"]
+        elif name == "large":
+            rec["bf16_frac"] = flops / (med / 1e3) / 1e12 / peaks["bf16_tflops"]
+        out[name] = rec
+        del hidden, weight, bias, target, call
+    A, B, dC = si.det_gemm_inputs(4096, 4096, 4096, seed=0, device=dev)
+    flop = 2.0 * 4096 ** 3
+    dg = {}
+    for op, fn in (("fwd", lambda: rlk.det_gemm_fwd(A, B)), ("da", lambda: rlk.det_gemm_da(dC, B)),
+                   ("db", lambda: rlk.det_gemm_db(A, dC))):
+        med, best, mhz = timed(fn, True)
+        dg[op] = {"ms_median": med, "ms_best": best, "sm_mhz": mhz,
+                  "bf16_frac": flop / (med / 1e3) / 1e12 / peaks["bf16_tflops"]}
+    out["det_gemm_4096"] = dg
+    del A, B, dC
+    w = si.MID
+    hidden, weight, bias, target = si.workload_inputs(w, seed=0, device=dev)
+    g = torch.randn(w.N, device=dev, generator=torch.Generator(device=dev).manual_seed(7))
+    _, lse = rlk.linear_logp(hidden, weight, target, bias)
+    med, best, mhz = timed(lambda: rlk.linear_logp_backward(hidden, weight, target, lse, g,
+                                                       out_dtype=torch.bfloat16), False)
+    out["backward_mid"] = {"ms_median": med, "ms_best": best, "sm_mhz": mhz,
+                           "bf16_frac": 3 * 2.0 * w.N * w.H * w.V / (med / 1e3) / 1e12 /
+                           peaks["bf16_tflops"],
+                           "what": "whole backward call (G kernel + grad_hidden + grad_weight, "
+                                   "outputs allocated by the binding)"}
+    assert rlk.device_error() == 0
+    return out
+
+
 def reference_arm(args):
     """The FP64 CPU oracle as the reference implementation, on a bounded sample.
 
@@ -1142,6 +1212,8 @@ def main():
     ap.add_argument("--shards", type=int, default=2, help="--workload shards: number of shards")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="default workload: skip the compact measurements of the other workloads")
     ap.add_argument("--phases", action="store_true",
                     help="linear-logp: per-phase breakdown of the partials kernel from the debug "
                          "build's trace (needs RLK_LIBRARY=debug)")
@@ -1171,6 +1243,9 @@ def main():
         line = shards_bench(args, dev, rank, world, peaks, src)
     else:
         line = linear_logp_bench(args, dev, rank, world, peaks, src)
+        if (args.workload == "mid" and not args.rows and not args.no_secondary and world == 1
+                and not args.phases):
+            line["secondary"] = secondary_measurements(dev, peaks)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
