@@ -525,6 +525,33 @@ def e2e_linear_logp(w, hidden, weight, target, bias, call, dev, world, K, stream
                           "the previous step's kernels"}
 
 
+def role_counters(used, H):
+    """The debug trace's role cycle counters (fields 8-15) of one launch, as means over
+    the CTAs that recorded them: the MMA issuer's cycles per accumulator tile against
+    the tensor-pipe ideal (4 MMAs of 128 cycles per 64-wide reduction block: a pair's
+    M=256 x N=256 x K=16 and a single CTA's M=128 x N=256 x K=16 MMA both do 2^20
+    FLOP per SM, 8192 dense BF16 FLOP per SM clock), and the fraction of each role's
+    cycles spent waiting."""
+    mma = used[used[:, 10] > 0]
+    load = used[used[:, 13] > 0]
+    epi = used[(used[:, 14] + used[:, 15]) > 0]
+    if len(mma) == 0:
+        return {}
+    ideal = -(-H // 64) * 4 * 128
+    per_tile = mma[:, 10] / np.maximum(mma[:, 11], 1)
+    return {
+        "mma_cycles_per_tile": float(per_tile.mean()),
+        "mma_ideal_cycles_per_tile": float(ideal),
+        "mma_issue_efficiency": float(ideal / per_tile.mean()),
+        "mma_operand_wait_frac": float((mma[:, 8] / mma[:, 10]).mean()),
+        "mma_accumulator_wait_frac": float((mma[:, 9] / mma[:, 10]).mean()),
+        "load_slot_wait_frac": float((load[:, 12] / load[:, 13]).mean()) if len(load) else None,
+        "epilogue_wait_frac": float((epi[:, 14] / (epi[:, 14] + epi[:, 15])).mean()) if len(epi) else None,
+        "epilogue_work_cycles_per_tile": float((epi[:, 15] / np.maximum(
+            mma[:, 11].mean(), 1)).mean()) if len(epi) else None,
+    }
+
+
 def phase_breakdown(rlk, call, flush, K, stream, alg_bytes, peaks):
     """Where a partials launch spends its time, from the debug build's per-CTA phase
     trace (%globaltimer): for K single launches (L2 flushed first when the weight
@@ -558,8 +585,10 @@ def phase_breakdown(rlk, call, flush, K, stream, alg_bytes, peaks):
             v = v[v > 0] - t0
             row[f"{n}_median_us"] = float(np.median(v)) / 1e3
             row[f"{n}_last_us"] = float(v.max()) / 1e3
+        row.update(role_counters(used, call.H))
         per.append(row)
-    out = {k: float(np.median([r[k] for r in per if r[k] is not None])) for k in per[0]}
+    out = {k: float(np.median([r[k] for r in per if r.get(k) is not None])) for k in per[0]
+           if any(r.get(k) is not None for r in per)}
     # the clock under load: the last of K launches run back to back
     rlk.debug_trace()
     for _ in range(K):
@@ -575,7 +604,10 @@ def phase_breakdown(rlk, call, flush, K, stream, alg_bytes, peaks):
     out["span_under_load_us"] = float(used[:, 5].max() - used[:, 0].min()) / 1e3
     out["hbm_floor_us"] = alg_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6
     out["note"] = ("debug build (store checks on); times from the first CTA's entry; "
-                   "event_us - exit_last_us = launch latency and event overhead")
+                   "event_us - exit_last_us = launch latency and event overhead; mma_* / "
+                   "load_* / epilogue_* from the roles' SM cycle counters (the MMA issuer "
+                   "runs ahead of the tensor pipe, so its operand waits include time the "
+                   "pipe is still busy with MMAs already issued)")
     return out
 
 

@@ -39,7 +39,7 @@ STATUS_NAMES = {0: "RLK_OK", 1: "RLK_ERR_NULL", 2: "RLK_ERR_SHAPE", 3: "RLK_ERR_
                 7: "RLK_ERR_CUDA", 8: "RLK_ERR_TIMEOUT", 9: "RLK_ERR_BOUNDS",
                 10: "RLK_ERR_NOT_DEBUG_BUILD"}
 RLK_DEVERR_TIMEOUT, RLK_DEVERR_BOUNDS = 0x1, 0x2
-TRACE_FIELDS, TRACE_MAX_CTAS = 8, 1024
+TRACE_FIELDS, TRACE_MAX_CTAS = 16, 1024
 
 
 class RlkError(RuntimeError):

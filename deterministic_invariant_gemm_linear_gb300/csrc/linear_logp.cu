@@ -169,6 +169,7 @@ __device__ __forceinline__ void logp_epilogue(const LogpSched& sc, const LogpArg
   int acc = 0;
   uint32_t acc_phase = 0;
   bool run = true;
+  long long c_wait = 0, c_work = 0;                         // debug-build counters
   for (int k = 0; run; ++k) {
     const int u = kSolo ? solo_unit(sc, k) : warp_unit_take(sc, ps, k, &g_err_linear_logp);
     if (u < 0) break;
@@ -181,10 +182,13 @@ __device__ __forceinline__ void logp_epilogue(const LogpSched& sc, const LogpArg
     bool have_zt = false;
     const int t0 = sc.first_tile(u), nt = sc.unit_tiles(u);
     for (int i = 0; i < nt; ++i) {
+      const long long c0 = RLK_CYCLES();
       if (!epilogue_acquire(ps, acc, acc_phase, &g_err_linear_logp)) {
         run = false;
         break;
       }
+      const long long c1 = RLK_CYCLES();
+      c_wait += c1 - c0;
       if (threadIdx.x == 64) RLK_TRACE(3);     // an accumulator is complete
       const int v0 = (sc.tile0 + t0 + i) * kBN;   // global vocabulary id of the tile
       const uint32_t taddr = tmem + acc * kAccCols + lane_off;
@@ -199,6 +203,7 @@ __device__ __forceinline__ void logp_epilogue(const LogpSched& sc, const LogpArg
         const float* bias = args.bias ? args.bias + (vbase - args.v_off) : nullptr;
         logp_chunk(r, vbase, args.V, bias, args.bias_vec4, tgt, m, s, have_zt, zt);
       }
+      c_work += RLK_CYCLES() - c1;
       if (kSolo)
         solo_release(ps, acc);
       else
@@ -214,6 +219,10 @@ __device__ __forceinline__ void logp_epilogue(const LogpSched& sc, const LogpArg
         args.ws_zt[row] = zt;
     }
     if (threadIdx.x == 64) RLK_TRACE(4);       // the unit's partials are written
+  }
+  if (threadIdx.x == 64) {
+    RLK_TRACE_SET(kTraceEpiAccWait, c_wait);
+    RLK_TRACE_SET(kTraceEpiWork, c_work);
   }
 }
 

@@ -53,9 +53,20 @@ __device__ __forceinline__ uint64_t globaltimer_ns();
 // translation unit has its own table; the linear-logp one is read back by
 // rlk_debug_trace_read.  Release builds compile the marks away.
 // Fields 6 and 7 hold the SM's cycle counter (clock64) at entry and exit, so that
-// cycles / elapsed ns gives the clock the CTA actually ran at.
-constexpr int kTraceFields = 8;
+// cycles / elapsed ns gives the clock the CTA actually ran at.  Fields 8 - 15 are
+// the roles' cycle counters (kTraceMma... below), each written once when its role
+// finishes.  RLK_CYCLES() reads the cycle counter in the debug build and is the
+// constant 0 in release builds, where the counter arithmetic folds away.
+constexpr int kTraceFields = 16;
 constexpr int kTraceCtas = 1024;
+constexpr int kTraceMmaOperandWait = 8;    // MMA issuer: cycles waiting for operand stages
+constexpr int kTraceMmaAccWait = 9;        // MMA issuer: cycles waiting for a free accumulator
+constexpr int kTraceMmaCycles = 10;        // MMA issuer: cycles from its first unit to its last MMA
+constexpr int kTraceMmaTiles = 11;         // MMA issuer: accumulator tiles issued
+constexpr int kTraceLoadSlotWait = 12;     // producer: cycles waiting for free ring slots
+constexpr int kTraceLoadCycles = 13;       // producer: cycles from its first unit to its last copy
+constexpr int kTraceEpiAccWait = 14;       // epilogue thread 64: cycles waiting for accumulators
+constexpr int kTraceEpiWork = 15;          // epilogue thread 64: cycles reading and folding them
 #ifdef RLK_DEBUG
 static __device__ unsigned long long g_trace[kTraceCtas * kTraceFields];
 __device__ __forceinline__ void trace_mark(int field) {
@@ -64,11 +75,18 @@ __device__ __forceinline__ void trace_mark(int field) {
 __device__ __forceinline__ void trace_cycles(int field) {
   if (blockIdx.x < kTraceCtas) g_trace[blockIdx.x * kTraceFields + field] = clock64();
 }
+__device__ __forceinline__ void trace_set(int field, long long v) {
+  if (blockIdx.x < kTraceCtas) g_trace[blockIdx.x * kTraceFields + field] = (unsigned long long)v;
+}
 #define RLK_TRACE(field) ::rlk::trace_mark(field)
 #define RLK_TRACE_CYCLES(field) ::rlk::trace_cycles(field)
+#define RLK_TRACE_SET(field, v) ::rlk::trace_set((field), (v))
+#define RLK_CYCLES() ((long long)clock64())
 #else
 #define RLK_TRACE(field) ((void)0)
 #define RLK_TRACE_CYCLES(field) ((void)0)
+#define RLK_TRACE_SET(field, v) ((void)(v))
+#define RLK_CYCLES() 0ll
 #endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

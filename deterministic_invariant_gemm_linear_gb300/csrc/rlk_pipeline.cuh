@@ -353,6 +353,8 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* ta, const CUten
   bool run = true;
   const int32_t half = (int32_t)ps.rank * kHalfRows;         // this CTA's left-operand rows
   const int32_t half_b = (int32_t)ps.rank * R::kBHalf;       // and right-operand rows
+  const long long c_begin = RLK_CYCLES();                   // debug-build counters
+  long long c_slot = 0;
   for (int k = 0; run; ++k) {
     const int u = unit_take(sc, ps, k, err);
     if (u < 0) {
@@ -364,10 +366,12 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* ta, const CUten
       int a0, b0;
       sc.tile_coords(u, i, a0, b0);
       for (int kb = 0; kb < sc.nkb; ++kb) {
+        const long long c0 = RLK_CYCLES();
         if (!mbar_wait(ps.empty(stage), phase ^ 1u, ps.abort_flag(), err)) {
           run = false;
           break;
         }
+        c_slot += RLK_CYCLES() - c0;
         if (ps.rank == 0) mbar_arrive_expect_tx(ps.full(stage), R::kTxBytes);
         const uint32_t leader_full = mapa_shared(ps.full(stage), 0);
         TA::template load<true>(R::a_stage(ps.stages, stage), ta, leader_full, a0 + half,
@@ -383,6 +387,8 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* ta, const CUten
       }
     }
   }
+  RLK_TRACE_SET(kTraceLoadSlotWait, c_slot);
+  RLK_TRACE_SET(kTraceLoadCycles, RLK_CYCLES() - c_begin);
   // No more units for this CTA: the next kernel in the stream may start its
   // prologue on the SMs this grid frees from here on (it waits for this grid
   // to complete before it touches memory).  Signalling only now keeps its
@@ -409,23 +415,31 @@ __device__ __forceinline__ void mma_role(const Sched& sc, const PipeSmem& ps, ui
   int stage = 0, acc = 0;
   uint32_t phase = 0, acc_phase = 0;
   bool run = true;
+  const long long c_begin = RLK_CYCLES();                   // debug-build counters
+  long long c_operand = 0, c_acc = 0, tiles = 0;
   for (int k = 0; run; ++k) {
     const int u = unit_take(sc, ps, k, err);
     if (u < 0) break;
     const int nt = sc.unit_tiles(u);
     for (int i = 0; run && i < nt; ++i) {
+      long long c0 = RLK_CYCLES();
       if (!mbar_wait(ps.acc_empty(acc), acc_phase ^ 1u, ps.abort_flag(), err)) {
         run = false;
         break;
       }
+      c_acc += RLK_CYCLES() - c0;
       tc_fence_after();
       const uint32_t d = tmem + acc * kAccCols;
       for (int kb = 0; kb < sc.nkb; ++kb) {
+        c0 = RLK_CYCLES();
         if (!mbar_wait(ps.full(stage), phase, ps.abort_flag(), err)) {
           run = false;
           break;
         }
-        if (k == 0 && i == 0 && kb == 0) RLK_TRACE(2);   // the CTA's first stage has landed
+        if (k == 0 && i == 0 && kb == 0)
+          RLK_TRACE(2);                                    // the CTA's first stage has landed
+        else
+          c_operand += RLK_CYCLES() - c0;                  // (the first wait is start-up)
         tc_fence_after();
         const uint32_t sa = R::a_stage(ps.stages, stage);
         const uint32_t sb = R::b_stage(ps.stages, stage);
@@ -440,10 +454,15 @@ __device__ __forceinline__ void mma_role(const Sched& sc, const PipeSmem& ps, ui
       }
       if (!run) break;
       umma_pair_commit(ps.acc_full(acc), 0x3);
+      ++tiles;
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
   }
+  RLK_TRACE_SET(kTraceMmaOperandWait, c_operand);
+  RLK_TRACE_SET(kTraceMmaAccWait, c_acc);
+  RLK_TRACE_SET(kTraceMmaCycles, RLK_CYCLES() - c_begin);
+  RLK_TRACE_SET(kTraceMmaTiles, tiles);
   umma_pair_commit(smem_u32(&ps.bars->drained), 0x1);
   mbar_wait_drain(smem_u32(&ps.bars->drained), 0, err);
 }

@@ -105,6 +105,8 @@ __device__ __forceinline__ void solo_producer(const CUtensorMap* ta, const CUten
   int stage = 0;
   uint32_t phase = 0, issued = 0, last_parity = 0;
   bool run = true;
+  const long long c_begin = RLK_CYCLES();                   // debug-build counters
+  long long c_slot = 0;
   for (int k = 0; run; ++k) {
     const int u = solo_unit(sc, k);
     if (u < 0) break;
@@ -113,10 +115,12 @@ __device__ __forceinline__ void solo_producer(const CUtensorMap* ta, const CUten
       int a0, b0;
       sc.tile_coords(u, i, a0, b0);
       for (int kb = 0; kb < sc.nkb; ++kb) {
+        const long long c0 = RLK_CYCLES();
         if (!mbar_wait(ps.empty(stage), phase ^ 1u, ps.abort_flag(), err)) {
           run = false;
           break;
         }
+        c_slot += RLK_CYCLES() - c0;
         const uint32_t full = ps.full(stage);
         mbar_arrive_expect_tx(full, R::kTxBytes);
         TA::load(R::a_stage(ps.stages, stage), ta, full, a0, kb * kBK);
@@ -130,6 +134,8 @@ __device__ __forceinline__ void solo_producer(const CUtensorMap* ta, const CUten
       }
     }
   }
+  RLK_TRACE_SET(kTraceLoadSlotWait, c_slot);
+  RLK_TRACE_SET(kTraceLoadCycles, RLK_CYCLES() - c_begin);
   griddep_launch_dependents();   // no more units: the next kernel may begin its prologue
   // Every issued copy lands before the CTA can exit.
   for (int s = 0; s < kStages; ++s)
@@ -143,23 +149,31 @@ __device__ __forceinline__ void solo_mma(const Sched& sc, const PipeSmem& ps, ui
   int stage = 0, acc = 0;
   uint32_t phase = 0, acc_phase = 0;
   bool run = true;
+  const long long c_begin = RLK_CYCLES();                   // debug-build counters
+  long long c_operand = 0, c_acc = 0, tiles = 0;
   for (int k = 0; run; ++k) {
     const int u = solo_unit(sc, k);
     if (u < 0) break;
     const int nt = sc.unit_tiles(u);
     for (int i = 0; run && i < nt; ++i) {
+      long long c0 = RLK_CYCLES();
       if (!mbar_wait(ps.acc_empty(acc), acc_phase ^ 1u, ps.abort_flag(), err)) {
         run = false;
         break;
       }
+      c_acc += RLK_CYCLES() - c0;
       tc_fence_after();
       const uint32_t d = tmem + acc * kAccCols;
       for (int kb = 0; kb < sc.nkb; ++kb) {
+        c0 = RLK_CYCLES();
         if (!mbar_wait(ps.full(stage), phase, ps.abort_flag(), err)) {
           run = false;
           break;
         }
-        if (k == 0 && i == 0 && kb == 0) RLK_TRACE(2);   // the CTA's first stage has landed
+        if (k == 0 && i == 0 && kb == 0)
+          RLK_TRACE(2);                                    // the CTA's first stage has landed
+        else
+          c_operand += RLK_CYCLES() - c0;                  // (the first wait is start-up)
         tc_fence_after();
         const uint32_t sa = R::a_stage(ps.stages, stage);
         const uint32_t sb = R::b_stage(ps.stages, stage);
@@ -174,10 +188,15 @@ __device__ __forceinline__ void solo_mma(const Sched& sc, const PipeSmem& ps, ui
       }
       if (!run) break;
       umma_commit(ps.acc_full(acc));
+      ++tiles;
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
   }
+  RLK_TRACE_SET(kTraceMmaOperandWait, c_operand);
+  RLK_TRACE_SET(kTraceMmaAccWait, c_acc);
+  RLK_TRACE_SET(kTraceMmaCycles, RLK_CYCLES() - c_begin);
+  RLK_TRACE_SET(kTraceMmaTiles, tiles);
   // Every MMA issued above completes before the CTA frees TMEM.
   umma_commit(smem_u32(&ps.bars->drained));
   mbar_wait_drain(smem_u32(&ps.bars->drained), 0, err);

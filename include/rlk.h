@@ -126,7 +126,8 @@ RLK_API rlk_status rlk_selftest_bounded_wait(uint32_t timeout_us, void* stream);
  * (same ABI, same arithmetic and output bits): there every kernel tests each
  * global store's index against the extent of the buffer it writes; a store
  * outside is skipped and raises RLK_DEVERR_BOUNDS (nothing traps), and the
- * linear-logp kernels record per-CTA phase timestamps (rlk_debug_trace_read).
+ * linear-logp kernels record per-CTA phase timestamps and role cycle counters
+ * (rlk_debug_trace_read).
  * rlk_is_debug_build returns 1 in that build, 0 in librlk.so.
  */
 RLK_API int rlk_is_debug_build(void);
@@ -140,18 +141,26 @@ RLK_API int rlk_is_debug_build(void);
 RLK_API rlk_status rlk_selftest_store_check(void* stream);
 
 /*
- * Debug build: copies the phase timestamps (%globaltimer, ns) that the linear-logp
- * partials kernels recorded since the last read, then clears them.  out receives
+ * Debug build: copies the phase timestamps (%globaltimer, ns) and role cycle
+ * counters that the linear-logp partials kernels recorded since the last read,
+ * then clears them.  out receives
  * max_ctas records of RLK_TRACE_FIELDS uint64 values, indexed by CTA (block)
  * index: [0] CTA entry, [1] set-up done (barriers, TMEM, wait for the previous
  * kernel), [2] first operand stage landed (seen by the MMA issuer), [3] last MMA of
  * the CTA complete (accumulator handed to the epilogue), [4] last partial
  * written (epilogue), [5] CTA exit; then the SM's cycle counter at [6] entry and
- * [7] exit (cycles, not ns); 0 = not recorded.  *n_ctas receives the
+ * [7] exit (cycles, not ns); then per-role SM cycle counts, each written when
+ * the role finishes: the MMA issuer's [8] cycles waiting for operand stages
+ * (after the first), [9] cycles waiting for a free accumulator, [10] cycles from
+ * its first unit to its last MMA issued and [11] accumulator tiles issued (the
+ * issuing CTA of a pair only); the TMA producer's [12] cycles waiting for free
+ * ring slots and [13] cycles from its first unit to its last copy issued; the
+ * first epilogue thread's [14] cycles waiting for complete accumulators and [15]
+ * cycles reading and folding them.  0 = not recorded.  *n_ctas receives the
  * number of records kept (at most RLK_TRACE_MAX_CTAS).  librlk.so returns
  * RLK_ERR_NOT_DEBUG_BUILD.
  */
-#define RLK_TRACE_FIELDS 8
+#define RLK_TRACE_FIELDS 16
 #define RLK_TRACE_MAX_CTAS 1024
 RLK_API rlk_status rlk_debug_trace_read(uint64_t* out, int64_t max_ctas, int64_t* n_ctas);
 

@@ -64,7 +64,13 @@ for N in (17, 300):
     used = tr[tr[:, 4] > 0]
     # the fields a CTA recorded (the second CTA of a pair issues no MMAs: no field 2)
     times = used[:, :6]                             # fields 6 and 7 are cycle counts
-    ordered.append([int(len(used)), all(bool(np.all(np.diff(r[r > 0]) >= 0)) for r in times)])
+    # role counters: every MMA issuer issued tiles, and no wait exceeds its role's span
+    mma = used[used[:, 10] > 0]
+    roles_ok = bool(len(mma) > 0 and np.all(mma[:, 11] > 0) and
+                    np.all(mma[:, 8] + mma[:, 9] <= mma[:, 10]) and
+                    np.all(used[:, 12] <= used[:, 13]) and np.all(used[:, 13] > 0))
+    ordered.append([int(len(used)), all(bool(np.all(np.diff(r[r > 0]) >= 0)) for r in times),
+                    roles_ok, int(len(mma))])
 res["trace"] = ordered
 res["final_word"] = rlk.device_error()
 print(json.dumps(res))
@@ -85,9 +91,12 @@ def test_debug_build_store_checks_and_trace(dev):
     assert res["selftest_status"] == 0
     assert res["selftest_word"] == rlk.RLK_DEVERR_BOUNDS and res["after"] == 0
     # 17 rows: one CTA per vocabulary tile (126); 300 rows: persistent CTA pairs
-    (n17, ok17), (n300, ok300) = res["trace"]
+    (n17, ok17, roles17, mma17), (n300, ok300, roles300, mma300) = res["trace"]
     assert n17 == 126 and ok17
     assert n300 > 0 and ok300
+    # one-CTA loop: every CTA issues its own MMAs; 2-SM loop: one issuer per pair
+    assert roles17 and mma17 == 126
+    assert roles300 and mma300 == n300 // 2
     assert res["final_word"] == 0
 
 
