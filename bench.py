@@ -121,7 +121,7 @@ _NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slow
 
 
 class _Nvml:
-    """Read-only NVML queries through ctypes (the driver's libnvidia-ml): the SM
+    """Read-only NVML queries through ctypes (the NVIDIA driver's libnvidia-ml): the SM
     clock, its maximum and the active clock-event reasons."""
 
     def __init__(self, device: torch.device):

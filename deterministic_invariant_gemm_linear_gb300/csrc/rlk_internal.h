@@ -20,7 +20,7 @@ rlk_status device_ready(DeviceInfo* info);
 
 // 2-D BF16 tensor map with 128-byte swizzle; zero fill outside the tensor.
 // inner = contiguous extent (elements), outer = row count, ld = row pitch
-// (elements).  Returns false when the driver rejects the description.
+// (elements).  Returns false when the CUDA driver rejects the description.
 bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                     uint64_t ld, uint32_t box_inner, uint32_t box_outer);
 
