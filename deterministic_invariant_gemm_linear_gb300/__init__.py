@@ -550,6 +550,43 @@ def linear_logp_backward(hidden: torch.Tensor, weight: torch.Tensor, target: tor
     return out
 
 
+class _LinearLogpGrad(torch.autograd.Function):
+    """Autograd wiring of rlk_linear_logp (forward) and rlk_linear_logp_backward: the
+    forward keeps lse, the backward asks the library for the gradients autograd
+    needs (BF16 for hidden and weight, FP32 for the bias).  lse is returned as a
+    constant: gradients flow through logp only."""
+
+    @staticmethod
+    def forward(ctx, hidden, weight, bias, target):
+        with torch.no_grad():
+            logp, lse = linear_logp(hidden.detach(), weight.detach(), target,
+                                    None if bias is None else bias.detach())
+        ctx.save_for_backward(hidden, weight, bias, target, lse)
+        ctx.mark_non_differentiable(lse)
+        return logp, lse
+
+    @staticmethod
+    def backward(ctx, grad_logp, _grad_lse):
+        hidden, weight, bias, target, lse = ctx.saved_tensors
+        want_h, want_w, want_b = ctx.needs_input_grad[:3]
+        if grad_logp is None or not (want_h or want_w or want_b):
+            return None, None, None, None
+        gh, gw, gb = linear_logp_backward(hidden, weight, target, lse, grad_logp, bias,
+                                          grad_hidden=want_h, grad_weight=want_w,
+                                          grad_bias=bool(want_b and bias is not None))
+        return gh, gw, gb, None
+
+
+def linear_logp_trainable(hidden: torch.Tensor, weight: torch.Tensor, target: torch.Tensor,
+                          bias: torch.Tensor | None = None):
+    """logp, lse as linear_logp, differentiable through logp with respect to hidden,
+    weight and bias (the fused backward: G = g * (onehot(target) - softmax(z)), then
+    grad_hidden = G . W and grad_weight = G^T . hidden in fixed order).  lse carries
+    no gradient.  linear_logp itself stays forward-only and rejects inputs that
+    require grad."""
+    return _LinearLogpGrad.apply(hidden, weight, bias, target)
+
+
 # ------------------------------------------------------------------ det_gemm
 def _gemm_ws(op, x, xdt, xld, y, ydt, yld, device):
     n = lib().rlk_det_gemm_workspace_size(op, _ptr(x), xdt, x.size(0), x.size(1), xld,

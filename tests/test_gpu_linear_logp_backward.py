@@ -269,3 +269,38 @@ def test_backward_fails_closed_on_a_misaligned_output(dev):
     torch.cuda.synchronize()
     assert bool((gh == -7.0).all()) and bool((ws == 0x5A).all())
     assert rlk.device_error() == 0
+
+
+@pytest.mark.parametrize("want", ["all", "hidden", "weight"])
+def test_trainable_autograd_matches_the_backward_entry(dev, want):
+    """linear_logp_trainable under autograd: forward bitwise equal to linear_logp,
+    gradients bitwise equal to linear_logp_backward with the same grad_logp, and
+    only the requested gradients are formed; lse carries no gradient."""
+    hidden, weight, b, target, g = _case(200, 512, 3001, True, seed=11, dev=dev)
+    h = hidden.clone().requires_grad_(want in ("all", "hidden"))
+    w = weight.clone().requires_grad_(want in ("all", "weight"))
+    bb = b.clone().requires_grad_(want == "all")
+    logp, lse = rlk.linear_logp_trainable(h, w, target, bb)
+    assert not lse.requires_grad and logp.requires_grad
+    ref_logp, ref_lse = rlk.linear_logp(hidden, weight, target, b)
+    assert torch.equal(logp.detach(), ref_logp) and torch.equal(lse, ref_lse)
+    (logp * g).sum().backward()
+    dh, dw, db = rlk.linear_logp_backward(hidden, weight, target, ref_lse, g, b)
+    torch.cuda.synchronize()
+    if want in ("all", "hidden"):
+        assert h.grad.dtype == torch.bfloat16 and torch.equal(h.grad, dh)
+    else:
+        assert h.grad is None
+    if want in ("all", "weight"):
+        assert w.grad.dtype == torch.bfloat16 and torch.equal(w.grad, dw)
+    else:
+        assert w.grad is None
+    if want == "all":
+        assert bb.grad.dtype == torch.float32 and torch.equal(bb.grad, db)
+    else:
+        assert bb.grad is None
+    with pytest.raises(RuntimeError):                 # the forward-only entry fails closed
+        if h.requires_grad:
+            rlk.linear_logp(h, weight, target)
+        else:
+            rlk.linear_logp(hidden, w, target)
