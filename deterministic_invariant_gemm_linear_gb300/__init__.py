@@ -16,6 +16,9 @@ Operators (web pages of the RL-Kernel project):
     deterministic gemm kernel": C = A B, dA = dC B^T, dB = A^T dC with FP32
     accumulation in a fixed ascending K order, BF16 or FP32 output; an FP32 dC
     is rounded to BF16 first (that page's review comment).
+  * ``linear_logp_trainable``, ``det_gemm_trainable``, ``det_linear_trainable`` —
+    opt-in torch.autograd wiring of the forward entries to the library's
+    backward entries (gradients bitwise equal to calling those entries).
 """
 from __future__ import annotations
 
@@ -775,3 +778,59 @@ def det_linear_backward(dY: torch.Tensor, X: torch.Tensor, W: torch.Tensor,
     return _two_grads(lib_.rlk_det_linear_backward, lib_.rlk_det_linear_backward_workspace_size, dY,
                       X, W, lambda M, N, K: ((M, K), (N, K)), out_dtype, (grad_x, grad_w),
                       stream)
+
+
+# ------------------------------------------------------------------ autograd wiring
+class _DetGemmGrad(torch.autograd.Function):
+    """C = A . B under autograd: det_gemm_fwd forward; det_gemm_backward for the
+    gradients autograd needs (an FP32 dC, from an FP32-output forward, is rounded
+    to BF16 once before both products)."""
+
+    @staticmethod
+    def forward(ctx, A, B, out_dtype):
+        with torch.no_grad():
+            C = det_gemm_fwd(A.detach(), B.detach(), out_dtype)
+        ctx.save_for_backward(A, B)
+        return C
+
+    @staticmethod
+    def backward(ctx, dC):
+        A, B = ctx.saved_tensors
+        want_a, want_b = ctx.needs_input_grad[:2]
+        if not (want_a or want_b):
+            return None, None, None
+        dA, dB = det_gemm_backward(dC, A, B, grad_a=want_a, grad_b=want_b)
+        return (None if dA is None else dA.reshape(A.shape)), dB, None
+
+
+class _DetLinearGrad(torch.autograd.Function):
+    """Y = X . W^T (W stored [N, K]) under autograd: det_linear forward,
+    det_linear_backward for dX and dW."""
+
+    @staticmethod
+    def forward(ctx, X, W, out_dtype):
+        with torch.no_grad():
+            Y = det_linear(X.detach(), W.detach(), out_dtype)
+        ctx.save_for_backward(X, W)
+        return Y
+
+    @staticmethod
+    def backward(ctx, dY):
+        X, W = ctx.saved_tensors
+        want_x, want_w = ctx.needs_input_grad[:2]
+        if not (want_x or want_w):
+            return None, None, None
+        dX, dW = det_linear_backward(dY, X, W, grad_x=want_x, grad_w=want_w)
+        return (None if dX is None else dX.reshape(X.shape)), dW, None
+
+
+def det_gemm_trainable(A: torch.Tensor, B: torch.Tensor, out_dtype=torch.bfloat16):
+    """det_gemm_fwd(A, B) differentiable with respect to A and B (BF16 gradients from
+    the fixed-order det_gemm backward products)."""
+    return _DetGemmGrad.apply(A, B, out_dtype)
+
+
+def det_linear_trainable(X: torch.Tensor, W: torch.Tensor, out_dtype=torch.bfloat16):
+    """det_linear(X, W) differentiable with respect to X and W: a deterministic,
+    batch-invariant stand-in for a bias-free nn.Linear forward and backward."""
+    return _DetLinearGrad.apply(X, W, out_dtype)

@@ -116,3 +116,33 @@ def test_rows_independent_and_run_to_run(dev):
     # 3-D activations are rows
     Y3 = rlk.det_linear(X.view(10, 100, 768), W, torch.float32)
     assert Y3.shape == (10, 100, 640) and torch.equal(Y3.reshape(1000, 640), full)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_trainable_autograd_matches_the_backward_entries(dev, out_dtype):
+    """det_gemm_trainable / det_linear_trainable under autograd: forwards bitwise
+    equal to det_gemm_fwd / det_linear, gradients bitwise equal to the two-product
+    backward entries with the same upstream gradient (an FP32 one rounded to BF16
+    once), for a 3-D left operand."""
+    g = torch.Generator(device=dev).manual_seed(5)
+    A = (torch.randn(3, 100, 384, generator=g, device=dev) / 20).to(torch.bfloat16)
+    B = (torch.randn(384, 200, generator=g, device=dev) / 20).to(torch.bfloat16)
+    W = (torch.randn(200, 384, generator=g, device=dev) / 20).to(torch.bfloat16)
+    up = torch.randn(3, 100, 200, generator=g, device=dev)
+    a, b, w = (t.clone().requires_grad_() for t in (A, B, W))
+    C = rlk.det_gemm_trainable(a, b, out_dtype)
+    assert torch.equal(C.detach(), rlk.det_gemm_fwd(A, B, out_dtype))
+    (C.float() * up).sum().backward()
+    dC = up.to(out_dtype)
+    dA, dB = rlk.det_gemm_backward(dC, A, B)
+    assert torch.equal(a.grad, dA.reshape(A.shape)) and torch.equal(b.grad, dB)
+    a2 = A.clone().requires_grad_()
+    Y = rlk.det_linear_trainable(a2, w, out_dtype)
+    assert torch.equal(Y.detach(), rlk.det_linear(A, W, out_dtype))
+    (Y.float() * up).sum().backward()
+    dX, dW = rlk.det_linear_backward(up.to(out_dtype), A, W)
+    assert torch.equal(a2.grad, dX.reshape(A.shape)) and torch.equal(w.grad, dW)
+    # only the requested gradient is formed
+    b3 = B.clone().requires_grad_()
+    rlk.det_gemm_trainable(A, b3, out_dtype).float().sum().backward()
+    assert b3.grad is not None and b3.grad.dtype == torch.bfloat16
