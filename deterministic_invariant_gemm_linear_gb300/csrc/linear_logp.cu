@@ -75,44 +75,37 @@ struct LogpArgs {
   int v_off;                  // first vocabulary id of the weight rows read (shard start, or 0)
   int64_t tstride;
   const float* bias;          // [weight rows read] (bias[v - v_off]) or null
-  bool bias_vec4;             // bias is 16-byte aligned: whole chunks read it 4 floats at a time
+  bool bias_vec4;             // bias is 16-byte aligned: a lane reads its 8 floats as 2 vectors
   const int64_t* target;
   float2* ws_ms;              // [N][ld_ms]: (m, s) per row and split of this call
   int64_t ld_ms;
   float* ws_zt;               // [N]: target logit (rows whose target lies in this call's ids)
 };
 
-// One 32-column chunk of a row: bias, vocabulary-tail mask, target capture and
-// the online (m, s) update.  z values are natural-unit logits; each exponential
-// is 2^((z - m) * log2(e)) with z - m formed first, so the running maximum's own
-// term is exactly 2^0 = 1: s >= 1 always, hence lse >= max logit and logp <= 0
-// hold exactly in FP32.
-// `bias` points at the chunk's first id (or is null).
+// One 32-column chunk (chunk c of its tile) of a row: bias, vocabulary-tail mask,
+// target capture and the online (m, s) update.  z values are natural-unit logits;
+// each exponential is 2^((z - m) * log2(e)) with z - m formed first, so the
+// running maximum's own term is exactly 2^0 = 1: s >= 1 always, hence lse >= max
+// logit and logp <= 0 hold exactly in FP32.  Column i's bias comes from the
+// warp's BiasTile (a shuffle: every lane of the warp takes part).
 __device__ __forceinline__ void logp_chunk(const uint32_t (&r)[32], int vbase, int V,
-                                           const float* bias, bool bias_vec4, int64_t tgt,
-                                           float& m, float& s, bool& have_zt, float& zt) {
+                                           bool has_bias, const BiasTile& bias, int c,
+                                           int64_t tgt, float& m, float& s, bool& have_zt,
+                                           float& zt) {
   float z[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) z[i] = __uint_as_float(r[i]);
-  if (bias != nullptr) {
-    if (vbase + 32 <= V && bias_vec4) {
-      // every lane reads the same 128 bytes: 8 vector loads instead of 32 scalar ones
-      const float4* b4 = reinterpret_cast<const float4*>(bias);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 b = __ldg(b4 + i);
-        z[4 * i] = __fadd_rn(z[4 * i], b.x);
-        z[4 * i + 1] = __fadd_rn(z[4 * i + 1], b.y);
-        z[4 * i + 2] = __fadd_rn(z[4 * i + 2], b.z);
-        z[4 * i + 3] = __fadd_rn(z[4 * i + 3], b.w);
-      }
-    } else if (vbase + 32 <= V) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) z[i] = __fadd_rn(z[i], __ldg(bias + i));
-    } else {
+  if (has_bias) {
+    if (vbase + 32 <= V) {
 #pragma unroll
       for (int i = 0; i < 32; ++i)
-        if (vbase + i < V) z[i] = __fadd_rn(z[i], __ldg(bias + i));
+        z[i] = __fadd_rn(z[i], bias_tile_at(bias, c, i));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float b = bias_tile_at(bias, c, i);
+        if (vbase + i < V) z[i] = __fadd_rn(z[i], b);
+      }
     }
   }
   if (vbase + 32 > V) {
@@ -181,7 +174,12 @@ __device__ __forceinline__ void logp_epilogue(const LogpSched& sc, const LogpArg
     float m = -INFINITY, s = 0.f, zt = 0.f;
     bool have_zt = false;
     const int t0 = sc.first_tile(u), nt = sc.unit_tiles(u);
+    const bool has_bias = args.bias != nullptr;
     for (int i = 0; i < nt; ++i) {
+      const int v0 = (sc.tile0 + t0 + i) * kBN;   // global vocabulary id of the tile
+      BiasTile bias;
+      if (has_bias)
+        load_bias_tile(args.bias + (v0 - args.v_off), args.V - v0, args.bias_vec4, lane, bias);
       const long long c0 = RLK_CYCLES();
       if (!epilogue_acquire(ps, acc, acc_phase, &g_err_linear_logp)) {
         run = false;
@@ -190,7 +188,6 @@ __device__ __forceinline__ void logp_epilogue(const LogpSched& sc, const LogpArg
       const long long c1 = RLK_CYCLES();
       c_wait += c1 - c0;
       if (threadIdx.x == 64) RLK_TRACE(3);     // an accumulator is complete
-      const int v0 = (sc.tile0 + t0 + i) * kBN;   // global vocabulary id of the tile
       const uint32_t taddr = tmem + acc * kAccCols + lane_off;
 #pragma unroll 1
       for (int c = 0; c < kBN / 32; ++c) {
@@ -200,8 +197,7 @@ __device__ __forceinline__ void logp_epilogue(const LogpSched& sc, const LogpArg
         __syncwarp();
         tmem_ld32(taddr + c * 32, r);
         tmem_wait_ld();
-        const float* bias = args.bias ? args.bias + (vbase - args.v_off) : nullptr;
-        logp_chunk(r, vbase, args.V, bias, args.bias_vec4, tgt, m, s, have_zt, zt);
+        logp_chunk(r, vbase, args.V, has_bias, bias, c, tgt, m, s, have_zt, zt);
       }
       c_work += RLK_CYCLES() - c1;
       if (kSolo)

@@ -51,7 +51,7 @@ struct GradArgs {
   int N, V;
   int64_t tstride;
   const float* bias;
-  bool bias_vec4;       // bias is 16-byte aligned: whole chunks read it 4 floats at a time
+  bool bias_vec4;       // bias is 16-byte aligned: a lane reads its 8 floats as 2 vectors
   const int64_t* target;
   const float* lse;
   const float* grad;
@@ -90,11 +90,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int k = 0;; ++k) {
       const int u = warp_unit_take(sc, ps, k, &g_err_linear_logp_bwd);
       if (u < 0) break;
-      if (!epilogue_acquire(ps, acc, acc_phase, &g_err_linear_logp_bwd)) break;
       int r0, v0;
       sc.tile_coords(u, 0, r0, v0);
       const int row = r0 + (int)ps.rank * kHalfRows + q * 32 + lane;
       const bool valid = row < a.N;
+      // the row's inputs and the tile's bias are read before the accumulator is
+      // waited for, so their latency hides behind the MMAs
       int64_t t = -1;
       float g = 0.f, L = 0.f;
       if (valid) {
@@ -102,6 +103,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         g = __ldg(a.grad + row);
         L = __ldg(a.lse + row);
       }
+      const bool has_bias = a.bias != nullptr;
+      BiasTile bias;
+      if (has_bias) load_bias_tile(a.bias + v0, a.V - v0, a.bias_vec4, lane, bias);
+      if (!epilogue_acquire(ps, acc, acc_phase, &g_err_linear_logp_bwd)) break;
       // A row whose target is outside [0, V) has no log-probability: zero gradient.
       const bool live = valid && t >= 0 && t < a.V;
       const uint32_t taddr = tmem + acc * kAccCols + lane_off;
@@ -113,28 +118,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
         tmem_ld32(taddr + c * 32, r);
         tmem_wait_ld();
-        float bv[32];
-        if (a.bias != nullptr && a.bias_vec4 && vbase + 32 <= a.V) {
-          const float4* b4 = reinterpret_cast<const float4*>(a.bias + vbase);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 b = __ldg(b4 + i);
-            bv[4 * i] = b.x;
-            bv[4 * i + 1] = b.y;
-            bv[4 * i + 2] = b.z;
-            bv[4 * i + 3] = b.w;
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            bv[i] = (a.bias != nullptr && vbase + i < a.V) ? __ldg(a.bias + vbase + i) : 0.f;
-        }
         float G[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int v = vbase + i;
           float z = __uint_as_float(r[i]);
-          if (a.bias != nullptr && v < a.V) z = __fadd_rn(z, bv[i]);
+          if (has_bias) {
+            const float b = bias_tile_at(bias, c, i);
+            if (v < a.V) z = __fadd_rn(z, b);
+          }
           const float p = ex2_approx(__fmul_rn(__fsub_rn(z, L), kLog2e));
           const float onehot = (int64_t)v == t ? 1.f : 0.f;
           G[i] = (live && v < a.V) ? __fmul_rn(g, __fsub_rn(onehot, p)) : 0.f;

@@ -89,6 +89,45 @@ __device__ __forceinline__ void trace_set(int field, long long v) {
 #define RLK_CYCLES() 0ll
 #endif
 
+// The bias values of one 256-id vocabulary tile spread over a warp: lane l holds
+// entries 8 l .. 8 l + 7 of the tile (0 past its n valid entries).  An epilogue
+// warp loads a tile's values once, before it waits for the tile's accumulator, so
+// the loads' latency hides behind the MMAs instead of stalling every 32-column
+// chunk; each column's value then comes from its lane by shuffle.  vec4: the tile
+// start is 16-byte aligned (a lane reads its 8 values as two vectors).
+struct BiasTile {
+  float q[8];
+};
+
+__device__ __forceinline__ void load_bias_tile(const float* tile, int n, bool vec4, int lane,
+                                               BiasTile& b) {
+  const int e = 8 * lane;
+  if (vec4 && e + 8 <= n) {
+    const float4 x = __ldg(reinterpret_cast<const float4*>(tile + e));
+    const float4 y = __ldg(reinterpret_cast<const float4*>(tile + e) + 1);
+    b.q[0] = x.x;
+    b.q[1] = x.y;
+    b.q[2] = x.z;
+    b.q[3] = x.w;
+    b.q[4] = y.x;
+    b.q[5] = y.y;
+    b.q[6] = y.z;
+    b.q[7] = y.w;
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      b.q[k] = 0.f;
+      if (e + k < n) b.q[k] = __ldg(tile + e + k);
+    }
+  }
+}
+
+// Entry 32 c + i of the tile (i a compile-time index in an unrolled loop); every
+// lane of the warp must take part.
+__device__ __forceinline__ float bias_tile_at(const BiasTile& b, int c, int i) {
+  return __shfl_sync(0xffffffffu, b.q[i & 7], 4 * c + (i >> 3));
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
