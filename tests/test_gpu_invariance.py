@@ -157,8 +157,9 @@ def test_small_call_loops_match_the_pair_loop(dev, n_small):
 
 @pytest.mark.parametrize("N", [17, 300])
 def test_bias_alignment_paths(dev, N):
-    """A 16-byte-aligned bias is read four floats at a time, any other one float at a
-    time; both add the same FP32 values, so the bits agree (one-CTA and 2-SM loops)."""
+    """A 16-byte-aligned bias is read as two 4-float vectors per lane, any other one
+    float at a time (and the 3-id tail tile of V = 32003 always so); both add the same
+    FP32 values, so the bits agree (one-CTA and 2-SM loops)."""
     H, V = 1024, 32003
     hidden, weight, bias, target = si.linear_logp_inputs(N, H, V, bias=True, seed=17, device=dev)
     assert bias.data_ptr() % 16 == 0
