@@ -311,6 +311,21 @@ def flush_l2(buf: torch.Tensor):
 
 
 # ---------------------------------------------------------------- workloads
+def linear_logp_metric(w) -> str:
+    return f"linear-logp tokens/s & TFLOP/s (N={w.N},H={w.H},V={w.V}); % BF16 dense peak"
+
+
+def linear_logp_config(w, world: int) -> dict:
+    """The `config` of a linear-logp line: the same for the GPU arm and the reference arm."""
+    w_bytes = w.V * w.H * 2
+    return {"workload": f"{w.name}: N={w.N} H={w.H} V={w.V}" + (" +bias" if w.bias else "")
+            + ", hidden~N(0,1), W~N(0,1/sqrt(H)), uniform int64 targets, seed=rank",
+            "global_batch": w.N * world, "seq_len": None, "parallelism": f"replicas x{world}",
+            "l2": (f"inputs larger than L2: W {w_bytes / 1e9:.3f} GB streamed per step"
+                   if w_bytes >= (512 << 20) else "L2 flushed (256 MB write, then read) before every "
+                   "step; step time = sum of per-step kernel events")}
+
+
 def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
     import deterministic_invariant_gemm_linear_gb300 as rlk
     if args.workload == "ragged":
@@ -414,17 +429,11 @@ def linear_logp_bench(args, dev, rank, world, peaks, peak_src):
     roof["traffic_unit"] = "bytes per launch (ncu dram read+write)"
     peak = peaks["bf16_tflops"]
     line = {
-        "metric": METRIC if (args.workload == "mid" and not args.rows) else
-        f"linear-logp tokens/s & TFLOP/s (N={w.N},H={w.H},V={w.V}); % BF16 dense peak",
+        "metric": linear_logp_metric(w),
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{w.name}: N={w.N} H={w.H} V={w.V}" + (" +bias" if w.bias else "")
-                   + ", hidden~N(0,1), W~N(0,1/sqrt(H)), uniform int64 targets, seed=rank",
-                   "global_batch": w.N * world, "seq_len": None, "parallelism": f"replicas x{world}",
-                   "l2": (f"inputs larger than L2: W {w_bytes / 1e9:.3f} GB streamed per step"
-                          if flush is None else "L2 flushed (256 MB write, then read) before every step; "
-                          "step time = sum of per-step kernel events")},
+        "config": linear_logp_config(w, world),
         "tflops": flops * world * K / t / 1e12,
         "frac_bf16_peak": flops * K / t_local / 1e12 / peak,
         "kernels_ms": {"linear_logp_partials": part_ms, "linear_logp_combine": comb_ms},
@@ -1218,12 +1227,13 @@ def reference_arm(args):
     value = cores * (Vs / w.V) * args.steps / dt
     sample = (f"{cores} rows x {Vs} of {w.V} vocabulary rows per step of the {w.name} workload "
               f"(full H); reported as full-vocabulary rows/s")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     return {
-        "impl": "reference", "metric": METRIC if args.workload == "mid" else args.workload,
+        "impl": "reference", "metric": linear_logp_metric(w),
         "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{w.name}: N={w.N} H={w.H} V={w.V}", "sample": sample},
+        "config": linear_logp_config(w, world),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
