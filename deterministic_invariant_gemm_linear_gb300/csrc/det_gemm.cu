@@ -334,8 +334,10 @@ __device__ __forceinline__ void dual_mma(const DualSched& sc, const PipeSmem& ps
   mbar_wait_drain(smem_u32(&ps.bars->drained), 0, err);
 }
 
-// Product 1: out1 = A1 . B1 in the forward configuration (A1 K-major, B1 MN-major);
-// product 2: out2 = A2^T . B2 in the dB configuration (both MN-major).
+// Product 1: out1 = A1 . B1 with A1 K-major and B1 MN-major (the forward
+// configuration, kB1MN) or K-major (the dA configuration); product 2:
+// out2 = A2^T . B2 in the dB configuration (both MN-major).
+template <bool kB1MN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     det_gemm_fwd_db_kernel(const __grid_constant__ CUtensorMap tm_a1,
                            const __grid_constant__ CUtensorMap tm_b1,
@@ -353,7 +355,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   const uint32_t tmem = pipe_setup(ps);
   using TA1 = OperandTile<false, kHalfRows>;
-  using TB1 = OperandTile<true, kHalfRows>;
+  using TB1 = OperandTile<kB1MN, kHalfRows>;
   using TA2 = OperandTile<true, kHalfRows>;
   using TB2 = OperandTile<true, kHalfRows>;
   if (warp == 0) {
@@ -363,7 +365,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0 && ps.rank == 0)
-      dual_mma<TA1, TB1, TA2, TB2>(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, false, true),
+      dual_mma<TA1, TB1, TA2, TB2>(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, false, kB1MN),
                                    idesc_bf16_f32(kPairRows, kBN, true, true), &g_err_det_gemm);
     __syncwarp();
   } else {
@@ -419,8 +421,11 @@ cudaError_t ensure_attrs(int dev) {
     if (e == cudaSuccess) e = set_attr<false, false, 128>();
     if (e == cudaSuccess) e = set_attr<true, true, 128>();
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(det_gemm_fwd_db_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSmemBytes);
+      e = cudaFuncSetAttribute(det_gemm_fwd_db_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(det_gemm_fwd_db_kernel<false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     g_attr_set[dev] = true;
   }
@@ -607,10 +612,10 @@ rlk_status check_output(int64_t rows, int64_t cols, const void* C, int c_dtype, 
 // Both products of a backward from one gradient g [M, N]: out1 = g . r1 (kind k1)
 // and out2 = (the kDb product of) x2 and g, with g staged (an FP32 g rounded to
 // BF16, or a misaligned BF16 g copied) once into the workspace and shared.
-// Workspace: [g staged][r1 staged][x2 staged], each 256-byte aligned.
+// Workspace: [g staged][r1 staged][x2 staged][unit counter], each 256-byte aligned.
 struct TwoProducts {
   Operand g, r1, x2;
-  size_t total = 0;
+  size_t off_ctr = 0, total = 0;
 };
 
 rlk_status plan_two(TwoProducts& t) {
@@ -622,7 +627,8 @@ rlk_status plan_two(TwoProducts& t) {
   plan_operand(t.g, off);
   plan_operand(t.r1, off);
   plan_operand(t.x2, off);
-  t.total = off;
+  t.off_ctr = align_up(off, 256);
+  t.total = t.off_ctr + 256;
   return RLK_OK;
 }
 
@@ -641,7 +647,7 @@ rlk_status run_two(TwoProducts t, Kind kind1, int64_t rows1, int64_t cols1, int6
   if (!ptr_aligned(t.g.ptr, esize(t.g.dtype)) || !ptr_aligned(t.r1.ptr, 2) ||
       !ptr_aligned(t.x2.ptr, 2))
     return RLK_ERR_ALIGN;
-  if (t.total > 0 && (!workspace || !ptr_aligned(workspace, 16) || workspace_bytes < t.total))
+  if (!workspace || !ptr_aligned(workspace, 16) || workspace_bytes < t.total)
     return RLK_ERR_WORKSPACE;
   DeviceInfo dev;
   if ((st = device_ready(&dev)) != RLK_OK) return st;
@@ -666,6 +672,42 @@ rlk_status run_two(TwoProducts t, Kind kind1, int64_t rows1, int64_t cols1, int6
     const int64_t ld = ops[i].staged ? ops[i].eff_ld : ops[i].ld;
     ops[i] = Operand{p, RLK_BF16, ops[i].rows, ops[i].cols, ld};
   }
+  // Both products wanted, each filling at least one wave of SM pairs with 256 x 256
+  // tiles, reductions within a factor of two: one launch over both tile lists, so
+  // the tiles of the second product fill the pairs the first one's last wave leaves
+  // idle (same bits; measured at 4096^3: 157 vs 167 us with a BF16 gradient; with
+  // fewer tiles, or very unequal reductions, two launches were as fast or faster).
+  const int64_t pairs = dev.sm_count / 2;
+  const int64_t tiles1 = ceil_div(rows1, kPairRows) * ceil_div(cols1, kBN);
+  const int64_t tiles2 = ceil_div(rows2, kPairRows) * ceil_div(cols2, kBN);
+  const int64_t red_lo = red1 < M ? red1 : M, red_hi = red1 < M ? M : red1;
+  if (out1 && out2 && tiles1 >= pairs && tiles2 >= pairs && red_hi <= 2 * red_lo) {
+    TwoProductArgs p;
+    p.a1 = ops[0].ptr;
+    p.lda1 = ops[0].ld;
+    p.b1 = ops[1].ptr;
+    p.ldb1 = ops[1].ld;
+    p.b1_mn = kind1 == Kind::kFwd;
+    p.rows1 = rows1;
+    p.cols1 = cols1;
+    p.red1 = red1;
+    const Operand& left2 = db_x2_is_left ? ops[2] : ops[0];
+    const Operand& right2 = db_x2_is_left ? ops[0] : ops[2];
+    p.a2 = left2.ptr;
+    p.lda2 = left2.ld;
+    p.b2 = right2.ptr;
+    p.ldb2 = right2.ld;
+    p.rows2 = rows2;
+    p.cols2 = cols2;
+    p.red2 = M;
+    p.out1 = out1;
+    p.dt1 = dt1;
+    p.ld1 = ld1;
+    p.out2 = out2;
+    p.dt2 = dt2;
+    p.ld2 = ld2;
+    return launch_two_products(p, reinterpret_cast<int*>(ws + t.off_ctr), s);
+  }
   if (out1) {
     st = run_gemm(kind1, ops[0], ops[1], rows1, cols1, red1, out1, dt1, ld1, nullptr, 0, stream);
     if (st != RLK_OK) return st;
@@ -683,30 +725,30 @@ rlk_status run_two(TwoProducts t, Kind kind1, int64_t rows1, int64_t cols1, int6
 
 }  // namespace
 
-rlk_status launch_fwd_and_db(const void* G, int64_t N, int64_t V, int64_t ldG, const void* W,
-                             int64_t H, int64_t ldw, void* out1, int dt1, int64_t ld1,
-                             const void* hidden, int64_t ldh, void* out2, int dt2, int64_t ld2,
-                             int* counter, cudaStream_t s) {
+rlk_status launch_two_products(const TwoProductArgs& p, int* counter, cudaStream_t s) {
   DeviceInfo dev;
   rlk_status st = device_ready(&dev);
   if (st != RLK_OK) return st;
   if (ensure_attrs(dev.device) != cudaSuccess) return RLK_ERR_CUDA;
   CUtensorMap ta1, tb1, ta2, tb2;
-  // product 1: [N, H] = G [N, V] (K-major) . W [V, H] (MN-major)
-  // product 2: [V, H] = G^T (G read MN-major, N reduced) . hidden [N, H] (MN-major)
-  if (!encode_bf16_2d(&ta1, G, V, N, ldG, kBK, kHalfRows) ||
-      !encode_bf16_2d(&tb1, W, H, V, ldw, 64, kBK) || !encode_bf16_2d(&ta2, G, V, N, ldG, 64, kBK) ||
-      !encode_bf16_2d(&tb2, hidden, H, N, ldh, 64, kBK))
+  // product 1: [rows1, cols1] = A1 [rows1, red1] (K-major) . B1 ([red1, cols1] MN-major,
+  // or [cols1, red1] K-major); product 2: [rows2, cols2] = A2^T . B2 with A2 [red2, rows2]
+  // and B2 [red2, cols2], both MN-major
+  const bool b1_ok = p.b1_mn ? encode_bf16_2d(&tb1, p.b1, p.cols1, p.red1, p.ldb1, 64, kBK)
+                             : encode_bf16_2d(&tb1, p.b1, p.red1, p.cols1, p.ldb1, kBK, kHalfRows);
+  if (!encode_bf16_2d(&ta1, p.a1, p.red1, p.rows1, p.lda1, kBK, kHalfRows) || !b1_ok ||
+      !encode_bf16_2d(&ta2, p.a2, p.rows2, p.red2, p.lda2, 64, kBK) ||
+      !encode_bf16_2d(&tb2, p.b2, p.cols2, p.red2, p.ldb2, 64, kBK))
     return RLK_ERR_CUDA;
   DualSched sc;
-  sc.order1.rows = (int)ceil_div(N, kPairRows);
-  sc.order1.cols = (int)ceil_div(H, kBN);
-  sc.order1.band = band_rows(sc.order1.rows, V, kPairRows);
-  sc.order2.rows = (int)ceil_div(V, kPairRows);
-  sc.order2.cols = (int)ceil_div(H, kBN);
-  sc.order2.band = band_rows(sc.order2.rows, N, kPairRows);
-  sc.nkb1 = (int)ceil_div(V, kBK);
-  sc.nkb2 = (int)ceil_div(N, kBK);
+  sc.order1.rows = (int)ceil_div(p.rows1, kPairRows);
+  sc.order1.cols = (int)ceil_div(p.cols1, kBN);
+  sc.order1.band = band_rows(sc.order1.rows, p.red1, kPairRows);
+  sc.order2.rows = (int)ceil_div(p.rows2, kPairRows);
+  sc.order2.cols = (int)ceil_div(p.cols2, kBN);
+  sc.order2.band = band_rows(sc.order2.rows, p.red2, kPairRows);
+  sc.nkb1 = (int)ceil_div(p.red1, kBK);
+  sc.nkb2 = (int)ceil_div(p.red2, kBK);
   sc.two_first = sc.nkb2 > sc.nkb1 ? 1 : 0;
   sc.counter = counter;
   auto make_out = [](int64_t M, int64_t Ncols, void* C, int dt, int64_t ld) {
@@ -720,17 +762,36 @@ rlk_status launch_fwd_and_db(const void* G, int64_t N, int64_t V, int64_t ldG, c
     o.vec_ok = ptr_aligned(C, 16) && ((ld * esize(dt)) % 16) == 0;
     return o;
   };
-  const GemmOut o1 = make_out(N, H, out1, dt1, ld1), o2 = make_out(V, H, out2, dt2, ld2);
+  const GemmOut o1 = make_out(p.rows1, p.cols1, p.out1, p.dt1, p.ld1);
+  const GemmOut o2 = make_out(p.rows2, p.cols2, p.out2, p.dt2, p.ld2);
   const int64_t units = (int64_t)sc.order1.rows * sc.order1.cols + (int64_t)sc.order2.rows * sc.order2.cols;
   const int64_t clusters = dev.sm_count / 2;
   const int grid = 2 * (int)(units < clusters ? units : clusters);
-  if (cudaMemsetAsync(counter, 0, sizeof(int), s) != cudaSuccess ||
-      launch_overlapped(det_gemm_fwd_db_kernel, grid, kThreads, kSmemBytes, s, ta1, tb1, ta2, tb2,
-                        sc, o1, o2) != cudaSuccess) {
+  cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(int), s);
+  if (e == cudaSuccess)
+    e = p.b1_mn ? launch_overlapped(det_gemm_fwd_db_kernel<true>, grid, kThreads, kSmemBytes, s,
+                                    ta1, tb1, ta2, tb2, sc, o1, o2)
+                : launch_overlapped(det_gemm_fwd_db_kernel<false>, grid, kThreads, kSmemBytes, s,
+                                    ta1, tb1, ta2, tb2, sc, o1, o2);
+  if (e != cudaSuccess) {
     cudaGetLastError();
     return RLK_ERR_CUDA;
   }
   return RLK_OK;
+}
+
+rlk_status launch_fwd_and_db(const void* G, int64_t N, int64_t V, int64_t ldG, const void* W,
+                             int64_t H, int64_t ldw, void* out1, int dt1, int64_t ld1,
+                             const void* hidden, int64_t ldh, void* out2, int dt2, int64_t ld2,
+                             int* counter, cudaStream_t s) {
+  // [N, H] = G [N, V] . W [V, H] and [V, H] = G^T . hidden [N, H]
+  TwoProductArgs p;
+  p.a1 = G; p.lda1 = ldG; p.b1 = W; p.ldb1 = ldw; p.b1_mn = true;
+  p.rows1 = N; p.cols1 = H; p.red1 = V;
+  p.a2 = G; p.lda2 = ldG; p.b2 = hidden; p.ldb2 = ldh;
+  p.rows2 = V; p.cols2 = H; p.red2 = N;
+  p.out1 = out1; p.dt1 = dt1; p.ld1 = ld1; p.out2 = out2; p.dt2 = dt2; p.ld2 = ld2;
+  return launch_two_products(p, counter, s);
 }
 
 uint32_t take_error_det_gemm() {

@@ -103,6 +103,32 @@ rlk_status launch_fwd_and_db(const void* G, int64_t N, int64_t V, int64_t ldG, c
                              const void* hidden, int64_t ldh, void* out2, int dt2, int64_t ld2,
                              int* counter, cudaStream_t s);
 
+// The general form: out1 [rows1, cols1] = A1 [rows1, red1] (K-major) . B1, with B1
+// [red1, cols1] row-major (b1_mn: the forward configuration) or [cols1, red1]
+// row-major (the dA configuration); out2 [rows2, cols2] = A2^T . B2 with A2
+// [red2, rows2] and B2 [red2, cols2] row-major (the dB configuration).  Each
+// product's tiles are computed exactly as by its own det_gemm launch.
+struct TwoProductArgs {
+  const void* a1 = nullptr;
+  int64_t lda1 = 0;
+  const void* b1 = nullptr;
+  int64_t ldb1 = 0;
+  bool b1_mn = true;
+  int64_t rows1 = 0, cols1 = 0, red1 = 0;
+  const void* a2 = nullptr;
+  int64_t lda2 = 0;
+  const void* b2 = nullptr;
+  int64_t ldb2 = 0;
+  int64_t rows2 = 0, cols2 = 0, red2 = 0;
+  void* out1 = nullptr;
+  int dt1 = 0;
+  int64_t ld1 = 0;
+  void* out2 = nullptr;
+  int dt2 = 0;
+  int64_t ld2 = 0;
+};
+rlk_status launch_two_products(const TwoProductArgs& p, int* counter, cudaStream_t s);
+
 // Per-translation-unit device error words: read-and-clear after a stream sync.
 uint32_t take_error_linear_logp();
 uint32_t take_error_det_gemm();

@@ -552,8 +552,11 @@ RLK_API rlk_status rlk_det_gemm_db(const void* A, int64_t M, int64_t K, int64_t 
  * the workspace, and both products read that copy (likewise a misaligned dC is
  * copied once).  dA or dB may be NULL to skip it.  Every argument of both products
  * is validated before the first launch.  M == 0: dA is empty, dB is written with
- * zeros.  workspace >= rlk_det_gemm_backward_workspace_size(...) bytes (0 when
- * nothing needs staging), 16-byte aligned.
+ * zeros.  When both products are wanted, each fills at least one wave of the SM
+ * pairs with 256 x 256 tiles and their reductions (N and M) are within a factor
+ * of two, both run in one launch over both tile lists (the same bits).
+ * workspace >= rlk_det_gemm_backward_workspace_size(...) bytes (the staged copies
+ * plus a 256-byte unit counter), 16-byte aligned.
  */
 RLK_API size_t rlk_det_gemm_backward_workspace_size(const void* dC, int dc_dtype, int64_t M,
                                                     int64_t N, int64_t lddc, const void* A,

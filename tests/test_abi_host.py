@@ -255,8 +255,10 @@ def test_two_product_backward_validates_before_any_device_use(lib):
     assert f(P16, 1, M, N, N, P16, 0, 1, P16, N, P16, 1, 1, P16, 1, N, P16, 1 << 20, None) == 2
     g = lib.rlk_det_linear_backward
     assert g(P16, 0, M, N, N, P16, K, K, P16, K, P16, 0, K - 1, None, 0, K, P16, 1 << 20, None) == 2
-    # workspace sizes: an FP32 dC is staged once (M x 8 ceil(N/8) BF16), 0 when nothing is staged
+    # workspace sizes: an FP32 dC is staged once (M x 8 ceil(N/8) BF16), then a 256-byte
+    # unit counter (the one-launch form of the two products); the counter alone when
+    # nothing is staged
     ws = lib.rlk_det_gemm_backward_workspace_size
-    assert ws(P16, 1, M, N, N, P16, K, K, P16, N) == M * N * 2
-    assert ws(P16, 0, M, N, N, P16, K, K, P16, N) == 0
+    assert ws(P16, 1, M, N, N, P16, K, K, P16, N) == M * N * 2 + 256
+    assert ws(P16, 0, M, N, N, P16, K, K, P16, N) == 256
     assert ws(P16, 1, M, N, N, P16, 0, 1, P16, N) == 0          # invalid: K = 0

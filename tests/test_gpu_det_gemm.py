@@ -214,12 +214,14 @@ def test_db_empty_reduction_is_zero(dev):
 
 
 @pytest.mark.parametrize("dc_dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("shape", [(300, 200, 520), (1000, 1000, 1000), (33, 33, 33), (0, 64, 96)])
+@pytest.mark.parametrize("shape", [(300, 200, 520), (1000, 1000, 1000), (33, 33, 33), (0, 64, 96),
+                                   (4096, 4096, 4096), (3000, 2500, 2900)])
 def test_two_product_backward_equals_separate_calls(dev, dc_dtype, shape):
     """rlk_det_gemm_backward (one shared BF16 rounding of an FP32 dC) and
     rlk_det_linear_backward give exactly the bits of the separate dA / dB (dX / dW)
     calls, with aligned and staged (odd-pitch) operands, and with M = 0 (empty dA,
-    zero dB)."""
+    zero dB).  The last two shapes give each product at least a wave of tiles with
+    comparable reductions, so both products run in one launch."""
     M, K, N = shape
     A, B, dC = si.det_gemm_inputs(max(M, 1), K, N, seed=M + K + N, device=dev, dc_dtype=dc_dtype)
     A, dC = A[:M], dC[:M]
