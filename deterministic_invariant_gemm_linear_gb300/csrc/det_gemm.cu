@@ -52,8 +52,17 @@ struct GemmOut {
   int64_t ldc;       // elements
   int fp32;          // 1: FP32 output, 0: BF16
   int accum;         // 1: FP32 C += product (C read once, added after the full reduction)
-  int vec_ok;        // 16-byte vector stores allowed (aligned base and pitch)
+  int vec_bytes;     // widest vector store (16, 8 or 4 bytes) the base and pitch allow, or 0
 };
+
+// The widest vector store width (16, 8 or 4 bytes) that both the output's base
+// address and its row pitch are multiples of (a chunk starts at a column that is
+// a multiple of 32, so at a multiple of 64 bytes within its row), 0 for none.
+inline int store_width(const void* C, int64_t ld, int64_t esize) {
+  for (int w = 16; w >= 4; w /= 2)
+    if (reinterpret_cast<uintptr_t>(C) % w == 0 && (ld * esize) % w == 0) return w;
+  return 0;
+}
 
 __device__ __forceinline__ void store_chunk(const GemmOut& o, int row, int col0,
                                             const uint32_t (&r)[32]) {
@@ -62,11 +71,13 @@ __device__ __forceinline__ void store_chunk(const GemmOut& o, int row, int col0,
                         (int64_t)min(col0 + 32, o.N) <= o.ldc,
                     &g_err_det_gemm))
     return;
-  const bool full = o.vec_ok && col0 + 32 <= o.N;
+  // whole chunks go out as the widest vector stores the output allows (the same
+  // values and roundings as element stores); a row's ragged last chunk element-wise
+  const int w = col0 + 32 <= o.N ? o.vec_bytes : 0;
   if (o.fp32) {
     float* dst = static_cast<float*>(o.C) + (int64_t)row * o.ldc + col0;
     if (o.accum) {
-      if (full) {
+      if (w == 16) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           float4 c = reinterpret_cast<const float4*>(dst)[i];
@@ -76,15 +87,27 @@ __device__ __forceinline__ void store_chunk(const GemmOut& o, int row, int col0,
           c.w = __fadd_rn(c.w, __uint_as_float(r[4 * i + 3]));
           reinterpret_cast<float4*>(dst)[i] = c;
         }
+      } else if (w == 8) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float2 c = reinterpret_cast<const float2*>(dst)[i];
+          c.x = __fadd_rn(c.x, __uint_as_float(r[2 * i]));
+          c.y = __fadd_rn(c.y, __uint_as_float(r[2 * i + 1]));
+          reinterpret_cast<float2*>(dst)[i] = c;
+        }
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i)
           if (col0 + i < o.N) dst[i] = __fadd_rn(dst[i], __uint_as_float(r[i]));
       }
-    } else if (full) {
+    } else if (w == 16) {
 #pragma unroll
       for (int i = 0; i < 8; ++i)
         reinterpret_cast<uint4*>(dst)[i] = make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+    } else if (w == 8) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        reinterpret_cast<uint2*>(dst)[i] = make_uint2(r[2 * i], r[2 * i + 1]);
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i)
@@ -92,16 +115,25 @@ __device__ __forceinline__ void store_chunk(const GemmOut& o, int row, int col0,
     }
   } else {
     __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(o.C) + (int64_t)row * o.ldc + col0;
-    if (full) {
+    if (w != 0) {
       uint32_t p[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
         p[i] = *reinterpret_cast<uint32_t*>(&b);
       }
+      if (w == 16) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        reinterpret_cast<uint4*>(dst)[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+        for (int i = 0; i < 4; ++i)
+          reinterpret_cast<uint4*>(dst)[i] = make_uint4(p[4 * i], p[4 * i + 1], p[4 * i + 2], p[4 * i + 3]);
+      } else if (w == 8) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          reinterpret_cast<uint2*>(dst)[i] = make_uint2(p[2 * i], p[2 * i + 1]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) reinterpret_cast<uint32_t*>(dst)[i] = p[i];
+      }
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i)
@@ -571,7 +603,7 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
   o.ldc = ldc;
   o.fp32 = c_dtype == RLK_FP32;
   o.accum = accum ? 1 : 0;
-  o.vec_ok = ptr_aligned(C, 16) && ((ldc * esize(c_dtype)) % 16) == 0;
+  o.vec_bytes = store_width(C, ldc, esize(c_dtype));
   const int64_t units = num_mb * num_nb;
   const int grid = 2 * (int)(units < clusters ? units : clusters);
   constexpr int kWide = PairRingT<kHalfRows>::kSmemBytes, kNarrow = PairRingT<kHalfRows / 2>::kSmemBytes;
@@ -759,7 +791,7 @@ rlk_status launch_two_products(const TwoProductArgs& p, int* counter, cudaStream
     o.ldc = ld;
     o.fp32 = dt == RLK_FP32;
     o.accum = 0;
-    o.vec_ok = ptr_aligned(C, 16) && ((ld * esize(dt)) % 16) == 0;
+    o.vec_bytes = store_width(C, ld, esize(dt));
     return o;
   };
   const GemmOut o1 = make_out(p.rows1, p.cols1, p.out1, p.dt1, p.ld1);
