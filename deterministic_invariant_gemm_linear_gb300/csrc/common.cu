@@ -85,50 +85,145 @@ bool encode_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t
 // ---------------------------------------------------------------- staging kernels
 namespace {
 
+// Rows are dealt to blocks (blockIdx.y, then in steps of gridDim.y) and each row's
+// columns to consecutive threads, so loads and stores are coalesced and no index
+// is divided.  Columns [cols, ld_dst) of dst are zero.
 __global__ void stage_bf16_kernel(const uint16_t* __restrict__ src, int64_t rows, int64_t cols,
                                   int64_t ld_src, uint16_t* __restrict__ dst, int64_t ld_dst) {
-  const int64_t total = rows * ld_dst;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / ld_dst, c = i - r * ld_dst;
-    if (RLK_STORE_OK(i >= 0 && i < rows * ld_dst, &g_err_common))
-      dst[i] = c < cols ? src[r * ld_src + c] : (uint16_t)0;
+  const int64_t c0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  const int64_t cstep = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+    const uint16_t* s = src + r * ld_src;
+    uint16_t* d = dst + r * ld_dst;
+    for (int64_t c = c0; c < ld_dst; c += cstep)
+      if (RLK_STORE_OK(r * ld_dst + c < rows * ld_dst, &g_err_common))
+        d[c] = c < cols ? s[c] : (uint16_t)0;
   }
 }
 
 __global__ void cast_f32_bf16_kernel(const float* __restrict__ src, int64_t rows, int64_t cols,
                                      int64_t ld_src, uint16_t* __restrict__ dst, int64_t ld_dst) {
-  const int64_t total = rows * ld_dst;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / ld_dst, c = i - r * ld_dst;
-    uint16_t v = 0;
-    if (c < cols) {
-      __nv_bfloat16 b = __float2bfloat16_rn(src[r * ld_src + c]);
-      v = *reinterpret_cast<uint16_t*>(&b);
+  const int64_t c0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  const int64_t cstep = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+    const float* s = src + r * ld_src;
+    uint16_t* d = dst + r * ld_dst;
+    for (int64_t c = c0; c < ld_dst; c += cstep) {
+      uint16_t v = 0;
+      if (c < cols) {
+        __nv_bfloat16 b = __float2bfloat16_rn(s[c]);
+        v = *reinterpret_cast<uint16_t*>(&b);
+      }
+      if (RLK_STORE_OK(r * ld_dst + c < rows * ld_dst, &g_err_common)) d[c] = v;
     }
-    if (RLK_STORE_OK(i >= 0 && i < rows * ld_dst, &g_err_common)) dst[i] = v;
   }
 }
 
-int stage_grid(int64_t total) {
-  int64_t g = ceil_div(total, 256);
-  return (int)(g < 4096 ? (g > 0 ? g : 1) : 4096);
+// The same copies, 8 columns per thread: dst rows are 16-byte aligned (a pitch of
+// a multiple of 8 elements from a 16-byte aligned base, as every staged operand's
+// is), so each thread writes one 16-byte vector; it reads its 8 source elements
+// as independent loads (two 16-byte vectors for an aligned FP32 source), so a
+// warp keeps several times more bytes in flight than one element per thread.
+__device__ __forceinline__ uint32_t pack2(uint16_t lo, uint16_t hi) {
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+__global__ void stage_bf16_vec8_kernel(const uint16_t* __restrict__ src, int64_t rows,
+                                       int64_t cols, int64_t ld_src, uint16_t* __restrict__ dst,
+                                       int64_t ld_dst) {
+  const int64_t c0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) * 8;
+  const int64_t cstep = (int64_t)gridDim.x * blockDim.x * 8;
+  for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+    const uint16_t* s = src + r * ld_src;
+    uint16_t* d = dst + r * ld_dst;
+    for (int64_t c = c0; c < ld_dst; c += cstep) {
+      uint16_t v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        v[k] = 0;
+        if (c + k < cols) v[k] = s[c + k];
+      }
+      if (RLK_STORE_OK(r * ld_dst + c + 8 <= rows * ld_dst, &g_err_common))
+        *reinterpret_cast<uint4*>(d + c) =
+            make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
+    }
+  }
+}
+
+__global__ void cast_f32_bf16_vec8_kernel(const float* __restrict__ src, int64_t rows,
+                                          int64_t cols, int64_t ld_src, int src_vec4,
+                                          uint16_t* __restrict__ dst, int64_t ld_dst) {
+  const int64_t c0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) * 8;
+  const int64_t cstep = (int64_t)gridDim.x * blockDim.x * 8;
+  for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+    const float* s = src + r * ld_src;
+    uint16_t* d = dst + r * ld_dst;
+    for (int64_t c = c0; c < ld_dst; c += cstep) {
+      float f[8];
+      if (src_vec4 && c + 8 <= cols) {
+        const float4 x = *reinterpret_cast<const float4*>(s + c);
+        const float4 y = *reinterpret_cast<const float4*>(s + c + 4);
+        f[0] = x.x; f[1] = x.y; f[2] = x.z; f[3] = x.w;
+        f[4] = y.x; f[5] = y.y; f[6] = y.z; f[7] = y.w;
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          f[k] = 0.f;
+          if (c + k < cols) f[k] = s[c + k];
+        }
+      }
+      uint16_t v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        __nv_bfloat16 b = __float2bfloat16_rn(f[k]);
+        v[k] = c + k < cols ? *reinterpret_cast<uint16_t*>(&b) : (uint16_t)0;
+      }
+      if (RLK_STORE_OK(r * ld_dst + c + 8 <= rows * ld_dst, &g_err_common))
+        *reinterpret_cast<uint4*>(d + c) =
+            make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
+    }
+  }
+}
+
+bool dst_vec8(const uint16_t* dst, int64_t ld_dst) {
+  return (reinterpret_cast<uintptr_t>(dst) & 15u) == 0 && ld_dst % 8 == 0;
+}
+
+// Blocks of 256 threads: enough column blocks to cover a row's `units` (elements,
+// or groups of 8) once (at most 64), and row blocks so that about 4096 blocks run
+// (at most 65535, the y limit).
+dim3 stage_grid(int64_t rows, int64_t units) {
+  int64_t gx = ceil_div(units, 256);
+  gx = gx < 1 ? 1 : (gx > 64 ? 64 : gx);
+  int64_t gy = ceil_div(4096, gx);
+  gy = gy > rows ? rows : gy;
+  gy = gy < 1 ? 1 : (gy > 65535 ? 65535 : gy);
+  return dim3((unsigned)gx, (unsigned)gy, 1);
 }
 
 }  // namespace
 
 cudaError_t launch_stage_bf16(const uint16_t* src, int64_t rows, int64_t cols, int64_t ld_src,
                               uint16_t* dst, int64_t ld_dst, cudaStream_t stream) {
-  stage_bf16_kernel<<<stage_grid(rows * ld_dst), 256, 0, stream>>>(src, rows, cols, ld_src, dst,
-                                                                   ld_dst);
+  if (dst_vec8(dst, ld_dst))
+    stage_bf16_vec8_kernel<<<stage_grid(rows, ceil_div(ld_dst, 8)), 256, 0, stream>>>(
+        src, rows, cols, ld_src, dst, ld_dst);
+  else
+    stage_bf16_kernel<<<stage_grid(rows, ld_dst), 256, 0, stream>>>(src, rows, cols, ld_src, dst,
+                                                                    ld_dst);
   return cudaGetLastError();
 }
 
 cudaError_t launch_cast_f32_bf16(const float* src, int64_t rows, int64_t cols, int64_t ld_src,
                                  uint16_t* dst, int64_t ld_dst, cudaStream_t stream) {
-  cast_f32_bf16_kernel<<<stage_grid(rows * ld_dst), 256, 0, stream>>>(src, rows, cols, ld_src, dst,
-                                                                      ld_dst);
+  if (dst_vec8(dst, ld_dst)) {
+    const int src_vec4 = (reinterpret_cast<uintptr_t>(src) & 15u) == 0 && ld_src % 4 == 0;
+    cast_f32_bf16_vec8_kernel<<<stage_grid(rows, ceil_div(ld_dst, 8)), 256, 0, stream>>>(
+        src, rows, cols, ld_src, src_vec4, dst, ld_dst);
+  } else {
+    cast_f32_bf16_kernel<<<stage_grid(rows, ld_dst), 256, 0, stream>>>(src, rows, cols, ld_src,
+                                                                       dst, ld_dst);
+  }
   return cudaGetLastError();
 }
 
