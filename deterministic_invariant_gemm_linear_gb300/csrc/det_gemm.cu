@@ -213,18 +213,21 @@ __global__ void __launch_bounds__(256)
                        int64_t ld_out) {
   griddep_wait();
   if (threadIdx.x == 0) griddep_launch_dependents();
-  const int64_t total = rows * cols;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / cols, c = i - r * cols;
-    const float* p = parts + r * ld_in + c;
-    float acc = __ldg(p);
-    for (int64_t q = 1; q < P; ++q) acc = __fadd_rn(acc, __ldg(p + q * part_stride));
-    if (!RLK_STORE_OK(r < rows && c < cols && c < ld_out, &g_err_det_gemm)) continue;
-    if (out_fp32) {
-      static_cast<float*>(out)[r * ld_out + c] = acc;
-    } else {
-      static_cast<__nv_bfloat16*>(out)[r * ld_out + c] = __float2bfloat16_rn(acc);
+  // rows to blocks (blockIdx.y, then in steps of gridDim.y), a row's columns to
+  // consecutive threads: coalesced, and no index division
+  const int64_t c0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  const int64_t cstep = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+    for (int64_t c = c0; c < cols; c += cstep) {
+      const float* p = parts + r * ld_in + c;
+      float acc = __ldg(p);
+      for (int64_t q = 1; q < P; ++q) acc = __fadd_rn(acc, __ldg(p + q * part_stride));
+      if (!RLK_STORE_OK(r < rows && c < cols && c < ld_out, &g_err_det_gemm)) continue;
+      if (out_fp32) {
+        static_cast<float*>(out)[r * ld_out + c] = acc;
+      } else {
+        static_cast<__nv_bfloat16*>(out)[r * ld_out + c] = __float2bfloat16_rn(acc);
+      }
     }
   }
 }
@@ -998,8 +1001,14 @@ rlk_status rlk_sum_partials_ordered(const float* partials, int64_t num_parts, in
   DeviceInfo dev;
   rlk_status st = device_ready(&dev);
   if (st != RLK_OK) return st;
-  const int64_t blocks = ceil_div(rows * cols, 256);
-  const int grid = (int)(blocks < 8 * (int64_t)dev.sm_count ? blocks : 8 * (int64_t)dev.sm_count);
+  // 256 threads per block: column blocks to cover a row once (at most 64), row
+  // blocks up to about 8 blocks per SM in all (at most 65535)
+  int64_t gx = ceil_div(cols, 256);
+  gx = gx > 64 ? 64 : gx;
+  int64_t gy = ceil_div(8 * (int64_t)dev.sm_count, gx);
+  gy = gy > rows ? rows : gy;
+  gy = gy < 1 ? 1 : (gy > 65535 ? 65535 : gy);
+  const dim3 grid((unsigned)gx, (unsigned)gy, 1);
   if (launch_overlapped(ordered_sum_kernel, grid, 256, 0, static_cast<cudaStream_t>(stream),
                         partials, num_parts, rows, cols, ld_partial, part_stride, out,
                         out_dtype == RLK_FP32 ? 1 : 0, ld_out) != cudaSuccess) {
