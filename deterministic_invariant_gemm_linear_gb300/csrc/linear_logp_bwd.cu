@@ -156,6 +156,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // grad_bias[v] = sum over rows r = 0..N-1 (ascending) of G[r, v], two columns per thread.
+// The row loop is unrolled 64 deep so that many rows' loads are issued before their
+// (still ascending) adds: 0.74 of HBM at the mid shape against 0.54 at depth 8.
 __global__ void __launch_bounds__(256)
     column_sum_bf16_kernel(const uint16_t* __restrict__ G, int N, int V, int64_t ldG,
                            float* __restrict__ out) {
@@ -166,7 +168,7 @@ __global__ void __launch_bounds__(256)
   float s0 = 0.f, s1 = 0.f;
   const uint32_t* p = reinterpret_cast<const uint32_t*>(G + v);
   const int64_t step = ldG / 2;
-#pragma unroll 8
+#pragma unroll 64
   for (int r = 0; r < N; ++r) {
     const uint32_t w = __ldg(p + (int64_t)r * step);
     s0 = __fadd_rn(s0, __uint_as_float(w << 16));
