@@ -774,8 +774,11 @@ def det_gemm_bench(args, dev, rank, world, peaks, peak_src):
     dC32 = dC.float()
     extra = [("linear_fwd", lambda: rlk.det_linear(A, W)), ("linear_dx", lambda: rlk.det_linear_dx(dC, W)),
              ("linear_dw", lambda: rlk.det_linear_dw(dC, A)),
+             ("backward_da_db_bf16_dC", lambda: rlk.det_gemm_backward(dC, A, B)),
+             ("da_then_db_bf16_dC", lambda: (rlk.det_gemm_da(dC, B), rlk.det_gemm_db(A, dC))),
              ("backward_da_db_fp32_dC", lambda: rlk.det_gemm_backward(dC32, A, B)),
-             ("da_then_db_fp32_dC", lambda: (rlk.det_gemm_da(dC32, B), rlk.det_gemm_db(A, dC32)))]
+             ("da_then_db_fp32_dC", lambda: (rlk.det_gemm_da(dC32, B), rlk.det_gemm_db(A, dC32))),
+             ("linear_backward_dx_dw_bf16_dY", lambda: rlk.det_linear_backward(dC, A, W))]
     extra_ms = {}
     for name, f in extra:
         f()
