@@ -16,18 +16,24 @@
  *  - Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
  *    default stream).  Work is enqueued asynchronously; outputs are valid once
  *    the stream reaches that point.
+ *  - Concurrency.  Entry points may be called from several host threads at once,
+ *    each call with its own stream and workspace: host-side caches are guarded,
+ *    no kernel waits on another launch's blocks, and the results are the bits of
+ *    serial calls.  The device error word is shared by all calls of a process.
  *  - Errors.  Arguments are validated on the host before anything is launched;
  *    on any error nothing is launched and no output is touched.  A launch that
  *    the CUDA runtime rejects returns RLK_ERR_CUDA.  A zero-row call (N == 0 in
  *    rlk_linear_logp, M == 0 in rlk_det_gemm_fwd / _da) is a no-op that
  *    returns RLK_OK.
  *  - Determinism.  For fixed inputs every output bit is identical run to run,
- *    across streams, across leading dimensions and pointer alignment, and across
- *    the number of rows in the call (row chunking).  Tile shapes, the K
- *    reduction order and the vocabulary split depend only on the reduction and
- *    vocabulary extents, never on the row count, the GPU's SM count or the
- *    operands' alignment.  rlk_numerics_version() changes whenever any of
- *    those choices change output bits.
+ *    across streams, across leading dimensions and pointer alignment, and -- for
+ *    every product whose reduction does not run over the rows (all but dB and
+ *    the weight gradients) -- across the number of rows in the call (row
+ *    chunking).  Which kernel, tile width and launch shape run may depend on the
+ *    extents and the GPU's SM count, but the arithmetic of each output element
+ *    (its ascending K reduction, the vocabulary split and merge order) depends
+ *    only on the reduction and vocabulary extents, so the bits do not.
+ *    rlk_numerics_version() changes whenever that arithmetic changes.
  *  - Alignment.  An operand whose base address is not 16-byte aligned, or
  *    whose leading dimension is not a multiple of 8 elements, is first copied
  *    into the workspace with a padded leading dimension (bit-identical result;
