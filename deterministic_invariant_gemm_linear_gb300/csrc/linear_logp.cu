@@ -223,7 +223,9 @@ __device__ __forceinline__ void logp_epilogue(const LogpSched& sc, const LogpArg
 }
 
 // A cluster of two CTAs computes a unit = (split j, 256-row block) on the 2-SM
-// tcgen05 loop; the CTA of rank r owns rows [256 * block + 128 r, +128).
+// tcgen05 loop; the CTA of rank r owns rows [256 * block + 128 r, +128).  kK:
+// reduction elements per pipeline stage (64 or 128; see kWideStageRows).
+template <int kK>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     linear_logp_partials_kernel(const __grid_constant__ CUtensorMap tm_hidden,
                                      const __grid_constant__ CUtensorMap tm_weight, LogpSched sc,
@@ -241,16 +243,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   const uint32_t tmem = pipe_setup(ps);
   if (threadIdx.x == 0) RLK_TRACE(1);
-  using THalf = OperandTile<false, kHalfRows>;
+  using THalf = OperandTile<false, kHalfRows, kK>;
+  using R = PairRingT<kHalfRows, kK>;
 
   if (warp == 0) {
-    if (lane == 0) producer_role<THalf, THalf>(&tm_hidden, &tm_weight, sc, ps, &g_err_linear_logp);
+    if (lane == 0)
+      producer_role<THalf, THalf, LogpSched, R>(&tm_hidden, &tm_weight, sc, ps, &g_err_linear_logp);
     if (lane == 1 && ps.rank == 0) scheduler_role(sc, ps, &g_err_linear_logp);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0 && ps.rank == 0)
-      mma_role<THalf, THalf>(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, false, false),
-                              &g_err_linear_logp);
+      mma_role<THalf, THalf, LogpSched, R>(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, false, false),
+                                           &g_err_linear_logp);
     __syncwarp();
   } else {
     logp_epilogue<false>(sc, args, ps, tmem);
@@ -395,9 +399,13 @@ cudaError_t ensure_attrs(int dev) {
   std::lock_guard<std::mutex> lock(g_attr_mutex);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!g_attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(linear_logp_partials_kernel,
+    cudaError_t e = cudaFuncSetAttribute(linear_logp_partials_kernel<64>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         PairRing::kSmemBytes);
+                                         PairRingT<kHalfRows, 64>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(linear_logp_partials_kernel<128>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             PairRingT<kHalfRows, 128>::kSmemBytes);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(linear_logp_solo_kernel<SoloFull>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, SoloFull::kSmemBytes);
@@ -577,7 +585,10 @@ rlk_status launch_partials(const PartialsLaunch& L, const DeviceInfo& dev, cudaS
   sc.vps = (int)L.vps;
   sc.vtiles = (int)ceil_div(L.w_rows, kBN);
   sc.tile0 = (int)(L.j0 * L.vps);
-  sc.nkb = (int)ceil_div(L.H, kBK);
+  // Calls of more than one 256-row block stage 128 reduction columns at a time on
+  // the 2-SM loop (see kWideStageRows); the others 64.
+  const int stage_k = !solo && L.N > kWideStageRows ? 128 : 64;
+  sc.nkb = (int)ceil_div(L.H, stage_k);
   LogpArgs a;
   a.N = (int)L.N;
   a.V = (int)L.V;
@@ -615,8 +626,12 @@ rlk_status launch_partials(const PartialsLaunch& L, const DeviceInfo& dev, cudaS
       return RLK_ERR_CUDA;
     }
   }
-  const cudaError_t e = launch_overlapped(linear_logp_partials_kernel, grid, kThreads,
-                                         PairRing::kSmemBytes, s, tm_h, tm_w, sc, a);
+  const cudaError_t e =
+      stage_k == 128
+          ? launch_overlapped(linear_logp_partials_kernel<128>, grid, kThreads,
+                              PairRingT<kHalfRows, 128>::kSmemBytes, s, tm_h, tm_w, sc, a)
+          : launch_overlapped(linear_logp_partials_kernel<64>, grid, kThreads,
+                              PairRingT<kHalfRows, 64>::kSmemBytes, s, tm_h, tm_w, sc, a);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return RLK_ERR_CUDA;

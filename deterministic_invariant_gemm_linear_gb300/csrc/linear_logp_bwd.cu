@@ -59,6 +59,8 @@ struct GradArgs {
   int64_t ldG;          // multiple of 8 elements
 };
 
+// kK: reduction elements per pipeline stage (64 or 128; see kWideStageRows).
+template <int kK>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     linear_logp_grad_kernel(const __grid_constant__ CUtensorMap tm_hidden,
                             const __grid_constant__ CUtensorMap tm_weight, GradSched sc,
@@ -71,15 +73,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_weight);
   }
   const uint32_t tmem = pipe_setup(ps);
-  using THalf = OperandTile<false, kHalfRows>;
+  using THalf = OperandTile<false, kHalfRows, kK>;
+  using R = PairRingT<kHalfRows, kK>;
 
   if (warp == 0) {
-    if (lane == 0) producer_role<THalf, THalf>(&tm_hidden, &tm_weight, sc, ps, &g_err_linear_logp_bwd);
+    if (lane == 0)
+      producer_role<THalf, THalf, GradSched, R>(&tm_hidden, &tm_weight, sc, ps,
+                                                &g_err_linear_logp_bwd);
     if (lane == 1 && ps.rank == 0) scheduler_role(sc, ps, &g_err_linear_logp_bwd);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0 && ps.rank == 0)
-      mma_role<THalf, THalf>(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, false, false),
+      mma_role<THalf, THalf, GradSched, R>(sc, ps, tmem, idesc_bf16_f32(kPairRows, kBN, false, false),
                               &g_err_linear_logp_bwd);
     __syncwarp();
   } else {
@@ -185,8 +190,13 @@ cudaError_t ensure_attrs(int dev) {
   std::lock_guard<std::mutex> lock(g_attr_mutex);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!g_attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(linear_logp_grad_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(linear_logp_grad_kernel<64>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         PairRingT<kHalfRows, 64>::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(linear_logp_grad_kernel<128>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               PairRingT<kHalfRows, 128>::kSmemBytes);
     if (e != cudaSuccess) return e;
     g_attr_set[dev] = true;
   }
@@ -347,7 +357,8 @@ rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H, in
   sc.order.rows = (int)ceil_div(N, kPairRows);
   sc.order.cols = (int)ceil_div(V, kBN);
   sc.order.band = band_rows(sc.order.rows, H, kPairRows);
-  sc.nkb = (int)ceil_div(H, kBK);
+  const int stage_k = N > kWideStageRows ? 128 : 64;   // as the forward's 2-SM loop
+  sc.nkb = (int)ceil_div(H, stage_k);
   GradArgs a;
   a.N = (int)N;
   a.V = (int)V;
@@ -370,8 +381,12 @@ rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H, in
       return RLK_ERR_CUDA;
     }
   }
-  if (launch_overlapped(linear_logp_grad_kernel, grid, kThreads, kSmemBytes, s, tm_h, tm_w, sc,
-                        a) != cudaSuccess) {
+  if ((stage_k == 128
+           ? launch_overlapped(linear_logp_grad_kernel<128>, grid, kThreads,
+                               PairRingT<kHalfRows, 128>::kSmemBytes, s, tm_h, tm_w, sc, a)
+           : launch_overlapped(linear_logp_grad_kernel<64>, grid, kThreads,
+                               PairRingT<kHalfRows, 64>::kSmemBytes, s, tm_h, tm_w, sc, a)) !=
+      cudaSuccess) {
     cudaGetLastError();
     return RLK_ERR_CUDA;
   }

@@ -19,7 +19,7 @@ namespace rlk {
 constexpr int kHalfRows = 128;     // accumulator rows (TMEM lanes) per CTA; operand rows per CTA
 constexpr int kPairRows = 2 * kHalfRows;      // accumulator rows per CTA pair (MMA M)
 constexpr int kBN = 256;           // accumulator columns (TMEM columns, MMA N)
-constexpr int kBK = 64;            // reduction block per pipeline stage
+constexpr int kBK = 64;            // reduction elements per TMA box row (one swizzle atom); a stage holds 64 or 128
 constexpr int kUmmaK = 16;         // reduction per tcgen05.mma (kind::f16)
 constexpr int kAccCols = kBN;      // FP32 accumulator columns per buffer
 constexpr int kTmemCols = 2 * kAccCols;       // double-buffered accumulator: 512 columns
@@ -361,29 +361,42 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-template <bool kMN, int kRows>
+// kStageK: reduction elements per stage, 64 (one 128-byte swizzle atom per row)
+// or 128.  A 128-deep K-major stage is two 64-wide boxes side by side (each row
+// of a box is one 128-byte swizzle row), the MMA descriptors stepping into the
+// second box after four 16-element steps; an MN-major stage's 64-element chunks
+// are 64 x kStageK x 2 bytes apart.  The stage depth changes only how the same
+// 16-element MMAs are grouped, never which run or their order.
+template <bool kMN, int kRows, int kStageK = kBK>
 struct OperandTile {
-  static constexpr uint32_t kBytes = kRows * kBK * 2;
+  static_assert(kStageK == 64 || kStageK == 128, "stages of 64 or 128 reduction elements");
+  static constexpr int kK = kStageK;
+  static constexpr uint32_t kBytes = kRows * kStageK * 2;
   // kPair: the copies complete on a barrier that may live in the pair's other CTA.
   template <bool kPair = false>
   static __device__ __forceinline__ void load(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                               int32_t row0, int32_t k0) {
     if constexpr (!kMN) {
-      if constexpr (kPair) tma_load_2d_pair(dst, map, bar, k0, row0);
-      else tma_load_2d(dst, map, bar, k0, row0);
+#pragma unroll
+      for (int i = 0; i < kStageK / 64; ++i) {
+        if constexpr (kPair) tma_load_2d_pair(dst + i * (kRows * 128), map, bar, k0 + 64 * i, row0);
+        else tma_load_2d(dst + i * (kRows * 128), map, bar, k0 + 64 * i, row0);
+      }
     } else {
 #pragma unroll
       for (int i = 0; i < kRows / 64; ++i) {
-        if constexpr (kPair) tma_load_2d_pair(dst + i * 8192, map, bar, row0 + 64 * i, k0);
-        else tma_load_2d(dst + i * 8192, map, bar, row0 + 64 * i, k0);
+        if constexpr (kPair) tma_load_2d_pair(dst + i * (64 * kStageK * 2), map, bar, row0 + 64 * i, k0);
+        else tma_load_2d(dst + i * (64 * kStageK * 2), map, bar, row0 + 64 * i, k0);
       }
     }
   }
   static __device__ __forceinline__ uint64_t desc(uint32_t base, int kstep) {
     if constexpr (!kMN) {
-      return sdesc_sw128(base + 32u * kstep, 16u, 1024u);
+      return sdesc_sw128(base + static_cast<uint32_t>(kstep / 4) * (kRows * 128u) +
+                             32u * static_cast<uint32_t>(kstep % 4),
+                         16u, 1024u);
     } else {
-      return sdesc_sw128(base + 2048u * kstep, 8192u, 1024u);
+      return sdesc_sw128(base + 2048u * kstep, 64u * kStageK * 2u, 1024u);
     }
   }
 };

@@ -29,14 +29,16 @@ constexpr int kMaxStages = 11;                        // barrier slots; the ring
 
 // The stage ring: each stage holds this CTA's 128 rows of the left operand and
 // its kBHalf rows of the right-operand tile (half of the tile's 2 kBHalf
-// columns; 64 reduction columns each, 16 KiB apiece for 256-wide tiles), in two
-// areas: left-operand blocks of all stages first, then the right-operand blocks.
-template <int kBHalf_>
+// columns), kK reduction columns each (64: 16 KiB apiece for 256-wide tiles, 7
+// stages; 128: 32 KiB apiece, 3 stages), in two areas: left-operand blocks of all
+// stages first, then the right-operand blocks.
+template <int kBHalf_, int kK_ = kBK>
 struct PairRingT {
   static constexpr int kBHalf = kBHalf_;
+  static constexpr int kK = kK_;                                    // reduction elements per stage
   static constexpr int kTileN = 2 * kBHalf;                         // MMA N
-  static constexpr int kABytes = kHalfRows * kBK * 2;              // 16 KiB
-  static constexpr int kBBytes = kBHalf * kBK * 2;                 // 16 or 8 KiB
+  static constexpr int kABytes = kHalfRows * kK * 2;               // 16 or 32 KiB
+  static constexpr int kBBytes = kBHalf * kK * 2;                  // 8 - 32 KiB
   static constexpr int kStages =
       (kSmemLimit - 1024 - kBarrierBlockBytes) / (kABytes + kBBytes) < kMaxStages
           ? (kSmemLimit - 1024 - kBarrierBlockBytes) / (kABytes + kBBytes)
@@ -56,6 +58,17 @@ struct PairRingT {
   static_assert(kBHalf == kHalfRows || kBHalf == kHalfRows / 2, "256- or 128-wide tiles");
 };
 using PairRing = PairRingT<kHalfRows>;                              // 256 x 256 tiles, 7 stages
+
+// Row-operand extent above which the linear-logp 2-SM loops (the partials and the
+// backward's G kernel) stage 128 reduction columns at a time (PairRingT<128, 128>,
+// three 64 KiB stages) instead of 64 (seven 32 KiB stages).  Each stage carries a
+// fixed cost besides its MMAs: with 128-column stages the MMA issuer spends about
+// a tenth fewer cycles per 256 x 256 tile (mid shape 39,180 -> 35,010 cycles for
+// 32,768 cycles of MMAs, debug-build role counters), while a call of a single
+// 256-row block streams W from HBM and keeps the deeper ring (128-column stages
+// made ragged N = 255 4.6% slower).  Either way the same 16-element MMAs run in
+// the same order, so the bits do not depend on the choice.
+constexpr int kWideStageRows = kPairRows;
 constexpr int kSmemBytes = PairRing::kSmemBytes;
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -347,6 +360,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* ta, const CUten
                                                const Sched& sc, const PipeSmem& ps,
                                                unsigned int* err) {
   static_assert(TA::kBytes == R::kABytes && TB::kBytes == R::kBBytes, "operand halves fit the ring");
+  static_assert(TA::kK == R::kK && TB::kK == R::kK, "operand tiles and ring stage the same depth");
   constexpr int kStages = R::kStages;
   int stage = 0;
   uint32_t phase = 0, issued = 0, last_parity = 0;
@@ -375,9 +389,9 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* ta, const CUten
         if (ps.rank == 0) mbar_arrive_expect_tx(ps.full(stage), R::kTxBytes);
         const uint32_t leader_full = mapa_shared(ps.full(stage), 0);
         TA::template load<true>(R::a_stage(ps.stages, stage), ta, leader_full, a0 + half,
-                                kb * kBK);
+                                kb * R::kK);
         TB::template load<true>(R::b_stage(ps.stages, stage), tb, leader_full, b0 + half_b,
-                                kb * kBK);
+                                kb * R::kK);
         issued |= 1u << stage;
         last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == kStages) {
@@ -444,7 +458,7 @@ __device__ __forceinline__ void mma_role(const Sched& sc, const PipeSmem& ps, ui
         const uint32_t sa = R::a_stage(ps.stages, stage);
         const uint32_t sb = R::b_stage(ps.stages, stage);
 #pragma unroll
-        for (int k = 0; k < kBK / kUmmaK; ++k)
+        for (int k = 0; k < R::kK / kUmmaK; ++k)
           umma_pair_bf16(d, TA::desc(sa, k), TB::desc(sb, k), idesc, (kb | k) != 0 ? 1u : 0u);
         umma_pair_commit(ps.empty(stage), 0x3);
         if (++stage == kStages) {
