@@ -13,8 +13,9 @@
 //   dA       dC [M,N] K-major,                       B [K,N] K-major (N is reduced)
 //   dB       A [M,K] MN-major (output rows = K),      dC [M,N] MN-major (M is reduced)
 // Output tiles are 256 x 256 per CTA pair (2-SM tcgen05 loop, M=256 x N=256 x
-// K=16 per MMA; 256 x 128 for outputs too small to fill the SM pairs), the
-// reduction runs over blocks of 64 in ascending order, each tile's accumulation starts from zero, and there is no
+// K=16 per MMA; 256 x 128 for outputs too small to fill the SM pairs and for a
+// last wave that would leave most pairs idle), the reduction runs in ascending
+// order in 16-element MMAs, each tile's accumulation starts from zero, and there is no
 // split of the reduction: every output bit is a function of its own row of the
 // left operand and column of the right operand only.
 #include <mutex>
@@ -32,17 +33,21 @@ __device__ unsigned int g_err_det_gemm = 0;
 namespace {
 
 struct GemmSched {
-  Banded order; // rows = 256-row output blocks (one per CTA pair), cols = tile_n-column blocks
+  Banded order; // rows = 256-row output blocks (one per CTA pair), cols = order_n-column blocks
   int* counter; // nullptr: cluster c takes units c, c + C, ... (a few rounds at most sizes)
-  int nkb;      // 64-wide reduction blocks
-  int tile_n;   // output columns per tile: 256, or 128 when that fills the last wave better
-  __device__ __forceinline__ int num_units() const { return order.count(); }
+  int nkb;      // reduction stages (64 or 128 wide)
+  int nkb64;    // 64-wide reduction blocks
+  int order_n;  // output columns per block of the order (256, or 128 for narrow tiles throughout)
+  int first;    // this launch's first block of the order
+  int units;    // this launch's units
+  int halves;   // 1: unit u is half (u & 1) of block first + u / 2 (128 of its 256 columns)
+  __device__ __forceinline__ int num_units() const { return units; }
   __device__ __forceinline__ int unit_tiles(int) const { return 1; }
   __device__ __forceinline__ void tile_coords(int u, int, int& a0, int& b0) const {
     int mb, nb;
-    order.unit(u, mb, nb);
+    order.unit(first + (halves ? u >> 1 : u), mb, nb);
     a0 = mb * kPairRows;
-    b0 = nb * tile_n;
+    b0 = nb * order_n + (halves ? (u & 1) * (order_n / 2) : 0);
   }
 };
 
@@ -147,7 +152,7 @@ __device__ __forceinline__ void store_chunk(const GemmOut& o, int row, int col0,
 // +kTileN/2) of the right operand, and stores its own 128 output rows.  Every
 // output element sums the same 16-wide products over the same ascending 64-wide
 // blocks whatever the tile width, so both widths give the same bits (tested).
-template <bool kAMN, bool kBMN, int kTileN>
+template <bool kAMN, bool kBMN, int kTileN, int kStageK>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     det_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     GemmSched sc, GemmOut out) {
@@ -159,9 +164,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_b);
   }
   const uint32_t tmem = pipe_setup(ps);
-  using R = PairRingT<kTileN / 2>;
-  using TA = OperandTile<kAMN, kHalfRows>;
-  using TB = OperandTile<kBMN, kTileN / 2>;
+  using R = PairRingT<kTileN / 2, kStageK>;
+  using TA = OperandTile<kAMN, kHalfRows, kStageK>;
+  using TB = OperandTile<kBMN, kTileN / 2, kStageK>;
 
   if (warp == 0) {
     if (lane == 0) producer_role<TA, TB, GemmSched, R>(&tm_a, &tm_b, sc, ps, &g_err_det_gemm);
@@ -438,23 +443,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 std::mutex g_attr_mutex;
 bool g_attr_set[64];
 
-template <bool kAMN, bool kBMN, int kTileN>
+template <bool kAMN, bool kBMN, int kTileN, int kStageK>
 cudaError_t set_attr() {
-  return cudaFuncSetAttribute(det_gemm_kernel<kAMN, kBMN, kTileN>,
+  return cudaFuncSetAttribute(det_gemm_kernel<kAMN, kBMN, kTileN, kStageK>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              PairRingT<kTileN / 2>::kSmemBytes);
+                              PairRingT<kTileN / 2, kStageK>::kSmemBytes);
 }
 
 cudaError_t ensure_attrs(int dev) {
   std::lock_guard<std::mutex> lock(g_attr_mutex);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!g_attr_set[dev]) {
-    cudaError_t e = set_attr<false, true, 256>();
-    if (e == cudaSuccess) e = set_attr<false, false, 256>();
-    if (e == cudaSuccess) e = set_attr<true, true, 256>();
-    if (e == cudaSuccess) e = set_attr<false, true, 128>();
-    if (e == cudaSuccess) e = set_attr<false, false, 128>();
-    if (e == cudaSuccess) e = set_attr<true, true, 128>();
+    cudaError_t e = set_attr<false, true, 256, 64>();
+    if (e == cudaSuccess) e = set_attr<false, false, 256, 64>();
+    if (e == cudaSuccess) e = set_attr<true, true, 256, 64>();
+    if (e == cudaSuccess) e = set_attr<false, true, 128, 128>();
+    if (e == cudaSuccess) e = set_attr<false, false, 128, 128>();
+    if (e == cudaSuccess) e = set_attr<true, true, 128, 128>();
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(det_gemm_fwd_db_kernel<true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -467,15 +472,32 @@ cudaError_t ensure_attrs(int dev) {
   return cudaSuccess;
 }
 
-// Output tile width, from the output's extents and the number of CTA pairs
-// only: 256 columns, or 128 when even twice as many 128-wide tiles fit in one
-// wave of pairs.  A 128-wide tile takes about 0.89 of a 256-wide tile's time
-// (measured on GB300), so narrow tiles pay off only where wide ones would leave
-// at least half the pairs idle (1000^3: 15.0 vs 17 - 19 us); at 4096^3 uniform
-// narrow tiles took 135.8 us against 86.7 us.  Bits are the same either way.
-int choose_tile_n(int64_t out_rows, int64_t out_cols, int64_t clusters) {
+// Tiling, from the output's extents, the reduction length and the number of CTA
+// pairs only.  Wide tiles are 256 x 256 with 64-element stages; narrow ones
+// 256 x 128 with 128-element stages (four MMAs of N = 128 per 64-element stage
+// left the pipe idle between stages).  A narrow tile takes about 0.69 of a wide
+// tile's time on GB300 (uniform narrow tiles at 4096^3: 105 us against 86.7 us;
+// 134 us with 64-element stages), so narrow tiles pay off where wide ones would
+// leave at least half the pairs idle:
+//  * throughout, when all wide tiles fit in half a wave (1000^3: 15.0 - 16.0 vs
+//    15.0 - 17.1 us with 64-element stages);
+//  * for a last, partial wave that would fill at most half the pairs, when the
+//    reduction is long: its wide blocks are computed as two narrow halves each
+//    in a second launch, which costs a few microseconds of its own (4096^3: 88.7
+//    vs 86.7 us; 4096 x 151936 x 4096: 2.80 vs 2.96 - 3.01 ms).
+// Every output element runs the same 16-element MMAs in the same order whatever
+// the tile, so the bits are the same.
+constexpr int64_t kSplitMinReduction = 16384;
+struct TilePlan {
+  bool narrow;     // narrow tiles throughout
+  int64_t split;   // wide blocks at the end of the order computed as narrow halves
+};
+TilePlan plan_tiles(int64_t out_rows, int64_t out_cols, int64_t red, int64_t clusters) {
   const int64_t wide = ceil_div(out_rows, kPairRows) * ceil_div(out_cols, kBN);
-  return 2 * wide <= clusters ? kBN / 2 : kBN;
+  if (2 * wide <= clusters) return {true, 0};
+  const int64_t tail = wide % clusters;
+  if (red >= kSplitMinReduction && wide > clusters && 2 * tail <= clusters) return {false, tail};
+  return {false, 0};
 }
 
 inline bool dtype_ok(int d) { return d == RLK_BF16 || d == RLK_FP32; }
@@ -570,35 +592,7 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
   if ((st = materialise(y, ws, s, &yp)) != RLK_OK) return st;
 
   const int64_t clusters = dev.sm_count / 2;
-  const int tile_n = choose_tile_n(out_rows, out_cols, clusters);
-  const int64_t num_nb = ceil_div(out_cols, tile_n);
-  // Tensor maps: {contiguous extent, row count}, pitch, box (per CTA: 128 left-operand
-  // rows, tile_n / 2 right-operand rows or columns).
-  CUtensorMap ta, tb;
-  bool ok = false;
-  switch (kind) {
-    case Kind::kFwd:   // A [M,K] K-major; B [K,N] MN-major
-      ok = encode_bf16_2d(&ta, xp, x.cols, x.rows, x.eff_ld, kBK, kHalfRows) &&
-           encode_bf16_2d(&tb, yp, y.cols, y.rows, y.eff_ld, 64, kBK);
-      break;
-    case Kind::kDa:    // dC [M,N] K-major; B [K,N] K-major (N reduced)
-      ok = encode_bf16_2d(&ta, xp, x.cols, x.rows, x.eff_ld, kBK, kHalfRows) &&
-           encode_bf16_2d(&tb, yp, y.cols, y.rows, y.eff_ld, kBK, tile_n / 2);
-      break;
-    case Kind::kDb:    // A [M,K] MN-major; dC [M,N] MN-major (M reduced)
-      ok = encode_bf16_2d(&ta, xp, x.cols, x.rows, x.eff_ld, 64, kBK) &&
-           encode_bf16_2d(&tb, yp, y.cols, y.rows, y.eff_ld, 64, kBK);
-      break;
-  }
-  if (!ok) return RLK_ERR_CUDA;
-
-  GemmSched sc;
-  sc.order.rows = (int)num_mb;
-  sc.order.cols = (int)num_nb;
-  sc.order.band = band_rows(num_mb, red, kPairRows);
-  sc.counter = nullptr;
-  sc.nkb = (int)ceil_div(red, kBK);
-  sc.tile_n = tile_n;
+  const TilePlan plan = plan_tiles(out_rows, out_cols, red, clusters);
   GemmOut o;
   o.M = (int)out_rows;
   o.N = (int)out_cols;
@@ -607,30 +601,76 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
   o.fp32 = c_dtype == RLK_FP32;
   o.accum = accum ? 1 : 0;
   o.vec_bytes = store_width(C, ldc, esize(c_dtype));
-  const int64_t units = num_mb * num_nb;
-  const int grid = 2 * (int)(units < clusters ? units : clusters);
-  constexpr int kWide = PairRingT<kHalfRows>::kSmemBytes, kNarrow = PairRingT<kHalfRows / 2>::kSmemBytes;
-  const bool wide = tile_n == 256;
-  cudaError_t e = cudaErrorInvalidValue;
-  switch (kind) {
-    case Kind::kFwd:
-      e = wide ? launch_overlapped(det_gemm_kernel<false, true, 256>, grid, kThreads, kWide, s, ta, tb, sc, o)
-               : launch_overlapped(det_gemm_kernel<false, true, 128>, grid, kThreads, kNarrow, s, ta, tb, sc, o);
-      break;
-    case Kind::kDa:
-      e = wide ? launch_overlapped(det_gemm_kernel<false, false, 256>, grid, kThreads, kWide, s, ta, tb, sc, o)
-               : launch_overlapped(det_gemm_kernel<false, false, 128>, grid, kThreads, kNarrow, s, ta, tb, sc, o);
-      break;
-    case Kind::kDb:
-      e = wide ? launch_overlapped(det_gemm_kernel<true, true, 256>, grid, kThreads, kWide, s, ta, tb, sc, o)
-               : launch_overlapped(det_gemm_kernel<true, true, 128>, grid, kThreads, kNarrow, s, ta, tb, sc, o);
-      break;
-  }
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return RLK_ERR_CUDA;
-  }
-  return RLK_OK;
+  GemmSched sc;
+  sc.order.rows = (int)num_mb;
+  sc.order.cols = (int)ceil_div(out_cols, plan.narrow ? kBN / 2 : kBN);
+  sc.order.band = band_rows(num_mb, red, kPairRows);
+  sc.order_n = plan.narrow ? kBN / 2 : kBN;
+  sc.counter = nullptr;
+  sc.nkb64 = (int)ceil_div(red, kBK);
+
+  // One launch over units [first, first + units) of the order (halves: two narrow
+  // units per wide block).  Tensor maps: {contiguous extent, row count}, pitch,
+  // box (per CTA: 128 left-operand rows, tile_n / 2 right-operand rows or columns;
+  // an MN-major box spans one stage of the reduction).
+  auto launch = [&](int64_t first, int64_t units, bool narrow, bool halves) -> rlk_status {
+    const int tile_n = narrow ? kBN / 2 : kBN, stage_k = narrow ? 128 : 64;
+    CUtensorMap ta, tb;
+    bool ok = false;
+    switch (kind) {
+      case Kind::kFwd:   // A [M,K] K-major; B [K,N] MN-major
+        ok = encode_bf16_2d(&ta, xp, x.cols, x.rows, x.eff_ld, kBK, kHalfRows) &&
+             encode_bf16_2d(&tb, yp, y.cols, y.rows, y.eff_ld, 64, stage_k);
+        break;
+      case Kind::kDa:    // dC [M,N] K-major; B [K,N] K-major (N reduced)
+        ok = encode_bf16_2d(&ta, xp, x.cols, x.rows, x.eff_ld, kBK, kHalfRows) &&
+             encode_bf16_2d(&tb, yp, y.cols, y.rows, y.eff_ld, kBK, tile_n / 2);
+        break;
+      case Kind::kDb:    // A [M,K] MN-major; dC [M,N] MN-major (M reduced)
+        ok = encode_bf16_2d(&ta, xp, x.cols, x.rows, x.eff_ld, 64, stage_k) &&
+             encode_bf16_2d(&tb, yp, y.cols, y.rows, y.eff_ld, 64, stage_k);
+        break;
+    }
+    if (!ok) return RLK_ERR_CUDA;
+    GemmSched part = sc;
+    part.nkb = (int)ceil_div(red, stage_k);
+    part.first = (int)first;
+    part.units = (int)units;
+    part.halves = halves ? 1 : 0;
+    const int grid = 2 * (int)(units < clusters ? units : clusters);
+    constexpr int kWideSmem = PairRingT<kHalfRows, 64>::kSmemBytes;
+    constexpr int kNarrowSmem = PairRingT<kHalfRows / 2, 128>::kSmemBytes;
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (kind) {
+      case Kind::kFwd:
+        e = narrow ? launch_overlapped(det_gemm_kernel<false, true, 128, 128>, grid, kThreads,
+                                       kNarrowSmem, s, ta, tb, part, o)
+                   : launch_overlapped(det_gemm_kernel<false, true, 256, 64>, grid, kThreads,
+                                       kWideSmem, s, ta, tb, part, o);
+        break;
+      case Kind::kDa:
+        e = narrow ? launch_overlapped(det_gemm_kernel<false, false, 128, 128>, grid, kThreads,
+                                       kNarrowSmem, s, ta, tb, part, o)
+                   : launch_overlapped(det_gemm_kernel<false, false, 256, 64>, grid, kThreads,
+                                       kWideSmem, s, ta, tb, part, o);
+        break;
+      case Kind::kDb:
+        e = narrow ? launch_overlapped(det_gemm_kernel<true, true, 128, 128>, grid, kThreads,
+                                       kNarrowSmem, s, ta, tb, part, o)
+                   : launch_overlapped(det_gemm_kernel<true, true, 256, 64>, grid, kThreads,
+                                       kWideSmem, s, ta, tb, part, o);
+        break;
+    }
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return RLK_ERR_CUDA;
+    }
+    return RLK_OK;
+  };
+  const int64_t blocks = num_mb * sc.order.cols;
+  if (plan.narrow) return launch(0, blocks, true, false);
+  if ((st = launch(0, blocks - plan.split, false, false)) != RLK_OK) return st;
+  return plan.split > 0 ? launch(blocks - plan.split, 2 * plan.split, true, true) : RLK_OK;
 }
 
 // Checks an output of a product before anything launches (the checks run_gemm

@@ -46,7 +46,8 @@ struct LogpSched {
   int vps;         // 256-id tiles per split
   int vtiles;      // 256-id tiles of the weight rows this call reads
   int tile0;       // global index of the first of those tiles (0 unless a vocabulary shard)
-  int nkb;         // 64-wide blocks of H
+  int nkb;         // reduction stages over H (64 or 128 wide)
+  int nkb64;       // 64-wide blocks of H
   __device__ __forceinline__ int num_units() const { return order.count(); }
   __device__ __forceinline__ int split_of(int u) const {
     int rb, j;
@@ -589,6 +590,7 @@ rlk_status launch_partials(const PartialsLaunch& L, const DeviceInfo& dev, cudaS
   // the 2-SM loop (see kWideStageRows); the others 64.
   const int stage_k = !solo && L.N > kWideStageRows ? 128 : 64;
   sc.nkb = (int)ceil_div(L.H, stage_k);
+  sc.nkb64 = (int)ceil_div(L.H, kBK);
   LogpArgs a;
   a.N = (int)L.N;
   a.V = (int)L.V;

@@ -36,7 +36,8 @@ namespace {
 struct GradSched {
   Banded order;    // rows = 256-row blocks (one per CTA pair), cols = 256-id vocabulary tiles
   int* counter;    // zeroed unit counter in the workspace (units in order), or null (round-robin)
-  int nkb;         // 64-wide blocks of H
+  int nkb;         // reduction stages over H (64 or 128 wide)
+  int nkb64;       // 64-wide blocks of H
   __device__ __forceinline__ int num_units() const { return order.count(); }
   __device__ __forceinline__ int unit_tiles(int) const { return 1; }
   __device__ __forceinline__ void tile_coords(int u, int, int& a0, int& b0) const {
@@ -359,6 +360,7 @@ rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H, in
   sc.order.band = band_rows(sc.order.rows, H, kPairRows);
   const int stage_k = N > kWideStageRows ? 128 : 64;   // as the forward's 2-SM loop
   sc.nkb = (int)ceil_div(H, stage_k);
+  sc.nkb64 = (int)ceil_div(H, kBK);
   GradArgs a;
   a.N = (int)N;
   a.V = (int)V;

@@ -350,7 +350,9 @@ __device__ __forceinline__ int warp_unit_take(const Sched& sc, const PipeSmem& p
 //   void tile_coords(int u, int i, int& a0, int& b0) const;
 //        a0 = first row of the pair's 256-row block of the left operand,
 //        b0 = first row of the 256-row right-operand tile
-//   int  nkb;                                  reduction blocks of 64 per tile
+//   int  nkb;                                  reduction stages (R::kK wide) per tile
+//   int  nkb64;                                64-wide reduction blocks per tile
+//        (read only by rings of 128-wide stages)
 // The reduction of every tile runs over its blocks in ascending order and starts
 // from zero, so a tile's arithmetic depends only on its operand tiles, never on
 // the schedule, the grid or the row count.  TA / TB are the 128-row operand
@@ -457,9 +459,16 @@ __device__ __forceinline__ void mma_role(const Sched& sc, const PipeSmem& ps, ui
         tc_fence_after();
         const uint32_t sa = R::a_stage(ps.stages, stage);
         const uint32_t sb = R::b_stage(ps.stages, stage);
+        // A 128-wide last stage that holds a single 64-wide block (an odd block
+        // count) runs only that block's MMAs: every tile issues exactly the MMAs
+        // of 64-wide staging, never an all-zero one (adding +0 would turn an
+        // accumulated -0 into +0).
+        bool one_block = false;
+        if constexpr (R::kK > kBK) one_block = kb == sc.nkb - 1 && (sc.nkb64 & 1);
 #pragma unroll
         for (int k = 0; k < R::kK / kUmmaK; ++k)
-          umma_pair_bf16(d, TA::desc(sa, k), TB::desc(sb, k), idesc, (kb | k) != 0 ? 1u : 0u);
+          if (k < kBK / kUmmaK || !one_block)
+            umma_pair_bf16(d, TA::desc(sa, k), TB::desc(sb, k), idesc, (kb | k) != 0 ? 1u : 0u);
         umma_pair_commit(ps.empty(stage), 0x3);
         if (++stage == kStages) {
           stage = 0;

@@ -19,6 +19,16 @@ def cuda_or_skip():
     return torch.device("cuda:0")
 
 
+def bits_equal(a: torch.Tensor, b: torch.Tensor) -> bool:
+    """Bit-pattern equality (torch.equal calls -0.0 and +0.0 equal and NaN unequal)."""
+    if a.dtype != b.dtype or a.shape != b.shape:
+        return False
+    if a.dtype in (torch.float32, torch.float16, torch.bfloat16):
+        view = torch.int32 if a.dtype == torch.float32 else torch.int16
+        return torch.equal(a.contiguous().view(view), b.contiguous().view(view))
+    return torch.equal(a, b)
+
+
 def dec_bf16(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 

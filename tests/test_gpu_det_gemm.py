@@ -13,7 +13,7 @@ import torch
 
 import deterministic_invariant_gemm_linear_gb300 as rlk
 import seeded_inputs as si
-from helpers import (GEMM_FP32_REL_FRO, bf16_within_one_ulp, cuda_or_skip, dec_bf16, rel_fro,
+from helpers import (GEMM_FP32_REL_FRO, bits_equal, bf16_within_one_ulp, cuda_or_skip, dec_bf16, rel_fro,
                      sample_rows)
 
 pytestmark = pytest.mark.gpu
@@ -263,6 +263,41 @@ def test_tile_widths_give_the_same_bits(dev, out_dtype):
     # a ragged narrow case: 33 rows x 2000 columns against the same rows of 4096
     assert torch.equal(rlk.det_gemm_fwd(A[100:133], B[:, :2000], out_dtype),
                        rlk.det_gemm_fwd(A, B[:, :2000], out_dtype)[100:133])
+    assert rlk.device_error() == 0
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_last_wave_split_gives_the_same_bits(dev, out_dtype):
+    """An output of 16 x 16 wide tiles on 76 SM pairs leaves a last wave of 28
+    tiles; with a long reduction (16384 here) those blocks are computed as two
+    128-wide halves each in a second launch.  For all three products (outputs
+    4096 x 3900, 4096 x 4000 and 4000 x 3900: a last column block of 60 columns,
+    whose second half is empty, and one of 160), integer inputs give the exact
+    product, and the rows equal the same rows of 1024-row calls (64 wide tiles,
+    one launch) and of 256-row calls (narrow tiles throughout), bit for bit."""
+    g = torch.Generator(device=dev).manual_seed(21)
+
+    def ints(r, c):
+        return torch.randint(-4, 5, (r, c), generator=g, device=dev).to(torch.bfloat16)
+
+    R = 16384
+    A, B = ints(4096, R), ints(R, 3900)                 # fwd: [4096, 3900]
+    dC, Bt = ints(4096, R), ints(4000, R)               # dA: dC [4096, R] . B^T, B [4000, R]
+    A2, dC2 = ints(R, 4000), ints(R, 3900)              # dB: A2^T . dC2 -> [4000, 3900]
+    cases = {
+        "fwd": (rlk.det_gemm_fwd(A, B, out_dtype), A.double() @ B.double(),
+                lambda s, c: rlk.det_gemm_fwd(A[s:s + c], B, out_dtype), 4096),
+        "da": (rlk.det_gemm_da(dC, Bt, out_dtype), dC.double() @ Bt.double().T,
+               lambda s, c: rlk.det_gemm_da(dC[s:s + c], Bt, out_dtype), 4096),
+        "db": (rlk.det_gemm_db(A2, dC2, out_dtype), A2.double().T @ dC2.double(),
+               lambda s, c: rlk.det_gemm_db(A2[:, s:s + c], dC2, out_dtype), 4000),
+    }
+    for name, (full, exact, part, rows) in cases.items():
+        # |sums| <= 16 * 16384 < 2^24: exact in FP32; the BF16 output is its RNE
+        assert torch.equal(full.double(), exact.float().to(out_dtype).double()), name
+        for chunk in (1024, 256):
+            parts = torch.cat([part(s, chunk) for s in range(0, rows, chunk)])
+            assert bits_equal(parts, full), (name, chunk)
     assert rlk.device_error() == 0
 
 

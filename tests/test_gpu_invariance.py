@@ -5,14 +5,14 @@ contract: the same row with the same V gives the same bits whatever the batch
 (author notes: full-batch bits == concatenation of the chunks' bits, checked
 with exact equality, never allclose; PR body: batch size, row position,
 neighbouring rows, chunking, layouts, vocabulary boundaries and CUDA streams).
-Every check here is torch.equal.
+Every check here compares bit patterns (signed zeros and NaN payloads included).
 """
 import pytest
 import torch
 
 import deterministic_invariant_gemm_linear_gb300 as rlk
 import seeded_inputs as si
-from helpers import cuda_or_skip
+from helpers import bits_equal, cuda_or_skip
 
 pytestmark = pytest.mark.gpu
 
@@ -39,7 +39,7 @@ def chunked(hidden, weight, target, bias, chunk):
 
 def assert_same(a, b, what):
     for x, y, name in zip(a, b, ("logp", "lse", "target_logit")):
-        assert torch.equal(x, y), f"{what}: {name} bits differ"
+        assert bits_equal(x, y), f"{what}: {name} bits differ"
 
 
 def test_run_to_run_mid(mid):
@@ -169,3 +169,28 @@ def test_bias_alignment_paths(dev, N):
     assert shifted.data_ptr() % 16 == 4
     assert_same(lp(hidden, weight, target, shifted), lp(hidden, weight, target, bias),
                 "bias read one float at a time vs four at a time")
+
+
+@pytest.mark.parametrize("H", [64, 320, 2112])
+def test_zero_rows_keep_their_signed_zero_across_loops(dev, H):
+    """A hidden row of zeros against an all-negative weight makes every product -0.
+    Calls of more than 256 rows stage 128 reduction columns at a time, smaller ones
+    64; with an odd number of 64-wide blocks the last 128-wide stage holds one
+    block and zero fill, and only that block's MMAs run, so the logits (and the
+    target logit read out as is) keep the same zero sign as in a 1-row call (one-CTA
+    loop) or a 200-row call (2-SM loop, 64-wide stages)."""
+    V = 1000
+    hidden, weight, _, target = si.linear_logp_inputs(300, H, V, bias=False, seed=18, device=dev)
+    weight = -(weight.abs() + 2.0 ** -8).to(torch.bfloat16)
+    hidden = hidden.clone()
+    zero_rows = (0, 7, 255, 256, 299)
+    hidden[list(zero_rows)] = 0
+    big = lp(hidden, weight, target)
+    mid_call = lp(hidden[:200], weight, target[:200])
+    for r in zero_rows:
+        one = lp(hidden[r:r + 1], weight, target[r:r + 1])
+        assert_same(tuple(o[r:r + 1] for o in big), one, f"zero row {r}: 300-row vs 1-row call")
+        if r < 200:
+            assert_same(tuple(o[r:r + 1] for o in mid_call), one, f"zero row {r}: 200-row call")
+    assert_same(tuple(o[:200] for o in big), mid_call, "300-row vs 200-row call")
+    assert rlk.device_error() == 0
