@@ -298,6 +298,12 @@ def test_last_wave_split_gives_the_same_bits(dev, out_dtype):
         for chunk in (1024, 256):
             parts = torch.cat([part(s, chunk) for s in range(0, rows, chunk)])
             assert bits_equal(parts, full), (name, chunk)
+    if out_dtype == torch.float32:
+        # C += A . B through both launches: every block is added exactly once
+        C0 = torch.randint(-8, 9, (4096, 3900), generator=g, device=dev).float()
+        C = C0.clone()
+        rlk.det_gemm_fwd_accum_fp32_(C, A, B)
+        assert torch.equal(C, C0 + cases["fwd"][0])
     assert rlk.device_error() == 0
 
 
