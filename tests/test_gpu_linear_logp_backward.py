@@ -113,6 +113,28 @@ def test_backward_mid_shape_runs_deterministically(dev):
     assert rlk.device_error() == 0
 
 
+def test_backward_mid_rows_equal_across_tilings(dev):
+    """At the mid vocabulary grad_hidden = G . W reduces over V = 151936.  A 4096-row
+    call has 16 x 16 output tiles, whose last wave runs as half tiles in a second
+    launch; 1024- and 600-row calls run wide tiles in one launch, 256-row calls
+    narrow tiles throughout.  The rows of all of them are the same bits."""
+    w = si.MID
+    hidden, weight, _, target = si.workload_inputs(w, seed=6, device=dev)
+    g = torch.randn(w.N, device=dev, generator=torch.Generator(device=dev).manual_seed(13))
+    _, lse = rlk.linear_logp(hidden, weight, target)
+
+    def dh(rows):
+        return rlk.linear_logp_backward(hidden[rows], weight, target[rows], lse[rows], g[rows],
+                                        grad_weight=False, grad_bias=False,
+                                        out_dtype=torch.float32)[0]
+
+    full = dh(slice(0, w.N))
+    for chunk in (1024, 600, 256):
+        parts = torch.cat([dh(slice(s, min(s + chunk, w.N))) for s in range(0, w.N, chunk)])
+        assert torch.equal(parts.view(torch.int32), full.view(torch.int32)), chunk
+    assert rlk.device_error() == 0
+
+
 def test_backward_zero_rows(dev):
     weight = torch.randn(50, 64, device=dev).to(torch.bfloat16)
     e = torch.empty(0, 64, dtype=torch.bfloat16, device=dev)
