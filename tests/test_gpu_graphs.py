@@ -86,6 +86,36 @@ def test_backward_and_det_gemm_graph_replay(dev):
     assert rlk.device_error() == 0
 
 
+def test_det_gemm_last_wave_split_graph_replay(dev):
+    """A product whose last wave runs as half tiles in a second launch (16 x 16 wide
+    tiles, reduction 16384) replays from a graph with the eager bits, after a torch
+    kernel that rewrites its input inside the same graph."""
+    A, B, _ = si.det_gemm_inputs(4096, 16384, 3900, seed=58, device=dev)
+    A0 = A.clone()
+
+    def step():
+        A.copy_(A0)
+        return rlk.det_gemm_fwd(A, B, out_dtype=torch.float32)
+
+    eager = step()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        out = step()
+    for _ in range(2):
+        out.zero_()
+        A.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int32), eager.view(torch.int32))
+    assert rlk.device_error() == 0
+
+
 @pytest.mark.parametrize("N", [17, 1000])
 def test_calls_see_inputs_written_just_before(dev, N):
     """Each library kernel may start while the previous kernel in the stream is
