@@ -193,6 +193,49 @@ def det_gemm_cases(dev, fails):
                     fails.append(f"{what}: a canary was overwritten")
 
 
+def det_gemm_split_cases(dev, fails):
+    """Products whose last wave runs as 128-wide halves in a second launch (16 x 16
+    wide tiles, reduction 16384): the halves, including the empty second half of a
+    60-column last block, write only their own columns of a pitched output."""
+    lib, P = rlk.lib(), rlk._ptr
+    sp = rlk._stream_ptr(None)
+    R = 16384
+    g = torch.Generator(device=dev).manual_seed(77)
+
+    def bf(r, c):
+        return torch.randn(r, c, generator=g, device=dev).to(torch.bfloat16)
+
+    A, B = bf(4096, R), bf(R, 3900)          # fwd -> [4096, 3900]
+    dC, Bt = bf(4096, R), bf(4000, R)        # dA = dC . Bt^T -> [4096, 4000]
+    A2, dC2 = bf(R, 4000), bf(R, 3900)       # dB = A2^T . dC2 -> [4000, 3900]
+    # (the 3900-column operands have an odd pitch and are staged through the workspace)
+    ops = {"fwd": (4096, 3900, (rlk.RLK_GEMM_FWD, A, 4096, R, B, R, 3900)),
+           "da": (4096, 4000, (rlk.RLK_GEMM_DA, dC, 4096, R, Bt, 4000, R)),
+           "db": (4000, 3900, (rlk.RLK_GEMM_DB, A2, R, 4000, dC2, R, 3900))}
+    for dtype, esize in ((rlk.RLK_FP32, 4), (rlk.RLK_BF16, 2)):
+        for op, (rows, cols, (code, x, xr, xc, y, yr, yc)) in ops.items():
+            ld = cols + 5
+            C = Guarded(rows * ld * esize, dev)
+            ws_n = lib.rlk_det_gemm_workspace_size(code, P(x), 0, xr, xc, xc, P(y), 0, yr, yc, yc)
+            ws = Guarded(max(ws_n, 0), dev)
+            if op == "fwd":
+                st = lib.rlk_det_gemm_fwd(P(A), 4096, R, R, P(B), 3900, 3900, C.ptr, dtype, ld,
+                                          ws.ptr, ws_n, sp)
+            elif op == "da":
+                st = lib.rlk_det_gemm_da(P(dC), rlk.RLK_BF16, 4096, R, R, P(Bt), 4000, R, C.ptr,
+                                         dtype, ld, ws.ptr, ws_n, sp)
+            else:
+                st = lib.rlk_det_gemm_db(P(A2), R, 4000, 4000, P(dC2), rlk.RLK_BF16, 3900, 3900,
+                                         C.ptr, dtype, ld, ws.ptr, ws_n, sp)
+            torch.cuda.synchronize()
+            what = f"det_gemm {op} split last wave esize={esize}"
+            if st != 0:
+                fails.append(f"{what}: status {st}")
+            elif not (C.bands_intact() and _pitched_untouched(C, rows, cols, ld, esize) and
+                      ws.bands_intact()):
+                fails.append(f"{what}: a canary was overwritten")
+
+
 def shard_cases(dev, fails):
     lib, P = rlk.lib(), rlk._ptr
     sp = rlk._stream_ptr(None)
@@ -230,5 +273,6 @@ def run_all(dev):
     linear_logp_cases(dev, fails)
     backward_cases(dev, fails)
     det_gemm_cases(dev, fails)
+    det_gemm_split_cases(dev, fails)
     shard_cases(dev, fails)
     return fails
