@@ -609,31 +609,37 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
   sc.counter = nullptr;
   sc.nkb64 = (int)ceil_div(red, kBK);
 
-  // One launch over units [first, first + units) of the order (halves: two narrow
-  // units per wide block).  Tensor maps: {contiguous extent, row count}, pitch,
-  // box (per CTA: 128 left-operand rows, tile_n / 2 right-operand rows or columns;
-  // an MN-major box spans one stage of the reduction).
-  auto launch = [&](int64_t first, int64_t units, bool narrow, bool halves) -> rlk_status {
+  // Tensor maps per tile width: {contiguous extent, row count}, pitch, box (per
+  // CTA: 128 left-operand rows, tile_n / 2 right-operand rows or columns; an
+  // MN-major box spans one stage of the reduction).  Both are encoded before
+  // anything launches, so a failure leaves the output untouched.
+  auto encode = [&](bool narrow, CUtensorMap* ta, CUtensorMap* tb) -> bool {
     const int tile_n = narrow ? kBN / 2 : kBN, stage_k = narrow ? 128 : 64;
-    CUtensorMap ta, tb;
-    bool ok = false;
     switch (kind) {
       case Kind::kFwd:   // A [M,K] K-major; B [K,N] MN-major
-        ok = encode_bf16_2d(&ta, xp, x.cols, x.rows, x.eff_ld, kBK, kHalfRows) &&
-             encode_bf16_2d(&tb, yp, y.cols, y.rows, y.eff_ld, 64, stage_k);
-        break;
+        return encode_bf16_2d(ta, xp, x.cols, x.rows, x.eff_ld, kBK, kHalfRows) &&
+               encode_bf16_2d(tb, yp, y.cols, y.rows, y.eff_ld, 64, stage_k);
       case Kind::kDa:    // dC [M,N] K-major; B [K,N] K-major (N reduced)
-        ok = encode_bf16_2d(&ta, xp, x.cols, x.rows, x.eff_ld, kBK, kHalfRows) &&
-             encode_bf16_2d(&tb, yp, y.cols, y.rows, y.eff_ld, kBK, tile_n / 2);
-        break;
+        return encode_bf16_2d(ta, xp, x.cols, x.rows, x.eff_ld, kBK, kHalfRows) &&
+               encode_bf16_2d(tb, yp, y.cols, y.rows, y.eff_ld, kBK, tile_n / 2);
       case Kind::kDb:    // A [M,K] MN-major; dC [M,N] MN-major (M reduced)
-        ok = encode_bf16_2d(&ta, xp, x.cols, x.rows, x.eff_ld, 64, stage_k) &&
-             encode_bf16_2d(&tb, yp, y.cols, y.rows, y.eff_ld, 64, stage_k);
-        break;
+        return encode_bf16_2d(ta, xp, x.cols, x.rows, x.eff_ld, 64, stage_k) &&
+               encode_bf16_2d(tb, yp, y.cols, y.rows, y.eff_ld, 64, stage_k);
     }
-    if (!ok) return RLK_ERR_CUDA;
+    return false;
+  };
+  CUtensorMap ta_w, tb_w, ta_n, tb_n;
+  const bool need_wide = !plan.narrow, need_narrow = plan.narrow || plan.split > 0;
+  if ((need_wide && !encode(false, &ta_w, &tb_w)) || (need_narrow && !encode(true, &ta_n, &tb_n)))
+    return RLK_ERR_CUDA;
+
+  // One launch over units [first, first + units) of the order (halves: two narrow
+  // units per wide block).
+  auto launch = [&](int64_t first, int64_t units, bool narrow, bool halves) -> rlk_status {
+    const CUtensorMap& ta = narrow ? ta_n : ta_w;
+    const CUtensorMap& tb = narrow ? tb_n : tb_w;
     GemmSched part = sc;
-    part.nkb = (int)ceil_div(red, stage_k);
+    part.nkb = (int)ceil_div(red, narrow ? 128 : 64);
     part.first = (int)first;
     part.units = (int)units;
     part.halves = halves ? 1 : 0;
