@@ -57,7 +57,8 @@ rlk_status device_ready(DeviceInfo* info) {
                     cudaSuccess &&
                 cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess;
       cudaGetLastError();
-      g_dev_state[dev] = (ok && major == 10 && minor == 3 && sms > 0) ? 1 : -1;
+      // the 2-SM kernels need at least one pair of SMs (and divide work by pairs)
+      g_dev_state[dev] = (ok && major == 10 && minor == 3 && sms >= 2) ? 1 : -1;
       g_dev_sms[dev] = sms;
     }
     if (g_dev_state[dev] != 1) return RLK_ERR_UNSUPPORTED_DEVICE;
