@@ -892,6 +892,19 @@ using namespace rlk;
 
 extern "C" {
 
+rlk_status rlk_det_gemm_tile_plan(int64_t out_rows, int64_t out_cols, int64_t red, int32_t sm_count,
+                                  int32_t* tile_cols, int64_t* split_blocks, int32_t* launches) {
+  if (!tile_cols || !split_blocks || !launches) return RLK_ERR_NULL;
+  if (out_rows < 1 || out_rows >= kMaxExtent || out_cols < 1 || out_cols >= kMaxExtent ||
+      red < 1 || red >= kMaxExtent || sm_count < 2)
+    return RLK_ERR_SHAPE;
+  const TilePlan plan = plan_tiles(out_rows, out_cols, red, sm_count / 2);
+  *tile_cols = plan.narrow ? kBN / 2 : kBN;
+  *split_blocks = plan.split;
+  *launches = plan.split > 0 ? 2 : 1;
+  return RLK_OK;
+}
+
 size_t rlk_det_gemm_workspace_size(int op, const void* x, int x_dtype, int64_t x_rows,
                                    int64_t x_cols, int64_t ldx, const void* y, int y_dtype,
                                    int64_t y_rows, int64_t y_cols, int64_t ldy) {

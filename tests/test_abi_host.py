@@ -206,6 +206,41 @@ def test_throughput_split_count(lib):
     assert f(10, 10, 152, None) == 1
 
 
+def test_det_gemm_tile_plan(lib):
+    """det_gemm tiling on 152 SMs (76 pairs): narrow tiles when all wide ones fit in
+    half a wave; the last partial wave as half tiles in a second launch when it
+    would fill at most half the pairs and the reduction is at least 16384."""
+    cases = [
+        ((4096, 4096, 4096), (256, 0, 1)),         # 256 tiles, tail 28: reduction too short
+        ((4096, 3900, 16384), (256, 28, 2)),       # tail 28 <= 38, long reduction
+        ((4096, 4096, 151936), (256, 28, 2)),      # the linear-logp backward's grad_hidden
+        ((4096, 151936, 4096), (256, 0, 1)),       # 9504 tiles, tail 4: reduction too short
+        ((151936, 4096, 16384), (256, 4, 2)),      # 9504 tiles, tail 4, long reduction
+        ((3072, 3072, 16384), (256, 0, 1)),        # 144 tiles: tail 68 > 38
+        ((256, 4096, 4096), (128, 0, 1)),          # 16 tiles: 2 x 16 <= 76, narrow throughout
+        ((1000, 1000, 1000), (128, 0, 1)),         # 16 tiles
+        ((2560, 2048, 4096), (256, 0, 1)),         # 80 tiles: 2 x 80 > 76
+        ((4864, 4096, 65536), (256, 0, 1)),        # 19 x 16 = 304 tiles = exactly 4 waves
+        ((4096, 4864, 65536), (256, 0, 1)),        # the same transposed
+    ]
+    for (rows, cols, red), want in cases:
+        got = rlk.det_gemm_tile_plan(rows, cols, red, 152)
+        assert (got["tile_cols"], got["split_blocks"], got["launches"]) == want, (rows, cols, red, got)
+    # 38 wide tiles exactly fill half the pairs: narrow throughout
+    assert rlk.det_gemm_tile_plan(9728, 256, 16384, 152)["tile_cols"] == 128
+    # 77 wide tiles on 76 pairs: a last wave of one tile, split when the reduction is long
+    assert rlk.det_gemm_tile_plan(256 * 77, 256, 16384, 152) == \
+        {"tile_cols": 256, "split_blocks": 1, "launches": 2}
+    # an odd SM count divides into floor(sm_count / 2) pairs
+    assert rlk.det_gemm_tile_plan(4096, 4096, 16384, 151)["split_blocks"] == 256 % 75
+    t, b, n = ctypes.c_int32(), ctypes.c_int64(), ctypes.c_int32()
+    f = lib.rlk_det_gemm_tile_plan
+    for bad in [(0, 10, 10, 152), (10, 0, 10, 152), (10, 10, 0, 152), (1 << 31, 10, 10, 152),
+                (10, 10, 10, 1), (10, 10, 10, 0)]:
+        assert f(*bad, ctypes.byref(t), ctypes.byref(b), ctypes.byref(n)) == 2, bad
+    assert f(10, 10, 10, 152, None, ctypes.byref(b), ctypes.byref(n)) == 1
+
+
 def test_splits_workspace_size(lib):
     f = lib.rlk_linear_logp_splits_workspace_size
     g = lib.rlk_linear_logp_workspace_size
