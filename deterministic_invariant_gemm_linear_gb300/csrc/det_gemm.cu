@@ -924,6 +924,7 @@ size_t rlk_det_gemm_workspace_size(int op, const void* x, int x_dtype, int64_t x
 rlk_status rlk_det_gemm_fwd(const void* A, int64_t M, int64_t K, int64_t lda, const void* B,
                             int64_t N, int64_t ldb, void* C, int c_dtype, int64_t ldc,
                             void* workspace, size_t workspace_bytes, void* stream) {
+  RLK_CALL_RANGE();
   Operand a{A, RLK_BF16, M, K, lda};
   Operand b{B, RLK_BF16, K, N, ldb};
   rlk_status st;
@@ -935,6 +936,7 @@ rlk_status rlk_det_gemm_fwd(const void* A, int64_t M, int64_t K, int64_t lda, co
 rlk_status rlk_det_gemm_da(const void* dC, int dc_dtype, int64_t M, int64_t N, int64_t lddc,
                            const void* B, int64_t K, int64_t ldb, void* dA, int out_dtype,
                            int64_t ldda, void* workspace, size_t workspace_bytes, void* stream) {
+  RLK_CALL_RANGE();
   Operand a{dC, dc_dtype, M, N, lddc};
   Operand b{B, RLK_BF16, K, N, ldb};
   rlk_status st;
@@ -947,6 +949,7 @@ rlk_status rlk_det_gemm_da(const void* dC, int dc_dtype, int64_t M, int64_t N, i
 rlk_status rlk_det_gemm_db(const void* A, int64_t M, int64_t K, int64_t lda, const void* dC,
                            int dc_dtype, int64_t N, int64_t lddc, void* dB, int out_dtype,
                            int64_t lddb, void* workspace, size_t workspace_bytes, void* stream) {
+  RLK_CALL_RANGE();
   Operand a{A, RLK_BF16, M, K, lda};
   Operand b{dC, dc_dtype, M, N, lddc};
   rlk_status st;
@@ -959,6 +962,7 @@ rlk_status rlk_det_gemm_fwd_accum_fp32(const void* A, int64_t M, int64_t K, int6
                                       const void* B, int64_t N, int64_t ldb, float* C,
                                       int64_t ldc, void* workspace, size_t workspace_bytes,
                                       void* stream) {
+  RLK_CALL_RANGE();
   Operand a{A, RLK_BF16, M, K, lda};
   Operand b{B, RLK_BF16, K, N, ldb};
   rlk_status st;
@@ -970,6 +974,7 @@ rlk_status rlk_det_gemm_fwd_accum_fp32(const void* A, int64_t M, int64_t K, int6
 rlk_status rlk_det_linear_fwd(const void* X, int64_t M, int64_t K, int64_t ldx, const void* W,
                               int64_t N, int64_t ldw, void* Y, int y_dtype, int64_t ldy,
                               void* workspace, size_t workspace_bytes, void* stream) {
+  RLK_CALL_RANGE();
   Operand a{X, RLK_BF16, M, K, ldx};
   Operand b{W, RLK_BF16, N, K, ldw};
   rlk_status st;
@@ -981,6 +986,7 @@ rlk_status rlk_det_linear_fwd(const void* X, int64_t M, int64_t K, int64_t ldx, 
 rlk_status rlk_det_linear_dx(const void* dY, int dy_dtype, int64_t M, int64_t N, int64_t lddy,
                              const void* W, int64_t K, int64_t ldw, void* dX, int out_dtype,
                              int64_t lddx, void* workspace, size_t workspace_bytes, void* stream) {
+  RLK_CALL_RANGE();
   Operand a{dY, dy_dtype, M, N, lddy};
   Operand b{W, RLK_BF16, N, K, ldw};
   rlk_status st;
@@ -993,6 +999,7 @@ rlk_status rlk_det_linear_dx(const void* dY, int dy_dtype, int64_t M, int64_t N,
 rlk_status rlk_det_linear_dw(const void* dY, int dy_dtype, int64_t M, int64_t N, int64_t lddy,
                              const void* X, int64_t K, int64_t ldx, void* dW, int out_dtype,
                              int64_t lddw, void* workspace, size_t workspace_bytes, void* stream) {
+  RLK_CALL_RANGE();
   Operand a{dY, dy_dtype, M, N, lddy};
   Operand b{X, RLK_BF16, M, K, ldx};
   rlk_status st;
@@ -1015,6 +1022,7 @@ rlk_status rlk_det_gemm_backward(const void* dC, int dc_dtype, int64_t M, int64_
                                  const void* B, int64_t ldb, void* dA, int da_dtype, int64_t ldda,
                                  void* dB, int db_dtype, int64_t lddb, void* workspace,
                                  size_t workspace_bytes, void* stream) {
+  RLK_CALL_RANGE();
   TwoProducts t{{dC, dc_dtype, M, N, lddc}, {B, RLK_BF16, K, N, ldb}, {A, RLK_BF16, M, K, lda}};
   if (K < 1) return RLK_ERR_SHAPE;
   rlk_status st = plan_two(t);
@@ -1037,6 +1045,7 @@ rlk_status rlk_det_linear_backward(const void* dY, int dy_dtype, int64_t M, int6
                                    const void* W, int64_t ldw, void* dX, int dx_dtype,
                                    int64_t lddx, void* dW, int dw_dtype, int64_t lddw,
                                    void* workspace, size_t workspace_bytes, void* stream) {
+  RLK_CALL_RANGE();
   TwoProducts t{{dY, dy_dtype, M, N, lddy}, {W, RLK_BF16, N, K, ldw}, {X, RLK_BF16, M, K, ldx}};
   if (K < 1) return RLK_ERR_SHAPE;
   rlk_status st = plan_two(t);
@@ -1049,6 +1058,7 @@ rlk_status rlk_det_linear_backward(const void* dY, int dy_dtype, int64_t M, int6
 rlk_status rlk_sum_partials_ordered(const float* partials, int64_t num_parts, int64_t rows,
                                     int64_t cols, int64_t ld_partial, int64_t part_stride,
                                     void* out, int out_dtype, int64_t ld_out, void* stream) {
+  RLK_CALL_RANGE();
   if (!dtype_ok(out_dtype)) return RLK_ERR_DTYPE;
   if (num_parts < 1 || num_parts >= kDimLimit || rows < 0 || rows >= kMaxExtent || cols < 1 ||
       cols >= kMaxExtent || ld_partial < cols || ld_partial >= kLdLimit || ld_out < cols ||

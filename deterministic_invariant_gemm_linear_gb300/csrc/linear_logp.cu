@@ -910,6 +910,7 @@ rlk_status rlk_linear_logp_partials(const void* hidden, int64_t N, int64_t H, in
                                     const float* bias, const int64_t* target,
                                     int64_t target_stride, void* workspace,
                                     size_t workspace_bytes, void* stream) {
+  RLK_CALL_RANGE();
   return partials_impl(hidden, N, H, ld_hidden, weight, V, ld_weight, bias, target, target_stride,
                        0, workspace, workspace_bytes, stream);
 }
@@ -918,6 +919,7 @@ rlk_status rlk_linear_logp_combine(int64_t N, int64_t V, const int64_t* target,
                                    int64_t target_stride, float* logp, float* lse,
                                    float* target_logit, const void* workspace,
                                    size_t workspace_bytes, void* stream) {
+  RLK_CALL_RANGE();
   return combine_impl(N, V, target, target_stride, logp, lse, target_logit, 0, workspace,
                       workspace_bytes, stream);
 }
@@ -927,6 +929,7 @@ rlk_status rlk_linear_logp(const void* hidden, int64_t N, int64_t H, int64_t ld_
                            const int64_t* target, int64_t target_stride, float* logp, float* lse,
                            float* target_logit, void* workspace, size_t workspace_bytes,
                            void* stream) {
+  RLK_CALL_RANGE();
   return linear_logp_impl(hidden, N, H, ld_hidden, weight, V, ld_weight, bias, target,
                           target_stride, logp, lse, target_logit, 0, workspace, workspace_bytes,
                           stream);
@@ -992,6 +995,7 @@ rlk_status rlk_linear_logp_shard_partials(const void* hidden, int64_t N, int64_t
                                           float* partials, int64_t ld_partials,
                                           float* target_logit, void* workspace,
                                           size_t workspace_bytes, void* stream) {
+  RLK_CALL_RANGE();
   return shard_partials_impl(hidden, N, H, ld_hidden, weight_shard, V, split_begin, split_end,
                              ld_weight, bias_shard, target, target_stride, partials, ld_partials,
                              target_logit, workspace, workspace_bytes, stream);
@@ -1004,6 +1008,7 @@ rlk_status rlk_linear_logp_combine_shards(int64_t N, int64_t V, const int64_t* t
                                           const float* target_logits, int64_t zt_stride,
                                           float* logp, float* lse, float* target_logit,
                                           void* stream) {
+  RLK_CALL_RANGE();
   return combine_shards_impl(N, V, target, target_stride, num_shards, split_offsets, partials,
                              ld_partials, shard_stride, target_logits, zt_stride, logp, lse,
                              target_logit, stream);
@@ -1023,6 +1028,7 @@ rlk_status rlk_linear_logp_splits(const void* hidden, int64_t N, int64_t H, int6
                                   float* logp, float* lse, float* target_logit,
                                   int64_t num_splits, void* workspace, size_t workspace_bytes,
                                   void* stream) {
+  RLK_CALL_RANGE();
   return linear_logp_impl(hidden, N, H, ld_hidden, weight, V, ld_weight, bias, target,
                           target_stride, logp, lse, target_logit, num_splits, workspace,
                           workspace_bytes, stream);
@@ -1138,6 +1144,7 @@ extern "C" rlk_status rlk_linear_logp_noalloc(const void* hidden, int64_t N, int
                                               const int64_t* target, int64_t target_stride,
                                               float* logp, float* lse, float* target_logit,
                                               void* stream) {
+  RLK_CALL_RANGE();
   const size_t need = rlk_linear_logp_workspace_size(hidden, N, H, ld_hidden, weight, V, ld_weight);
   if (need > rlk::kNoAllocScratchBytes) return RLK_ERR_WORKSPACE;
   if (N == 0 || need == 0)   // empty call, or arguments the regular entry point rejects

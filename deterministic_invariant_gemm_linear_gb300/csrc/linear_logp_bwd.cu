@@ -291,6 +291,7 @@ rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64_t H, in
                                     int64_t ld_grad_hidden, void* grad_weight,
                                     int grad_weight_dtype, int64_t ld_grad_weight, float* grad_bias,
                                     void* workspace, size_t workspace_bytes, void* stream) {
+  RLK_CALL_RANGE();
   // ---- every check, including those of the products below, before the first launch
   BwdPlan p;
   rlk_status st = bwd_plan(hidden, N, H, ld_hidden, weight, V, ld_weight, &p);

@@ -6,9 +6,22 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "rlk.h"
 
 namespace rlk {
+
+// Names a C-ABI call in profiler timelines: an NVTX range around the call (the
+// kernels it launches fall inside it; `ncu --nvtx --nvtx-include "<name>/"`
+// selects them).  Without an attached tool NVTX calls return at once.
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
+#define RLK_CALL_RANGE() ::rlk::CallRange rlk_call_range_(__func__)
 
 struct DeviceInfo {
   int device = -1;
