@@ -101,6 +101,8 @@ def test_debug_build_store_checks_and_trace(dev):
 
 
 def test_release_build_has_no_debug_entry_points(dev):
+    if os.environ.get("RLK_LIBRARY") == "debug":
+        pytest.skip("the whole suite is running against the debug build (RLK_LIBRARY=debug)")
     assert not rlk.is_debug_build()
     assert rlk.lib().rlk_selftest_store_check(rlk._stream_ptr(None)) == 10  # NOT_DEBUG_BUILD
     assert rlk.device_error() == 0
