@@ -793,6 +793,9 @@ def det_gemm_bench(args, dev, rank, world, peaks, peak_src):
             ts.append(s0.elapsed_time(s1))
         extra_ms[name] = float(np.median(ts))
     best = min(ms, key=ms.get)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    tiling = {"fwd": rlk.det_gemm_tile_plan(M, N, K_, sms), "da": rlk.det_gemm_tile_plan(M, K_, N, sms),
+              "db": rlk.det_gemm_tile_plan(K_, N, M, sms)}
     line = {
         "metric": "det_gemm fwd+da+db TFLOP/s (M=N=K=4096, BF16 in/out, FP32 accumulate)",
         "value": 3 * flop * world * K / t / 1e12, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
@@ -813,7 +816,8 @@ def det_gemm_bench(args, dev, rank, world, peaks, peak_src):
         "cublas_bf16_tflops_context": cublas,
         "other_entry_points_ms_median": extra_ms,
         "clocks": clocks.summary(),
-        "gpu_launches": 3 * K,
+        "tiling": tiling,
+        "gpu_launches": K * sum(p["launches"] for p in tiling.values()),
     }
     line["roofline"].update(per_clock(line["roofline"]["achieved"], line["clocks"], dev))
     # ---- e2e: host buffers (pinned) in, all three results out, copies timed.  Two
