@@ -794,8 +794,9 @@ def det_gemm_bench(args, dev, rank, world, peaks, peak_src):
         extra_ms[name] = float(np.median(ts))
     best = min(ms, key=ms.get)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    tiling = {"fwd": rlk.det_gemm_tile_plan(M, N, K_, sms), "da": rlk.det_gemm_tile_plan(M, K_, N, sms),
-              "db": rlk.det_gemm_tile_plan(K_, N, M, sms)}
+    tiling = {"fwd": rlk.det_gemm_tile_plan(rlk.RLK_GEMM_FWD, M, N, K_, sms),
+              "da": rlk.det_gemm_tile_plan(rlk.RLK_GEMM_DA, M, K_, N, sms),
+              "db": rlk.det_gemm_tile_plan(rlk.RLK_GEMM_DB, K_, N, M, sms)}
     line = {
         "metric": "det_gemm fwd+da+db TFLOP/s (M=N=K=4096, BF16 in/out, FP32 accumulate)",
         "value": 3 * flop * world * K / t / 1e12, "unit": "TFLOP/s", "n_gpus": world, "steps": K,

@@ -74,8 +74,9 @@ SIGNATURES = {
     "rlk_linear_logp_noalloc": (_I, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _P, _I64,
                                      _P, _P, _P, _P]),
     "rlk_throughput_split_count": (_I, [_I64, _I64, ctypes.c_int32, ctypes.POINTER(_I64)]),
-    "rlk_det_gemm_tile_plan": (_I, [_I64, _I64, _I64, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32),
-                                    ctypes.POINTER(_I64), ctypes.POINTER(ctypes.c_int32)]),
+    "rlk_det_gemm_tile_plan": (_I, [_I, _I64, _I64, _I64, ctypes.c_int32,
+                                    ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(_I64),
+                                    ctypes.POINTER(ctypes.c_int32)]),
     "rlk_vocab_shard_range": (_I, [_I64, _I64, _I64, ctypes.POINTER(_I64), ctypes.POINTER(_I64),
                                    ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
     "rlk_linear_logp_shard_workspace_size": (_SZ, [_P, _I64, _I64, _I64, _P, _I64, _I64, _I64,
@@ -221,11 +222,12 @@ def throughput_split_count(N: int, V: int, sm_count: int = 0) -> int:
     return s.value
 
 
-def det_gemm_tile_plan(out_rows: int, out_cols: int, red: int, sm_count: int) -> dict:
-    """The det_gemm output tiling for these extents on sm_count SMs (host arithmetic):
-    {"tile_cols": 256 | 128, "split_blocks": wide blocks run as halves, "launches": 1 | 2}."""
+def det_gemm_tile_plan(op: int, out_rows: int, out_cols: int, red: int, sm_count: int) -> dict:
+    """The output tiling of det_gemm op (RLK_GEMM_*) for these extents on sm_count SMs
+    (host arithmetic): {"tile_cols": 256 | 224 | 128, "split_blocks": wide blocks run as
+    halves, "launches": 1 | 2}."""
     t, b, n = ctypes.c_int32(), _I64(), ctypes.c_int32()
-    _check(lib().rlk_det_gemm_tile_plan(out_rows, out_cols, red, sm_count, ctypes.byref(t),
+    _check(lib().rlk_det_gemm_tile_plan(op, out_rows, out_cols, red, sm_count, ctypes.byref(t),
                                         ctypes.byref(b), ctypes.byref(n)), "rlk_det_gemm_tile_plan")
     return {"tile_cols": t.value, "split_blocks": b.value, "launches": n.value}
 

@@ -32,6 +32,8 @@ __device__ unsigned int g_err_det_gemm = 0;
 
 namespace {
 
+constexpr int kMidTileN = 224;   // tiles of K-major right operands (112 rows per CTA)
+
 struct GemmSched {
   Banded order; // rows = 256-row output blocks (one per CTA pair), cols = order_n-column blocks
   int* counter; // nullptr: cluster c takes units c, c + C, ... (a few rounds at most sizes)
@@ -460,6 +462,7 @@ cudaError_t ensure_attrs(int dev) {
     if (e == cudaSuccess) e = set_attr<false, true, 128, 128>();
     if (e == cudaSuccess) e = set_attr<false, false, 128, 128>();
     if (e == cudaSuccess) e = set_attr<true, true, 128, 128>();
+    if (e == cudaSuccess) e = set_attr<false, false, kMidTileN, 128>();
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(det_gemm_fwd_db_kernel<true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -472,32 +475,50 @@ cudaError_t ensure_attrs(int dev) {
   return cudaSuccess;
 }
 
-// Tiling, from the output's extents, the reduction length and the number of CTA
-// pairs only.  Wide tiles are 256 x 256 with 64-element stages; narrow ones
-// 256 x 128 with 128-element stages (four MMAs of N = 128 per 64-element stage
-// left the pipe idle between stages).  A narrow tile takes about 0.69 of a wide
-// tile's time on GB300 (uniform narrow tiles at 4096^3: 105 us against 86.7 us;
-// 134 us with 64-element stages), so narrow tiles pay off where wide ones would
-// leave at least half the pairs idle:
-//  * throughout, when all wide tiles fit in half a wave (1000^3: 15.0 - 16.0 vs
-//    15.0 - 17.1 us with 64-element stages);
+// Tiling, from the output's extents, the reduction length, the right operand's
+// majorness and the number of CTA pairs only.  Wide tiles are 256 x 256 with
+// 64-element stages; narrow ones 256 x 128 and, for a K-major right operand
+// (dA, the linear forward), 256 x 224 tiles, both with 128-element stages.  Times
+// per tile relative to a wide one, measured on GB300: narrow 0.69 (uniform
+// narrow tiles at 4096^3: 105 us against 86.7 us; 134 us with 64-element
+// stages), 224-wide 0.89 - 0.93 (0.99 with 64-element stages).  The plan with
+// the fewest wide-tile times per pair wins:
+//  * narrow tiles throughout when all wide tiles fit in half a wave (1000^3:
+//    15.0 - 16.0 vs 15.0 - 17.1 us with 64-element stages);
 //  * for a last, partial wave that would fill at most half the pairs, when the
-//    reduction is long: its wide blocks are computed as two narrow halves each
-//    in a second launch, which costs a few microseconds of its own (4096^3: 88.7
-//    vs 86.7 us; 4096 x 151936 x 4096: 2.80 vs 2.96 - 3.01 ms).
+//    reduction is long: its wide blocks computed as two narrow halves each in a
+//    second launch, which costs a few microseconds of its own (4096^3: 88.7 vs
+//    86.7 us; 4096 x 151936 x 4096: 2.80 vs 2.96 - 3.01 ms);
+//  * 224-wide tiles where their waves cost less (dA at 4096^3: 19 x 16 = 304
+//    tiles fill 4 waves, 80.6 - 82.6 against 86.7 - 87.5 us; at 3072 x 4096 x
+//    3072 51.9 against 53.9 us; where they add a wave, 2 - 3% slower: not chosen).
 // Every output element runs the same 16-element MMAs in the same order whatever
 // the tile, so the bits are the same.
 constexpr int64_t kSplitMinReduction = 16384;
+constexpr int64_t kHalfTileCost = 70;    // a narrow half tile, in hundredths of a wide tile's time
+constexpr int64_t kMidTileCost = 93;     // a 224-wide tile
 struct TilePlan {
   bool narrow;     // narrow tiles throughout
   int64_t split;   // wide blocks at the end of the order computed as narrow halves
+  int wide_n;      // columns of the other tiles: 256, or 224 (K-major right operand)
 };
-TilePlan plan_tiles(int64_t out_rows, int64_t out_cols, int64_t red, int64_t clusters) {
-  const int64_t wide = ceil_div(out_rows, kPairRows) * ceil_div(out_cols, kBN);
-  if (2 * wide <= clusters) return {true, 0};
+TilePlan plan_tiles(int64_t out_rows, int64_t out_cols, int64_t red, int64_t clusters,
+                    bool b_kmajor) {
+  const int64_t rb = ceil_div(out_rows, kPairRows);
+  const int64_t wide = rb * ceil_div(out_cols, kBN);
+  if (2 * wide <= clusters) return {true, 0, kBN};
+  TilePlan plan{false, 0, kBN};
+  int64_t best = 100 * ceil_div(wide, clusters);
   const int64_t tail = wide % clusters;
-  if (red >= kSplitMinReduction && wide > clusters && 2 * tail <= clusters) return {false, tail};
-  return {false, 0};
+  if (red >= kSplitMinReduction && wide > clusters && 2 * tail <= clusters) {
+    plan.split = tail;
+    best = 100 * (wide / clusters) + kHalfTileCost;
+  }
+  if (b_kmajor) {
+    const int64_t mid = kMidTileCost * ceil_div(rb * ceil_div(out_cols, kMidTileN), clusters);
+    if (100 * mid < 98 * best) plan = TilePlan{false, 0, kMidTileN};   // a 2% margin
+  }
+  return plan;
 }
 
 inline bool dtype_ok(int d) { return d == RLK_BF16 || d == RLK_FP32; }
@@ -592,7 +613,7 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
   if ((st = materialise(y, ws, s, &yp)) != RLK_OK) return st;
 
   const int64_t clusters = dev.sm_count / 2;
-  const TilePlan plan = plan_tiles(out_rows, out_cols, red, clusters);
+  const TilePlan plan = plan_tiles(out_rows, out_cols, red, clusters, kind == Kind::kDa);
   GemmOut o;
   o.M = (int)out_rows;
   o.N = (int)out_cols;
@@ -603,9 +624,9 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
   o.vec_bytes = store_width(C, ldc, esize(c_dtype));
   GemmSched sc;
   sc.order.rows = (int)num_mb;
-  sc.order.cols = (int)ceil_div(out_cols, plan.narrow ? kBN / 2 : kBN);
+  sc.order.cols = (int)ceil_div(out_cols, plan.narrow ? kBN / 2 : plan.wide_n);
   sc.order.band = band_rows(num_mb, red, kPairRows);
-  sc.order_n = plan.narrow ? kBN / 2 : kBN;
+  sc.order_n = plan.narrow ? kBN / 2 : plan.wide_n;
   sc.counter = nullptr;
   sc.nkb64 = (int)ceil_div(red, kBK);
 
@@ -614,7 +635,8 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
   // MN-major box spans one stage of the reduction).  Both are encoded before
   // anything launches, so a failure leaves the output untouched.
   auto encode = [&](bool narrow, CUtensorMap* ta, CUtensorMap* tb) -> bool {
-    const int tile_n = narrow ? kBN / 2 : kBN, stage_k = narrow ? 128 : 64;
+    const int tile_n = narrow ? kBN / 2 : plan.wide_n;
+    const int stage_k = narrow || plan.wide_n == kMidTileN ? 128 : 64;
     switch (kind) {
       case Kind::kFwd:   // A [M,K] K-major; B [K,N] MN-major
         return encode_bf16_2d(ta, xp, x.cols, x.rows, x.eff_ld, kBK, kHalfRows) &&
@@ -639,7 +661,7 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
     const CUtensorMap& ta = narrow ? ta_n : ta_w;
     const CUtensorMap& tb = narrow ? tb_n : tb_w;
     GemmSched part = sc;
-    part.nkb = (int)ceil_div(red, narrow ? 128 : 64);
+    part.nkb = (int)ceil_div(red, narrow || plan.wide_n == kMidTileN ? 128 : 64);
     part.first = (int)first;
     part.units = (int)units;
     part.halves = halves ? 1 : 0;
@@ -657,8 +679,11 @@ rlk_status run_gemm(Kind kind, Operand x, Operand y, int64_t out_rows, int64_t o
       case Kind::kDa:
         e = narrow ? launch_overlapped(det_gemm_kernel<false, false, 128, 128>, grid, kThreads,
                                        kNarrowSmem, s, ta, tb, part, o)
-                   : launch_overlapped(det_gemm_kernel<false, false, 256, 64>, grid, kThreads,
-                                       kWideSmem, s, ta, tb, part, o);
+            : plan.wide_n == kMidTileN
+                ? launch_overlapped(det_gemm_kernel<false, false, kMidTileN, 128>, grid, kThreads,
+                                    PairRingT<kMidTileN / 2, 128>::kSmemBytes, s, ta, tb, part, o)
+                : launch_overlapped(det_gemm_kernel<false, false, 256, 64>, grid, kThreads,
+                                    kWideSmem, s, ta, tb, part, o);
         break;
       case Kind::kDb:
         e = narrow ? launch_overlapped(det_gemm_kernel<true, true, 128, 128>, grid, kThreads,
@@ -892,14 +917,18 @@ using namespace rlk;
 
 extern "C" {
 
-rlk_status rlk_det_gemm_tile_plan(int64_t out_rows, int64_t out_cols, int64_t red, int32_t sm_count,
-                                  int32_t* tile_cols, int64_t* split_blocks, int32_t* launches) {
+rlk_status rlk_det_gemm_tile_plan(int op, int64_t out_rows, int64_t out_cols, int64_t red,
+                                  int32_t sm_count, int32_t* tile_cols, int64_t* split_blocks,
+                                  int32_t* launches) {
   if (!tile_cols || !split_blocks || !launches) return RLK_ERR_NULL;
+  if (op < RLK_GEMM_FWD || op > RLK_GEMM_FWD_ACCUM) return RLK_ERR_SHAPE;
   if (out_rows < 1 || out_rows >= kMaxExtent || out_cols < 1 || out_cols >= kMaxExtent ||
       red < 1 || red >= kMaxExtent || sm_count < 2)
     return RLK_ERR_SHAPE;
-  const TilePlan plan = plan_tiles(out_rows, out_cols, red, sm_count / 2);
-  *tile_cols = plan.narrow ? kBN / 2 : kBN;
+  // the products whose right operand is read K-major: dA and the linear forward
+  const bool b_kmajor = op == RLK_GEMM_DA || op == RLK_GEMM_LINEAR_FWD;
+  const TilePlan plan = plan_tiles(out_rows, out_cols, red, sm_count / 2, b_kmajor);
+  *tile_cols = plan.narrow ? kBN / 2 : plan.wide_n;
   *split_blocks = plan.split;
   *launches = plan.split > 0 ? 2 : 1;
   return RLK_OK;

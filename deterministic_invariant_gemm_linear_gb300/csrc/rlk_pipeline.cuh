@@ -55,7 +55,8 @@ struct PairRingT {
   static_assert(kSmemBytes <= kSmemLimit, "exceeds the 227 KiB per-CTA shared memory limit");
   // One CTA per SM: a second resident CTA could not get TMEM columns.
   static_assert(kSmemBytes > kSmemLimit / 2, "tcgen05 kernels must own their SM");
-  static_assert(kBHalf == kHalfRows || kBHalf == kHalfRows / 2, "256- or 128-wide tiles");
+  static_assert(kBHalf == kHalfRows || kBHalf == kHalfRows / 2 || kBHalf == 112,
+                "256-, 224- or 128-wide tiles");
 };
 using PairRing = PairRingT<kHalfRows>;                              // 256 x 256 tiles, 7 stages
 

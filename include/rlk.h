@@ -503,11 +503,13 @@ RLK_API rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64
 #define RLK_GEMM_FWD_ACCUM 6
 
 /*
- * The output tiling the det_gemm products use (host arithmetic only, no device
- * call), for an out_rows x out_cols output reduced over `red` elements on a
- * device of sm_count SMs:
- *  *tile_cols     256, or 128 when all 256-wide tiles fit in half a wave of SM
- *                 pairs (2 x tiles <= sm_count / 2);
+ * The output tiling a det_gemm product uses (host arithmetic only, no device
+ * call), for op (RLK_GEMM_*) with an out_rows x out_cols output reduced over
+ * `red` elements on a device of sm_count SMs:
+ *  *tile_cols     256; 128 when all 256-wide tiles fit in half a wave of SM pairs
+ *                 (2 x tiles <= sm_count / 2); 224 for dA and the linear forward
+ *                 (right operand read K-major) where 224-wide tiles cost fewer
+ *                 wave-times per pair;
  *  *split_blocks  the number of 256-wide blocks at the end of the unit order that
  *                 are computed as two 128-wide halves in a second launch: the last
  *                 partial wave, when it would fill at most half the pairs and red
@@ -515,12 +517,12 @@ RLK_API rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64
  *  *launches      1 or 2.
  * The tiling never changes an output bit (each element runs the same MMAs in the
  * same order); this reports it for tests and measurements.  RLK_ERR_NULL for a
- * null output pointer, RLK_ERR_SHAPE for an extent outside [1, 2^31 - 256) or
- * sm_count < 2.  The two-product entries (rlk_det_gemm_backward,
+ * null output pointer, RLK_ERR_SHAPE for an unknown op, an extent outside
+ * [1, 2^31 - 256) or sm_count < 2.  The two-product entries (rlk_det_gemm_backward,
  * rlk_det_linear_backward) follow it for each product when they run the products
  * as separate launches; their one-launch path keeps 256-wide tiles.
  */
-RLK_API rlk_status rlk_det_gemm_tile_plan(int64_t out_rows, int64_t out_cols, int64_t red,
+RLK_API rlk_status rlk_det_gemm_tile_plan(int op, int64_t out_rows, int64_t out_cols, int64_t red,
                                           int32_t sm_count, int32_t* tile_cols,
                                           int64_t* split_blocks, int32_t* launches);
 

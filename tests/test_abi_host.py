@@ -207,38 +207,50 @@ def test_throughput_split_count(lib):
 
 
 def test_det_gemm_tile_plan(lib):
-    """det_gemm tiling on 152 SMs (76 pairs): narrow tiles when all wide ones fit in
-    half a wave; the last partial wave as half tiles in a second launch when it
-    would fill at most half the pairs and the reduction is at least 16384."""
+    """det_gemm tiling on 152 SMs (76 pairs), in wide-tile times per pair: narrow tiles
+    when all wide ones fit in half a wave; the last partial wave as half tiles (0.70
+    each) in a second launch when it would fill at most half the pairs and the
+    reduction is at least 16384; for a K-major right operand (dA, linear forward)
+    224-wide tiles (0.93 each) when their waves cost at least 2% less."""
+    FWD, DA, DB, LIN = rlk.RLK_GEMM_FWD, rlk.RLK_GEMM_DA, rlk.RLK_GEMM_DB, rlk.RLK_GEMM_LINEAR_FWD
     cases = [
-        ((4096, 4096, 4096), (256, 0, 1)),         # 256 tiles, tail 28: reduction too short
-        ((4096, 3900, 16384), (256, 28, 2)),       # tail 28 <= 38, long reduction
-        ((4096, 4096, 151936), (256, 28, 2)),      # the linear-logp backward's grad_hidden
-        ((4096, 151936, 4096), (256, 0, 1)),       # 9504 tiles, tail 4: reduction too short
-        ((151936, 4096, 16384), (256, 4, 2)),      # 9504 tiles, tail 4, long reduction
-        ((3072, 3072, 16384), (256, 0, 1)),        # 144 tiles: tail 68 > 38
-        ((256, 4096, 4096), (128, 0, 1)),          # 16 tiles: 2 x 16 <= 76, narrow throughout
-        ((1000, 1000, 1000), (128, 0, 1)),         # 16 tiles
-        ((2560, 2048, 4096), (256, 0, 1)),         # 80 tiles: 2 x 80 > 76
-        ((4864, 4096, 65536), (256, 0, 1)),        # 19 x 16 = 304 tiles = exactly 4 waves
-        ((4096, 4864, 65536), (256, 0, 1)),        # the same transposed
+        ((FWD, 4096, 4096, 4096), (256, 0, 1)),       # 256 tiles, tail 28: reduction too short
+        ((DB, 4096, 4096, 4096), (256, 0, 1)),
+        ((DA, 4096, 4096, 4096), (224, 0, 1)),        # 16 x 19 = 304 tiles: 4 x 0.93 < 4
+        ((LIN, 4096, 4096, 4096), (224, 0, 1)),       # Y = X . W^T: the same right operand
+        ((DA, 3072, 4096, 3072), (224, 0, 1)),        # 192 tiles: 3 waves; 228 of 224: 3 x 0.93
+        ((DA, 3072, 3072, 4096), (256, 0, 1)),        # 144 tiles: 2 waves; 168 of 224: 3 waves
+        ((DA, 8192, 4096, 8192), (256, 0, 1)),        # 512 tiles: 7 waves; 608 of 224: 8 x 0.93
+        ((DA, 4096, 16384, 4096), (256, 0, 1)),       # 1024 tiles: 14 waves; 1184: 16 x 0.93
+        ((FWD, 4096, 3900, 16384), (256, 28, 2)),     # tail 28 <= 38, long reduction
+        ((FWD, 4096, 4096, 151936), (256, 28, 2)),    # the linear-logp backward's grad_hidden
+        ((DA, 4096, 4096, 151936), (256, 28, 2)),     # split 3.70 against 224-wide 3.72
+        ((FWD, 4096, 151936, 4096), (256, 0, 1)),     # 9504 tiles, tail 4: reduction too short
+        ((DB, 151936, 4096, 16384), (256, 4, 2)),     # 9504 tiles, tail 4, long reduction
+        ((FWD, 3072, 3072, 16384), (256, 0, 1)),      # 144 tiles: tail 68 > 38
+        ((DA, 256, 4096, 4096), (128, 0, 1)),         # 16 tiles: 2 x 16 <= 76, narrow throughout
+        ((FWD, 1000, 1000, 1000), (128, 0, 1)),       # 16 tiles
+        ((FWD, 2560, 2048, 4096), (256, 0, 1)),       # 80 tiles: 2 x 80 > 76
+        ((FWD, 4864, 4096, 65536), (256, 0, 1)),      # 19 x 16 = 304 tiles = exactly 4 waves
     ]
-    for (rows, cols, red), want in cases:
-        got = rlk.det_gemm_tile_plan(rows, cols, red, 152)
-        assert (got["tile_cols"], got["split_blocks"], got["launches"]) == want, (rows, cols, red, got)
+    for (op, rows, cols, red), want in cases:
+        got = rlk.det_gemm_tile_plan(op, rows, cols, red, 152)
+        assert (got["tile_cols"], got["split_blocks"], got["launches"]) == want, \
+            (op, rows, cols, red, got)
     # 38 wide tiles exactly fill half the pairs: narrow throughout
-    assert rlk.det_gemm_tile_plan(9728, 256, 16384, 152)["tile_cols"] == 128
+    assert rlk.det_gemm_tile_plan(FWD, 9728, 256, 16384, 152)["tile_cols"] == 128
     # 77 wide tiles on 76 pairs: a last wave of one tile, split when the reduction is long
-    assert rlk.det_gemm_tile_plan(256 * 77, 256, 16384, 152) == \
+    assert rlk.det_gemm_tile_plan(FWD, 256 * 77, 256, 16384, 152) == \
         {"tile_cols": 256, "split_blocks": 1, "launches": 2}
     # an odd SM count divides into floor(sm_count / 2) pairs
-    assert rlk.det_gemm_tile_plan(4096, 4096, 16384, 151)["split_blocks"] == 256 % 75
+    assert rlk.det_gemm_tile_plan(FWD, 4096, 4096, 16384, 151)["split_blocks"] == 256 % 75
     t, b, n = ctypes.c_int32(), ctypes.c_int64(), ctypes.c_int32()
     f = lib.rlk_det_gemm_tile_plan
-    for bad in [(0, 10, 10, 152), (10, 0, 10, 152), (10, 10, 0, 152), (1 << 31, 10, 10, 152),
-                (10, 10, 10, 1), (10, 10, 10, 0)]:
+    for bad in [(FWD, 0, 10, 10, 152), (FWD, 10, 0, 10, 152), (FWD, 10, 10, 0, 152),
+                (FWD, 1 << 31, 10, 10, 152), (FWD, 10, 10, 10, 1), (FWD, 10, 10, 10, 0),
+                (-1, 10, 10, 10, 152), (7, 10, 10, 10, 152)]:
         assert f(*bad, ctypes.byref(t), ctypes.byref(b), ctypes.byref(n)) == 2, bad
-    assert f(10, 10, 10, 152, None, ctypes.byref(b), ctypes.byref(n)) == 1
+    assert f(FWD, 10, 10, 10, 152, None, ctypes.byref(b), ctypes.byref(n)) == 1
 
 
 def test_splits_workspace_size(lib):

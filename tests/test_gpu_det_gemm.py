@@ -267,6 +267,42 @@ def test_tile_widths_give_the_same_bits(dev, out_dtype):
 
 
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_mid_width_tiles_give_the_same_bits(dev, out_dtype):
+    """dA and the linear forward read their right operand K-major; a 4096 x 4096 output
+    runs 19 x 16 = 304 tiles 224 wide (4 full waves on 76 SM pairs) instead of 256
+    tiles 256 wide.  Integer inputs give the exact product, and its rows equal the
+    same rows of a 2304-row call (256-wide tiles), a 1792-row call (224) and 256-row
+    calls (128-wide tiles), bit for bit."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    DA, LIN = rlk.RLK_GEMM_DA, rlk.RLK_GEMM_LINEAR_FWD
+    if sms == 152:
+        assert rlk.det_gemm_tile_plan(DA, 4096, 4096, 4096, sms)["tile_cols"] == 224
+        assert rlk.det_gemm_tile_plan(DA, 2304, 4096, 4096, sms)["tile_cols"] == 256
+        assert rlk.det_gemm_tile_plan(DA, 1792, 4096, 4096, sms)["tile_cols"] == 224
+        assert rlk.det_gemm_tile_plan(LIN, 4096, 4096, 4096, sms)["tile_cols"] == 224
+    g = torch.Generator(device=dev).manual_seed(22)
+
+    def ints(r, c):
+        return torch.randint(-4, 5, (r, c), generator=g, device=dev).to(torch.bfloat16)
+
+    dC, B = ints(4096, 4096), ints(4096, 4096)     # dA = dC . B^T -> [4096, 4096]
+    X, W = ints(4096, 4096), ints(4096, 4096)      # Y = X . W^T
+    cases = {
+        "da": (rlk.det_gemm_da(dC, B, out_dtype), dC.double() @ B.double().T,
+               lambda r: rlk.det_gemm_da(dC[r], B, out_dtype)),
+        "linear": (rlk.det_linear(X, W, out_dtype), X.double() @ W.double().T,
+                   lambda r: rlk.det_linear(X[r], W, out_dtype)),
+    }
+    for name, (full, exact, part) in cases.items():
+        assert torch.equal(full.double(), exact.float().to(out_dtype).double()), name
+        split = torch.cat([part(slice(0, 2304)), part(slice(2304, 4096))])
+        assert bits_equal(split, full), name
+        small = torch.cat([part(slice(s, s + 256)) for s in range(0, 4096, 256)])
+        assert bits_equal(small, full), name
+    assert rlk.device_error() == 0
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_last_wave_split_gives_the_same_bits(dev, out_dtype):
     """An output of 16 x 16 wide tiles on 76 SM pairs leaves a last wave of 28
     tiles; with a long reduction (16384 here) those blocks are computed as two
