@@ -483,8 +483,9 @@ RLK_API rlk_status rlk_linear_logp_backward(const void* hidden, int64_t N, int64
  * 256-wide tiles would leave at least half of the SM pairs idle; with a
  * reduction of 16384 or more, a last wave of 256-wide tiles that would fill at
  * most half the pairs runs as 128-wide halves in a second launch on the same
- * stream.  Each output element is the same sum whatever its tile, so the tiling
- * never changes a bit.
+ * stream; dA and the linear forward use 256 x 224 tiles where those fill the
+ * waves better (rlk_det_gemm_tile_plan reports the choice).  Each output element
+ * is the same sum whatever its tile, so the tiling never changes a bit.
  * Outputs are BF16 (round to nearest even from the FP32 accumulator) or FP32.
  * A batched operand [b, M, K] is passed flattened as [b * M, K] (a leading
  * shape is a row count), so fwd and dA are bitwise equal per row whatever the
