@@ -14,7 +14,8 @@
 //   dB       A [M,K] MN-major (output rows = K),      dC [M,N] MN-major (M is reduced)
 // Output tiles are 256 x 256 per CTA pair (2-SM tcgen05 loop, M=256 x N=256 x
 // K=16 per MMA; 256 x 128 for outputs too small to fill the SM pairs and for a
-// last wave that would leave most pairs idle), the reduction runs in ascending
+// last wave that would leave most pairs idle; 256 x 224 for a K-major right
+// operand where that fills the waves better), the reduction runs in ascending
 // order in 16-element MMAs, each tile's accumulation starts from zero, and there is no
 // split of the reduction: every output bit is a function of its own row of the
 // left operand and column of the right operand only.
