@@ -236,6 +236,38 @@ def det_gemm_split_cases(dev, fails):
                 fails.append(f"{what}: a canary was overwritten")
 
 
+def det_gemm_mid_width_cases(dev, fails):
+    """dA and the linear forward on 256 x 224 tiles (a 4096 x 4000 output: 16 x 18
+    tiles, the last column block 192 wide) write only their own columns of a pitched
+    output."""
+    lib, P = rlk.lib(), rlk._ptr
+    sp = rlk._stream_ptr(None)
+    g = torch.Generator(device=dev).manual_seed(78)
+
+    def bf(r, c):
+        return torch.randn(r, c, generator=g, device=dev).to(torch.bfloat16)
+
+    dC, B = bf(4096, 4096), bf(4000, 4096)   # dA = dC . B^T -> [4096, 4000]
+    X, W = bf(4096, 4096), bf(4000, 4096)    # Y = X . W^T -> [4096, 4000]
+    for dtype, esize in ((rlk.RLK_FP32, 4), (rlk.RLK_BF16, 2)):
+        for op in ("da", "linear"):
+            rows, cols = 4096, 4000
+            ld = cols + 5
+            C = Guarded(rows * ld * esize, dev)
+            if op == "da":
+                st = lib.rlk_det_gemm_da(P(dC), rlk.RLK_BF16, 4096, 4096, 4096, P(B), 4000, 4096,
+                                         C.ptr, dtype, ld, None, 0, sp)
+            else:
+                st = lib.rlk_det_linear_fwd(P(X), 4096, 4096, 4096, P(W), 4000, 4096, C.ptr, dtype,
+                                            ld, None, 0, sp)
+            torch.cuda.synchronize()
+            what = f"det_gemm {op} 224-wide tiles esize={esize}"
+            if st != 0:
+                fails.append(f"{what}: status {st}")
+            elif not (C.bands_intact() and _pitched_untouched(C, rows, cols, ld, esize)):
+                fails.append(f"{what}: a canary was overwritten")
+
+
 def shard_cases(dev, fails):
     lib, P = rlk.lib(), rlk._ptr
     sp = rlk._stream_ptr(None)
@@ -274,5 +306,6 @@ def run_all(dev):
     backward_cases(dev, fails)
     det_gemm_cases(dev, fails)
     det_gemm_split_cases(dev, fails)
+    det_gemm_mid_width_cases(dev, fails)
     shard_cases(dev, fails)
     return fails
